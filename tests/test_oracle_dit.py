@@ -1,0 +1,221 @@
+"""Pins for oracle.dit (block math in float64).
+
+The pages print no block math; each function is pinned to torch library
+routines (a different implementation of the same standard definition), to
+closed forms and to invariants.
+"""
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import synth
+from oracle import dit, fp8
+
+torch.set_default_dtype(torch.float64)
+
+
+def T(a):
+    return torch.from_numpy(np.asarray(a, dtype=np.float64))
+
+
+def test_layernorm_vs_torch():
+    x = np.random.default_rng(0).standard_normal((7, 96)) * 3 + 1
+    ref = F.layer_norm(T(x), (96,), eps=1e-6).numpy()
+    np.testing.assert_allclose(dit.layernorm(x), ref, rtol=1e-12, atol=1e-12)
+    y = dit.layernorm(x)
+    np.testing.assert_allclose(y.mean(-1), 0, atol=1e-12)
+    np.testing.assert_allclose(y.var(-1), 1, atol=1e-5)   # eps shifts it by ~1e-6
+
+
+def test_rmsnorm_vs_torch():
+    g = np.random.default_rng(1)
+    x = g.standard_normal((5, 64))
+    w = 1 + 0.1 * g.standard_normal(64)
+    ref = F.rms_norm(T(x), (64,), weight=T(w), eps=1e-6).numpy()
+    np.testing.assert_allclose(dit.rmsnorm(x, w), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_activations_vs_torch():
+    x = np.linspace(-8, 8, 1001)
+    np.testing.assert_allclose(dit.gelu_tanh(x), F.gelu(T(x), approximate="tanh").numpy(),
+                               rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(dit.silu(x), F.silu(T(x)).numpy(), rtol=1e-13, atol=1e-15)
+
+
+@pytest.mark.parametrize("nq,nk,heads,hd", [(9, 9, 2, 8), (5, 13, 3, 72), (16, 7, 1, 16)])
+def test_attention_vs_torch_sdpa(nq, nk, heads, hd):
+    g = np.random.default_rng(nq * 31 + nk)
+    q = g.standard_normal((nq, heads * hd))
+    k = g.standard_normal((nk, heads * hd))
+    v = g.standard_normal((nk, heads * hd))
+    th = lambda a, n: T(a).reshape(n, heads, hd).transpose(0, 1)
+    ref = F.scaled_dot_product_attention(th(q, nq), th(k, nk), th(v, nk))
+    ref = ref.transpose(0, 1).reshape(nq, heads * hd).numpy()
+    np.testing.assert_allclose(dit.attention(q, k, v, heads), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_attention_equal_keys_is_mean_of_v():
+    g = np.random.default_rng(3)
+    k = np.tile(g.standard_normal((1, 32)), (11, 1))
+    v = g.standard_normal((11, 32))
+    q = g.standard_normal((4, 32))
+    out = dit.attention(q, k, v, heads=4)
+    np.testing.assert_allclose(out, np.tile(v.mean(0), (4, 1)), rtol=1e-12, atol=1e-12)
+
+
+def _tiny(kind, **kw):
+    if kind == synth.KIND_DIT:
+        base = synth.StackConfig("t", kind, 2, 32, 2, 16, 64, 2, 10, cond_dim=24, **kw)
+    else:
+        base = synth.StackConfig("t", kind, 2, 32, 2, 16, 64, 2, 10, text_dim=48,
+                                 text_tokens=6, **kw)
+    return base
+
+
+def _inputs(cfg):
+    x = synth.activations(cfg)
+    cond = synth.condition(cfg) if cfg.kind == synth.KIND_VIDEO else \
+        np.random.default_rng(9).standard_normal((cfg.batch, cfg.cond_dim))
+    ctx = synth.text_context(cfg) if cfg.kind == synth.KIND_VIDEO else None
+    return x, cond, ctx
+
+
+def _big_weights(P, scale=10.0):
+    """Larger weights so every term of the block visibly moves the output."""
+    return {k: (v * scale if k.endswith("weight") and "norm" not in k else v)
+            for k, v in P.items()}
+
+
+def test_dit_block_vs_torch_modules():
+    cfg = _tiny(synth.KIND_DIT)
+    P = _big_weights(dit.prepare_block(synth.block_params(cfg, 0)))
+    x, c, _ = _inputs(cfg)
+    D, H = cfg.hidden, cfg.heads
+    ln = torch.nn.LayerNorm(D, eps=1e-6, elementwise_affine=False)
+    mha = torch.nn.MultiheadAttention(D, H, batch_first=True)
+    with torch.no_grad():
+        mha.in_proj_weight.copy_(T(P["attn.qkv.weight"]))
+        mha.in_proj_bias.copy_(T(P["attn.qkv.bias"]))
+        mha.out_proj.weight.copy_(T(P["attn.proj.weight"]))
+        mha.out_proj.bias.copy_(T(P["attn.proj.bias"]))
+        ada = torch.nn.Sequential(torch.nn.SiLU(), torch.nn.Linear(cfg.cond_dim, 6 * D))
+        ada[1].weight.copy_(T(P["adaLN.weight"]))
+        ada[1].bias.copy_(T(P["adaLN.bias"]))
+        mlp = torch.nn.Sequential(torch.nn.Linear(D, cfg.ffn), torch.nn.GELU(approximate="tanh"),
+                                  torch.nn.Linear(cfg.ffn, D))
+        mlp[0].weight.copy_(T(P["mlp.fc1.weight"]))
+        mlp[0].bias.copy_(T(P["mlp.fc1.bias"]))
+        mlp[2].weight.copy_(T(P["mlp.fc2.weight"]))
+        mlp[2].bias.copy_(T(P["mlp.fc2.bias"]))
+        xt, ct = T(x), T(c)
+        sh1, sc1, g1, sh2, sc2, g2 = ada(ct).unsqueeze(1).chunk(6, dim=-1)
+        h = ln(xt) * (1 + sc1) + sh1
+        xt = xt + g1 * mha(h, h, h, need_weights=False)[0]
+        h = ln(xt) * (1 + sc2) + sh2
+        ref = (xt + g2 * mlp(h)).numpy()
+    out = dit.dit_block(x, c, P, H)
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-10)
+    # the check is not vacuous: the block moves x by O(1)
+    assert np.abs(out - x).mean() > 0.1
+
+
+def test_video_block_vs_torch_primitives():
+    cfg = _tiny(synth.KIND_VIDEO)
+    P = _big_weights(dit.prepare_block(synth.block_params(cfg, 1)))
+    x, e, ctx = _inputs(cfg)
+    H, hd = cfg.heads, cfg.head_dim
+    t = {k: T(v) for k, v in P.items()}
+
+    def mha(q, k, v):
+        sp = lambda a: a.reshape(a.shape[0], a.shape[1], H, hd).transpose(1, 2)
+        o = F.scaled_dot_product_attention(sp(q), sp(k), sp(v))
+        return o.transpose(1, 2).reshape(q.shape)
+
+    D = cfg.hidden
+    xt, et, ct = T(x), T(e), T(ctx)
+    m = (et + t["modulation"][None]).unsqueeze(2)   # [B, 6, 1, D]
+    ln = lambda a: F.layer_norm(a, (D,), eps=1e-6)
+    rms = lambda a, w: F.rms_norm(a, (D,), weight=w, eps=1e-6)
+    lin = lambda a, n: F.linear(a, t[n + ".weight"], t[n + ".bias"])
+    h = ln(xt) * (1 + m[:, 1]) + m[:, 0]
+    q = rms(lin(h, "self_attn.q"), t["self_attn.norm_q.weight"])
+    k = rms(lin(h, "self_attn.k"), t["self_attn.norm_k.weight"])
+    xt = xt + m[:, 2] * lin(mha(q, k, lin(h, "self_attn.v")), "self_attn.o")
+    hc = F.layer_norm(xt, (D,), t["norm_cross.weight"], t["norm_cross.bias"], eps=1e-6)
+    q = rms(lin(hc, "cross_attn.q"), t["cross_attn.norm_q.weight"])
+    k = rms(lin(ct, "cross_attn.k"), t["cross_attn.norm_k.weight"])
+    xt = xt + lin(mha(q, k, lin(ct, "cross_attn.v")), "cross_attn.o")
+    h = ln(xt) * (1 + m[:, 4]) + m[:, 3]
+    ref = (xt + m[:, 5] * lin(F.gelu(lin(h, "ffn.fc1"), approximate="tanh"), "ffn.fc2")).numpy()
+    out = dit.video_block(x, e, ctx, P, H)
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-10)
+    assert np.abs(out - x).mean() > 0.1
+
+
+def test_zero_gates_give_identity():
+    cfg = _tiny(synth.KIND_DIT)
+    P = dit.prepare_block(synth.block_params(cfg, 0))
+    D = cfg.hidden
+    for chunk in (2, 5):                       # gate_msa, gate_mlp
+        P["adaLN.weight"][chunk * D:(chunk + 1) * D] = 0
+        P["adaLN.bias"][chunk * D:(chunk + 1) * D] = 0
+    x, c, _ = _inputs(cfg)
+    np.testing.assert_array_equal(dit.dit_block(x, c, P, cfg.heads), x)
+
+    cfgv = _tiny(synth.KIND_VIDEO)
+    Pv = dit.prepare_block(synth.block_params(cfgv, 0))
+    Pv["modulation"][[2, 5]] = 0
+    Pv["cross_attn.o.weight"][:] = 0
+    Pv["cross_attn.o.bias"][:] = 0
+    x, e, ctx = _inputs(cfgv)
+    e = e.copy()
+    e[:, [2, 5]] = 0
+    np.testing.assert_array_equal(dit.video_block(x, e, ctx, Pv, cfgv.heads), x)
+
+
+@pytest.mark.parametrize("kind", [synth.KIND_DIT, synth.KIND_VIDEO])
+def test_token_permutation_and_batch_independence(kind):
+    cfg = _tiny(kind)
+    P = _big_weights(dit.prepare_block(synth.block_params(cfg, 0)))
+    x, cond, ctx = _inputs(cfg)
+    out = dit.block_forward(kind, x, cond, ctx, P, cfg.heads)
+    perm = np.random.default_rng(5).permutation(cfg.tokens)
+    outp = dit.block_forward(kind, x[:, perm], cond, ctx, P, cfg.heads)
+    np.testing.assert_allclose(outp, out[:, perm], rtol=1e-11, atol=1e-11)
+    x2 = x.copy()
+    x2[1] += 1.0
+    out2 = dit.block_forward(kind, x2, cond, ctx, P, cfg.heads)
+    np.testing.assert_array_equal(out2[0], out[0])
+    assert not np.allclose(out2[1], out[1])
+
+
+@pytest.mark.parametrize("kind", [synth.KIND_DIT, synth.KIND_VIDEO])
+def test_rows_subset_matches_full(kind):
+    cfg = _tiny(kind)
+    P = dit.prepare_block(synth.block_params(cfg, 0))
+    x, cond, ctx = _inputs(cfg)
+    full = dit.block_forward(kind, x, cond, ctx, P, cfg.heads)
+    rows = [0, 3, 9]
+    sub = dit.block_forward(kind, x, cond, ctx, P, cfg.heads, rows=rows)
+    np.testing.assert_allclose(sub, full[:, rows], rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_prepare_uses_decoded_weights():
+    cfg = _tiny(synth.KIND_VIDEO, wdtype=synth.W_E4M3, master_fp32=True)
+    raw = synth.block_params(cfg, 0)
+    P = dit.prepare_block(raw, fp8_linears=True)
+    q, s = fp8.quantize_per_tensor(raw["ffn.fc1.weight"])
+    np.testing.assert_array_equal(P["ffn.fc1.codes"], q)
+    np.testing.assert_array_equal(P["ffn.fc1.weight"], fp8.decode_e4m3(q) * np.float64(s))
+    # non-linear tensors are bf16-exact in an FP8 stack
+    b = raw["ffn.fc1.bias"]
+    np.testing.assert_array_equal(synth.round_bf16(b), b)
+
+
+def test_max_rel_l2():
+    ref = np.ones((2, 3, 4))
+    y = ref.copy()
+    y[1] *= 1.1
+    assert abs(dit.max_rel_l2(y, ref) - 0.1) < 1e-12
+    assert dit.max_rel_l2(ref, ref) == 0.0
