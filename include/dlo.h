@@ -1,0 +1,356 @@
+/*
+ * dlo.h -- layerwise weight offload of a DiT block stack through two device
+ * slots, for one GB300 (sm_103a).  C ABI of libdlo.so.
+ *
+ * Every block's weights live flattened in host memory (pinned, or registered
+ * by this library).  Two device slots hold streamed blocks.  While streamed
+ * block i computes on the caller's compute stream, the next block (block i+1,
+ * or the first streamed block again after the last one) is copied into the
+ * other slot on the caller's copy stream; CUDA events order slot reuse.  The
+ * first k blocks may stay resident in caller-provided device buffers.
+ *
+ * Sources (vLLM-Omni documentation pages):
+ *  [LW]  "CPU Offloading for Diffusion Models", section "Layerwise (Blockwise)
+ *        Offloading": How It Works and the Execution Flow table.
+ *  [DLO] "Distributed Layerwise Offload": Feature compatibility table,
+ *        "Startup and runtime sequence", "Host backing and transfer
+ *        composition", "Failure and lifecycle boundaries", "Registered
+ *        runtime-cache transfer", "Rank-local path without DLO AllGather".
+ *  [OFF] "CPU Offloading" (offloader design README): "Shared lifecycle",
+ *        "Cross-strategy invariants".
+ * The DiT block math is not on those pages; it is the standard DiT adaLN-zero
+ * block and a video-DiT block (self-attention, cross-attention to text, FFN),
+ * stated in full at dlo_forward.
+ *
+ * Conventions for every call:
+ *  - Pointers named d_* (or documented as device) are device pointers of the
+ *    context's device; host pointers are plain process addresses.
+ *  - Streams are cudaStream_t passed as void*.
+ *  - The caller owns every buffer it passes and keeps it alive until
+ *    dlo_destroy returns.  The library owns only its events, the host ranges
+ *    it registered itself and the context object.
+ *  - Calls are not thread-safe on one context.  Different contexts are
+ *    independent.
+ *  - Errors return a negative dlo_status; dlo_last_error() gives the message.
+ *    Argument errors are detected before any state changes.
+ */
+#ifndef DLO_H
+#define DLO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DLO_ABI_VERSION 1
+
+typedef int dlo_status;
+#define DLO_OK            0
+#define DLO_EINVAL       -1  /* bad argument; nothing changed                    */
+#define DLO_ESTATE       -2  /* call out of lifecycle order; nothing changed     */
+#define DLO_ENOMEM       -3  /* a caller buffer is too small                     */
+#define DLO_ECUDA        -4  /* a CUDA runtime call failed (message has the code) */
+#define DLO_EREGISTER    -5  /* host registration failed and was rolled back     */
+#define DLO_ETIMEDOUT    -6  /* a bounded wait ran out (host or device side)     */
+#define DLO_EUNSUPPORTED -7  /* valid but not implemented combination            */
+#define DLO_EMISMATCH    -8  /* dlo_verify_slot: slot bytes differ from the host */
+
+/* block kinds */
+#define DLO_BLOCK_DIT    0   /* DiT adaLN-zero block, self-attention only        */
+#define DLO_BLOCK_VIDEO  1   /* video-DiT block: self-attn, cross-attn, FFN      */
+
+/* weight storage of the linears in a block */
+#define DLO_W_BF16       0
+#define DLO_W_E4M3       1   /* e4m3 weight + one fp32 scale per linear tensor   */
+
+/* slot staging engine */
+#define DLO_STAGE_MEMCPY 0   /* cudaMemcpyAsync on the copy stream (copy engine) */
+#define DLO_STAGE_GATHER 1   /* SM kernel reading mapped host memory, 16-B loads */
+
+/* host block flags for dlo_register_host_blocks */
+#define DLO_HOST_PINNED   1u /* caller's memory is already page-locked           */
+#define DLO_HOST_REGISTER 2u /* library page-locks it (all-or-nothing)           */
+
+/* tensor dtypes in the flat block layout */
+#define DLO_DT_BF16 0
+#define DLO_DT_E4M3 1
+#define DLO_DT_F32  2
+
+/* Stack description.  Constraints (else DLO_EINVAL): abi_version ==
+ * DLO_ABI_VERSION; n_blocks >= 1; hidden == heads * head_dim; hidden % 16 == 0;
+ * head_dim % 8 == 0 and head_dim <= 128; ffn % 16 == 0; max_batch >= 1;
+ * max_tokens >= 1; DiT: cond_dim % 8 == 0; video: text_dim % 16 == 0 and
+ * max_text_tokens >= 1; eps > 0.  DLO_W_E4M3 requires DLO_BLOCK_VIDEO
+ * (else DLO_EUNSUPPORTED). */
+typedef struct dlo_desc {
+    int abi_version;
+    int block_kind;      /* DLO_BLOCK_*                                          */
+    int wdtype;          /* DLO_W_*                                              */
+    int n_blocks;        /* blocks in the stack                                  */
+    int hidden;          /* D                                                    */
+    int heads;           /* H                                                    */
+    int head_dim;        /* hd = D / H                                           */
+    int ffn;             /* F, MLP width                                         */
+    int cond_dim;        /* DiT: width of the conditioning vector c              */
+    int text_dim;        /* video: width Dt of the text context                  */
+    int max_batch;       /* largest B passed to dlo_forward                      */
+    int max_tokens;      /* largest N                                            */
+    int max_text_tokens; /* video: largest L                                     */
+    float eps;           /* LayerNorm / RMSNorm epsilon                          */
+    int staging;         /* DLO_STAGE_*                                          */
+    /* [DLO] "Registered runtime-cache transfer": the complete registration byte
+     * count is checked against this budget before any registration; 0 = none. */
+    unsigned long long register_budget_bytes;
+} dlo_desc;
+
+typedef struct dlo_tensor_info {
+    char name[40];              /* e.g. "attn.qkv.weight"                       */
+    unsigned long long offset;  /* byte offset in the flat block, 256-B aligned
+                                   for the first tensor of each group            */
+    unsigned long long bytes;
+    int dtype;                  /* DLO_DT_*                                     */
+    int ndim;                   /* 1 or 2                                       */
+    long long shape[2];         /* [out, in] for linear weights                 */
+    int source;                 /* 1: supplied by the caller to dlo_pack_block;
+                                   0: derived by dlo_pack_block (FP8 scales)    */
+} dlo_tensor_info;
+
+typedef struct dlo_ctx dlo_ctx;
+
+/* ---------------------------------------------------------------- layout */
+
+/* Bytes of one flattened block (K0 layout table), identical for all blocks.
+ * [LW] How It Works: block parameters are kept as flattened tensors in pinned
+ * host memory and re-materialised from them.  Returns 0 for an invalid desc. */
+size_t dlo_block_bytes(const dlo_desc* desc);
+
+/* Layout table of one flat block, in storage order.  out may be NULL to query
+ * the count.  cap = entries available in out.  DLO_EINVAL on a bad desc,
+ * DLO_ENOMEM when cap is too small (count is still set). */
+dlo_status dlo_block_layout(const dlo_desc* desc, dlo_tensor_info* out, int cap, int* count);
+
+/* Device workspace bytes dlo_create needs for this desc (activations of
+ * max_batch x max_tokens, scratch for the block kernels, the kernels' error
+ * word).  Returns 0 for an invalid desc. */
+size_t dlo_workspace_bytes(const dlo_desc* desc);
+
+/* Fill one flat host block from fp32 source tensors.
+ * tensors[i] points at the fp32 values of layout entry i (row-major, the
+ * entry's shape) for every entry with source == 1, and is ignored (may be
+ * NULL) for derived entries.  bf16 entries are rounded to nearest even; with
+ * DLO_W_E4M3 each linear weight is quantised per tensor (dlo_quantize_e4m3)
+ * and its scale written into the "linear_scales" entry.  flat must hold
+ * dlo_block_bytes(desc) bytes; padding bytes are zeroed.  Host only. */
+dlo_status dlo_pack_block(const dlo_desc* desc, const float* const* tensors, int n_tensors,
+                          void* flat, size_t flat_bytes);
+
+/* Per-tensor FP8 quantiser ([DLO] Feature compatibility, row "Per-tensor online
+ * FP8 linears"): s = amax|w| / 448 in fp32 (1 when amax == 0); codes[i] =
+ * E4M3(w[i] / s) with w[i] / s in fp32, round to nearest even, saturating at
+ * +-448 (OCP 8-bit floating point, E4M3).  Host only; n may be 0. */
+dlo_status dlo_quantize_e4m3(const float* w, size_t n, uint8_t* codes, float* scale);
+
+/* ---------------------------------------------------------------- lifecycle */
+
+/* Create a context ([OFF] Shared lifecycle "enable"; [DLO] Startup and runtime
+ * sequence "allocate device slots").
+ *  device:        CUDA ordinal; made current by every call on the context.
+ *  slot0, slot1:  device buffers of slot_bytes >= dlo_block_bytes(desc) each,
+ *                 256-B aligned, not overlapping (the two device slots).
+ *  workspace:     device buffer of ws_bytes >= dlo_workspace_bytes(desc),
+ *                 256-B aligned, owned by the context until destroy.
+ *  compute_stream, copy_stream: distinct caller streams; blocks compute on the
+ *                 first, slot copies run on the second ([LW] copy_stream).
+ * On error *out is NULL and nothing is retained. */
+dlo_status dlo_create(const dlo_desc* desc, int device, void* slot0, void* slot1,
+                      size_t slot_bytes, void* workspace, size_t ws_bytes,
+                      void* compute_stream, void* copy_stream, dlo_ctx** out);
+
+/* Attach the n = desc->n_blocks flat host blocks (host_blocks[i], block_bytes
+ * = dlo_block_bytes(desc) each; immutable while attached: [OFF] "a parameter
+ * has one authoritative host representation").
+ *  DLO_HOST_PINNED:   memory is already page-locked (cudaHostAlloc or
+ *                     registered); verified with cudaPointerGetAttributes.
+ *  DLO_HOST_REGISTER: the library page-aligns the block ranges, merges
+ *                     overlapping or adjacent ones, checks the total against
+ *                     register_budget_bytes before any mutation, then
+ *                     registers each range (read-only where the platform
+ *                     supports it) and verifies every block reads as pinned
+ *                     ([DLO] Registered runtime-cache transfer).  Any failure
+ *                     unregisters the ranges already registered and returns
+ *                     DLO_EREGISTER with the context unchanged, so the call can
+ *                     be retried ([DLO] Failure and lifecycle boundaries).
+ * Exactly one of the two flags.  With DLO_STAGE_GATHER the blocks must be
+ * device-accessible (mapped); checked here.  Allowed once, before forward. */
+dlo_status dlo_register_host_blocks(dlo_ctx* ctx, int n, const void* const* host_blocks,
+                                    size_t block_bytes, unsigned flags);
+
+/* Keep blocks 0..k-1 resident ([DLO] Feature compatibility, row "Resident
+ * leading layers").  device_blocks[i] (i < k) are caller device buffers of
+ * block_bytes, 256-B aligned; the library copies host block i into each on
+ * the copy stream.  Then the first streamed block k is staged into slot 0
+ * (priming, [DLO] Startup and runtime sequence).  0 <= k <= n.  Allowed once,
+ * after registration and before the first forward; without it the first
+ * forward primes block 0 itself (k = 0). */
+dlo_status dlo_set_resident(dlo_ctx* ctx, int k, void* const* device_blocks);
+
+/* One forward of the block stack (one denoising step), enqueued on the compute
+ * stream; returns after enqueue ([LW] Execution Flow; [DLO] "each streamed
+ * block during pipeline.forward").
+ *  x_in, x_out:  device bf16 [batch, tokens, hidden]; x_out may equal x_in.
+ *  cond:         DiT: device bf16 c [batch, cond_dim];
+ *                video: device fp32 e [batch, 6, hidden].
+ *  ctx_tokens:   video: device bf16 text context [batch, text_tokens,
+ *                text_dim]; DiT: NULL.
+ * 1 <= batch <= max_batch, 1 <= tokens <= max_tokens, video: 1 <= text_tokens
+ * <= max_text_tokens.
+ * Per streamed execution j (over all forwards) of block i: the copy stream
+ * waits until the compute that last read slot (j+1)%2 is done, stages block
+ * i+1 (or the first streamed block after the last) into it and records
+ * copy_done; the compute stream waits on copy_done of slot j%2, runs block i
+ * from that slot and records compute_done.
+ * DiT block (eps = desc->eps; LN has no affine and biased variance):
+ *   m = SiLU(c) W_ada^T + b_ada -> shift1, scale1, gate1, shift2, scale2, gate2
+ *   x += gate1 * (Attn(LN(x)(1+scale1)+shift1) W_o^T + b_o)
+ *   x += gate2 * (GELU_tanh((LN(x)(1+scale2)+shift2) W_1^T + b_1) W_2^T + b_2)
+ *   Attn: qkv = h W_qkv^T + b_qkv, q|k|v each [H, hd] per token,
+ *         softmax(q k^T / sqrt(hd)) v per head, non-causal.
+ * Video block: m = e + T_mod; self-attention as above with separate q,k,v
+ *   linears and RMSNorm (gain, over hidden) on q and k, x += gate1 * o;
+ *   cross-attention with q = RMSNorm(LN_affine(x) W_q^T + b_q), k = RMSNorm(
+ *   ctx W_k^T + b_k), v = ctx W_v^T + b_v, x += o; FFN as DiT with gate2.
+ * The hidden state is carried in fp32 between kernels; x_out is its bf16
+ * rounding.  Device-side bounded waits that run out are reported by the next
+ * dlo_wait / dlo_forward_host / dlo_get_stats as DLO_ETIMEDOUT. */
+dlo_status dlo_forward(dlo_ctx* ctx, const void* x_in, const void* cond, const void* ctx_tokens,
+                       int batch, int tokens, int text_tokens, void* x_out);
+
+/* dlo_forward with HOST inputs and output: copies x_in, cond and ctx_tokens
+ * (same layouts as dlo_forward) into the workspace on the compute stream,
+ * runs the stack, copies the bf16 result back into x_out and waits for it
+ * (bounded by timeout_ms; <= 0 means 60000).  Pinned host buffers give
+ * asynchronous copies; pageable ones work too. */
+dlo_status dlo_forward_host(dlo_ctx* ctx, const void* x_in, const void* cond,
+                            const void* ctx_tokens, int batch, int tokens, int text_tokens,
+                            void* x_out, int timeout_ms);
+
+/* Host wait for all work of the context on both streams, polling with a time
+ * limit; DLO_ETIMEDOUT when it runs out or when a kernel reported a timed-out
+ * device wait.  timeout_ms <= 0 means 60000. */
+dlo_status dlo_wait(dlo_ctx* ctx, int timeout_ms);
+
+/* Tear down ([DLO] Failure and lifecycle boundaries, shutdown order):
+ * synchronise both streams, unregister the ranges this library registered,
+ * destroy events, free the context.  NULL is accepted.  Returns the first
+ * error met but always frees the context. */
+dlo_status dlo_destroy(dlo_ctx* ctx);
+
+/* Message of the last error on ctx, or of the last failed dlo_create in this
+ * thread when ctx is NULL.  Never NULL. */
+const char* dlo_last_error(const dlo_ctx* ctx);
+
+/* ---------------------------------------------------------------- introspection */
+
+typedef struct dlo_stats {
+    unsigned long long forwards;         /* dlo_forward calls completed enqueue  */
+    unsigned long long stagings;         /* block copies into slots (incl. prime) */
+    unsigned long long staged_bytes;
+    unsigned long long streamed_execs;   /* streamed block executions            */
+    unsigned long long kernel_launches;  /* kernels this library launched        */
+    int resident;                        /* k                                    */
+    int slot_block[2];                   /* block last staged into each slot, -1 */
+    int registered_ranges;               /* host ranges this library registered  */
+    int registered_read_only;            /* 1 if they were registered read-only  */
+    int device_error;                    /* kernels' error word (0 = none)       */
+    /* With dlo_set_timing(ctx, 1): sums over timed streamed executions, in ms. */
+    int timed_execs;
+    double copy_ms;                      /* slot copy durations                  */
+    double compute_ms;                   /* block compute durations              */
+    double exposed_wait_ms;              /* compute stream idle waiting on copies */
+} dlo_stats;
+
+/* Counters and timing.  Timing sums need the timed work finished (call
+ * dlo_wait first); they are read from CUDA events. */
+dlo_status dlo_get_stats(dlo_ctx* ctx, dlo_stats* out);
+
+/* Ordered log of enqueued staging and execution events since create or the
+ * last dlo_reset_log: kind[i] 0 = stage, 1 = execute; block[i]; slot[i] (-1
+ * for a resident execution).  Up to cap entries are written; *count gets the
+ * total logged (the log keeps the first 65536). */
+dlo_status dlo_get_log(dlo_ctx* ctx, int* kind, int* block, int* slot, int cap, int* count);
+dlo_status dlo_reset_log(dlo_ctx* ctx);
+
+/* Per-execution CUDA-event timing on (1) or off (0, default); it records four
+ * events per streamed execution. */
+dlo_status dlo_set_timing(dlo_ctx* ctx, int on);
+
+/* Debug: wait for the copy that last wrote `slot`, copy the slot back and
+ * compare it byte for byte with host block `block` (-1: the block the library
+ * staged there last).  DLO_OK if identical, DLO_EMISMATCH if not.  Blocks the
+ * host (bounded, 60 s). */
+dlo_status dlo_verify_slot(dlo_ctx* ctx, int slot, int block);
+
+/* Test hook (process-wide): make the nth cudaHostRegister call issued by
+ * dlo_register_host_blocks from now on report failure (n >= 1), or disable
+ * with n <= 0.  Exercises the rollback path without a platform fault. */
+void dlo_debug_fail_register(int nth);
+
+/* ---------------------------------------------------------------- unit ops
+ * The kernels one block is made of, callable on their own (device pointers,
+ * enqueued on `stream`).  They check arguments and return DLO_EINVAL before
+ * launching.  `err` is a device int (0 on entry) that a kernel sets when one
+ * of its bounded waits runs out; it may be NULL for kernels without waits. */
+
+/* GEMM epilogues */
+#define DLO_EPI_BIAS      0  /* out bf16 [M, ldo] = acc*s + bias                 */
+#define DLO_EPI_GELU      1  /* out bf16 = GELU_tanh(acc*s + bias)               */
+#define DLO_EPI_RESIDUAL  2  /* out fp32 [M, ldo] += gate * (acc*s + bias)       */
+
+/* Y = A W^T on the tensor cores (tcgen05, TMA), fp32 accumulate, fused
+ * epilogue.  A: bf16 [M, K] row-major (lda = K).  W: [N, K] row-major, bf16
+ * or e4m3 (w_dtype DLO_DT_*).  scales: NULL (s = 1) or fp32 per column
+ * segment, s = scales[col / scale_seg] (e4m3 per-tensor scales of the
+ * concatenated tensors).  bias: bf16 [N] or NULL.  gate (RESIDUAL only): NULL
+ * (1) or fp32 with gate[(row / rows_per_batch) * gate_ld + col].
+ * M >= 1, N % 16 == 0, K % 16 == 0, K >= 16; pointers 16-B aligned, ldo % 8 == 0. */
+dlo_status dlo_op_gemm(const void* A, const void* W, int w_dtype, const float* scales,
+                       int scale_seg, const void* bias, int M, int N, int K, int epilogue,
+                       void* out, int ldo, const float* gate, int gate_ld, int rows_per_batch,
+                       int* err, void* stream);
+
+/* Multi-head softmax attention, non-causal: O = softmax(Q K^T / sqrt(hd)) V per
+ * (batch, head).  Q, K, V, O bf16; row r of batch b of Q starts at
+ * Q + (b * nq + r) * ldq, head h at column h * head_dim (same for K, V with nk
+ * and ldk / ldv, O with nq and ldo).  head_dim % 8 == 0, <= 128; ld* % 8 == 0. */
+dlo_status dlo_op_attention(const void* Q, const void* K, const void* V, void* O, int batch,
+                            int heads, int head_dim, int nq, int nk, int ldq, int ldk, int ldv,
+                            int ldo, void* stream);
+
+/* out bf16 [rows, D] = LN(x) * (1 + scale) + shift   (shift/scale non-NULL), or
+ *                    = LN(x) * w + b                  (w/b non-NULL), or LN(x).
+ * x fp32 [rows, D]; shift/scale fp32 indexed [(row / rows_per_batch) * mod_ld + d];
+ * w, b bf16 [D]. */
+dlo_status dlo_op_layernorm(const float* x, int rows, int D, int rows_per_batch,
+                            const float* shift, const float* scale, int mod_ld,
+                            const void* w, const void* b, float eps, void* out, void* stream);
+
+/* In place on bf16 x: row r, columns col0 .. col0+D-1 of a row stride ld:
+ * x = x / sqrt(mean(x^2) + eps) * w, w bf16 [D]. */
+dlo_status dlo_op_rmsnorm(void* x, int rows, int D, int ld, int col0, const void* w, float eps,
+                          void* stream);
+
+/* m fp32 [B, N] = SiLU(c) W^T + bias; c bf16 [B, C], W bf16 [N, C], bias bf16 [N]. */
+dlo_status dlo_op_adaln(const void* c, int B, int C, const void* W, const void* bias, int N,
+                        float* m, void* stream);
+
+/* Copy `bytes` (% 16 == 0, both pointers 16-B aligned) from device-accessible
+ * src (device memory or mapped host memory) to device dst with the gather
+ * kernel (mode DLO_STAGE_GATHER) or cudaMemcpyAsync (DLO_STAGE_MEMCPY). */
+dlo_status dlo_op_stage(void* dst, const void* src, size_t bytes, int mode, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DLO_H */

@@ -1,0 +1,830 @@
+// Host runtime of the layerwise offload: context lifecycle, host block
+// registration with all-or-nothing rollback, resident leading blocks,
+// priming, the event-ordered two-slot circular prefetch, block orchestration,
+// timing/overlap accounting and the C ABI.
+//
+// Sources: "CPU Offloading for Diffusion Models", Layerwise (Blockwise)
+// Offloading (How It Works, Execution Flow table); "Distributed Layerwise
+// Offload" (Startup and runtime sequence, Host backing and transfer
+// composition, Failure and lifecycle boundaries, Registered runtime-cache
+// transfer); "CPU Offloading" (Shared lifecycle, Cross-strategy invariants).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <chrono>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <memory>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "internal.h"
+
+using namespace dlo;
+
+namespace {
+
+thread_local std::string g_create_error;
+std::atomic<int> g_fail_register_nth{0};
+
+enum State { kCreated = 0, kRegistered = 1, kBroken = 9 };
+
+struct TimedExec {
+    cudaEvent_t copy0, copy1, wait0, comp0, comp1;
+};
+
+struct Offsets {
+    // DiT
+    size_t ada_w, ada_b, qkv_w, qkv_b, proj_w, proj_b, fc1_w, fc1_b, fc2_w, fc2_b;
+    // video
+    size_t mod, sq_w, sq_b, so_w, so_b, snq, snk, ncw, ncb, cq_w, cq_b, ck_w, ck_b, co_w, co_b, cnq,
+        cnk, scales;
+    bool has_scales;
+};
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+struct dlo_ctx {
+    dlo_desc d{};
+    int device = 0;
+    std::vector<Entry> L;
+    size_t block_bytes = 0;
+    Workspace ws;
+    Offsets off{};
+    uint8_t* slot[2] = {nullptr, nullptr};
+    size_t slot_bytes = 0;
+    uint8_t* wsp = nullptr;
+    cudaStream_t cs = nullptr;   // compute
+    cudaStream_t xs = nullptr;   // copy
+    cudaEvent_t copy_done[2] = {nullptr, nullptr};
+    cudaEvent_t compute_done[2] = {nullptr, nullptr};
+    cudaEvent_t resident_ev = nullptr;
+    bool resident_pending = false;
+    int state = kCreated;
+    bool resident_set = false;
+    bool primed = false;
+    int k = 0;
+    std::vector<const uint8_t*> host;
+    std::vector<const uint8_t*> host_dev;
+    std::vector<std::pair<void*, size_t>> reg_ranges;
+    bool reg_read_only = false;
+    std::vector<uint8_t*> resident;
+    unsigned long long exec_counter = 0;
+    int slot_block[2] = {-1, -1};
+    dlo_stats st{};
+    std::vector<int> log_kind, log_block, log_slot;
+    size_t log_total = 0;
+    bool timing = false;
+    std::vector<TimedExec> timed_pending;
+    std::vector<cudaEvent_t> ev_pool;
+    std::string err;
+
+    dlo_status fail(dlo_status s, const char* fmt, ...) {
+        char buf[512];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof(buf), fmt, ap);
+        va_end(ap);
+        err = buf;
+        return s;
+    }
+    dlo_status cuda_fail(cudaError_t e, const char* what) {
+        return fail(DLO_ECUDA, "%s: %s (%d)", what, cudaGetErrorString(e), static_cast<int>(e));
+    }
+    void log(int kind, int block, int slot_) {
+        ++log_total;
+        if (log_kind.size() < 65536) {
+            log_kind.push_back(kind);
+            log_block.push_back(block);
+            log_slot.push_back(slot_);
+        }
+    }
+    int* err_word() { return reinterpret_cast<int*>(wsp + ws.err); }
+    cudaEvent_t get_event() {
+        if (!ev_pool.empty()) {
+            cudaEvent_t e = ev_pool.back();
+            ev_pool.pop_back();
+            return e;
+        }
+        cudaEvent_t e = nullptr;
+        cudaEventCreate(&e);
+        return e;
+    }
+};
+
+namespace {
+
+size_t off_of(const std::vector<Entry>& L, const char* n) {
+    const int i = find_entry(L, n);
+    return i < 0 ? 0 : L[i].offset;
+}
+
+void fill_offsets(dlo_ctx* c) {
+    const auto& L = c->L;
+    Offsets& o = c->off;
+    if (c->d.block_kind == DLO_BLOCK_DIT) {
+        o.ada_w = off_of(L, "adaLN.weight");
+        o.ada_b = off_of(L, "adaLN.bias");
+        o.qkv_w = off_of(L, "attn.qkv.weight");
+        o.qkv_b = off_of(L, "attn.qkv.bias");
+        o.proj_w = off_of(L, "attn.proj.weight");
+        o.proj_b = off_of(L, "attn.proj.bias");
+        o.fc1_w = off_of(L, "mlp.fc1.weight");
+        o.fc1_b = off_of(L, "mlp.fc1.bias");
+        o.fc2_w = off_of(L, "mlp.fc2.weight");
+        o.fc2_b = off_of(L, "mlp.fc2.bias");
+        o.has_scales = false;
+    } else {
+        o.mod = off_of(L, "modulation");
+        o.sq_w = off_of(L, "self_attn.q.weight");
+        o.sq_b = off_of(L, "self_attn.q.bias");
+        o.so_w = off_of(L, "self_attn.o.weight");
+        o.so_b = off_of(L, "self_attn.o.bias");
+        o.snq = off_of(L, "self_attn.norm_q.weight");
+        o.snk = off_of(L, "self_attn.norm_k.weight");
+        o.ncw = off_of(L, "norm_cross.weight");
+        o.ncb = off_of(L, "norm_cross.bias");
+        o.cq_w = off_of(L, "cross_attn.q.weight");
+        o.cq_b = off_of(L, "cross_attn.q.bias");
+        o.ck_w = off_of(L, "cross_attn.k.weight");
+        o.ck_b = off_of(L, "cross_attn.k.bias");
+        o.co_w = off_of(L, "cross_attn.o.weight");
+        o.co_b = off_of(L, "cross_attn.o.bias");
+        o.cnq = off_of(L, "cross_attn.norm_q.weight");
+        o.cnk = off_of(L, "cross_attn.norm_k.weight");
+        o.fc1_w = off_of(L, "ffn.fc1.weight");
+        o.fc1_b = off_of(L, "ffn.fc1.bias");
+        o.fc2_w = off_of(L, "ffn.fc2.weight");
+        o.fc2_b = off_of(L, "ffn.fc2.bias");
+        o.has_scales = find_entry(L, "linear_scales") >= 0;
+        o.scales = off_of(L, "linear_scales");
+    }
+}
+
+// Poll a stream until idle or the limit runs out.
+bool stream_wait(cudaStream_t s, int timeout_ms, cudaError_t* e) {
+    const auto t0 = std::chrono::steady_clock::now();
+    int spins = 0;
+    for (;;) {
+        cudaError_t q = cudaStreamQuery(s);
+        if (q == cudaSuccess) return true;
+        if (q != cudaErrorNotReady) {
+            *e = q;
+            return false;
+        }
+        const auto el = std::chrono::steady_clock::now() - t0;
+        if (std::chrono::duration_cast<std::chrono::milliseconds>(el).count() > timeout_ms) {
+            *e = cudaErrorNotReady;
+            return false;
+        }
+        if (++spins > 64) std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+}
+
+// Copy host block `blk` into slot `s` on the copy stream.
+dlo_status stage(dlo_ctx* c, int blk, int s) {
+    cudaError_t e;
+    if (c->d.staging == DLO_STAGE_GATHER) {
+        e = launch_gather(c->slot[s], c->host_dev[blk], c->block_bytes, c->xs, &c->st.kernel_launches);
+    } else {
+        e = cudaMemcpyAsync(c->slot[s], c->host[blk], c->block_bytes, cudaMemcpyHostToDevice, c->xs);
+    }
+    if (e != cudaSuccess) return c->cuda_fail(e, "slot staging");
+    c->slot_block[s] = blk;
+    ++c->st.stagings;
+    c->st.staged_bytes += c->block_bytes;
+    c->log(0, blk, s);
+    return DLO_OK;
+}
+
+dlo_status prime(dlo_ctx* c) {
+    if (c->primed) return DLO_OK;
+    if (c->k < c->d.n_blocks) {
+        dlo_status r = stage(c, c->k, 0);
+        if (r != DLO_OK) return r;
+        cudaError_t e = cudaEventRecord(c->copy_done[0], c->xs);
+        if (e != cudaSuccess) return c->cuda_fail(e, "event record");
+    }
+    c->primed = true;
+    return DLO_OK;
+}
+
+#define LCHECK(expr, what)                                   \
+    do {                                                     \
+        cudaError_t e_ = (expr);                             \
+        if (e_ != cudaSuccess) return c->cuda_fail(e_, what); \
+    } while (0)
+
+// One block from weights at `W` (a slot or a resident buffer).
+dlo_status run_block(dlo_ctx* c, const uint8_t* W, int B, int N, int L, const void* cond,
+                     const void* ctx_tokens) {
+    const dlo_desc& d = c->d;
+    const Offsets& o = c->off;
+    const int D = d.hidden, F = d.ffn, H = d.heads, hd = d.head_dim;
+    const int BN = B * N;
+    uint8_t* w = c->wsp;
+    float* x = reinterpret_cast<float*>(w + c->ws.x);
+    void* h = w + c->ws.h;
+    void* big = w + c->ws.big;
+    void* a = w + c->ws.a;
+    float* m = reinterpret_cast<float*>(w + c->ws.mod);
+    unsigned long long* nl = &c->st.kernel_launches;
+    cudaStream_t s = c->cs;
+    const int D6 = 6 * D;
+    auto gemm = [&](const void* A, size_t woff, size_t boff, int M, int Nn, int K, int epi,
+                    void* out, int ldo, const float* gate, int rpb, int scale_idx, int seg) {
+        GemmParams p;
+        p.A = A;
+        p.W = W + woff;
+        p.w_dtype = d.wdtype == DLO_W_E4M3 ? DLO_DT_E4M3 : DLO_DT_BF16;
+        p.scales = o.has_scales ? reinterpret_cast<const float*>(W + o.scales) + scale_idx : nullptr;
+        p.scale_seg = seg;
+        p.bias = W + boff;
+        p.M = M;
+        p.N = Nn;
+        p.K = K;
+        p.epi = epi;
+        p.out = out;
+        p.ldo = ldo;
+        p.gate = gate;
+        p.gate_ld = D6;
+        p.rows_per_batch = rpb;
+        p.err = c->err_word();
+        return launch_gemm(p, s, nl);
+    };
+    if (d.block_kind == DLO_BLOCK_DIT) {
+        LCHECK(launch_adaln(cond, B, d.cond_dim, W + o.ada_w, W + o.ada_b, D6, m, s, nl), "adaLN");
+        LCHECK(launch_layernorm(x, BN, D, N, m, m + D, D6, nullptr, nullptr, d.eps, h, s, nl), "LN1");
+        LCHECK(gemm(h, o.qkv_w, o.qkv_b, BN, 3 * D, D, DLO_EPI_BIAS, big, 3 * D, nullptr, N, 0, 3 * D), "qkv");
+        LCHECK(launch_attention(big, static_cast<uint8_t*>(big) + 2 * D, static_cast<uint8_t*>(big) + 4 * D, a, B,
+                                H, hd, N, N, 3 * D, 3 * D, 3 * D, D, s, nl),
+               "attention");
+        LCHECK(gemm(a, o.proj_w, o.proj_b, BN, D, D, DLO_EPI_RESIDUAL, x, D, m + 2 * D, N, 0, D), "proj");
+        LCHECK(launch_layernorm(x, BN, D, N, m + 3 * D, m + 4 * D, D6, nullptr, nullptr, d.eps, h, s, nl), "LN2");
+        LCHECK(gemm(h, o.fc1_w, o.fc1_b, BN, F, D, DLO_EPI_GELU, big, F, nullptr, N, 0, F), "fc1");
+        LCHECK(gemm(big, o.fc2_w, o.fc2_b, BN, D, F, DLO_EPI_RESIDUAL, x, D, m + 5 * D, N, 0, D), "fc2");
+        return DLO_OK;
+    }
+    void* q2 = w + c->ws.q2;
+    void* kv2 = w + c->ws.kv2;
+    const int Dt = d.text_dim;
+    LCHECK(launch_mod_add(static_cast<const float*>(cond), W + o.mod, B, D6, m, s, nl), "modulation");
+    LCHECK(launch_layernorm(x, BN, D, N, m, m + D, D6, nullptr, nullptr, d.eps, h, s, nl), "LN1");
+    LCHECK(gemm(h, o.sq_w, o.sq_b, BN, 3 * D, D, DLO_EPI_BIAS, big, 3 * D, nullptr, N, 0, D), "self qkv");
+    LCHECK(launch_rmsnorm2(big, BN, D, 3 * D, 0, W + o.snq, D, W + o.snk, d.eps, s, nl), "self q/k norm");
+    LCHECK(launch_attention(big, static_cast<uint8_t*>(big) + 2 * D, static_cast<uint8_t*>(big) + 4 * D, a, B, H,
+                            hd, N, N, 3 * D, 3 * D, 3 * D, D, s, nl),
+           "self attention");
+    LCHECK(gemm(a, o.so_w, o.so_b, BN, D, D, DLO_EPI_RESIDUAL, x, D, m + 2 * D, N, 3, D), "self o");
+    LCHECK(launch_layernorm(x, BN, D, N, nullptr, nullptr, 0, W + o.ncw, W + o.ncb, d.eps, h, s, nl), "LN cross");
+    LCHECK(gemm(h, o.cq_w, o.cq_b, BN, D, D, DLO_EPI_BIAS, q2, D, nullptr, N, 4, D), "cross q");
+    LCHECK(gemm(ctx_tokens, o.ck_w, o.ck_b, B * L, 2 * D, Dt, DLO_EPI_BIAS, kv2, 2 * D, nullptr, L, 5, D),
+           "cross kv");
+    LCHECK(launch_rmsnorm(q2, BN, D, D, 0, W + o.cnq, d.eps, s, nl), "cross q norm");
+    LCHECK(launch_rmsnorm(kv2, B * L, D, 2 * D, 0, W + o.cnk, d.eps, s, nl), "cross k norm");
+    LCHECK(launch_attention(q2, kv2, static_cast<uint8_t*>(kv2) + 2 * D, a, B, H, hd, N, L, D, 2 * D, 2 * D, D,
+                            s, nl),
+           "cross attention");
+    LCHECK(gemm(a, o.co_w, o.co_b, BN, D, D, DLO_EPI_RESIDUAL, x, D, nullptr, N, 7, D), "cross o");
+    LCHECK(launch_layernorm(x, BN, D, N, m + 3 * D, m + 4 * D, D6, nullptr, nullptr, d.eps, h, s, nl), "LN2");
+    LCHECK(gemm(h, o.fc1_w, o.fc1_b, BN, F, D, DLO_EPI_GELU, big, F, nullptr, N, 8, F), "fc1");
+    LCHECK(gemm(big, o.fc2_w, o.fc2_b, BN, D, F, DLO_EPI_RESIDUAL, x, D, m + 5 * D, N, 9, D), "fc2");
+    return DLO_OK;
+}
+
+void collect_timing(dlo_ctx* c) {
+    std::vector<TimedExec> keep;
+    for (auto& t : c->timed_pending) {
+        float cp = 0, cm = 0, wt = 0;
+        if (cudaEventElapsedTime(&cp, t.copy0, t.copy1) != cudaSuccess ||
+            cudaEventElapsedTime(&cm, t.comp0, t.comp1) != cudaSuccess ||
+            cudaEventElapsedTime(&wt, t.wait0, t.comp0) != cudaSuccess) {
+            cudaGetLastError();
+            keep.push_back(t);
+            continue;
+        }
+        c->st.copy_ms += cp;
+        c->st.compute_ms += cm;
+        c->st.exposed_wait_ms += wt;
+        ++c->st.timed_execs;
+        for (cudaEvent_t e : {t.copy0, t.copy1, t.wait0, t.comp0, t.comp1}) c->ev_pool.push_back(e);
+    }
+    c->timed_pending.swap(keep);
+}
+
+dlo_status check_device_error(dlo_ctx* c) {
+    int v = 0;
+    cudaError_t e = cudaMemcpy(&v, c->err_word(), sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return c->cuda_fail(e, "reading the kernels' error word");
+    c->st.device_error = v;
+    if (v) {
+        cudaMemset(c->err_word(), 0, sizeof(int));
+        return c->fail(DLO_ETIMEDOUT, "a kernel's bounded wait ran out (error word %d)", v);
+    }
+    return DLO_OK;
+}
+
+}  // namespace
+
+// ===================================================================== C ABI
+
+extern "C" const char* dlo_last_error(const dlo_ctx* ctx) {
+    if (!ctx) return g_create_error.c_str();
+    return ctx->err.c_str();
+}
+
+extern "C" void dlo_debug_fail_register(int nth) { g_fail_register_nth.store(nth > 0 ? nth : 0); }
+
+extern "C" dlo_status dlo_create(const dlo_desc* desc, int device, void* slot0, void* slot1,
+                                 size_t slot_bytes, void* workspace, size_t ws_bytes,
+                                 void* compute_stream, void* copy_stream, dlo_ctx** out) {
+    if (out) *out = nullptr;
+    std::string msg;
+    dlo_status st = validate_desc(desc, &msg);
+    auto cfail = [&](dlo_status s, const std::string& m) {
+        g_create_error = m;
+        return s;
+    };
+    if (!out) return cfail(DLO_EINVAL, "out is NULL");
+    if (st != DLO_OK) return cfail(st, msg);
+    std::vector<Entry> L;
+    const size_t bb = build_layout(*desc, &L);
+    const Workspace ws = plan_workspace(*desc);
+    if (!slot0 || !slot1 || slot0 == slot1) return cfail(DLO_EINVAL, "two distinct slots are required");
+    if (!aligned(slot0, 256) || !aligned(slot1, 256) || !aligned(workspace, 256))
+        return cfail(DLO_EINVAL, "slots and workspace must be 256-byte aligned");
+    if (slot_bytes < bb) return cfail(DLO_ENOMEM, "slot_bytes < block bytes");
+    {
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(slot0), a1 = reinterpret_cast<uintptr_t>(slot1);
+        if ((a0 < a1 && a0 + slot_bytes > a1) || (a1 < a0 && a1 + slot_bytes > a0))
+            return cfail(DLO_EINVAL, "slots overlap");
+    }
+    if (!workspace || ws_bytes < ws.total) return cfail(DLO_ENOMEM, "workspace too small");
+    if (!compute_stream || !copy_stream || compute_stream == copy_stream)
+        return cfail(DLO_EINVAL, "distinct non-NULL compute and copy streams are required");
+    int ndev = 0;
+    cudaError_t e = cudaGetDeviceCount(&ndev);
+    if (e != cudaSuccess) return cfail(DLO_ECUDA, std::string("cudaGetDeviceCount: ") + cudaGetErrorString(e));
+    if (device < 0 || device >= ndev) return cfail(DLO_EINVAL, "bad device ordinal");
+    e = cudaSetDevice(device);
+    if (e != cudaSuccess) return cfail(DLO_ECUDA, std::string("cudaSetDevice: ") + cudaGetErrorString(e));
+
+    std::unique_ptr<dlo_ctx> c(new dlo_ctx());
+    c->d = *desc;
+    c->device = device;
+    c->L = std::move(L);
+    c->block_bytes = bb;
+    c->ws = ws;
+    c->slot[0] = static_cast<uint8_t*>(slot0);
+    c->slot[1] = static_cast<uint8_t*>(slot1);
+    c->slot_bytes = slot_bytes;
+    c->wsp = static_cast<uint8_t*>(workspace);
+    c->cs = static_cast<cudaStream_t>(compute_stream);
+    c->xs = static_cast<cudaStream_t>(copy_stream);
+    fill_offsets(c.get());
+    auto evfail = [&](cudaError_t err) {
+        for (int i = 0; i < 2; ++i) {
+            if (c->copy_done[i]) cudaEventDestroy(c->copy_done[i]);
+            if (c->compute_done[i]) cudaEventDestroy(c->compute_done[i]);
+        }
+        if (c->resident_ev) cudaEventDestroy(c->resident_ev);
+        return cfail(DLO_ECUDA, std::string("event create: ") + cudaGetErrorString(err));
+    };
+    for (int i = 0; i < 2; ++i) {
+        if ((e = cudaEventCreateWithFlags(&c->copy_done[i], cudaEventDisableTiming)) != cudaSuccess) return evfail(e);
+        if ((e = cudaEventCreateWithFlags(&c->compute_done[i], cudaEventDisableTiming)) != cudaSuccess)
+            return evfail(e);
+    }
+    if ((e = cudaEventCreateWithFlags(&c->resident_ev, cudaEventDisableTiming)) != cudaSuccess) return evfail(e);
+    e = cudaMemsetAsync(c->err_word(), 0, 64 * sizeof(int), c->cs);
+    if (e != cudaSuccess) return evfail(e);
+    gemm_num_sms();
+    c->st.slot_block[0] = c->st.slot_block[1] = -1;
+    *out = c.release();
+    return DLO_OK;
+}
+
+extern "C" dlo_status dlo_register_host_blocks(dlo_ctx* c, int n, const void* const* host_blocks,
+                                               size_t block_bytes, unsigned flags) {
+    if (!c) return DLO_EINVAL;
+    if (c->state != kCreated) return c->fail(DLO_ESTATE, "host blocks are already attached");
+    if (n != c->d.n_blocks) return c->fail(DLO_EINVAL, "n (%d) != n_blocks (%d)", n, c->d.n_blocks);
+    if (!host_blocks) return c->fail(DLO_EINVAL, "host_blocks is NULL");
+    if (block_bytes != c->block_bytes)
+        return c->fail(DLO_EINVAL, "block_bytes %zu != layout bytes %zu", block_bytes, c->block_bytes);
+    const bool pinned = flags == DLO_HOST_PINNED, reg = flags == DLO_HOST_REGISTER;
+    if (!pinned && !reg) return c->fail(DLO_EINVAL, "flags must be DLO_HOST_PINNED or DLO_HOST_REGISTER");
+    for (int i = 0; i < n; ++i) {
+        if (!host_blocks[i]) return c->fail(DLO_EINVAL, "host block %d is NULL", i);
+        if (!aligned(host_blocks[i], 16)) return c->fail(DLO_EINVAL, "host block %d is not 16-byte aligned", i);
+    }
+    cudaSetDevice(c->device);
+    std::vector<std::pair<void*, size_t>> done;
+    bool ro = false;
+    if (reg) {
+        // page-align the block ranges and merge overlapping or adjacent ones
+        const size_t page = 4096;
+        std::vector<std::pair<uintptr_t, uintptr_t>> r;
+        for (int i = 0; i < n; ++i) {
+            const uintptr_t a = reinterpret_cast<uintptr_t>(host_blocks[i]);
+            r.push_back({a / page * page, (a + block_bytes + page - 1) / page * page});
+        }
+        std::sort(r.begin(), r.end());
+        std::vector<std::pair<uintptr_t, uintptr_t>> merged;
+        for (auto& x : r) {
+            if (!merged.empty() && x.first <= merged.back().second)
+                merged.back().second = std::max(merged.back().second, x.second);
+            else
+                merged.push_back(x);
+        }
+        unsigned long long total = 0;
+        for (auto& x : merged) total += x.second - x.first;
+        if (c->d.register_budget_bytes && total > c->d.register_budget_bytes)
+            return c->fail(DLO_EREGISTER, "registration needs %llu bytes, budget is %llu (nothing registered)",
+                           total, c->d.register_budget_bytes);
+        int ro_ok = 0;
+        cudaDeviceGetAttribute(&ro_ok, cudaDevAttrHostRegisterReadOnlySupported, c->device);
+        ro = ro_ok != 0;
+        const unsigned rflags = cudaHostRegisterPortable | cudaHostRegisterMapped | (ro ? cudaHostRegisterReadOnly : 0u);
+        for (auto& x : merged) {
+            void* p = reinterpret_cast<void*>(x.first);
+            const size_t len = x.second - x.first;
+            cudaError_t e;
+            int nth = g_fail_register_nth.load();
+            if (nth > 0 && g_fail_register_nth.fetch_sub(1) == 1) {
+                e = cudaErrorHostMemoryAlreadyRegistered;   // injected failure; no call made
+            } else {
+                e = cudaHostRegister(p, len, rflags);
+            }
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                std::string why = cudaGetErrorString(e);
+                bool rollback_ok = true;
+                for (auto& u : done) {
+                    if (cudaHostUnregister(u.first) != cudaSuccess) {
+                        cudaGetLastError();
+                        rollback_ok = false;
+                        c->reg_ranges.push_back(u);   // still registered: destroy retries
+                    }
+                }
+                if (!rollback_ok) {
+                    c->state = kBroken;
+                    return c->fail(DLO_EREGISTER,
+                                   "cudaHostRegister failed (%s) and the rollback failed; the context "
+                                   "is unusable, destroy it",
+                                   why.c_str());
+                }
+                return c->fail(DLO_EREGISTER, "cudaHostRegister of %zu bytes failed (%s); %zu ranges rolled back",
+                               len, why.c_str(), done.size());
+            }
+            done.push_back({p, len});
+        }
+    }
+    // every block must read as page-locked host memory; record device addresses
+    std::vector<const uint8_t*> hd(n);
+    for (int i = 0; i < n; ++i) {
+        cudaPointerAttributes at{};
+        cudaError_t e = cudaPointerGetAttributes(&at, host_blocks[i]);
+        const uint8_t* last = static_cast<const uint8_t*>(host_blocks[i]) + block_bytes - 1;
+        cudaPointerAttributes at2{};
+        cudaError_t e2 = cudaPointerGetAttributes(&at2, last);
+        if (e != cudaSuccess || e2 != cudaSuccess || at.type != cudaMemoryTypeHost ||
+            at2.type != cudaMemoryTypeHost) {
+            cudaGetLastError();
+            for (auto& u : done) cudaHostUnregister(u.first);
+            cudaGetLastError();
+            return c->fail(reg ? DLO_EREGISTER : DLO_EINVAL, "host block %d is not page-locked host memory", i);
+        }
+        hd[i] = static_cast<const uint8_t*>(at.devicePointer);
+        if (c->d.staging == DLO_STAGE_GATHER && !hd[i]) {
+            for (auto& u : done) cudaHostUnregister(u.first);
+            cudaGetLastError();
+            return c->fail(DLO_EINVAL, "host block %d is not mapped into the device address space", i);
+        }
+    }
+    c->host.assign(reinterpret_cast<const uint8_t* const*>(host_blocks),
+                   reinterpret_cast<const uint8_t* const*>(host_blocks) + n);
+    c->host_dev = hd;
+    c->reg_ranges.insert(c->reg_ranges.end(), done.begin(), done.end());
+    c->reg_read_only = ro && !done.empty();
+    c->state = kRegistered;
+    return DLO_OK;
+}
+
+extern "C" dlo_status dlo_set_resident(dlo_ctx* c, int k, void* const* device_blocks) {
+    if (!c) return DLO_EINVAL;
+    if (c->state != kRegistered) return c->fail(DLO_ESTATE, "register host blocks first");
+    if (c->resident_set || c->primed) return c->fail(DLO_ESTATE, "resident blocks must be set once, before the first forward");
+    if (k < 0 || k > c->d.n_blocks) return c->fail(DLO_EINVAL, "k must be in [0, n_blocks]");
+    if (k > 0 && !device_blocks) return c->fail(DLO_EINVAL, "device_blocks is NULL");
+    for (int i = 0; i < k; ++i)
+        if (!device_blocks[i] || !aligned(device_blocks[i], 256))
+            return c->fail(DLO_EINVAL, "resident buffer %d is NULL or not 256-byte aligned", i);
+    cudaSetDevice(c->device);
+    for (int i = 0; i < k; ++i) {
+        cudaError_t e = cudaMemcpyAsync(device_blocks[i], c->host[i], c->block_bytes, cudaMemcpyHostToDevice, c->xs);
+        if (e != cudaSuccess) return c->cuda_fail(e, "resident copy");
+    }
+    if (k > 0) {
+        cudaError_t e = cudaEventRecord(c->resident_ev, c->xs);
+        if (e != cudaSuccess) return c->cuda_fail(e, "event record");
+        c->resident_pending = true;
+    }
+    c->k = k;
+    c->resident.assign(reinterpret_cast<uint8_t* const*>(device_blocks),
+                       reinterpret_cast<uint8_t* const*>(device_blocks) + k);
+    c->resident_set = true;
+    c->st.resident = k;
+    return prime(c);
+}
+
+extern "C" dlo_status dlo_forward(dlo_ctx* c, const void* x_in, const void* cond,
+                                  const void* ctx_tokens, int batch, int tokens, int text_tokens,
+                                  void* x_out) {
+    if (!c) return DLO_EINVAL;
+    if (c->state != kRegistered) return c->fail(DLO_ESTATE, "register host blocks first");
+    const dlo_desc& d = c->d;
+    if (batch < 1 || batch > d.max_batch) return c->fail(DLO_EINVAL, "batch out of range");
+    if (tokens < 1 || tokens > d.max_tokens) return c->fail(DLO_EINVAL, "tokens out of range");
+    if (!x_in || !x_out || !cond) return c->fail(DLO_EINVAL, "NULL input/output");
+    if (!aligned(x_in, 16) || !aligned(x_out, 16) || !aligned(cond, 16))
+        return c->fail(DLO_EINVAL, "inputs/outputs must be 16-byte aligned");
+    if (d.block_kind == DLO_BLOCK_VIDEO) {
+        if (text_tokens < 1 || text_tokens > d.max_text_tokens) return c->fail(DLO_EINVAL, "text_tokens out of range");
+        if (!ctx_tokens || !aligned(ctx_tokens, 16)) return c->fail(DLO_EINVAL, "ctx_tokens NULL or misaligned");
+    }
+    cudaSetDevice(c->device);
+    dlo_status r = prime(c);
+    if (r != DLO_OK) return r;
+    const int n = d.n_blocks, k = c->k;
+    const size_t nx = static_cast<size_t>(batch) * tokens * d.hidden;
+    float* x = reinterpret_cast<float*>(c->wsp + c->ws.x);
+    LCHECK(launch_bf16_to_f32(x_in, x, nx, c->cs, &c->st.kernel_launches), "input conversion");
+    if (c->resident_pending) {
+        LCHECK(cudaStreamWaitEvent(c->cs, c->resident_ev, 0), "wait resident");
+        c->resident_pending = false;
+    }
+    for (int i = 0; i < k; ++i) {
+        c->log(1, i, -1);
+        r = run_block(c, c->resident[i], batch, tokens, text_tokens, cond, ctx_tokens);
+        if (r != DLO_OK) return r;
+    }
+    for (int i = k; i < n; ++i) {
+        const int s = static_cast<int>(c->exec_counter & 1), t = s ^ 1;
+        const int nb = i < n - 1 ? i + 1 : k;
+        TimedExec te{};
+        if (c->timing) {
+            te.copy0 = c->get_event();
+            te.copy1 = c->get_event();
+            te.wait0 = c->get_event();
+            te.comp0 = c->get_event();
+            te.comp1 = c->get_event();
+        }
+        // prefetch the next block into the other slot once its last reader is done
+        LCHECK(cudaStreamWaitEvent(c->xs, c->compute_done[t], 0), "copy waits compute");
+        if (c->timing) LCHECK(cudaEventRecord(te.copy0, c->xs), "event");
+        r = stage(c, nb, t);
+        if (r != DLO_OK) return r;
+        if (c->timing) LCHECK(cudaEventRecord(te.copy1, c->xs), "event");
+        LCHECK(cudaEventRecord(c->copy_done[t], c->xs), "event record");
+        // compute block i from slot s once its copy landed
+        if (c->timing) LCHECK(cudaEventRecord(te.wait0, c->cs), "event");
+        LCHECK(cudaStreamWaitEvent(c->cs, c->copy_done[s], 0), "compute waits copy");
+        if (c->timing) LCHECK(cudaEventRecord(te.comp0, c->cs), "event");
+        c->log(1, i, s);
+        r = run_block(c, c->slot[s], batch, tokens, text_tokens, cond, ctx_tokens);
+        if (r != DLO_OK) return r;
+        if (c->timing) LCHECK(cudaEventRecord(te.comp1, c->cs), "event");
+        LCHECK(cudaEventRecord(c->compute_done[s], c->cs), "event record");
+        if (c->timing) c->timed_pending.push_back(te);
+        ++c->exec_counter;
+        ++c->st.streamed_execs;
+    }
+    LCHECK(launch_f32_to_bf16(x, x_out, nx, c->cs, &c->st.kernel_launches), "output conversion");
+    ++c->st.forwards;
+    return DLO_OK;
+}
+
+extern "C" dlo_status dlo_wait(dlo_ctx* c, int timeout_ms) {
+    if (!c) return DLO_EINVAL;
+    if (timeout_ms <= 0) timeout_ms = 60000;
+    cudaSetDevice(c->device);
+    cudaError_t e = cudaSuccess;
+    if (!stream_wait(c->cs, timeout_ms, &e) || !stream_wait(c->xs, timeout_ms, &e)) {
+        if (e == cudaErrorNotReady) return c->fail(DLO_ETIMEDOUT, "streams still busy after %d ms", timeout_ms);
+        return c->cuda_fail(e, "stream query");
+    }
+    return check_device_error(c);
+}
+
+extern "C" dlo_status dlo_forward_host(dlo_ctx* c, const void* x_in, const void* cond,
+                                       const void* ctx_tokens, int batch, int tokens,
+                                       int text_tokens, void* x_out, int timeout_ms) {
+    if (!c) return DLO_EINVAL;
+    if (c->state != kRegistered) return c->fail(DLO_ESTATE, "register host blocks first");
+    const dlo_desc& d = c->d;
+    if (batch < 1 || batch > d.max_batch || tokens < 1 || tokens > d.max_tokens)
+        return c->fail(DLO_EINVAL, "batch/tokens out of range");
+    if (!x_in || !x_out || !cond) return c->fail(DLO_EINVAL, "NULL input/output");
+    if (d.block_kind == DLO_BLOCK_VIDEO &&
+        (!ctx_tokens || text_tokens < 1 || text_tokens > d.max_text_tokens))
+        return c->fail(DLO_EINVAL, "ctx_tokens/text_tokens invalid");
+    cudaSetDevice(c->device);
+    const size_t xb = static_cast<size_t>(batch) * tokens * d.hidden * 2;
+    void* dx = c->wsp + c->ws.in_x;
+    void* dc = c->wsp + c->ws.in_cond;
+    void* dt = d.block_kind == DLO_BLOCK_VIDEO ? c->wsp + c->ws.in_ctx : nullptr;
+    const size_t cb = d.block_kind == DLO_BLOCK_DIT ? static_cast<size_t>(batch) * d.cond_dim * 2
+                                                    : static_cast<size_t>(batch) * 6 * d.hidden * 4;
+    LCHECK(cudaMemcpyAsync(dx, x_in, xb, cudaMemcpyHostToDevice, c->cs), "H2D x");
+    LCHECK(cudaMemcpyAsync(dc, cond, cb, cudaMemcpyHostToDevice, c->cs), "H2D cond");
+    if (dt)
+        LCHECK(cudaMemcpyAsync(dt, ctx_tokens, static_cast<size_t>(batch) * text_tokens * d.text_dim * 2,
+                               cudaMemcpyHostToDevice, c->cs),
+               "H2D ctx");
+    dlo_status r = dlo_forward(c, dx, dc, dt, batch, tokens, text_tokens, dx);
+    if (r != DLO_OK) return r;
+    LCHECK(cudaMemcpyAsync(x_out, dx, xb, cudaMemcpyDeviceToHost, c->cs), "D2H x");
+    return dlo_wait(c, timeout_ms);
+}
+
+extern "C" dlo_status dlo_destroy(dlo_ctx* c) {
+    if (!c) return DLO_OK;
+    cudaSetDevice(c->device);
+    dlo_status first = DLO_OK;
+    cudaError_t e = cudaSuccess;
+    const bool idle = stream_wait(c->cs, 60000, &e) && stream_wait(c->xs, 60000, &e);
+    if (!idle) first = DLO_ETIMEDOUT;
+    if (idle) {
+        // unregister only after the device no longer reads the ranges
+        for (auto& u : c->reg_ranges) {
+            if (cudaHostUnregister(u.first) != cudaSuccess) {
+                cudaGetLastError();
+                if (first == DLO_OK) first = DLO_EREGISTER;
+            }
+        }
+    }
+    for (int i = 0; i < 2; ++i) {
+        if (c->copy_done[i]) cudaEventDestroy(c->copy_done[i]);
+        if (c->compute_done[i]) cudaEventDestroy(c->compute_done[i]);
+    }
+    if (c->resident_ev) cudaEventDestroy(c->resident_ev);
+    for (auto& t : c->timed_pending)
+        for (cudaEvent_t ev : {t.copy0, t.copy1, t.wait0, t.comp0, t.comp1}) cudaEventDestroy(ev);
+    for (cudaEvent_t ev : c->ev_pool) cudaEventDestroy(ev);
+    delete c;
+    return first;
+}
+
+extern "C" dlo_status dlo_get_stats(dlo_ctx* c, dlo_stats* out) {
+    if (!c || !out) return DLO_EINVAL;
+    cudaSetDevice(c->device);
+    collect_timing(c);
+    c->st.slot_block[0] = c->slot_block[0];
+    c->st.slot_block[1] = c->slot_block[1];
+    c->st.registered_ranges = static_cast<int>(c->reg_ranges.size());
+    c->st.registered_read_only = c->reg_read_only ? 1 : 0;
+    *out = c->st;
+    return DLO_OK;
+}
+
+extern "C" dlo_status dlo_get_log(dlo_ctx* c, int* kind, int* block, int* slot, int cap, int* count) {
+    if (!c) return DLO_EINVAL;
+    if (count) *count = static_cast<int>(c->log_total);
+    const int n = std::min<int>(cap, static_cast<int>(c->log_kind.size()));
+    for (int i = 0; i < n; ++i) {
+        if (kind) kind[i] = c->log_kind[i];
+        if (block) block[i] = c->log_block[i];
+        if (slot) slot[i] = c->log_slot[i];
+    }
+    return DLO_OK;
+}
+
+extern "C" dlo_status dlo_reset_log(dlo_ctx* c) {
+    if (!c) return DLO_EINVAL;
+    c->log_kind.clear();
+    c->log_block.clear();
+    c->log_slot.clear();
+    c->log_total = 0;
+    return DLO_OK;
+}
+
+extern "C" dlo_status dlo_set_timing(dlo_ctx* c, int on) {
+    if (!c) return DLO_EINVAL;
+    c->timing = on != 0;
+    return DLO_OK;
+}
+
+extern "C" dlo_status dlo_verify_slot(dlo_ctx* c, int slot, int block) {
+    if (!c) return DLO_EINVAL;
+    if (slot < 0 || slot > 1) return c->fail(DLO_EINVAL, "slot must be 0 or 1");
+    if (c->state != kRegistered) return c->fail(DLO_ESTATE, "no host blocks attached");
+    if (block < 0) block = c->slot_block[slot];
+    if (block < 0 || block >= c->d.n_blocks) return c->fail(DLO_EINVAL, "no block staged in slot %d", slot);
+    cudaSetDevice(c->device);
+    cudaError_t e = cudaSuccess;
+    if (!stream_wait(c->xs, 60000, &e)) return c->fail(DLO_ETIMEDOUT, "copy stream busy");
+    std::vector<uint8_t> tmp(c->block_bytes);
+    e = cudaMemcpy(tmp.data(), c->slot[slot], c->block_bytes, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return c->cuda_fail(e, "slot read-back");
+    if (std::memcmp(tmp.data(), c->host[block], c->block_bytes) != 0)
+        return c->fail(DLO_EMISMATCH, "slot %d differs from host block %d", slot, block);
+    return DLO_OK;
+}
+
+// ===================================================================== unit ops
+
+namespace {
+unsigned long long g_op_launches = 0;
+thread_local std::string g_op_error;
+dlo_status op_result(cudaError_t e) {
+    if (e == cudaSuccess) return DLO_OK;
+    g_create_error = std::string("kernel launch: ") + cudaGetErrorString(e);
+    cudaGetLastError();
+    return DLO_ECUDA;
+}
+dlo_status op_inval(const char* m) {
+    g_create_error = m;
+    return DLO_EINVAL;
+}
+}  // namespace
+
+extern "C" dlo_status dlo_op_gemm(const void* A, const void* W, int w_dtype, const float* scales,
+                                  int scale_seg, const void* bias, int M, int N, int K, int epilogue,
+                                  void* out, int ldo, const float* gate, int gate_ld,
+                                  int rows_per_batch, int* err, void* stream) {
+    if (!A || !W || !out) return op_inval("NULL operand");
+    if (M < 1 || N < 16 || N % 16 || K < 16 || K % 16) return op_inval("need M >= 1, N % 16 == 0, K % 16 == 0");
+    if (!aligned(A, 16) || !aligned(W, 16) || !aligned(out, 16) || ldo % 8 || ldo < N)
+        return op_inval("operands must be 16-byte aligned and ldo % 8 == 0, ldo >= N");
+    if (w_dtype != DLO_DT_BF16 && w_dtype != DLO_DT_E4M3) return op_inval("w_dtype");
+    if (epilogue < DLO_EPI_BIAS || epilogue > DLO_EPI_RESIDUAL) return op_inval("epilogue");
+    if (scales && (scale_seg < 16 || scale_seg % 16)) return op_inval("scale_seg % 16 != 0");
+    if (bias && !aligned(bias, 16)) return op_inval("bias must be 16-byte aligned");
+    if (gate && (!aligned(gate, 16) || gate_ld % 4 || rows_per_batch < 1)) return op_inval("gate layout");
+    GemmParams p;
+    p.A = A;
+    p.W = W;
+    p.w_dtype = w_dtype;
+    p.scales = scales;
+    p.scale_seg = scale_seg;
+    p.bias = bias;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.epi = epilogue;
+    p.out = out;
+    p.ldo = ldo;
+    p.gate = gate;
+    p.gate_ld = gate_ld;
+    p.rows_per_batch = rows_per_batch > 0 ? rows_per_batch : 1;
+    p.err = err;
+    return op_result(launch_gemm(p, static_cast<cudaStream_t>(stream), &g_op_launches));
+}
+
+extern "C" dlo_status dlo_op_attention(const void* Q, const void* K, const void* V, void* O, int batch,
+                                       int heads, int head_dim, int nq, int nk, int ldq, int ldk, int ldv,
+                                       int ldo, void* stream) {
+    if (!Q || !K || !V || !O) return op_inval("NULL operand");
+    if (batch < 1 || heads < 1 || nq < 1 || nk < 1) return op_inval("sizes must be >= 1");
+    if (head_dim < 8 || head_dim % 8 || head_dim > 128) return op_inval("head_dim % 8 != 0 or > 128");
+    if (ldq % 8 || ldk % 8 || ldv % 8 || ldo % 8) return op_inval("ld % 8 != 0");
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16)) return op_inval("alignment");
+    return op_result(launch_attention(Q, K, V, O, batch, heads, head_dim, nq, nk, ldq, ldk, ldv, ldo,
+                                      static_cast<cudaStream_t>(stream), &g_op_launches));
+}
+
+extern "C" dlo_status dlo_op_layernorm(const float* x, int rows, int D, int rows_per_batch,
+                                       const float* shift, const float* scale, int mod_ld, const void* w,
+                                       const void* b, float eps, void* out, void* stream) {
+    if (!x || !out || rows < 1 || D < 4 || D % 4 || rows_per_batch < 1) return op_inval("layernorm args");
+    if ((shift == nullptr) != (scale == nullptr) || (w == nullptr) != (b == nullptr)) return op_inval("pairs");
+    if (scale && (mod_ld % 4 || !aligned(scale, 16) || !aligned(shift, 16))) return op_inval("mod layout");
+    return op_result(launch_layernorm(x, rows, D, rows_per_batch, shift, scale, mod_ld, w, b, eps, out,
+                                      static_cast<cudaStream_t>(stream), &g_op_launches));
+}
+
+extern "C" dlo_status dlo_op_rmsnorm(void* x, int rows, int D, int ld, int col0, const void* w, float eps,
+                                     void* stream) {
+    if (!x || !w || rows < 1 || D < 8 || D % 8 || ld % 8 || col0 % 8 || col0 + D > ld) return op_inval("rmsnorm args");
+    return op_result(launch_rmsnorm(x, rows, D, ld, col0, w, eps, static_cast<cudaStream_t>(stream), &g_op_launches));
+}
+
+extern "C" dlo_status dlo_op_adaln(const void* cvec, int B, int C, const void* W, const void* bias, int N,
+                                   float* m, void* stream) {
+    if (!cvec || !W || !bias || !m || B < 1 || C < 8 || C % 8 || N < 1) return op_inval("adaln args");
+    return op_result(launch_adaln(cvec, B, C, W, bias, N, m, static_cast<cudaStream_t>(stream), &g_op_launches));
+}
+
+extern "C" dlo_status dlo_op_stage(void* dst, const void* src, size_t bytes, int mode, void* stream) {
+    if (!dst || !src || bytes % 16 || !aligned(dst, 16) || !aligned(src, 16)) return op_inval("stage args");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (mode == DLO_STAGE_GATHER) return op_result(launch_gather(dst, src, bytes, s, &g_op_launches));
+    if (mode == DLO_STAGE_MEMCPY) return op_result(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, s));
+    return op_inval("mode");
+}

@@ -1,0 +1,425 @@
+// Y = A W^T on the 5th-generation tensor cores (tcgen05), sm_103a.
+//
+// Persistent kernel, one CTA per SM, 6 warps:
+//   warp 0      TMA producer: 128x64 A tile and BNx64 W tile per stage,
+//               128-byte swizzle, into a STAGES-deep shared-memory ring
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16 (M=128,
+//               N=BN, K=16) x 4 per stage into one of two fp32 TMEM
+//               accumulators; tcgen05.commit frees the stage / publishes the
+//               accumulator
+//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, scale (FP8
+//               per-tensor), + bias, GELU or gate * y + residual, store
+// The two accumulators let the epilogue of tile t overlap the mainloop of
+// tile t+1.  E4M3 weights take the same path after a converter stage (see
+// the _fp8 kernel below): codes are widened to bf16 in shared memory (exact)
+// and the per-tensor scale is applied to the fp32 accumulator.
+//
+// Every mbarrier wait is bounded (2 s); a wait that runs out sets the
+// kernel's error word and a CTA-wide abort flag, after which every role
+// leaves its loop, in-flight TMA loads are drained (bounded) and TMEM is
+// freed before exit.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dlo {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;             // 64 bf16 = 128 bytes = one swizzle row
+constexpr int A_TILE = BM * BK * 2;
+constexpr int kThreads = 192;
+
+struct EpiArgs {
+    int M, N, K;
+    int epi;
+    void* out;
+    int ldo;
+    const __nv_bfloat16* bias;
+    const float* scales;
+    int scale_seg;
+    const float* gate;
+    int gate_ld;
+    int rows_per_batch;
+    int* err;
+    int num_m, num_n, num_tiles;
+    const uint8_t* w8;   // e4m3 weights (FP8 kernel), [N, K]
+};
+
+// Grouped tile order: groups of 8 M-blocks sweep all N-blocks, so one
+// group's A rows stay in L2 while the weights stream.
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mb, int& nb) {
+    constexpr int G = 8;
+    const int per_group = G * num_n;
+    const int g = t / per_group;
+    const int first = g * G;
+    const int gsz = min(num_m - first, G);
+    const int r = t - g * per_group;
+    mb = first + r % gsz;
+    nb = r / gsz;
+}
+
+__device__ __forceinline__ float gelu_tanh(float x) {
+    const float k0 = 0.7978845608028654f, k1 = 0.044715f;
+    return 0.5f * x * (1.f + tanhf(k0 * (x + k1 * x * x * x)));
+}
+
+// Epilogue of one 32-column chunk held by this thread (row `row`, columns
+// col0 .. col0 + ncols - 1, ncols in {16, 32}).
+__device__ __forceinline__ void epilogue_chunk(const EpiArgs& a, int row, int col0, int ncols,
+                                               const uint32_t (&r)[32]) {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    if (a.scales) {
+        const float s0 = a.scales[col0 / a.scale_seg];
+        const float s1 = ncols > 16 ? a.scales[(col0 + 16) / a.scale_seg] : s0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] *= s0;
+#pragma unroll
+        for (int i = 16; i < 32; ++i) v[i] *= s1;
+    }
+    if (a.bias) {
+        const uint4* bp = reinterpret_cast<const uint4*>(a.bias + col0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (q * 8 < ncols) {
+                const uint4 bv = bp[q];
+                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 f = __bfloat1622float2(b2[j]);
+                    v[q * 8 + 2 * j] += f.x;
+                    v[q * 8 + 2 * j + 1] += f.y;
+                }
+            }
+        }
+    }
+    if (a.epi == DLO_EPI_RESIDUAL) {
+        float* o = static_cast<float*>(a.out) + static_cast<size_t>(row) * a.ldo + col0;
+        const float* g = a.gate
+                             ? a.gate + static_cast<size_t>(row / a.rows_per_batch) * a.gate_ld + col0
+                             : nullptr;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            if (q * 4 < ncols) {
+                float4 x = reinterpret_cast<float4*>(o)[q];
+                float4 gg = g ? reinterpret_cast<const float4*>(g)[q] : make_float4(1.f, 1.f, 1.f, 1.f);
+                x.x += gg.x * v[q * 4 + 0];
+                x.y += gg.y * v[q * 4 + 1];
+                x.z += gg.z * v[q * 4 + 2];
+                x.w += gg.w * v[q * 4 + 3];
+                reinterpret_cast<float4*>(o)[q] = x;
+            }
+        }
+    } else {
+        if (a.epi == DLO_EPI_GELU) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+        }
+        uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
+                                            static_cast<size_t>(row) * a.ldo + col0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (q * 8 < ncols) {
+                uint4 w;
+                w.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+                w.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+                w.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+                w.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+                o[q] = w;
+            }
+        }
+    }
+}
+
+template <int BN, int STAGES>
+struct SmemPlan {
+    static constexpr int B_TILE = BN * BK * 2;
+    static constexpr int A_OFF = 0;
+    static constexpr int B_OFF = STAGES * A_TILE;
+    static constexpr int BAR_OFF = B_OFF + STAGES * B_TILE;
+    // full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+    static constexpr int TMEM_SLOT_OFF = BAR_OFF + (2 * STAGES + 5) * 8;
+    static constexpr int ABORT_OFF = TMEM_SLOT_OFF + 4;
+    static constexpr int BYTES = ABORT_OFF + 4 + 1024;  // + alignment slack
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const EpiArgs args) {
+    using P = SmemPlan<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_full = sbase + P::BAR_OFF;
+    const uint32_t bar_empty = bar_full + STAGES * 8;
+    const uint32_t bar_tfull = bar_empty + STAGES * 8;
+    const uint32_t bar_tempty = bar_tfull + 2 * 8;
+    const uint32_t bar_drain = bar_tempty + 2 * 8;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + P::TMEM_SLOT_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P::ABORT_OFF);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + s * 8, 1);
+            mbar_init(bar_empty + s * 8, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar_tfull + a * 8, 1);
+            mbar_init(bar_tempty + a * 8, 4);
+        }
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(sbase + P::TMEM_SLOT_OFF, 2 * BN);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int kblocks = (args.K + BK - 1) / BK;
+
+    auto fail = [&]() {
+        *abort_flag = 1;
+        if (args.err) atomicExch(args.err, 1);
+    };
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        uint32_t issued = 0, last_par = 0;   // per-stage bit masks
+        for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, args.num_m, args.num_n, mb, nb);
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait(bar_empty + s * 8, ph ^ 1, abort_flag)) {
+                    fail();
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = bar_full + s * 8;
+                mbar_arrive_expect_tx(fb, A_TILE + P::B_TILE);
+                tma_load_2d(sbase + P::A_OFF + s * A_TILE, &tmA, kb * BK, mb * BM, fb);
+                tma_load_2d(sbase + P::B_OFF + s * P::B_TILE, &tmB, kb * BK, nb * BN, fb);
+                issued |= 1u << s;
+                last_par = (last_par & ~(1u << s)) | (ph << s);
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+        }
+        if (!ok || *abort_flag) {
+            // drain: the last load issued into each stage must land before
+            // the CTA exits (bounded wait on that fill's phase)
+            for (int i = 0; i < STAGES; ++i)
+                if (issued & (1u << i)) mbar_wait(bar_full + i * 8, (last_par >> i) & 1u, nullptr);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+        int s = 0;
+        uint32_t ph = 0;
+        int t = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x, ++t) {
+            const int acc = t & 1;
+            const uint32_t aph = (t >> 1) & 1;
+            if (!mbar_wait(bar_tempty + acc * 8, aph ^ 1, abort_flag)) {
+                fail();
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * BN;
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait(bar_full + s * 8, ph, abort_flag)) {
+                    fail();
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = sbase + P::A_OFF + s * A_TILE;
+                const uint32_t b0 = sbase + P::B_OFF + s * P::B_TILE;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    tc_mma_f16(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32),
+                               idesc, (kb | kk) != 0);
+                }
+                tc_commit(bar_empty + s * 8);
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+            if (ok) tc_commit(bar_tfull + acc * 8);
+        }
+        if (*abort_flag) {
+            // drain: wait (bounded) until every MMA issued so far completed
+            tc_commit(bar_drain);
+            mbar_wait(bar_drain, 0, nullptr);
+        }
+    } else if (warp >= 2) {
+        // ---------------- epilogue
+        const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
+        int t = 0;
+        for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++t) {
+            const int acc = t & 1;
+            const uint32_t aph = (t >> 1) & 1;
+            int mb, nb;
+            tile_coords(tile, args.num_m, args.num_n, mb, nb);
+            bool ok = mbar_wait(bar_tfull + acc * 8, aph, abort_flag);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) {
+                if (lane == 0) fail();
+                break;
+            }
+            tc_fence_after();
+            const int row = mb * BM + quarter * 32 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + c0, r);
+                tmem_wait_ld();
+                const int col0 = nb * BN + c0;
+                const int ncols = min(32, args.N - col0);
+                if (row < args.M && ncols > 0) epilogue_chunk(args, row, col0, ncols, r);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_tempty + acc * 8);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 2 * BN);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Row-major [rows, cols] bf16 matrix with row pitch ld elements; box of
+// box_rows x 64 columns, 128-byte swizzle, zero fill out of bounds.
+bool make_map_bf16(CUtensorMap* m, const void* base, long long rows, long long cols, long long ld,
+                   int box_rows) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+int g_num_sms = 0;
+
+template <int BN, int STAGES>
+cudaError_t run_bf16(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
+    using PL = SmemPlan<BN, STAGES>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<BN, STAGES>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, PL::BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    CUtensorMap ta, tb;
+    if (!make_map_bf16(&ta, p.A, p.M, p.K, p.K, BM)) return cudaErrorInvalidValue;
+    if (!make_map_bf16(&tb, p.W, p.N, p.K, p.K, BN)) return cudaErrorInvalidValue;
+    EpiArgs a;
+    a.M = p.M;
+    a.N = p.N;
+    a.K = p.K;
+    a.epi = p.epi;
+    a.out = p.out;
+    a.ldo = p.ldo;
+    a.bias = static_cast<const __nv_bfloat16*>(p.bias);
+    a.scales = p.scales;
+    a.scale_seg = p.scale_seg > 0 ? p.scale_seg : p.N;
+    a.gate = p.gate;
+    a.gate_ld = p.gate_ld;
+    a.rows_per_batch = p.rows_per_batch > 0 ? p.rows_per_batch : 1;
+    a.err = p.err;
+    a.num_m = (p.M + BM - 1) / BM;
+    a.num_n = (p.N + BN - 1) / BN;
+    a.num_tiles = a.num_m * a.num_n;
+    a.w8 = nullptr;
+    const int grid = a.num_tiles < g_num_sms ? a.num_tiles : g_num_sms;
+    gemm_bf16_kernel<BN, STAGES><<<grid, kThreads, PL::BYTES, s>>>(ta, tb, a);
+    ++*launches;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_num_sms() {
+    if (!g_num_sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (g_num_sms <= 0) g_num_sms = 1;
+    }
+    return g_num_sms;
+}
+
+cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
+    if (p.M <= 0) return cudaSuccess;
+    gemm_num_sms();
+    if (p.w_dtype != DLO_DT_BF16) return cudaErrorNotSupported;
+    // Pick the N tile that minimises (waves x tile width) over the SMs.
+    const long long num_m = (p.M + BM - 1) / BM;
+    auto cost = [&](int bn) {
+        const long long tiles = num_m * ((p.N + bn - 1) / bn);
+        return ((tiles + g_num_sms - 1) / g_num_sms) * bn;
+    };
+    if (cost(256) <= cost(128)) return run_bf16<256, 4>(p, s, launches);
+    return run_bf16<128, 6>(p, s, launches);
+}
+
+}  // namespace dlo

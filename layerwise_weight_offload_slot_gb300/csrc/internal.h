@@ -1,0 +1,101 @@
+// Internal declarations shared by the host runtime and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "dlo.h"
+
+namespace dlo {
+
+// ------------------------------------------------------------------ layout
+
+struct Entry {
+    std::string name;
+    size_t offset = 0;
+    size_t bytes = 0;
+    int dtype = DLO_DT_BF16;
+    int ndim = 1;
+    long long shape[2] = {0, 0};
+    int source = 1;
+};
+
+// Validates the description; returns DLO_OK or an error with a message.
+dlo_status validate_desc(const dlo_desc* d, std::string* msg);
+// Builds the flat block layout (groups start 256-B aligned; members of a
+// group are contiguous).  Returns total bytes (multiple of 256).
+size_t build_layout(const dlo_desc& d, std::vector<Entry>* out);
+int find_entry(const std::vector<Entry>& L, const char* name);
+
+// Device workspace carve-up for max_batch x max_tokens activations.
+struct Workspace {
+    size_t x = 0;        // fp32 [BN, D]   hidden state
+    size_t h = 0;        // bf16 [BN, D]   norm output
+    size_t big = 0;      // bf16 [BN, max(3D, F)]  qkv, then FFN hidden
+    size_t a = 0;        // bf16 [BN, D]   attention output
+    size_t q2 = 0;       // bf16 [BN, D]   cross-attention q (video)
+    size_t kv2 = 0;      // bf16 [B*L, 2D] cross-attention k|v (video)
+    size_t mod = 0;      // fp32 [B, 6D]   modulation
+    size_t in_x = 0;     // bf16 [BN, D]   staging of host inputs (forward_host)
+    size_t in_cond = 0;  // cond staging (forward_host)
+    size_t in_ctx = 0;   // bf16 [B*L, Dt] (forward_host)
+    size_t err = 0;      // int[64] kernels' error words
+    size_t total = 0;
+};
+Workspace plan_workspace(const dlo_desc& d);
+
+// ------------------------------------------------------------------ host math
+
+uint16_t f32_to_bf16_rne(float f);
+uint8_t f32_to_e4m3_rne_sat(float v);
+
+// ------------------------------------------------------------------ kernel launchers
+// All return cudaSuccess or the launch error; arguments are validated by the
+// callers.  Each increments *launches by the kernels it launched.
+
+struct GemmParams {
+    const void* A = nullptr;      // bf16 [M, K]
+    const void* W = nullptr;      // [N, K] bf16 or e4m3
+    int w_dtype = DLO_DT_BF16;
+    const float* scales = nullptr;
+    int scale_seg = 0;
+    const void* bias = nullptr;   // bf16 [N]
+    int M = 0, N = 0, K = 0;
+    int epi = DLO_EPI_BIAS;
+    void* out = nullptr;
+    int ldo = 0;
+    const float* gate = nullptr;
+    int gate_ld = 0;
+    int rows_per_batch = 1;
+    int* err = nullptr;
+};
+cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches);
+int gemm_num_sms();
+
+cudaError_t launch_attention(const void* Q, const void* K, const void* V, void* O, int batch,
+                             int heads, int hd, int nq, int nk, int ldq, int ldk, int ldv, int ldo,
+                             cudaStream_t s, unsigned long long* launches);
+
+cudaError_t launch_layernorm(const float* x, int rows, int D, int rpb, const float* shift,
+                             const float* scale, int mod_ld, const void* w, const void* b,
+                             float eps, void* out, cudaStream_t s, unsigned long long* launches);
+cudaError_t launch_rmsnorm(void* x, int rows, int D, int ld, int col0, const void* w, float eps,
+                           cudaStream_t s, unsigned long long* launches);
+// Two segments of one row set in one launch (q and k of the same rows).
+cudaError_t launch_rmsnorm2(void* x, int rows, int D, int ld, int col0a, const void* wa,
+                            int col0b, const void* wb, float eps, cudaStream_t s,
+                            unsigned long long* launches);
+cudaError_t launch_adaln(const void* c, int B, int C, const void* W, const void* bias, int N,
+                         float* m, cudaStream_t s, unsigned long long* launches);
+cudaError_t launch_mod_add(const float* e, const void* table, int B, int n6d, float* m,
+                           cudaStream_t s, unsigned long long* launches);
+cudaError_t launch_bf16_to_f32(const void* in, float* out, size_t n, cudaStream_t s,
+                               unsigned long long* launches);
+cudaError_t launch_f32_to_bf16(const float* in, void* out, size_t n, cudaStream_t s,
+                               unsigned long long* launches);
+cudaError_t launch_gather(void* dst, const void* src, size_t bytes, cudaStream_t s,
+                          unsigned long long* launches);
+
+}  // namespace dlo

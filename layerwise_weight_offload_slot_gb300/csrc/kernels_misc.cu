@@ -1,0 +1,327 @@
+// Bandwidth-bound kernels of one block: LayerNorm (+adaLN modulate or affine),
+// RMSNorm on q/k, the adaLN GEMV SiLU(c) W^T + b, the video modulation add,
+// dtype conversions of the carried hidden state, and the zero-copy slot
+// gather that reads mapped host memory with 16-byte loads.
+//
+// One warp per row for the row-wise kernels: a row (<= 5120 fp32 = 20 KB)
+// stays in L1 across the passes, so HBM sees one read of x and one write.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dlo {
+
+namespace {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float bf(const __nv_bfloat16 v) { return __bfloat162float(v); }
+
+// out = LN(x) * (1 + scale) + shift | LN(x) * w + b | LN(x)
+__global__ void __launch_bounds__(256) layernorm_kernel(const float* __restrict__ x, int rows,
+                                                        int D, int rpb,
+                                                        const float* __restrict__ shift,
+                                                        const float* __restrict__ scale,
+                                                        int mod_ld,
+                                                        const __nv_bfloat16* __restrict__ w,
+                                                        const __nv_bfloat16* __restrict__ b,
+                                                        float eps,
+                                                        __nv_bfloat16* __restrict__ out) {
+    const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(row) * D);
+    const int n4 = D >> 2;
+    float s = 0.f;
+    for (int i = lane; i < n4; i += 32) {
+        const float4 v = xr[i];
+        s += (v.x + v.y) + (v.z + v.w);
+    }
+    const float mean = warp_sum(s) / static_cast<float>(D);
+    float q = 0.f;
+    for (int i = lane; i < n4; i += 32) {
+        const float4 v = xr[i];
+        const float a = v.x - mean, bb = v.y - mean, c = v.z - mean, d = v.w - mean;
+        q += (a * a + bb * bb) + (c * c + d * d);
+    }
+    const float var = warp_sum(q) / static_cast<float>(D);
+    const float rstd = rsqrtf(var + eps);
+    const int bt = row / rpb;
+    uint2* orow = reinterpret_cast<uint2*>(out + static_cast<size_t>(row) * D);
+    for (int i = lane; i < n4; i += 32) {
+        const float4 v = xr[i];
+        float y0 = (v.x - mean) * rstd, y1 = (v.y - mean) * rstd;
+        float y2 = (v.z - mean) * rstd, y3 = (v.w - mean) * rstd;
+        const int d = i * 4;
+        if (scale) {
+            const float4 sc = *reinterpret_cast<const float4*>(scale + static_cast<size_t>(bt) * mod_ld + d);
+            const float4 sh = *reinterpret_cast<const float4*>(shift + static_cast<size_t>(bt) * mod_ld + d);
+            y0 = y0 * (1.f + sc.x) + sh.x;
+            y1 = y1 * (1.f + sc.y) + sh.y;
+            y2 = y2 * (1.f + sc.z) + sh.z;
+            y3 = y3 * (1.f + sc.w) + sh.w;
+        } else if (w) {
+            y0 = y0 * bf(w[d]) + bf(b[d]);
+            y1 = y1 * bf(w[d + 1]) + bf(b[d + 1]);
+            y2 = y2 * bf(w[d + 2]) + bf(b[d + 2]);
+            y3 = y3 * bf(w[d + 3]) + bf(b[d + 3]);
+        }
+        uint2 o;
+        o.x = pack_bf16x2(y0, y1);
+        o.y = pack_bf16x2(y2, y3);
+        orow[i] = o;
+    }
+}
+
+// x[row, col0 + d] = x * rsqrt(mean(x^2) + eps) * w[d], in place, bf16; up to
+// two column segments of the same rows (q and k).
+__global__ void __launch_bounds__(256) rmsnorm_kernel(__nv_bfloat16* __restrict__ x, int rows,
+                                                      int D, int ld, int col0a,
+                                                      const __nv_bfloat16* __restrict__ wa,
+                                                      int col0b,
+                                                      const __nv_bfloat16* __restrict__ wb,
+                                                      float eps) {
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nseg = wb ? 2 : 1;
+    if (gw >= rows * nseg) return;
+    const int row = gw / nseg, seg = gw % nseg;
+    const int col0 = seg ? col0b : col0a;
+    const __nv_bfloat16* w = seg ? wb : wa;
+    uint4* xr = reinterpret_cast<uint4*>(x + static_cast<size_t>(row) * ld + col0);
+    const int n8 = D >> 3;
+    float s = 0.f;
+    for (int i = lane; i < n8; i += 32) {
+        const uint4 v = xr[i];
+        const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(p[j]);
+            s += f.x * f.x + f.y * f.y;
+        }
+    }
+    const float r = rsqrtf(warp_sum(s) / static_cast<float>(D) + eps);
+    const uint4* wr = reinterpret_cast<const uint4*>(w);
+    for (int i = lane; i < n8; i += 32) {
+        uint4 v = xr[i];
+        const uint4 g = wr[i];
+        __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&v);
+        const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(p[j]);
+            const float2 gg = __bfloat1622float2(gp[j]);
+            p[j] = __floats2bfloat162_rn(f.x * r * gg.x, f.y * r * gg.y);
+        }
+        xr[i] = v;
+    }
+}
+
+// m[b, n] = sum_i SiLU(c[b, i]) W[n, i] + bias[n]; one warp per output n,
+// W read once with 16-byte loads for all batch rows (B <= 8 per pass).
+__global__ void __launch_bounds__(256) adaln_kernel(const __nv_bfloat16* __restrict__ c, int B,
+                                                    int C, const __nv_bfloat16* __restrict__ W,
+                                                    const __nv_bfloat16* __restrict__ bias,
+                                                    int N, float* __restrict__ m) {
+    const int n = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (n >= N) return;
+    const uint4* wr = reinterpret_cast<const uint4*>(W + static_cast<size_t>(n) * C);
+    const int n8 = C >> 3;
+    for (int b0 = 0; b0 < B; b0 += 8) {
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+        for (int i = lane; i < n8; i += 32) {
+            const uint4 wv = wr[i];
+            const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wv);
+            float wf[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = __bfloat1622float2(wp[j]);
+                wf[2 * j] = f.x;
+                wf[2 * j + 1] = f.y;
+            }
+#pragma unroll
+            for (int bb = 0; bb < 8; ++bb) {
+                if (b0 + bb < B) {
+                    const uint4 cv = *reinterpret_cast<const uint4*>(c + static_cast<size_t>(b0 + bb) * C + i * 8);
+                    const __nv_bfloat162* cp = reinterpret_cast<const __nv_bfloat162*>(&cv);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 f = __bfloat1622float2(cp[j]);
+                        const float s0 = f.x / (1.f + __expf(-f.x));
+                        const float s1 = f.y / (1.f + __expf(-f.y));
+                        acc[bb] += s0 * wf[2 * j] + s1 * wf[2 * j + 1];
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int bb = 0; bb < 8; ++bb) {
+            const float v = warp_sum(acc[bb]);
+            if (lane == 0 && b0 + bb < B) m[static_cast<size_t>(b0 + bb) * N + n] = v + bf(bias[n]);
+        }
+    }
+}
+
+// m[b, r] = e[b, r] + table[r] over r < 6D
+__global__ void mod_add_kernel(const float* __restrict__ e, const __nv_bfloat16* __restrict__ t,
+                               int B, int n6d, float* __restrict__ m) {
+    const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= static_cast<size_t>(B) * n6d) return;
+    m[i] = e[i] + bf(t[i % n6d]);
+}
+
+__global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ in, float* __restrict__ out,
+                                   size_t n8) {
+    const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n8) return;
+    const uint4 v = reinterpret_cast<const uint4*>(in)[i];
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+    float4 a, b;
+    float2 f0 = __bfloat1622float2(p[0]), f1 = __bfloat1622float2(p[1]);
+    float2 f2 = __bfloat1622float2(p[2]), f3 = __bfloat1622float2(p[3]);
+    a = make_float4(f0.x, f0.y, f1.x, f1.y);
+    b = make_float4(f2.x, f2.y, f3.x, f3.y);
+    reinterpret_cast<float4*>(out)[2 * i] = a;
+    reinterpret_cast<float4*>(out)[2 * i + 1] = b;
+}
+
+__global__ void f32_to_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* __restrict__ out,
+                                   size_t n8) {
+    const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n8) return;
+    const float4 a = reinterpret_cast<const float4*>(in)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(in)[2 * i + 1];
+    uint4 o;
+    o.x = pack_bf16x2(a.x, a.y);
+    o.y = pack_bf16x2(a.z, a.w);
+    o.z = pack_bf16x2(b.x, b.y);
+    o.w = pack_bf16x2(b.z, b.w);
+    reinterpret_cast<uint4*>(out)[i] = o;
+}
+
+// dst[i] = src[i] over 16-byte words; src may be mapped host memory.  Four
+// independent loads per thread are in flight before the stores.
+__global__ void __launch_bounds__(1024) gather_kernel(uint4* __restrict__ dst,
+                                                      const uint4* __restrict__ src, size_t n16) {
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+        const uint4 a = src[i];
+        const uint4 b = src[i + stride];
+        const uint4 c = src[i + 2 * stride];
+        const uint4 d = src[i + 3 * stride];
+        dst[i] = a;
+        dst[i + stride] = b;
+        dst[i + 2 * stride] = c;
+        dst[i + 3 * stride] = d;
+    }
+    for (; i < n16; i += stride) dst[i] = src[i];
+}
+
+inline unsigned blocks_for(size_t threads, unsigned per) {
+    return static_cast<unsigned>((threads + per - 1) / per);
+}
+
+}  // namespace
+
+cudaError_t launch_layernorm(const float* x, int rows, int D, int rpb, const float* shift,
+                             const float* scale, int mod_ld, const void* w, const void* b,
+                             float eps, void* out, cudaStream_t s, unsigned long long* launches) {
+    if (rows <= 0) return cudaSuccess;
+    layernorm_kernel<<<blocks_for(static_cast<size_t>(rows) * 32, 256), 256, 0, s>>>(
+        x, rows, D, rpb, shift, scale, mod_ld, static_cast<const __nv_bfloat16*>(w),
+        static_cast<const __nv_bfloat16*>(b), eps, static_cast<__nv_bfloat16*>(out));
+    ++*launches;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(void* x, int rows, int D, int ld, int col0, const void* w, float eps,
+                           cudaStream_t s, unsigned long long* launches) {
+    if (rows <= 0) return cudaSuccess;
+    rmsnorm_kernel<<<blocks_for(static_cast<size_t>(rows) * 32, 256), 256, 0, s>>>(
+        static_cast<__nv_bfloat16*>(x), rows, D, ld, col0, static_cast<const __nv_bfloat16*>(w),
+        0, nullptr, eps);
+    ++*launches;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm2(void* x, int rows, int D, int ld, int col0a, const void* wa,
+                            int col0b, const void* wb, float eps, cudaStream_t s,
+                            unsigned long long* launches) {
+    if (rows <= 0) return cudaSuccess;
+    rmsnorm_kernel<<<blocks_for(static_cast<size_t>(rows) * 64, 256), 256, 0, s>>>(
+        static_cast<__nv_bfloat16*>(x), rows, D, ld, col0a,
+        static_cast<const __nv_bfloat16*>(wa), col0b, static_cast<const __nv_bfloat16*>(wb), eps);
+    ++*launches;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_adaln(const void* c, int B, int C, const void* W, const void* bias, int N,
+                         float* m, cudaStream_t s, unsigned long long* launches) {
+    if (N <= 0 || B <= 0) return cudaSuccess;
+    adaln_kernel<<<blocks_for(static_cast<size_t>(N) * 32, 256), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(c), B, C, static_cast<const __nv_bfloat16*>(W),
+        static_cast<const __nv_bfloat16*>(bias), N, m);
+    ++*launches;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mod_add(const float* e, const void* table, int B, int n6d, float* m,
+                           cudaStream_t s, unsigned long long* launches) {
+    const size_t n = static_cast<size_t>(B) * n6d;
+    if (!n) return cudaSuccess;
+    mod_add_kernel<<<blocks_for(n, 256), 256, 0, s>>>(e, static_cast<const __nv_bfloat16*>(table),
+                                                      B, n6d, m);
+    ++*launches;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bf16_to_f32(const void* in, float* out, size_t n, cudaStream_t s,
+                               unsigned long long* launches) {
+    const size_t n8 = n / 8;
+    if (!n8) return cudaSuccess;
+    bf16_to_f32_kernel<<<blocks_for(n8, 256), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(in),
+                                                           out, n8);
+    ++*launches;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_f32_to_bf16(const float* in, void* out, size_t n, cudaStream_t s,
+                               unsigned long long* launches) {
+    const size_t n8 = n / 8;
+    if (!n8) return cudaSuccess;
+    f32_to_bf16_kernel<<<blocks_for(n8, 256), 256, 0, s>>>(in, static_cast<__nv_bfloat16*>(out),
+                                                           n8);
+    ++*launches;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(void* dst, const void* src, size_t bytes, cudaStream_t s,
+                          unsigned long long* launches) {
+    const size_t n16 = bytes / 16;
+    if (!n16) return cudaSuccess;
+    static int grid = 0;
+    if (!grid) {
+        int dev = 0, sms = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        grid = sms > 0 ? sms / 4 : 32;   // a quarter of the SMs
+    }
+    unsigned g = static_cast<unsigned>(grid);
+    const size_t need = (n16 + 1023) / 1024;
+    if (need < g) g = static_cast<unsigned>(need);
+    gather_kernel<<<g, 1024, 0, s>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src),
+                                     n16);
+    ++*launches;
+    return cudaGetLastError();
+}
+
+}  // namespace dlo

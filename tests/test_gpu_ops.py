@@ -1,0 +1,185 @@
+"""Kernel-level parity through the C ABI unit ops against the CPU oracle's
+primitives (float64)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import dit
+from tests.helpers import bf16
+
+dlo = pytest.importorskip("layerwise_weight_offload_slot_gb300")
+
+pytestmark = pytest.mark.gpu
+
+
+def f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def rel(y, ref):
+    y = np.asarray(y, np.float64)
+    return float(np.linalg.norm(y - ref) / max(np.linalg.norm(ref), 1e-30))
+
+
+def stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+GEMM_SHAPES = [(1, 16, 16), (100, 48, 64), (128, 128, 64), (300, 272, 80), (256, 384, 1152),
+               (2048, 1152, 1152), (2048, 3456, 1152), (1000, 4608, 1152), (777, 1152, 4608),
+               (129, 256, 5120)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+@pytest.mark.parametrize("epi", [0, 1, 2])
+def test_gemm_matches_oracle(M, N, K, epi):
+    g = np.random.default_rng(M * 7 + N * 3 + K + epi)
+    A = bf16(g.standard_normal((M, K)))
+    W = bf16(g.standard_normal((N, K)) * 0.05)
+    b = bf16(g.standard_normal(N) * 0.1)
+    ref = dit.linear(f64(A), f64(W), f64(b))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if epi == dlo.EPI_RESIDUAL:
+        rows_per_batch = max(1, M // 2)
+        nb = (M + rows_per_batch - 1) // rows_per_batch
+        gate = torch.from_numpy(g.standard_normal((nb, N)).astype(np.float32)).cuda()
+        x0 = torch.from_numpy(g.standard_normal((M, N)).astype(np.float32)).cuda()
+        out = x0.clone()
+        dlo.dlo_op_gemm(A.data_ptr(), W.data_ptr(), dlo.DT_BF16, None, 0, b.data_ptr(), M, N, K, epi,
+                        out.data_ptr(), N, gate.data_ptr(), N, rows_per_batch, err.data_ptr(), stream())
+        gidx = np.arange(M) // rows_per_batch
+        ref = f64(x0) + f64(gate)[gidx] * ref
+        tol = 1e-5
+    else:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        dlo.dlo_op_gemm(A.data_ptr(), W.data_ptr(), dlo.DT_BF16, None, 0, b.data_ptr(), M, N, K, epi,
+                        out.data_ptr(), N, None, 0, 1, err.data_ptr(), stream())
+        if epi == dlo.EPI_GELU:
+            ref = dit.gelu_tanh(ref)
+        tol = 6e-3
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert rel(f64(out), ref) < tol
+
+
+def test_gemm_output_stride_and_no_bias():
+    g = np.random.default_rng(3)
+    M, N, K, ldo = 200, 96, 128, 160
+    A = bf16(g.standard_normal((M, K)))
+    W = bf16(g.standard_normal((N, K)) * 0.05)
+    out = torch.full((M, ldo), 7.0, dtype=torch.bfloat16, device="cuda")
+    dlo.dlo_op_gemm(A.data_ptr(), W.data_ptr(), dlo.DT_BF16, None, 0, None, M, N, K, 0,
+                    out.data_ptr(), ldo, None, 0, 1, None, stream())
+    torch.cuda.synchronize()
+    assert rel(f64(out[:, :N]), f64(A) @ f64(W).T) < 6e-3
+    assert bool((out[:, N:] == 7.0).all())
+
+
+def test_gemm_scale_segments():
+    g = np.random.default_rng(4)
+    M, N, K = 64, 96, 64
+    A = bf16(g.standard_normal((M, K)))
+    W = bf16(g.standard_normal((N, K)) * 0.05)
+    sc = torch.tensor([0.5, 2.0, 3.0], dtype=torch.float32, device="cuda")
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    dlo.dlo_op_gemm(A.data_ptr(), W.data_ptr(), dlo.DT_BF16, sc.data_ptr(), 32, None, M, N, K, 0,
+                    out.data_ptr(), N, None, 0, 1, None, stream())
+    torch.cuda.synchronize()
+    ref = f64(A) @ f64(W).T * np.repeat([0.5, 2.0, 3.0], 32)[None]
+    assert rel(f64(out), ref) < 6e-3
+
+
+@pytest.mark.parametrize("B,H,hd,nq,nk", [(1, 1, 64, 64, 64), (2, 3, 72, 100, 300), (1, 2, 128, 257, 129),
+                                          (2, 16, 72, 1024, 1024), (1, 4, 64, 1, 5), (1, 2, 32, 70, 512),
+                                          (1, 40, 128, 200, 512)])
+def test_attention_matches_oracle(B, H, hd, nq, nk):
+    g = np.random.default_rng(B + H + hd + nq + nk)
+    D = H * hd
+    # q/k/v inside wider rows (qkv-fused layout, row stride 3D)
+    qkv_q = bf16(g.standard_normal((B * nq, 3 * D)))
+    kv = bf16(g.standard_normal((B * nk, 3 * D)))
+    Q = qkv_q
+    K = kv[:, D:]
+    V = kv[:, 2 * D:]
+    O = torch.zeros((B * nq, D), dtype=torch.bfloat16, device="cuda")
+    dlo.dlo_op_attention(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), B, H, hd, nq, nk,
+                         3 * D, 3 * D, 3 * D, D, stream())
+    torch.cuda.synchronize()
+    q, k, v = f64(Q)[:, :D], f64(kv)[:, D:2 * D], f64(kv)[:, 2 * D:]
+    for b in range(B):
+        ref = dit.attention(q[b * nq:(b + 1) * nq], k[b * nk:(b + 1) * nk], v[b * nk:(b + 1) * nk], H)
+        assert rel(f64(O[b * nq:(b + 1) * nq]), ref) < 1e-2
+
+
+@pytest.mark.parametrize("mode", ["modulate", "affine", "plain"])
+def test_layernorm_matches_oracle(mode):
+    g = np.random.default_rng(11)
+    B, N, D = 2, 37, 1152
+    x = torch.from_numpy((g.standard_normal((B * N, D)) * 3 + 1).astype(np.float32)).cuda()
+    out = torch.empty((B * N, D), dtype=torch.bfloat16, device="cuda")
+    ref = dit.layernorm(f64(x), 1e-6)
+    shift = scale = w = b = None
+    if mode == "modulate":
+        m = torch.from_numpy(g.standard_normal((B, 6 * D)).astype(np.float32)).cuda()
+        shift, scale = m[:, :D], m[:, D:2 * D]
+        dlo.dlo_op_layernorm(x.data_ptr(), B * N, D, N, shift.data_ptr(), scale.data_ptr(), 6 * D,
+                             None, None, 1e-6, out.data_ptr(), stream())
+        idx = np.arange(B * N) // N
+        ref = ref * (1 + f64(scale)[idx]) + f64(shift)[idx]
+    elif mode == "affine":
+        w = bf16(1 + 0.1 * g.standard_normal(D))
+        b = bf16(0.1 * g.standard_normal(D))
+        dlo.dlo_op_layernorm(x.data_ptr(), B * N, D, N, None, None, 0, w.data_ptr(), b.data_ptr(),
+                             1e-6, out.data_ptr(), stream())
+        ref = ref * f64(w) + f64(b)
+    else:
+        dlo.dlo_op_layernorm(x.data_ptr(), B * N, D, N, None, None, 0, None, None, 1e-6,
+                             out.data_ptr(), stream())
+    torch.cuda.synchronize()
+    assert rel(f64(out), ref) < 5e-3
+
+
+def test_rmsnorm_matches_oracle():
+    g = np.random.default_rng(12)
+    rows, D, ld, col0 = 50, 640, 1920, 640
+    buf = bf16(g.standard_normal((rows, ld)) * 2)
+    before = f64(buf)
+    w = bf16(1 + 0.1 * g.standard_normal(D))
+    dlo.dlo_op_rmsnorm(buf.data_ptr(), rows, D, ld, col0, w.data_ptr(), 1e-6, stream())
+    torch.cuda.synchronize()
+    after = f64(buf)
+    ref = dit.rmsnorm(before[:, col0:col0 + D], f64(w), 1e-6)
+    assert rel(after[:, col0:col0 + D], ref) < 5e-3
+    np.testing.assert_array_equal(after[:, :col0], before[:, :col0])
+    np.testing.assert_array_equal(after[:, col0 + D:], before[:, col0 + D:])
+
+
+@pytest.mark.parametrize("B", [1, 2, 9])
+def test_adaln_matches_oracle(B):
+    g = np.random.default_rng(13 + B)
+    C, N = 1152, 6912
+    c = bf16(g.standard_normal((B, C)))
+    W = bf16(g.standard_normal((N, C)) * 0.02)
+    bias = bf16(g.standard_normal(N) * 0.02)
+    m = torch.empty((B, N), dtype=torch.float32, device="cuda")
+    dlo.dlo_op_adaln(c.data_ptr(), B, C, W.data_ptr(), bias.data_ptr(), N, m.data_ptr(), stream())
+    torch.cuda.synchronize()
+    ref = dit.linear(dit.silu(f64(c)), f64(W), f64(bias))
+    assert rel(f64(m), ref) < 1e-5
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_stage_copies_host_bytes_exactly(mode):
+    n = (3 << 20) + 48
+    h = torch.randint(0, 256, (n,), dtype=torch.uint8).pin_memory()
+    d = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    dlo.dlo_op_stage(d.data_ptr(), h.data_ptr(), n, mode, stream())
+    torch.cuda.synchronize()
+    assert torch.equal(d.cpu(), h)
+
+
+def test_op_argument_errors():
+    with pytest.raises(dlo.DloError):
+        dlo.dlo_op_gemm(16, 16, 0, None, 0, None, 10, 15, 16, 0, 16, 16, None, 0, 1, None, None)
+    with pytest.raises(dlo.DloError):
+        dlo.dlo_op_attention(16, 16, 16, 16, 1, 1, 12, 4, 4, 16, 16, 16, 16, None)

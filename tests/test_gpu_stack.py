@@ -1,0 +1,205 @@
+"""Stack-level checks through the C ABI: parity with the oracle, the circular
+schedule, bit-exact slot bytes, residency invariance, staging engines,
+registration rollback and lifecycle errors."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import schedule as osched
+from tests import helpers as H
+
+dlo = pytest.importorskip("layerwise_weight_offload_slot_gb300")
+
+pytestmark = pytest.mark.gpu
+
+# small stacks that still span several GEMM tiles and a ragged tail
+SMALL_DIT = synth.StackConfig("dit-small", synth.KIND_DIT, 6, 256, 4, 64, 512, 2, 200, cond_dim=256)
+SMALL_VID = synth.StackConfig("video-small", synth.KIND_VIDEO, 4, 256, 2, 128, 512, 2, 300,
+                              text_dim=192, text_tokens=77)
+
+
+def run(st, cfg, step=0):
+    x, cond, ctx = H.device_inputs(cfg, step)
+    out = st.forward(x, cond, ctx)
+    torch.cuda.synchronize()
+    st.wait()
+    return x, cond, ctx, out
+
+
+def test_tiny_stack_matches_oracle():
+    cfg = synth.CFG_TINY
+    st = H.make_stack(cfg)
+    st.attach()
+    x, cond, ctx, out = run(st, cfg)
+    ref = H.oracle_forward(cfg, x, cond, ctx, H.oracle_blocks(cfg))
+    err = H.rel_l2(out.float().cpu().numpy(), ref)
+    print("tiny stack max rel L2", err)
+    assert err <= 2e-2
+    st.close()
+
+
+@pytest.mark.parametrize("cfg", [SMALL_DIT, SMALL_VID], ids=lambda c: c.name)
+def test_small_stacks_match_oracle(cfg):
+    st = H.make_stack(cfg)
+    st.attach()
+    x, cond, ctx, out = run(st, cfg)
+    ref = H.oracle_forward(cfg, x, cond, ctx, H.oracle_blocks(cfg))
+    y = out.float().cpu().numpy()
+    err = H.rel_l2(y, ref)
+    # the residual dominates x; also bound the error of the stack's update
+    x0 = x.float().cpu().numpy().astype(np.float64)
+    derr = H.rel_l2(y - x0, ref - x0)
+    print(cfg.name, "rel L2", err, "update rel L2", derr)
+    assert err <= 2e-2 and derr <= 5e-2
+    st.close()
+
+
+@pytest.mark.parametrize("k", [0, 2, 5, 6])
+@pytest.mark.parametrize("steps", [1, 3])
+def test_schedule_log_and_slots(k, steps):
+    cfg = SMALL_DIT
+    st = H.make_stack(cfg)
+    st.attach()
+    st.set_resident(k)
+    for s in range(steps):
+        run(st, cfg, s)
+    log = st.log()
+    assert log == osched.schedule(cfg.n_blocks, k, steps)
+    stats = st.stats()
+    assert stats["stagings"] == (0 if k == cfg.n_blocks else 1 + steps * (cfg.n_blocks - k))
+    # both slots hold the bytes of the block last staged into them
+    for s in (0, 1):
+        if stats["slot_block"][s] >= 0:
+            assert st.verify_slot(s)
+    if k < cfg.n_blocks:
+        # the tail prefetch re-staged the first streamed block
+        last_stage = [e for e in log if e[0] == "stage"][-1]
+        assert last_stage[1] == k
+    st.close()
+
+
+def test_verify_slot_detects_wrong_block():
+    cfg = SMALL_DIT
+    st = H.make_stack(cfg)
+    st.attach()
+    run(st, cfg)
+    s = st.stats()["slot_block"]
+    other = (s[0] + 1) % cfg.n_blocks
+    assert not st.verify_slot(0, other)
+    assert st.verify_slot(0, s[0])
+    st.close()
+
+
+def test_residency_invariance_bit_exact():
+    cfg = SMALL_DIT
+    outs = []
+    for k in (0, 2, 4, 6):
+        st = H.make_stack(cfg)
+        st.attach()
+        st.set_resident(k)
+        outs.append(run(st, cfg)[3].cpu())
+        st.close()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
+def test_gather_staging_and_registered_memory_bit_exact():
+    cfg = SMALL_VID
+    outs = []
+    for staging, mode in ((dlo.STAGE_MEMCPY, "pinned"), (dlo.STAGE_GATHER, "pinned"),
+                          (dlo.STAGE_MEMCPY, "register"), (dlo.STAGE_GATHER, "register")):
+        st = H.make_stack(cfg, staging=staging, host_mode=mode)
+        st.attach()
+        if mode == "register":
+            assert st.stats()["registered_ranges"] >= 1
+        outs.append(run(st, cfg)[3].cpu())
+        for s in (0, 1):
+            assert st.verify_slot(s)
+        st.close()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
+def test_steps_chain_and_restage():
+    cfg = SMALL_DIT
+    st = H.make_stack(cfg)
+    st.attach()
+    x, cond, ctx = H.device_inputs(cfg, 0)
+    blocks = H.oracle_blocks(cfg)
+    for s in range(3):
+        cond = torch.from_numpy(synth.condition(cfg, s)).to(torch.bfloat16).cuda()
+        out = st.forward(x, cond, ctx)
+        torch.cuda.synchronize()
+        ref = H.oracle_forward(cfg, x, cond, ctx, blocks)
+        assert H.rel_l2(out.float().cpu().numpy(), ref) <= 2e-2
+        x = out
+    st.wait()
+    st.close()
+
+
+def test_forward_host_matches_device_forward():
+    cfg = SMALL_VID
+    st = H.make_stack(cfg)
+    st.attach()
+    x, cond, ctx, out = run(st, cfg)
+    xh = x.cpu().view(torch.int16).numpy().copy()
+    ch = cond.cpu().numpy().copy()
+    th = ctx.cpu().view(torch.int16).numpy().copy()
+    oh = np.empty_like(xh)
+    st.forward_host(xh, ch, th, oh)
+    np.testing.assert_array_equal(oh, out.cpu().view(torch.int16).numpy())
+    st.close()
+
+
+def test_registration_rollback_and_retry():
+    cfg = SMALL_DIT
+    st = H.make_stack(cfg, host_mode="register")
+    # blocks are page-aligned and adjacent -> one merged range; force two
+    # failures at the first register call, then retry succeeds
+    dlo.dlo_debug_fail_register(1)
+    with pytest.raises(dlo.DloError) as e:
+        st.attach()
+    assert e.value.status == dlo.EREGISTER
+    assert st.stats()["registered_ranges"] == 0
+    dlo.dlo_debug_fail_register(0)
+    st.attach()
+    assert st.stats()["registered_ranges"] == 1
+    run(st, cfg)
+    st.close()
+
+
+def test_registration_budget_checked_before_mutation():
+    cfg = SMALL_DIT
+    st = H.make_stack(cfg, host_mode="register", register_budget_bytes=4096)
+    with pytest.raises(dlo.DloError) as e:
+        st.attach()
+    assert e.value.status == dlo.EREGISTER and "budget" in str(e.value)
+    assert st.stats()["registered_ranges"] == 0
+    st.close()
+
+
+def test_lifecycle_errors():
+    cfg = SMALL_DIT
+    st = H.make_stack(cfg)
+    x, cond, ctx = H.device_inputs(cfg)
+    with pytest.raises(dlo.DloError) as e:
+        st.forward(x, cond, ctx)
+    assert e.value.status == dlo.ESTATE
+    st.attach()
+    with pytest.raises(dlo.DloError) as e:
+        st.attach()
+    assert e.value.status == dlo.ESTATE
+    with pytest.raises(dlo.DloError) as e:
+        dlo.dlo_set_resident(st.ctx, [0] * 7)
+    assert e.value.status == dlo.EINVAL
+    st.set_resident(1)
+    with pytest.raises(dlo.DloError) as e:
+        st.set_resident(1)
+    assert e.value.status == dlo.ESTATE
+    xb = torch.zeros((cfg.batch, cfg.tokens + 1, cfg.hidden), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(dlo.DloError) as e:
+        st.forward(xb, cond, ctx)
+    assert e.value.status == dlo.EINVAL
+    run(st, cfg)
+    assert st.close() == 0
