@@ -182,12 +182,12 @@ def video_modulation(cfg: StackConfig, step: int = 0) -> np.ndarray:
             * np.float32(0.1))
 
 
-def timesteps(cfg: StackConfig) -> np.ndarray:
-    """Per-step timesteps: t = 500 for a single-step stack, else U[0, 1000) seeded."""
-    if cfg.steps == 1:
-        return np.full((1, cfg.batch), 500.0, dtype=np.float64)
-    g = _rng(cfg.seed, 4)
-    return g.uniform(0.0, 1000.0, size=(cfg.steps, cfg.batch))
+def timesteps(cfg: StackConfig, step: int = 0) -> np.ndarray:
+    """Timesteps [B] of one denoising step: t = 500 for a single-step stack,
+    else U[0, 1000) seeded per step."""
+    if cfg.steps == 1 and step == 0:
+        return np.full((cfg.batch,), 500.0, dtype=np.float64)
+    return _rng(cfg.seed, 4, step).uniform(0.0, 1000.0, size=(cfg.batch,))
 
 
 def sinusoidal(t: np.ndarray, dim: int) -> np.ndarray:
@@ -206,7 +206,7 @@ def timestep_condition(cfg: StackConfig, step: int = 0) -> np.ndarray:
     timestep embedder (sinusoidal 256 -> Linear -> SiLU -> Linear, weights
     N(0, 0.02), seed 1) that is input preparation, not part of the stack.
     """
-    t = timesteps(cfg)[step]
+    t = timesteps(cfg, step)
     f = sinusoidal(t, 256)
     if cfg.cond_dim == 256:
         return round_bf16(f.astype(np.float32))

@@ -48,10 +48,12 @@ def test_small_stacks_match_oracle(cfg):
     y = out.float().cpu().numpy()
     err = H.rel_l2(y, ref)
     # the residual dominates x; also bound the error of the stack's update
+    # y - x, allowing for the bf16 rounding of the output itself
     x0 = x.float().cpu().numpy().astype(np.float64)
     derr = H.rel_l2(y - x0, ref - x0)
-    print(cfg.name, "rel L2", err, "update rel L2", derr)
-    assert err <= 2e-2 and derr <= 5e-2
+    rounding = H.rel_l2(synth.round_bf16(ref.astype(np.float32)) - x0, ref - x0)
+    print(cfg.name, "rel L2", err, "update rel L2", derr, "of which output rounding", rounding)
+    assert err <= 2e-2 and derr <= 2e-2 + 2 * rounding
     st.close()
 
 
