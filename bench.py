@@ -1,0 +1,427 @@
+"""Benchmark: denoising steps/s of the streamed DiT-XL-like block stack on GB300.
+
+One step = one forward of the 28-block stack (hidden 1152, 16 heads, MLP 4608,
+batch 2, 1024 tokens), every block streamed from pinned host memory through
+the two device slots, the next step's input being this step's output.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--staging memcpy|gather] [--resident k]
+                    [--host pinned|register] [--no-cpu-baseline]
+
+Prints ONE JSON line (rank 0).  With N > 1 (torchrun) every rank runs an
+independent replica (the path has no exchange step) and `value` is the sum of
+the steps all ranks completed over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "denoise steps/sec of streamed DiT stack on 1 GB300; % of max(compute,H2D) roofline"
+UNIT = "steps/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default=synth.CFG_DITXL.name, choices=list(synth.CONFIGS))
+    p.add_argument("--staging", default="memcpy", choices=["memcpy", "gather"])
+    p.add_argument("--resident", type=int, default=0)
+    p.add_argument("--host", default="pinned", choices=["pinned", "register"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------- peaks / clocks
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.device = device
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = [l.strip().split(", ") for l in self.tmp.read().splitlines() if l.strip()]
+        self.tmp.close()
+        os.unlink(self.tmp.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 8:
+                continue
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+def oracle_block_seconds(cfg, budget_s: float, max_blocks: int | None = None):
+    """Time the CPU oracle (float64 numpy, as it stands) on blocks of the workload."""
+    from oracle import dit
+    x = synth.activations(cfg).astype(np.float64)
+    cond = synth.condition(cfg).astype(np.float64)
+    ctx = synth.text_context(cfg).astype(np.float64) if cfg.kind == synth.KIND_VIDEO else None
+    times = []
+    t_start = time.perf_counter()
+    i = 0
+    limit = cfg.n_blocks if max_blocks is None else max_blocks
+    while i < limit:
+        P = dit.prepare_block(synth.block_params(cfg, i), fp8_linears=cfg.wdtype == synth.W_E4M3)
+        t0 = time.perf_counter()
+        x = dit.block_forward(cfg.kind, x, cond, ctx, P, cfg.heads)
+        times.append(time.perf_counter() - t0)
+        i += 1
+        if time.perf_counter() - t_start > budget_s:
+            break
+    return times
+
+
+def cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, cfg, rank: int, world: int):
+    if rank != 0:
+        return
+    # each reference "step": one block of the stack's step on the host cores,
+    # the steps/s figure extrapolated to the whole stack (n_blocks blocks)
+    if args.warmup:
+        oracle_block_seconds(cfg, 0.0, max_blocks=1)
+    times = []
+    for s in range(args.steps):
+        times += oracle_block_seconds(cfg, 0.0, max_blocks=1)
+    per_block = statistics.mean(times)
+    value = 1.0 / (per_block * cfg.n_blocks)
+    sample = f"1 of {cfg.n_blocks} blocks per step, float64 numpy oracle, extrapolated x{cfg.n_blocks}"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": cfg.name, "parallelism": "replicas"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def traffic_record(kernel_class: str):
+    """ncu DRAM bytes per launch of the dominant kernel, if the committed
+    record was taken on the current source of that kernel."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    r = rec.get(kernel_class)
+    if not r:
+        return None
+    src = os.path.join(ROOT, "layerwise_weight_offload_slot_gb300", "csrc", r["source"])
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if h != r.get("source_sha"):
+        return None
+    return r
+
+
+def run_ours(args, cfg, rank: int, world: int, local_rank: int):
+    import torch
+    import layerwise_weight_offload_slot_gb300 as dlo
+    from layerwise_weight_offload_slot_gb300.stack import OffloadStack
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks = measured_peaks()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    staging = dlo.STAGE_MEMCPY if args.staging == "memcpy" else dlo.STAGE_GATHER
+    st = OffloadStack(block_kind=cfg.kind, n_blocks=cfg.n_blocks, hidden=cfg.hidden,
+                      heads=cfg.heads, head_dim=cfg.head_dim, ffn=cfg.ffn, cond_dim=cfg.cond_dim,
+                      text_dim=cfg.text_dim, max_batch=cfg.batch, max_tokens=cfg.tokens,
+                      max_text_tokens=cfg.text_tokens, wdtype=cfg.wdtype, staging=staging,
+                      host_mode=args.host, device=local_rank)
+    st.pack_all(lambda i: synth.block_params(cfg, i))
+    st.attach()
+    st.set_resident(args.resident)
+    streamed_bytes = (cfg.n_blocks - args.resident) * st.block_bytes
+
+    # link peak: best pinned 1 GiB host->device copy (copy engine), this run
+    hbuf = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    dbuf = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    link = 0.0
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dbuf.copy_(hbuf, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        link = max(link, (1 << 30) / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    del hbuf, dbuf
+
+    steps_total = args.warmup + args.steps
+    x0 = torch.from_numpy(synth.activations(cfg)).to(torch.bfloat16).to(dev)
+    conds, ctxs = [], []
+    for s in range(max(steps_total, 1)):
+        c = synth.condition(cfg, s % max(cfg.steps, 1))
+        conds.append(torch.from_numpy(c).to(torch.bfloat16 if cfg.kind == synth.KIND_DIT
+                                            else torch.float32).to(dev))
+        ctxs.append(torch.from_numpy(synth.text_context(cfg)).to(torch.bfloat16).to(dev)
+                    if cfg.kind == synth.KIND_VIDEO else None)
+    xa = x0.clone()
+    xb = torch.empty_like(x0)
+    cs = st.compute_stream
+
+    def step(i):
+        nonlocal xa, xb
+        st.forward(xa, conds[i], ctxs[i], out=xb)
+        xa, xb = xb, xa
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    st.wait()
+
+    # ---------------- timed region
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = st.stats()["kernel_launches"]
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(cs)
+    for i in range(args.steps):
+        step(args.warmup + i)
+    ev1.record(cs)
+    torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    st.wait()
+    launches = st.stats()["kernel_launches"] - launches0
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * args.steps / (ms * 1e-3)
+
+    # ---------------- overlap pass (events per streamed execution)
+    st.set_timing(1)
+    s0 = st.stats()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    torch.cuda.synchronize()
+    st.wait()
+    s1 = st.stats()
+    st.set_timing(0)
+    n_exec = s1["timed_execs"] - s0["timed_execs"]
+    copy_ms = s1["copy_ms"] - s0["copy_ms"]
+    exposed = s1["exposed_wait_ms"] - s0["exposed_wait_ms"]
+    overlap = {"fraction": (1.0 - exposed / copy_ms) if copy_ms > 0 else None,
+               "copy_ms_per_step": copy_ms / args.steps,
+               "exposed_wait_ms_per_step": exposed / args.steps,
+               "compute_ms_per_step": (s1["compute_ms"] - s0["compute_ms"]) / args.steps,
+               "h2d_gbs": (st.block_bytes * n_exec) / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else None,
+               "timed_execs": n_exec}
+
+    # ---------------- per-kernel-class pass (event pair around every launch)
+    st.set_timing(2)
+    k0 = st.stats()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    torch.cuda.synchronize()
+    st.wait()
+    k1 = st.stats()
+    st.set_timing(0)
+    cls = {}
+    for j, name in enumerate(dlo.KCLASS_NAMES):
+        n = k1["kclass_launches"][j] - k0["kclass_launches"][j]
+        if n:
+            cls[name] = {"launches": n, "ms": k1["kclass_ms"][j] - k0["kclass_ms"][j],
+                         "flops": k1["kclass_flops"][j] - k0["kclass_flops"][j],
+                         "bytes": k1["kclass_bytes"][j] - k0["kclass_bytes"][j]}
+    dom = max(cls, key=lambda n: cls[n]["ms"])
+    d = cls[dom]
+    tensor_bound = dom in ("gemm_bf16", "gemm_e4m3", "attention")
+    if tensor_bound:
+        achieved = d["flops"] / (d["ms"] * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel timed inside a long step)"}
+    else:
+        achieved = d["bytes"] / (d["ms"] * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "peak_source": f"{peaks['source']} hbm_gbs"}
+    roof["frac"] = achieved / peak
+    tr = traffic_record(dom)
+    roof["traffic"] = tr["bytes_per_launch"] if tr else None
+    roof["kernel"] = dom
+    roof["launches_per_step"] = d["launches"] / args.steps
+    roof["avg_launch_us"] = d["ms"] * 1e3 / d["launches"]
+    flops_step = sum(v["flops"] for v in cls.values()) / args.steps
+    t_compute = flops_step / (peaks["bf16_tflops_sustained"] * 1e12) * 1e3
+    t_link = streamed_bytes / (link * 1e9) * 1e3
+    t_roof = max(t_compute, t_link)
+    step_roof = {"t_roof_ms": t_roof, "compute_ms_at_peak": t_compute, "link_ms_at_peak": t_link,
+                 "link_gbs_measured": link, "streamed_bytes_per_step": streamed_bytes,
+                 "flops_per_step": flops_step, "frac": t_roof / ms_per_step,
+                 "bound": "link" if t_link >= t_compute else "tensor"}
+    kernels = {n: {"launches_per_step": v["launches"] / args.steps,
+                   "ms_per_step": v["ms"] / args.steps} for n, v in cls.items()}
+
+    # ---------------- end to end through the public host-buffer call
+    B, N, D = cfg.batch, cfg.tokens, cfg.hidden
+    hx = torch.empty((B, N, D), dtype=torch.bfloat16).pin_memory()
+    hx.copy_(x0.cpu())
+    hout = torch.empty_like(hx).pin_memory()
+    hconds = [c.cpu().pin_memory() for c in conds]
+    hctxs = [c.cpu().pin_memory() if c is not None else None for c in ctxs]
+    xin = hx.view(torch.int16).numpy()
+    xout = hout.view(torch.int16).numpy()
+
+    def host_step(i):
+        nonlocal xin, xout
+        c = hconds[i]
+        cn = c.view(torch.int16).numpy() if c.dtype == torch.bfloat16 else c.numpy()
+        t = hctxs[i].view(torch.int16).numpy() if hctxs[i] is not None else None
+        st.forward_host(xin, cn, t, xout)
+        xin, xout = xout, xin
+
+    for i in range(args.warmup):
+        host_step(i)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        host_step(args.warmup + i)
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = B * N * D * 2 + hconds[0].numel() * hconds[0].element_size() + \
+        (hctxs[0].numel() * 2 if hctxs[0] is not None else 0)
+    e2e = {"value": world * args.steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": B * N * D * 2}
+
+    stats = st.stats()
+    st.close()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        times = oracle_block_seconds(cfg, 15.0)
+        per_block = statistics.mean(times)
+        cpu = {"value": 1.0 / (per_block * cfg.n_blocks), "unit": UNIT, "cores": cores(),
+               "kind": "oracle",
+               "sample": f"{len(times)} of {cfg.n_blocks} blocks of one step (float64 numpy), "
+                         f"{per_block:.2f} s per block, extrapolated to the {cfg.n_blocks}-block step"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations)",
+                "config": {"workload": cfg.name, "blocks": cfg.n_blocks, "hidden": cfg.hidden,
+                           "heads": cfg.heads, "ffn": cfg.ffn, "batch": cfg.batch,
+                           "tokens": cfg.tokens, "resident": args.resident,
+                           "staging": args.staging, "host": args.host,
+                           "parallelism": "replicas" if world > 1 else "single",
+                           "l2": f"inputs larger than L2: {streamed_bytes / 1e9:.2f} GB of weights "
+                                 "streamed from host per step"},
+                "roofline": roof, "step_roofline": step_roof, "overlap": overlap,
+                "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "clocks": clk, "registered_read_only": stats["registered_read_only"]}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus else 1)))
+    if "WORLD_SIZE" not in os.environ:
+        world = 1
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = synth.CONFIGS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, cfg, rank, world)
+        return
+    run_ours(args, cfg, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

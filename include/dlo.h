@@ -264,12 +264,30 @@ typedef struct dlo_stats {
     int registered_ranges;               /* host ranges this library registered  */
     int registered_read_only;            /* 1 if they were registered read-only  */
     int device_error;                    /* kernels' error word (0 = none)       */
-    /* With dlo_set_timing(ctx, 1): sums over timed streamed executions, in ms. */
+    /* With dlo_set_timing(ctx, >= 1): sums over timed streamed executions, ms. */
     int timed_execs;
     double copy_ms;                      /* slot copy durations                  */
     double compute_ms;                   /* block compute durations              */
     double exposed_wait_ms;              /* compute stream idle waiting on copies */
+    /* With dlo_set_timing(ctx, 2): per kernel class (DLO_K_*), CUDA-event time
+     * of each launch on its own stream, launches, and the algorithmic work of
+     * those launches: 2*M*N*K per GEMM, 4*B*H*nq*nk*hd per attention, bytes
+     * read + written once per element for the bandwidth-bound kernels. */
+    double kclass_ms[8];
+    double kclass_flops[8];
+    double kclass_bytes[8];
+    unsigned long long kclass_launches[8];
 } dlo_stats;
+
+/* kernel classes of dlo_stats.kclass_* */
+#define DLO_K_GEMM_BF16  0
+#define DLO_K_GEMM_E4M3  1
+#define DLO_K_ATTENTION  2
+#define DLO_K_LAYERNORM  3
+#define DLO_K_RMSNORM    4
+#define DLO_K_MODULATION 5   /* adaLN GEMV or modulation-table add            */
+#define DLO_K_CONVERT    6   /* bf16 <-> fp32 of the carried hidden state      */
+#define DLO_K_GATHER     7   /* zero-copy slot staging kernel                  */
 
 /* Counters and timing.  Timing sums need the timed work finished (call
  * dlo_wait first); they are read from CUDA events. */
@@ -282,8 +300,9 @@ dlo_status dlo_get_stats(dlo_ctx* ctx, dlo_stats* out);
 dlo_status dlo_get_log(dlo_ctx* ctx, int* kind, int* block, int* slot, int cap, int* count);
 dlo_status dlo_reset_log(dlo_ctx* ctx);
 
-/* Per-execution CUDA-event timing on (1) or off (0, default); it records four
- * events per streamed execution. */
+/* CUDA-event timing: 0 off (default); 1 five events per streamed execution
+ * (copy, wait and compute intervals); 2 also an event pair around every
+ * kernel launch (per-class stats).  Timing adds event records to the streams. */
 dlo_status dlo_set_timing(dlo_ctx* ctx, int on);
 
 /* Debug: wait for the copy that last wrote `slot`, copy the slot back and

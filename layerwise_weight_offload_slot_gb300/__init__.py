@@ -64,14 +64,20 @@ class dlo_stats(ctypes.Structure):
                 ("slot_block", ctypes.c_int * 2), ("registered_ranges", ctypes.c_int),
                 ("registered_read_only", ctypes.c_int), ("device_error", ctypes.c_int),
                 ("timed_execs", ctypes.c_int), ("copy_ms", ctypes.c_double),
-                ("compute_ms", ctypes.c_double), ("exposed_wait_ms", ctypes.c_double)]
+                ("compute_ms", ctypes.c_double), ("exposed_wait_ms", ctypes.c_double),
+                ("kclass_ms", ctypes.c_double * 8), ("kclass_flops", ctypes.c_double * 8),
+                ("kclass_bytes", ctypes.c_double * 8), ("kclass_launches", ctypes.c_ulonglong * 8)]
 
     def as_dict(self) -> dict:
         d = {}
         for name, _ in self._fields_:
             v = getattr(self, name)
-            d[name] = list(v) if name == "slot_block" else v
+            d[name] = list(v) if isinstance(v, ctypes.Array) else v
         return d
+
+
+KCLASS_NAMES = ("gemm_bf16", "gemm_e4m3", "attention", "layernorm", "rmsnorm", "modulation",
+                "convert", "gather")
 
 
 _vp, _sz, _int, _uint, _f32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint, ctypes.c_float
@@ -251,8 +257,8 @@ def dlo_reset_log(ctx: int) -> None:
     _check(_c["dlo_reset_log"](ctx), ctx)
 
 
-def dlo_set_timing(ctx: int, on: bool) -> None:
-    _check(_c["dlo_set_timing"](ctx, 1 if on else 0), ctx)
+def dlo_set_timing(ctx: int, level: int) -> None:
+    _check(_c["dlo_set_timing"](ctx, int(level)), ctx)
 
 
 def dlo_verify_slot(ctx: int, slot: int, block: int = -1) -> int:

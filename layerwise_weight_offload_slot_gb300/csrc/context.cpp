@@ -36,6 +36,12 @@ struct TimedExec {
     cudaEvent_t copy0, copy1, wait0, comp0, comp1;
 };
 
+struct TimedKernel {
+    int cls;
+    cudaEvent_t a, b;
+    double flops, bytes;
+};
+
 struct Offsets {
     // DiT
     size_t ada_w, ada_b, qkv_w, qkv_b, proj_w, proj_b, fc1_w, fc1_b, fc2_w, fc2_b;
@@ -79,8 +85,9 @@ struct dlo_ctx {
     dlo_stats st{};
     std::vector<int> log_kind, log_block, log_slot;
     size_t log_total = 0;
-    bool timing = false;
+    int timing = 0;
     std::vector<TimedExec> timed_pending;
+    std::vector<TimedKernel> kernels_pending;
     std::vector<cudaEvent_t> ev_pool;
     std::string err;
 
@@ -105,6 +112,18 @@ struct dlo_ctx {
         }
     }
     int* err_word() { return reinterpret_cast<int*>(wsp + ws.err); }
+    // Launch through f(); with timing level 2 bracket it with events on `s`
+    // and remember its class and algorithmic work.
+    template <class Fn>
+    cudaError_t timed(int cls, double flops, double bytes, cudaStream_t s, Fn f) {
+        if (timing < 2) return f();
+        TimedKernel t{cls, get_event(), get_event(), flops, bytes};
+        cudaError_t e = cudaEventRecord(t.a, s);
+        if (e == cudaSuccess) e = f();
+        if (e == cudaSuccess) e = cudaEventRecord(t.b, s);
+        kernels_pending.push_back(t);
+        return e;
+    }
     cudaEvent_t get_event() {
         if (!ev_pool.empty()) {
             cudaEvent_t e = ev_pool.back();
@@ -190,7 +209,9 @@ bool stream_wait(cudaStream_t s, int timeout_ms, cudaError_t* e) {
 dlo_status stage(dlo_ctx* c, int blk, int s) {
     cudaError_t e;
     if (c->d.staging == DLO_STAGE_GATHER) {
-        e = launch_gather(c->slot[s], c->host_dev[blk], c->block_bytes, c->xs, &c->st.kernel_launches);
+        e = c->timed(DLO_K_GATHER, 0.0, 2.0 * c->block_bytes, c->xs, [&] {
+            return launch_gather(c->slot[s], c->host_dev[blk], c->block_bytes, c->xs, &c->st.kernel_launches);
+        });
     } else {
         e = cudaMemcpyAsync(c->slot[s], c->host[blk], c->block_bytes, cudaMemcpyHostToDevice, c->xs);
     }
@@ -236,12 +257,14 @@ dlo_status run_block(dlo_ctx* c, const uint8_t* W, int B, int N, int L, const vo
     unsigned long long* nl = &c->st.kernel_launches;
     cudaStream_t s = c->cs;
     const int D6 = 6 * D;
+    const bool e4m3 = d.wdtype == DLO_W_E4M3;
+    const int wsize = e4m3 ? 1 : 2;
     auto gemm = [&](const void* A, size_t woff, size_t boff, int M, int Nn, int K, int epi,
                     void* out, int ldo, const float* gate, int rpb, int scale_idx, int seg) {
         GemmParams p;
         p.A = A;
         p.W = W + woff;
-        p.w_dtype = d.wdtype == DLO_W_E4M3 ? DLO_DT_E4M3 : DLO_DT_BF16;
+        p.w_dtype = e4m3 ? DLO_DT_E4M3 : DLO_DT_BF16;
         p.scales = o.has_scales ? reinterpret_cast<const float*>(W + o.scales) + scale_idx : nullptr;
         p.scale_seg = seg;
         p.bias = W + boff;
@@ -255,43 +278,66 @@ dlo_status run_block(dlo_ctx* c, const uint8_t* W, int B, int N, int L, const vo
         p.gate_ld = D6;
         p.rows_per_batch = rpb;
         p.err = c->err_word();
-        return launch_gemm(p, s, nl);
+        const double flops = 2.0 * M * Nn * K;
+        const double bytes = 1.0 * M * K * 2 + 1.0 * Nn * K * wsize +
+                             1.0 * M * Nn * (epi == DLO_EPI_RESIDUAL ? 8 : 2);
+        return c->timed(e4m3 ? DLO_K_GEMM_E4M3 : DLO_K_GEMM_BF16, flops, bytes, s,
+                        [&] { return launch_gemm(p, s, nl); });
     };
+    auto attn = [&](const void* q, const void* k, const void* v, void* out, int nq, int nk, int ldq, int ldk,
+                    int ldv) {
+        const double flops = 4.0 * B * H * nq * static_cast<double>(nk) * hd;
+        const double bytes = 2.0 * B * (2.0 * nq + 2.0 * nk) * D;
+        return c->timed(DLO_K_ATTENTION, flops, bytes, s, [&] {
+            return launch_attention(q, k, v, out, B, H, hd, nq, nk, ldq, ldk, ldv, D, s, nl);
+        });
+    };
+    auto ln = [&](const float* shift, const float* scale, const void* lw, const void* lb) {
+        return c->timed(DLO_K_LAYERNORM, 0.0, 6.0 * BN * D, s, [&] {
+            return launch_layernorm(x, BN, D, N, shift, scale, D6, lw, lb, d.eps, h, s, nl);
+        });
+    };
+    char* bigc = static_cast<char*>(big);
     if (d.block_kind == DLO_BLOCK_DIT) {
-        LCHECK(launch_adaln(cond, B, d.cond_dim, W + o.ada_w, W + o.ada_b, D6, m, s, nl), "adaLN");
-        LCHECK(launch_layernorm(x, BN, D, N, m, m + D, D6, nullptr, nullptr, d.eps, h, s, nl), "LN1");
+        LCHECK(c->timed(DLO_K_MODULATION, 2.0 * B * D6 * d.cond_dim, 2.0 * D6 * d.cond_dim, s,
+                        [&] { return launch_adaln(cond, B, d.cond_dim, W + o.ada_w, W + o.ada_b, D6, m, s, nl); }),
+               "adaLN");
+        LCHECK(ln(m, m + D, nullptr, nullptr), "LN1");
         LCHECK(gemm(h, o.qkv_w, o.qkv_b, BN, 3 * D, D, DLO_EPI_BIAS, big, 3 * D, nullptr, N, 0, 3 * D), "qkv");
-        LCHECK(launch_attention(big, static_cast<uint8_t*>(big) + 2 * D, static_cast<uint8_t*>(big) + 4 * D, a, B,
-                                H, hd, N, N, 3 * D, 3 * D, 3 * D, D, s, nl),
-               "attention");
+        LCHECK(attn(big, bigc + 2 * D, bigc + 4 * D, a, N, N, 3 * D, 3 * D, 3 * D), "attention");
         LCHECK(gemm(a, o.proj_w, o.proj_b, BN, D, D, DLO_EPI_RESIDUAL, x, D, m + 2 * D, N, 0, D), "proj");
-        LCHECK(launch_layernorm(x, BN, D, N, m + 3 * D, m + 4 * D, D6, nullptr, nullptr, d.eps, h, s, nl), "LN2");
+        LCHECK(ln(m + 3 * D, m + 4 * D, nullptr, nullptr), "LN2");
         LCHECK(gemm(h, o.fc1_w, o.fc1_b, BN, F, D, DLO_EPI_GELU, big, F, nullptr, N, 0, F), "fc1");
         LCHECK(gemm(big, o.fc2_w, o.fc2_b, BN, D, F, DLO_EPI_RESIDUAL, x, D, m + 5 * D, N, 0, D), "fc2");
         return DLO_OK;
     }
     void* q2 = w + c->ws.q2;
     void* kv2 = w + c->ws.kv2;
+    char* kv2c = static_cast<char*>(kv2);
     const int Dt = d.text_dim;
-    LCHECK(launch_mod_add(static_cast<const float*>(cond), W + o.mod, B, D6, m, s, nl), "modulation");
-    LCHECK(launch_layernorm(x, BN, D, N, m, m + D, D6, nullptr, nullptr, d.eps, h, s, nl), "LN1");
+    LCHECK(c->timed(DLO_K_MODULATION, 0.0, 10.0 * B * D6, s,
+                    [&] { return launch_mod_add(static_cast<const float*>(cond), W + o.mod, B, D6, m, s, nl); }),
+           "modulation");
+    LCHECK(ln(m, m + D, nullptr, nullptr), "LN1");
     LCHECK(gemm(h, o.sq_w, o.sq_b, BN, 3 * D, D, DLO_EPI_BIAS, big, 3 * D, nullptr, N, 0, D), "self qkv");
-    LCHECK(launch_rmsnorm2(big, BN, D, 3 * D, 0, W + o.snq, D, W + o.snk, d.eps, s, nl), "self q/k norm");
-    LCHECK(launch_attention(big, static_cast<uint8_t*>(big) + 2 * D, static_cast<uint8_t*>(big) + 4 * D, a, B, H,
-                            hd, N, N, 3 * D, 3 * D, 3 * D, D, s, nl),
-           "self attention");
+    LCHECK(c->timed(DLO_K_RMSNORM, 0.0, 8.0 * BN * D, s,
+                    [&] { return launch_rmsnorm2(big, BN, D, 3 * D, 0, W + o.snq, D, W + o.snk, d.eps, s, nl); }),
+           "self q/k norm");
+    LCHECK(attn(big, bigc + 2 * D, bigc + 4 * D, a, N, N, 3 * D, 3 * D, 3 * D), "self attention");
     LCHECK(gemm(a, o.so_w, o.so_b, BN, D, D, DLO_EPI_RESIDUAL, x, D, m + 2 * D, N, 3, D), "self o");
-    LCHECK(launch_layernorm(x, BN, D, N, nullptr, nullptr, 0, W + o.ncw, W + o.ncb, d.eps, h, s, nl), "LN cross");
+    LCHECK(ln(nullptr, nullptr, W + o.ncw, W + o.ncb), "LN cross");
     LCHECK(gemm(h, o.cq_w, o.cq_b, BN, D, D, DLO_EPI_BIAS, q2, D, nullptr, N, 4, D), "cross q");
     LCHECK(gemm(ctx_tokens, o.ck_w, o.ck_b, B * L, 2 * D, Dt, DLO_EPI_BIAS, kv2, 2 * D, nullptr, L, 5, D),
            "cross kv");
-    LCHECK(launch_rmsnorm(q2, BN, D, D, 0, W + o.cnq, d.eps, s, nl), "cross q norm");
-    LCHECK(launch_rmsnorm(kv2, B * L, D, 2 * D, 0, W + o.cnk, d.eps, s, nl), "cross k norm");
-    LCHECK(launch_attention(q2, kv2, static_cast<uint8_t*>(kv2) + 2 * D, a, B, H, hd, N, L, D, 2 * D, 2 * D, D,
-                            s, nl),
-           "cross attention");
+    LCHECK(c->timed(DLO_K_RMSNORM, 0.0, 4.0 * BN * D, s,
+                    [&] { return launch_rmsnorm(q2, BN, D, D, 0, W + o.cnq, d.eps, s, nl); }),
+           "cross q norm");
+    LCHECK(c->timed(DLO_K_RMSNORM, 0.0, 4.0 * B * L * D, s,
+                    [&] { return launch_rmsnorm(kv2, B * L, D, 2 * D, 0, W + o.cnk, d.eps, s, nl); }),
+           "cross k norm");
+    LCHECK(attn(q2, kv2, kv2c + 2 * D, a, N, L, D, 2 * D, 2 * D), "cross attention");
     LCHECK(gemm(a, o.co_w, o.co_b, BN, D, D, DLO_EPI_RESIDUAL, x, D, nullptr, N, 7, D), "cross o");
-    LCHECK(launch_layernorm(x, BN, D, N, m + 3 * D, m + 4 * D, D6, nullptr, nullptr, d.eps, h, s, nl), "LN2");
+    LCHECK(ln(m + 3 * D, m + 4 * D, nullptr, nullptr), "LN2");
     LCHECK(gemm(h, o.fc1_w, o.fc1_b, BN, F, D, DLO_EPI_GELU, big, F, nullptr, N, 8, F), "fc1");
     LCHECK(gemm(big, o.fc2_w, o.fc2_b, BN, D, F, DLO_EPI_RESIDUAL, x, D, m + 5 * D, N, 9, D), "fc2");
     return DLO_OK;
@@ -315,6 +361,22 @@ void collect_timing(dlo_ctx* c) {
         for (cudaEvent_t e : {t.copy0, t.copy1, t.wait0, t.comp0, t.comp1}) c->ev_pool.push_back(e);
     }
     c->timed_pending.swap(keep);
+    std::vector<TimedKernel> kk;
+    for (auto& t : c->kernels_pending) {
+        float ms = 0;
+        if (cudaEventElapsedTime(&ms, t.a, t.b) != cudaSuccess) {
+            cudaGetLastError();
+            kk.push_back(t);
+            continue;
+        }
+        c->st.kclass_ms[t.cls] += ms;
+        c->st.kclass_flops[t.cls] += t.flops;
+        c->st.kclass_bytes[t.cls] += t.bytes;
+        ++c->st.kclass_launches[t.cls];
+        c->ev_pool.push_back(t.a);
+        c->ev_pool.push_back(t.b);
+    }
+    c->kernels_pending.swap(kk);
 }
 
 dlo_status check_device_error(dlo_ctx* c) {
@@ -564,7 +626,9 @@ extern "C" dlo_status dlo_forward(dlo_ctx* c, const void* x_in, const void* cond
     const int n = d.n_blocks, k = c->k;
     const size_t nx = static_cast<size_t>(batch) * tokens * d.hidden;
     float* x = reinterpret_cast<float*>(c->wsp + c->ws.x);
-    LCHECK(launch_bf16_to_f32(x_in, x, nx, c->cs, &c->st.kernel_launches), "input conversion");
+    LCHECK(c->timed(DLO_K_CONVERT, 0.0, 6.0 * nx, c->cs,
+                    [&] { return launch_bf16_to_f32(x_in, x, nx, c->cs, &c->st.kernel_launches); }),
+           "input conversion");
     if (c->resident_pending) {
         LCHECK(cudaStreamWaitEvent(c->cs, c->resident_ev, 0), "wait resident");
         c->resident_pending = false;
@@ -605,7 +669,9 @@ extern "C" dlo_status dlo_forward(dlo_ctx* c, const void* x_in, const void* cond
         ++c->exec_counter;
         ++c->st.streamed_execs;
     }
-    LCHECK(launch_f32_to_bf16(x, x_out, nx, c->cs, &c->st.kernel_launches), "output conversion");
+    LCHECK(c->timed(DLO_K_CONVERT, 0.0, 6.0 * nx, c->cs,
+                    [&] { return launch_f32_to_bf16(x, x_out, nx, c->cs, &c->st.kernel_launches); }),
+           "output conversion");
     ++c->st.forwards;
     return DLO_OK;
 }
@@ -676,6 +742,10 @@ extern "C" dlo_status dlo_destroy(dlo_ctx* c) {
     if (c->resident_ev) cudaEventDestroy(c->resident_ev);
     for (auto& t : c->timed_pending)
         for (cudaEvent_t ev : {t.copy0, t.copy1, t.wait0, t.comp0, t.comp1}) cudaEventDestroy(ev);
+    for (auto& t : c->kernels_pending) {
+        cudaEventDestroy(t.a);
+        cudaEventDestroy(t.b);
+    }
     for (cudaEvent_t ev : c->ev_pool) cudaEventDestroy(ev);
     delete c;
     return first;
@@ -716,7 +786,8 @@ extern "C" dlo_status dlo_reset_log(dlo_ctx* c) {
 
 extern "C" dlo_status dlo_set_timing(dlo_ctx* c, int on) {
     if (!c) return DLO_EINVAL;
-    c->timing = on != 0;
+    if (on < 0 || on > 2) return c->fail(DLO_EINVAL, "timing level must be 0, 1 or 2");
+    c->timing = on;
     return DLO_OK;
 }
 
@@ -741,7 +812,6 @@ extern "C" dlo_status dlo_verify_slot(dlo_ctx* c, int slot, int block) {
 
 namespace {
 unsigned long long g_op_launches = 0;
-thread_local std::string g_op_error;
 dlo_status op_result(cudaError_t e) {
     if (e == cudaSuccess) return DLO_OK;
     g_create_error = std::string("kernel launch: ") + cudaGetErrorString(e);

@@ -162,8 +162,8 @@ class OffloadStack:
     def reset_log(self) -> None:
         dlo_reset_log(self.ctx)
 
-    def set_timing(self, on: bool) -> None:
-        dlo_set_timing(self.ctx, on)
+    def set_timing(self, level: int) -> None:
+        dlo_set_timing(self.ctx, level)
 
     def verify_slot(self, slot: int, block: int = -1) -> bool:
         return dlo_verify_slot(self.ctx, slot, block) == OK
