@@ -3,8 +3,7 @@
 // dtype conversions of the carried hidden state, and the zero-copy slot
 // gather that reads mapped host memory with 16-byte loads.
 //
-// One warp per row for the row-wise kernels: a row (<= 5120 fp32 = 20 KB)
-// stays in L1 across the passes, so HBM sees one read of x and one write.
+// One warp per row for the row-wise kernels.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -23,6 +22,10 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ float bf(const __nv_bfloat16 v) { return __bfloat162float(v); }
 
 // out = LN(x) * (1 + scale) + shift | LN(x) * w + b | LN(x)
+// One warp per row; the row (up to 32 * 4 * V4 floats) is read once into
+// registers, mean and variance come from the registers (two passes), so HBM
+// sees one read of x and one write of the bf16 output.
+template <int V4>
 __global__ void __launch_bounds__(256) layernorm_kernel(const float* __restrict__ x, int rows,
                                                         int D, int rpb,
                                                         const float* __restrict__ shift,
@@ -37,26 +40,34 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const float* __restrict_
     if (row >= rows) return;
     const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(row) * D);
     const int n4 = D >> 2;
-    float s = 0.f;
-    for (int i = lane; i < n4; i += 32) {
-        const float4 v = xr[i];
-        s += (v.x + v.y) + (v.z + v.w);
+    float4 v[V4];
+#pragma unroll
+    for (int j = 0; j < V4; ++j) {
+        const int i = lane + 32 * j;
+        v[j] = i < n4 ? xr[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < V4; ++j) s += (v[j].x + v[j].y) + (v[j].z + v[j].w);
     const float mean = warp_sum(s) / static_cast<float>(D);
     float q = 0.f;
-    for (int i = lane; i < n4; i += 32) {
-        const float4 v = xr[i];
-        const float a = v.x - mean, bb = v.y - mean, c = v.z - mean, d = v.w - mean;
-        q += (a * a + bb * bb) + (c * c + d * d);
+#pragma unroll
+    for (int j = 0; j < V4; ++j) {
+        if (lane + 32 * j < n4) {
+            const float a = v[j].x - mean, bb = v[j].y - mean, c = v[j].z - mean, d = v[j].w - mean;
+            q += (a * a + bb * bb) + (c * c + d * d);
+        }
     }
     const float var = warp_sum(q) / static_cast<float>(D);
     const float rstd = rsqrtf(var + eps);
     const int bt = row / rpb;
     uint2* orow = reinterpret_cast<uint2*>(out + static_cast<size_t>(row) * D);
-    for (int i = lane; i < n4; i += 32) {
-        const float4 v = xr[i];
-        float y0 = (v.x - mean) * rstd, y1 = (v.y - mean) * rstd;
-        float y2 = (v.z - mean) * rstd, y3 = (v.w - mean) * rstd;
+#pragma unroll
+    for (int j = 0; j < V4; ++j) {
+        const int i = lane + 32 * j;
+        if (i >= n4) break;
+        float y0 = (v[j].x - mean) * rstd, y1 = (v[j].y - mean) * rstd;
+        float y2 = (v[j].z - mean) * rstd, y3 = (v[j].w - mean) * rstd;
         const int d = i * 4;
         if (scale) {
             const float4 sc = *reinterpret_cast<const float4*>(scale + static_cast<size_t>(bt) * mod_ld + d);
@@ -66,10 +77,16 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const float* __restrict_
             y2 = y2 * (1.f + sc.z) + sh.z;
             y3 = y3 * (1.f + sc.w) + sh.w;
         } else if (w) {
-            y0 = y0 * bf(w[d]) + bf(b[d]);
-            y1 = y1 * bf(w[d + 1]) + bf(b[d + 1]);
-            y2 = y2 * bf(w[d + 2]) + bf(b[d + 2]);
-            y3 = y3 * bf(w[d + 3]) + bf(b[d + 3]);
+            const uint2 wv = *reinterpret_cast<const uint2*>(w + d);
+            const uint2 bv = *reinterpret_cast<const uint2*>(b + d);
+            const float2 w01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv.x));
+            const float2 w23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv.y));
+            const float2 b01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bv.x));
+            const float2 b23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bv.y));
+            y0 = y0 * w01.x + b01.x;
+            y1 = y1 * w01.y + b01.y;
+            y2 = y2 * w23.x + b23.x;
+            y3 = y3 * w23.y + b23.y;
         }
         uint2 o;
         o.x = pack_bf16x2(y0, y1);
@@ -122,50 +139,80 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(__nv_bfloat16* __restrict_
     }
 }
 
-// m[b, n] = sum_i SiLU(c[b, i]) W[n, i] + bias[n]; one warp per output n,
-// W read once with 16-byte loads for all batch rows (B <= 8 per pass).
+// m[b, n] = sum_i SiLU(c[b, i]) W[n, i] + bias[n].
+// SiLU(c) is computed once per CTA into shared memory (fp32, up to 8 batch
+// rows x 1024 columns per pass); each warp owns ADALN_ROWS output rows and
+// issues all of its 16-byte W loads for a column chunk before the FMAs, so
+// enough bytes are in flight to stream W (a third of a DiT block) at HBM rate.
+constexpr int ADALN_ROWS = 2;
+constexpr int ADALN_CCHUNK = 1024;
+constexpr int ADALN_BCHUNK = 8;
+
 __global__ void __launch_bounds__(256) adaln_kernel(const __nv_bfloat16* __restrict__ c, int B,
                                                     int C, const __nv_bfloat16* __restrict__ W,
                                                     const __nv_bfloat16* __restrict__ bias,
                                                     int N, float* __restrict__ m) {
-    const int n = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (n >= N) return;
-    const uint4* wr = reinterpret_cast<const uint4*>(W + static_cast<size_t>(n) * C);
-    const int n8 = C >> 3;
-    for (int b0 = 0; b0 < B; b0 += 8) {
-        float acc[8];
+    __shared__ float sc[ADALN_BCHUNK * ADALN_CCHUNK];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = (blockIdx.x * 8 + warp) * ADALN_ROWS;
+    for (int b0 = 0; b0 < B; b0 += ADALN_BCHUNK) {
+        const int nb = min(ADALN_BCHUNK, B - b0);
+        float acc[ADALN_ROWS][ADALN_BCHUNK];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-        for (int i = lane; i < n8; i += 32) {
-            const uint4 wv = wr[i];
-            const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wv);
-            float wf[8];
+        for (int r = 0; r < ADALN_ROWS; ++r)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 f = __bfloat1622float2(wp[j]);
-                wf[2 * j] = f.x;
-                wf[2 * j + 1] = f.y;
+            for (int j = 0; j < ADALN_BCHUNK; ++j) acc[r][j] = 0.f;
+        for (int c0 = 0; c0 < C; c0 += ADALN_CCHUNK) {
+            const int cn = min(ADALN_CCHUNK, C - c0);
+            __syncthreads();
+            for (int i = threadIdx.x; i < nb * cn; i += blockDim.x) {
+                const int bb = i / cn, cc = i % cn;
+                const float v = __bfloat162float(c[static_cast<size_t>(b0 + bb) * C + c0 + cc]);
+                sc[bb * ADALN_CCHUNK + cc] = v / (1.f + __expf(-v));
+            }
+            __syncthreads();
+            const int n8 = cn >> 3;
+            // up to 4 uint4 per lane per row per chunk (1024 columns)
+            uint4 wv[ADALN_ROWS][4];
+#pragma unroll
+            for (int r = 0; r < ADALN_ROWS; ++r) {
+                const int n = n0 + r;
+                const uint4* wr = reinterpret_cast<const uint4*>(W + static_cast<size_t>(min(n, N - 1)) * C + c0);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int i = lane + 32 * k;
+                    wv[r][k] = (i < n8 && n < N) ? __ldcs(wr + i) : make_uint4(0, 0, 0, 0);
+                }
             }
 #pragma unroll
-            for (int bb = 0; bb < 8; ++bb) {
-                if (b0 + bb < B) {
-                    const uint4 cv = *reinterpret_cast<const uint4*>(c + static_cast<size_t>(b0 + bb) * C + i * 8);
-                    const __nv_bfloat162* cp = reinterpret_cast<const __nv_bfloat162*>(&cv);
+            for (int k = 0; k < 4; ++k) {
+                const int i = lane + 32 * k;
+                if (i >= n8) break;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float2 f = __bfloat1622float2(cp[j]);
-                        const float s0 = f.x / (1.f + __expf(-f.x));
-                        const float s1 = f.y / (1.f + __expf(-f.y));
-                        acc[bb] += s0 * wf[2 * j] + s1 * wf[2 * j + 1];
+                for (int bb = 0; bb < ADALN_BCHUNK; ++bb) {
+                    if (bb >= nb) break;
+                    const float4 s0 = *reinterpret_cast<const float4*>(&sc[bb * ADALN_CCHUNK + i * 8]);
+                    const float4 s1 = *reinterpret_cast<const float4*>(&sc[bb * ADALN_CCHUNK + i * 8 + 4]);
+#pragma unroll
+                    for (int r = 0; r < ADALN_ROWS; ++r) {
+                        const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wv[r][k]);
+                        const float2 w0 = __bfloat1622float2(wp[0]), w1 = __bfloat1622float2(wp[1]);
+                        const float2 w2 = __bfloat1622float2(wp[2]), w3 = __bfloat1622float2(wp[3]);
+                        acc[r][bb] += s0.x * w0.x + s0.y * w0.y + s0.z * w1.x + s0.w * w1.y +
+                                      s1.x * w2.x + s1.y * w2.y + s1.z * w3.x + s1.w * w3.y;
                     }
                 }
             }
         }
 #pragma unroll
-        for (int bb = 0; bb < 8; ++bb) {
-            const float v = warp_sum(acc[bb]);
-            if (lane == 0 && b0 + bb < B) m[static_cast<size_t>(b0 + bb) * N + n] = v + bf(bias[n]);
+        for (int r = 0; r < ADALN_ROWS; ++r) {
+#pragma unroll
+            for (int bb = 0; bb < ADALN_BCHUNK; ++bb) {
+                const float v = warp_sum(acc[r][bb]);
+                const int n = n0 + r;
+                if (lane == 0 && bb < nb && n < N)
+                    m[static_cast<size_t>(b0 + bb) * N + n] = v + __bfloat162float(bias[n]);
+            }
         }
     }
 }
@@ -236,9 +283,23 @@ cudaError_t launch_layernorm(const float* x, int rows, int D, int rpb, const flo
                              const float* scale, int mod_ld, const void* w, const void* b,
                              float eps, void* out, cudaStream_t s, unsigned long long* launches) {
     if (rows <= 0) return cudaSuccess;
-    layernorm_kernel<<<blocks_for(static_cast<size_t>(rows) * 32, 256), 256, 0, s>>>(
-        x, rows, D, rpb, shift, scale, mod_ld, static_cast<const __nv_bfloat16*>(w),
-        static_cast<const __nv_bfloat16*>(b), eps, static_cast<__nv_bfloat16*>(out));
+    const unsigned g = blocks_for(static_cast<size_t>(rows) * 32, 256);
+    const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w);
+    const __nv_bfloat16* bb = static_cast<const __nv_bfloat16*>(b);
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+    const int v4 = (D / 4 + 31) / 32;   // float4 per lane
+#define DLO_LN(V)                                                                          \
+    layernorm_kernel<V><<<g, 256, 0, s>>>(x, rows, D, rpb, shift, scale, mod_ld, wb, bb, eps, o)
+    if (v4 <= 2) DLO_LN(2);
+    else if (v4 <= 4) DLO_LN(4);
+    else if (v4 <= 8) DLO_LN(8);
+    else if (v4 <= 10) DLO_LN(10);
+    else if (v4 <= 16) DLO_LN(16);
+    else if (v4 <= 24) DLO_LN(24);
+    else if (v4 <= 32) DLO_LN(32);
+    else if (v4 <= 40) DLO_LN(40);
+    else return cudaErrorInvalidValue;
+#undef DLO_LN
     ++*launches;
     return cudaGetLastError();
 }
@@ -267,7 +328,8 @@ cudaError_t launch_rmsnorm2(void* x, int rows, int D, int ld, int col0a, const v
 cudaError_t launch_adaln(const void* c, int B, int C, const void* W, const void* bias, int N,
                          float* m, cudaStream_t s, unsigned long long* launches) {
     if (N <= 0 || B <= 0) return cudaSuccess;
-    adaln_kernel<<<blocks_for(static_cast<size_t>(N) * 32, 256), 256, 0, s>>>(
+    const unsigned g = static_cast<unsigned>((N + 8 * ADALN_ROWS - 1) / (8 * ADALN_ROWS));
+    adaln_kernel<<<g, 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(c), B, C, static_cast<const __nv_bfloat16*>(W),
         static_cast<const __nv_bfloat16*>(bias), N, m);
     ++*launches;
