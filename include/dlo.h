@@ -339,6 +339,27 @@ dlo_status dlo_op_gemm(const void* A, const void* W, int w_dtype, const float* s
                        void* out, int ldo, const float* gate, int gate_ld, int rows_per_batch,
                        int* err, void* stream);
 
+/* dlo_op_gemm for callers that cannot allocate device memory (for example code
+ * running where the CUDA allocator is unavailable or forbidden, such as inside
+ * another framework's memory pool or a host callback).  The pages have no
+ * counterpart; this is an addition of this library.
+ * Same arguments and results as dlo_op_gemm minus `err`: the kernel's scratch
+ * (its device error word) lives in a static device array of at most 256 bytes
+ * that every GPU which loads this library holds until the process exits; this
+ * entry uses 4 bytes of it and clears them before each launch.  It calls no
+ * cudaMalloc, cudaFree or allocating library routine.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the one array, so calls that
+ * overlap on the GPU race on the error word; a bounded wait that runs out
+ * leaves `out` incomplete and is not reported (use dlo_op_gemm with your own
+ * error word when you need that report).  Argument errors return DLO_EINVAL
+ * (message on stderr) before anything is enqueued. */
+dlo_status dlo_op_gemm_noalloc(const void* A, const void* W, int w_dtype, const float* scales,
+                               int scale_seg, const void* bias, int M, int N, int K,
+                               int epilogue, void* out, int ldo, const float* gate, int gate_ld,
+                               int rows_per_batch, void* stream);
+
 /* Multi-head softmax attention, non-causal: O = softmax(Q K^T / sqrt(hd)) V per
  * (batch, head).  Q, K, V, O bf16; row r of batch b of Q starts at
  * Q + (b * nq + r) * ldq, head h at column h * head_dim (same for K, V with nk

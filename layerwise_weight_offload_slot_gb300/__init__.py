@@ -113,6 +113,8 @@ _c = {
     "dlo_debug_fail_register": _decl("dlo_debug_fail_register", None, _int),
     "dlo_op_gemm": _decl("dlo_op_gemm", _int, _vp, _vp, _int, _vp, _int, _vp, _int, _int, _int, _int,
                          _vp, _int, _vp, _int, _int, _vp, _vp),
+    "dlo_op_gemm_noalloc": _decl("dlo_op_gemm_noalloc", _int, _vp, _vp, _int, _vp, _int, _vp, _int, _int,
+                                 _int, _int, _vp, _int, _vp, _int, _int, _vp),
     "dlo_op_attention": _decl("dlo_op_attention", _int, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int,
                               _int, _int, _int, _int, _vp),
     "dlo_op_layernorm": _decl("dlo_op_layernorm", _int, _vp, _int, _int, _int, _vp, _vp, _int, _vp, _vp,
@@ -279,6 +281,14 @@ def dlo_op_gemm(A, W, w_dtype, scales, scale_seg, bias, M, N, K, epilogue, out, 
                 rows_per_batch, err, stream) -> None:
     _check(_c["dlo_op_gemm"](A, W, w_dtype, scales, scale_seg, bias, M, N, K, epilogue, out, ldo,
                              gate, gate_ld, rows_per_batch, err, stream))
+
+
+def dlo_op_gemm_noalloc(A, W, w_dtype, scales, scale_seg, bias, M, N, K, epilogue, out, ldo, gate,
+                        gate_ld, rows_per_batch, stream) -> None:
+    st = _c["dlo_op_gemm_noalloc"](A, W, w_dtype, scales, scale_seg, bias, M, N, K, epilogue, out,
+                                   ldo, gate, gate_ld, rows_per_batch, stream)
+    if st != OK:
+        raise DloError(st, "dlo_op_gemm_noalloc rejected the call (see stderr)")
 
 
 def dlo_op_attention(Q, K, V, O, batch, heads, head_dim, nq, nk, ldq, ldk, ldv, ldo, stream) -> None:
