@@ -1,6 +1,6 @@
 // Y = A W^T on the 5th-generation tensor cores (tcgen05), sm_103a.
 //
-// Persistent kernel, one CTA per SM, 6 warps:
+// Persistent kernel, one CTA per SM, 6 warps (+4 converter warps for E4M3):
 //   warp 0      TMA producer: 128x64 A tile and BNx64 W tile per stage,
 //               128-byte swizzle, into a STAGES-deep shared-memory ring
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16 (M=128,
@@ -10,9 +10,9 @@
 //   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, scale (FP8
 //               per-tensor), + bias, GELU or gate * y + residual, store
 // The two accumulators let the epilogue of tile t overlap the mainloop of
-// tile t+1.  E4M3 weights take the same path after a converter stage (see
-// the _fp8 kernel below): codes are widened to bf16 in shared memory (exact)
-// and the per-tensor scale is applied to the fp32 accumulator.
+// tile t+1.  With E4M3 weights (FP8 = true) TMA loads the raw codes, four
+// more warps widen them to bf16 in the swizzled layout the MMA reads (exact),
+// and the per-tensor scale is applied to the fp32 accumulator in the epilogue.
 //
 // Every mbarrier wait is bounded (2 s); a wait that runs out sets the
 // kernel's error word and a CTA-wide abort flag, after which every role
@@ -141,30 +141,56 @@ __device__ __forceinline__ void epilogue_chunk(const EpiArgs& a, int row, int co
     }
 }
 
-template <int BN, int STAGES>
+// e4m3 -> bf16, four codes at a time, exactly: each code's sign goes to the
+// bf16 sign bit and its 7 exponent/mantissa bits to bf16 bits 4..10, which is
+// the same number scaled by 2^-120 (bf16 subnormals included); one bf16x2
+// multiply by 2^120 restores it.  out0 holds codes 0,1 and out1 codes 2,3.
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t x, uint32_t& out0, uint32_t& out1) {
+    constexpr uint32_t kScale = 0x7B807B80u;   // bf16x2 (2^120, 2^120)
+    uint32_t w0, w1;
+    asm("prmt.b32 %0, %1, 0, 0x4140;" : "=r"(w0) : "r"(x));
+    asm("prmt.b32 %0, %1, 0, 0x4342;" : "=r"(w1) : "r"(x));
+    w0 = ((w0 & 0x00800080u) << 8) | ((w0 & 0x007F007Fu) << 4);
+    w1 = ((w1 & 0x00800080u) << 8) | ((w1 & 0x007F007Fu) << 4);
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out0) : "r"(w0), "r"(kScale));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out1) : "r"(w1), "r"(kScale));
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+constexpr int kConvWarps = 4;
+
+template <int BN, int STAGES, bool FP8>
 struct SmemPlan {
-    static constexpr int B_TILE = BN * BK * 2;
+    static constexpr int B_TILE = BN * BK * 2;            // bf16 operand tile (MMA reads)
+    static constexpr int RAW_TILE = FP8 ? BN * BK : 0;     // e4m3 tile as loaded by TMA
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = STAGES * A_TILE;
-    static constexpr int BAR_OFF = B_OFF + STAGES * B_TILE;
-    // full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
-    static constexpr int TMEM_SLOT_OFF = BAR_OFF + (2 * STAGES + 5) * 8;
+    static constexpr int RAW_OFF = B_OFF + STAGES * B_TILE;
+    static constexpr int BAR_OFF = RAW_OFF + STAGES * RAW_TILE;
+    // full[STAGES], empty[STAGES], conv[STAGES], tfull[2], tempty[2], drain
+    static constexpr int TMEM_SLOT_OFF = BAR_OFF + (3 * STAGES + 5) * 8;
     static constexpr int ABORT_OFF = TMEM_SLOT_OFF + 4;
     static constexpr int BYTES = ABORT_OFF + 4 + 1024;  // + alignment slack
+    static constexpr int THREADS = kThreads + (FP8 ? kConvWarps * 32 : 0);
+    static constexpr uint32_t TX = A_TILE + (FP8 ? RAW_TILE : B_TILE);
 };
 
-template <int BN, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, const EpiArgs args) {
-    using P = SmemPlan<BN, STAGES>;
+template <int BN, int STAGES, bool FP8>
+__global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8>::THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const EpiArgs args) {
+    using P = SmemPlan<BN, STAGES, FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar_full = sbase + P::BAR_OFF;
     const uint32_t bar_empty = bar_full + STAGES * 8;
-    const uint32_t bar_tfull = bar_empty + STAGES * 8;
+    const uint32_t bar_conv = bar_empty + STAGES * 8;
+    const uint32_t bar_tfull = bar_conv + STAGES * 8;
     const uint32_t bar_tempty = bar_tfull + 2 * 8;
     const uint32_t bar_drain = bar_tempty + 2 * 8;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + P::TMEM_SLOT_OFF);
@@ -177,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + s * 8, 1);
             mbar_init(bar_empty + s * 8, 1);
+            mbar_init(bar_conv + s * 8, kConvWarps);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar_tfull + a * 8, 1);
@@ -219,9 +246,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint32_t fb = bar_full + s * 8;
-                mbar_arrive_expect_tx(fb, A_TILE + P::B_TILE);
+                mbar_arrive_expect_tx(fb, P::TX);
                 tma_load_2d(sbase + P::A_OFF + s * A_TILE, &tmA, kb * BK, mb * BM, fb);
-                tma_load_2d(sbase + P::B_OFF + s * P::B_TILE, &tmB, kb * BK, nb * BN, fb);
+                if constexpr (FP8)
+                    tma_load_2d(sbase + P::RAW_OFF + s * P::RAW_TILE, &tmB, kb * BK, nb * BN, fb);
+                else
+                    tma_load_2d(sbase + P::B_OFF + s * P::B_TILE, &tmB, kb * BK, nb * BN, fb);
                 issued |= 1u << s;
                 last_par = (last_par & ~(1u << s)) | (ph << s);
                 if (++s == STAGES) {
@@ -239,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer
         constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+        const uint32_t bar_ready = FP8 ? bar_conv : bar_full;
         int s = 0;
         uint32_t ph = 0;
         int t = 0;
@@ -253,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * BN;
             for (int kb = 0; kb < kblocks; ++kb) {
-                if (!mbar_wait(bar_full + s * 8, ph, abort_flag)) {
+                if (!mbar_wait(bar_ready + s * 8, ph, abort_flag)) {
                     fail();
                     ok = false;
                     break;
@@ -279,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(bar_drain);
             mbar_wait(bar_drain, 0, nullptr);
         }
-    } else if (warp >= 2) {
+    } else if (warp >= 2 && warp < 6) {
         // ---------------- epilogue
         const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
         int t = 0;
@@ -309,6 +340,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_tempty + acc * 8);
+        }
+    } else if constexpr (FP8) {
+        if (warp >= 6) {
+            // ---------------- e4m3 -> bf16 converters (4 warps)
+            const int ct = threadIdx.x - 6 * 32;       // 0..127
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    bool got = mbar_wait(bar_full + s * 8, ph, abort_flag);
+                    got = __all_sync(0xFFFFFFFFu, got);
+                    if (!got) {
+                        if (lane == 0) fail();
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t* raw = smem + P::RAW_OFF + s * P::RAW_TILE;
+                    uint8_t* dst = smem + P::B_OFF + s * P::B_TILE;
+#pragma unroll 4
+                    for (int i = ct; i < BN * 8; i += kConvWarps * 32) {
+                        const int r = i >> 3, c = i & 7;
+                        const uint2 v = *reinterpret_cast<const uint2*>(raw + r * 64 + c * 8);
+                        uint4 o;
+                        e4m3x4_to_bf16x4(v.x, o.x, o.y);
+                        e4m3x4_to_bf16x4(v.y, o.z, o.w);
+                        *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = o;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_conv + s * 8);
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
         }
     }
 
@@ -342,37 +410,42 @@ EncodeTiledFn get_encode() {
     return fn;
 }
 
-// Row-major [rows, cols] bf16 matrix with row pitch ld elements; box of
-// box_rows x 64 columns, 128-byte swizzle, zero fill out of bounds.
-bool make_map_bf16(CUtensorMap* m, const void* base, long long rows, long long cols, long long ld,
-                   int box_rows) {
+// Row-major [rows, cols] matrix with row pitch ld elements; box of box_rows
+// x 64 elements, zero fill out of bounds.  bf16 tiles use the 128-byte
+// swizzle the MMA descriptors expect; e4m3 tiles (64-byte rows) are loaded
+// unswizzled for the converter warps.
+bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, long long ld,
+              int box_rows, bool e4m3) {
     EncodeTiledFn enc = get_encode();
     if (!enc) return false;
+    const int es_bytes = e4m3 ? 1 : 2;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * es_bytes};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    return enc(m, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+               const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               e4m3 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
 
 int g_num_sms = 0;
 
-template <int BN, int STAGES>
-cudaError_t run_bf16(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
-    using PL = SmemPlan<BN, STAGES>;
+template <int BN, int STAGES, bool FP8>
+cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
+    using PL = SmemPlan<BN, STAGES, FP8>;
+    static_assert(PL::BYTES <= 227 * 1024, "shared memory plan exceeds 227 KB");
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<BN, STAGES>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, STAGES, FP8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, PL::BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     CUtensorMap ta, tb;
-    if (!make_map_bf16(&ta, p.A, p.M, p.K, p.K, BM)) return cudaErrorInvalidValue;
-    if (!make_map_bf16(&tb, p.W, p.N, p.K, p.K, BN)) return cudaErrorInvalidValue;
+    if (!make_map(&ta, p.A, p.M, p.K, p.K, BM, false)) return cudaErrorInvalidValue;
+    if (!make_map(&tb, p.W, p.N, p.K, p.K, BN, FP8)) return cudaErrorInvalidValue;
     EpiArgs a;
     a.M = p.M;
     a.N = p.N;
@@ -392,7 +465,7 @@ cudaError_t run_bf16(const GemmParams& p, cudaStream_t s, unsigned long long* la
     a.num_tiles = a.num_m * a.num_n;
     a.w8 = nullptr;
     const int grid = a.num_tiles < g_num_sms ? a.num_tiles : g_num_sms;
-    gemm_bf16_kernel<BN, STAGES><<<grid, kThreads, PL::BYTES, s>>>(ta, tb, a);
+    gemm_kernel<BN, STAGES, FP8><<<grid, PL::THREADS, PL::BYTES, s>>>(ta, tb, a);
     ++*launches;
     return cudaGetLastError();
 }
@@ -412,15 +485,17 @@ int gemm_num_sms() {
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
     if (p.M <= 0) return cudaSuccess;
     gemm_num_sms();
-    if (p.w_dtype != DLO_DT_BF16) return cudaErrorNotSupported;
     // Pick the N tile that minimises (waves x tile width) over the SMs.
     const long long num_m = (p.M + BM - 1) / BM;
     auto cost = [&](int bn) {
         const long long tiles = num_m * ((p.N + bn - 1) / bn);
         return ((tiles + g_num_sms - 1) / g_num_sms) * bn;
     };
-    if (cost(256) <= cost(128)) return run_bf16<256, 4>(p, s, launches);
-    return run_bf16<128, 6>(p, s, launches);
+    const bool wide = cost(256) <= cost(128);
+    if (p.w_dtype == DLO_DT_E4M3)
+        return wide ? run_gemm<256, 3, true>(p, s, launches) : run_gemm<128, 5, true>(p, s, launches);
+    if (p.w_dtype != DLO_DT_BF16) return cudaErrorNotSupported;
+    return wide ? run_gemm<256, 4, false>(p, s, launches) : run_gemm<128, 6, false>(p, s, launches);
 }
 
 }  // namespace dlo

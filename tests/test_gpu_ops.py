@@ -183,3 +183,63 @@ def test_op_argument_errors():
         dlo.dlo_op_gemm(16, 16, 0, None, 0, None, 10, 15, 16, 0, 16, 16, None, 0, 1, None, None)
     with pytest.raises(dlo.DloError):
         dlo.dlo_op_attention(16, 16, 16, 16, 1, 1, 12, 4, 4, 16, 16, 16, 16, None)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (300, 272, 1152), (2048, 3456, 1152),
+                                   (777, 1152, 4608), (64, 512, 4096)])
+@pytest.mark.parametrize("epi", [0, 1, 2])
+def test_gemm_e4m3_weights_match_oracle(M, N, K, epi):
+    from oracle import fp8
+    g = np.random.default_rng(M + N + K + 31 * epi)
+    A = bf16(g.standard_normal((M, K)))
+    # every finite code appears; NaN codes (0x7F, 0xFF) are never produced by the quantiser
+    codes = g.integers(0, 256, size=(N, K), dtype=np.uint8)
+    codes[codes == 0x7F] = 0x7E
+    codes[codes == 0xFF] = 0xFE
+    flat = codes.ravel()
+    flat[:254] = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    Wq = torch.from_numpy(codes).cuda()
+    seg = N // 2 if (N // 2) % 16 == 0 else N
+    nseg = N // seg
+    sc = (0.02 / 448.0) * (1.0 + np.arange(nseg, dtype=np.float32))
+    scales = torch.from_numpy(sc.astype(np.float32)).cuda()
+    b = bf16(g.standard_normal(N) * 0.1)
+    wdeq = fp8.decode_e4m3(codes) * np.repeat(sc.astype(np.float64), seg)[:, None]
+    ref = dit.linear(f64(A), wdeq, f64(b))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if epi == dlo.EPI_RESIDUAL:
+        gate = torch.from_numpy(g.standard_normal((1, N)).astype(np.float32)).cuda()
+        x0 = torch.from_numpy(g.standard_normal((M, N)).astype(np.float32)).cuda()
+        out = x0.clone()
+        dlo.dlo_op_gemm(A.data_ptr(), Wq.data_ptr(), dlo.DT_E4M3, scales.data_ptr(), seg, b.data_ptr(),
+                        M, N, K, epi, out.data_ptr(), N, gate.data_ptr(), N, M, err.data_ptr(), stream())
+        ref = f64(x0) + f64(gate) * ref
+        tol = 1e-5
+    else:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        dlo.dlo_op_gemm(A.data_ptr(), Wq.data_ptr(), dlo.DT_E4M3, scales.data_ptr(), seg, b.data_ptr(),
+                        M, N, K, epi, out.data_ptr(), N, None, 0, 1, err.data_ptr(), stream())
+        if epi == dlo.EPI_GELU:
+            ref = dit.gelu_tanh(ref)
+        tol = 6e-3
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert rel(f64(out), ref) < tol
+
+
+def test_gemm_e4m3_decodes_every_code_exactly():
+    """A = identity rows pick single weight columns: Y[i, n] = s * decode(W[n, i])."""
+    from oracle import fp8
+    K, N = 256, 16
+    codes = np.zeros((N, K), dtype=np.uint8)
+    allc = np.array([c for c in range(256) if c not in (0x7F, 0xFF)] + [0, 0], dtype=np.uint8)
+    codes[:] = np.roll(allc, 0)[None, :]
+    codes[1] = allc[::-1]
+    A = torch.eye(K, dtype=torch.bfloat16, device="cuda")
+    Wq = torch.from_numpy(codes).cuda()
+    out = torch.empty((K, N), dtype=torch.float32, device="cuda").zero_()
+    s = torch.ones(1, dtype=torch.float32, device="cuda")
+    dlo.dlo_op_gemm(A.data_ptr(), Wq.data_ptr(), dlo.DT_E4M3, s.data_ptr(), N, None, K, N, K,
+                    dlo.EPI_RESIDUAL, out.data_ptr(), N, None, 0, K, None, stream())
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.cpu().numpy().astype(np.float64), fp8.decode_e4m3(codes).T)
