@@ -60,6 +60,7 @@ typedef int dlo_status;
 /* block kinds */
 #define DLO_BLOCK_DIT    0   /* DiT adaLN-zero block, self-attention only        */
 #define DLO_BLOCK_VIDEO  1   /* video-DiT block: self-attn, cross-attn, FFN      */
+#define DLO_BLOCK_BYTES  2   /* opaque bytes; compute = checksum of the slot     */
 
 /* weight storage of the linears in a block */
 #define DLO_W_BF16       0
@@ -77,13 +78,19 @@ typedef int dlo_status;
 #define DLO_DT_BF16 0
 #define DLO_DT_E4M3 1
 #define DLO_DT_F32  2
+#define DLO_DT_U8   3   /* opaque bytes (DLO_BLOCK_BYTES)                     */
 
 /* Stack description.  Constraints (else DLO_EINVAL): abi_version ==
  * DLO_ABI_VERSION; n_blocks >= 1; hidden == heads * head_dim; hidden % 16 == 0;
  * head_dim % 8 == 0 and head_dim <= 128; ffn % 16 == 0; max_batch >= 1;
  * max_tokens >= 1; DiT: cond_dim % 8 == 0; video: text_dim % 16 == 0 and
  * max_text_tokens >= 1; eps > 0.  DLO_W_E4M3 requires DLO_BLOCK_VIDEO
- * (else DLO_EUNSUPPORTED). */
+ * (else DLO_EUNSUPPORTED).
+ * DLO_BLOCK_BYTES streams opaque blocks of bytes_block bytes (a multiple of
+ * 256) through the same slots and schedule; only n_blocks, staging,
+ * register_budget_bytes and bytes_block are read.  Its "compute" reads the
+ * whole slot and adds its 64-bit little-endian words (mod 2^64) into a
+ * per-block checksum, so a slot reused too early shows up as a wrong sum. */
 typedef struct dlo_desc {
     int abi_version;
     int block_kind;      /* DLO_BLOCK_*                                          */
@@ -103,6 +110,7 @@ typedef struct dlo_desc {
     /* [DLO] "Registered runtime-cache transfer": the complete registration byte
      * count is checked against this budget before any registration; 0 = none. */
     unsigned long long register_budget_bytes;
+    unsigned long long bytes_block;  /* DLO_BLOCK_BYTES: bytes per block          */
 } dlo_desc;
 
 typedef struct dlo_tensor_info {
@@ -217,6 +225,10 @@ dlo_status dlo_set_resident(dlo_ctx* ctx, int k, void* const* device_blocks);
  *   x += gate2 * (GELU_tanh((LN(x)(1+scale2)+shift2) W_1^T + b_1) W_2^T + b_2)
  *   Attn: qkv = h W_qkv^T + b_qkv, q|k|v each [H, hd] per token,
  *         softmax(q k^T / sqrt(hd)) v per head, non-causal.
+ * Bytes block (DLO_BLOCK_BYTES): batch = tokens = 1; x_in, cond, ctx_tokens
+ *   are ignored (may be NULL); x_out is a device uint64 array [n_blocks] that
+ *   receives, for every block executed by this call, the sum of its 64-bit
+ *   words as read from the slot (or resident buffer) it ran from.
  * Video block: m = e + T_mod; self-attention as above with separate q,k,v
  *   linears and RMSNorm (gain, over hidden) on q and k, x += gate1 * o;
  *   cross-attention with q = RMSNorm(LN_affine(x) W_q^T + b_q), k = RMSNorm(
@@ -286,7 +298,8 @@ typedef struct dlo_stats {
 #define DLO_K_LAYERNORM  3
 #define DLO_K_RMSNORM    4
 #define DLO_K_MODULATION 5   /* adaLN GEMV or modulation-table add            */
-#define DLO_K_CONVERT    6   /* bf16 <-> fp32 of the carried hidden state      */
+#define DLO_K_CONVERT    6   /* bf16 <-> fp32 of the hidden state; bytes-block
+                                checksum                                       */
 #define DLO_K_GATHER     7   /* zero-copy slot staging kernel                  */
 
 /* Counters and timing.  Timing sums need the timed work finished (call

@@ -24,11 +24,11 @@ _lib = ctypes.CDLL(LIB_PATH)
 ABI_VERSION = 1
 OK, EINVAL, ESTATE, ENOMEM, ECUDA, EREGISTER, ETIMEDOUT, EUNSUPPORTED, EMISMATCH = \
     0, -1, -2, -3, -4, -5, -6, -7, -8
-BLOCK_DIT, BLOCK_VIDEO = 0, 1
+BLOCK_DIT, BLOCK_VIDEO, BLOCK_BYTES = 0, 1, 2
 W_BF16, W_E4M3 = 0, 1
 STAGE_MEMCPY, STAGE_GATHER = 0, 1
 HOST_PINNED, HOST_REGISTER = 1, 2
-DT_BF16, DT_E4M3, DT_F32 = 0, 1, 2
+DT_BF16, DT_E4M3, DT_F32, DT_U8 = 0, 1, 2, 3
 EPI_BIAS, EPI_GELU, EPI_RESIDUAL = 0, 1, 2
 
 STATUS_NAMES = {0: "OK", -1: "EINVAL", -2: "ESTATE", -3: "ENOMEM", -4: "ECUDA",
@@ -48,7 +48,8 @@ class dlo_desc(ctypes.Structure):
                 ("cond_dim", ctypes.c_int), ("text_dim", ctypes.c_int),
                 ("max_batch", ctypes.c_int), ("max_tokens", ctypes.c_int),
                 ("max_text_tokens", ctypes.c_int), ("eps", ctypes.c_float),
-                ("staging", ctypes.c_int), ("register_budget_bytes", ctypes.c_ulonglong)]
+                ("staging", ctypes.c_int), ("register_budget_bytes", ctypes.c_ulonglong),
+                ("bytes_block", ctypes.c_ulonglong)]
 
 
 class dlo_tensor_info(ctypes.Structure):
@@ -141,10 +142,10 @@ def _check(st: int, ctx=None):
 
 def make_desc(*, block_kind, n_blocks, hidden, heads, head_dim, ffn, cond_dim=0, text_dim=0,
               max_batch=1, max_tokens=1, max_text_tokens=0, wdtype=W_BF16, eps=1e-6,
-              staging=STAGE_MEMCPY, register_budget_bytes=0) -> dlo_desc:
+              staging=STAGE_MEMCPY, register_budget_bytes=0, bytes_block=0) -> dlo_desc:
     return dlo_desc(ABI_VERSION, block_kind, wdtype, n_blocks, hidden, heads, head_dim, ffn,
                     cond_dim, text_dim, max_batch, max_tokens, max_text_tokens, eps, staging,
-                    register_budget_bytes)
+                    register_budget_bytes, bytes_block)
 
 
 def dlo_block_bytes(desc: dlo_desc) -> int:

@@ -243,8 +243,16 @@ dlo_status prime(dlo_ctx* c) {
 
 // One block from weights at `W` (a slot or a resident buffer).
 dlo_status run_block(dlo_ctx* c, const uint8_t* W, int B, int N, int L, const void* cond,
-                     const void* ctx_tokens) {
+                     const void* ctx_tokens, int block, void* x_out) {
     const dlo_desc& d = c->d;
+    if (d.block_kind == DLO_BLOCK_BYTES) {
+        unsigned long long* sums = static_cast<unsigned long long*>(x_out) + block;
+        LCHECK(c->timed(DLO_K_CONVERT, 0.0, static_cast<double>(c->block_bytes), c->cs, [&] {
+                   return launch_checksum(W, c->block_bytes, sums, c->cs, &c->st.kernel_launches);
+               }),
+               "checksum");
+        return DLO_OK;
+    }
     const Offsets& o = c->off;
     const int D = d.hidden, F = d.ffn, H = d.heads, hd = d.head_dim;
     const int BN = B * N;
@@ -611,6 +619,11 @@ extern "C" dlo_status dlo_forward(dlo_ctx* c, const void* x_in, const void* cond
     if (!c) return DLO_EINVAL;
     if (c->state != kRegistered) return c->fail(DLO_ESTATE, "register host blocks first");
     const dlo_desc& d = c->d;
+    const bool bytes_kind = d.block_kind == DLO_BLOCK_BYTES;
+    if (bytes_kind) {
+        if (batch != 1 || tokens != 1) return c->fail(DLO_EINVAL, "bytes blocks take batch = tokens = 1");
+        if (!x_out || !aligned(x_out, 8)) return c->fail(DLO_EINVAL, "x_out must be an 8-byte aligned uint64 array");
+    } else {
     if (batch < 1 || batch > d.max_batch) return c->fail(DLO_EINVAL, "batch out of range");
     if (tokens < 1 || tokens > d.max_tokens) return c->fail(DLO_EINVAL, "tokens out of range");
     if (!x_in || !x_out || !cond) return c->fail(DLO_EINVAL, "NULL input/output");
@@ -620,22 +633,27 @@ extern "C" dlo_status dlo_forward(dlo_ctx* c, const void* x_in, const void* cond
         if (text_tokens < 1 || text_tokens > d.max_text_tokens) return c->fail(DLO_EINVAL, "text_tokens out of range");
         if (!ctx_tokens || !aligned(ctx_tokens, 16)) return c->fail(DLO_EINVAL, "ctx_tokens NULL or misaligned");
     }
+    }
     cudaSetDevice(c->device);
     dlo_status r = prime(c);
     if (r != DLO_OK) return r;
     const int n = d.n_blocks, k = c->k;
-    const size_t nx = static_cast<size_t>(batch) * tokens * d.hidden;
+    const size_t nx = bytes_kind ? 0 : static_cast<size_t>(batch) * tokens * d.hidden;
     float* x = reinterpret_cast<float*>(c->wsp + c->ws.x);
-    LCHECK(c->timed(DLO_K_CONVERT, 0.0, 6.0 * nx, c->cs,
-                    [&] { return launch_bf16_to_f32(x_in, x, nx, c->cs, &c->st.kernel_launches); }),
-           "input conversion");
+    if (bytes_kind) {
+        LCHECK(cudaMemsetAsync(x_out, 0, static_cast<size_t>(n) * 8, c->cs), "clear checksums");
+    } else {
+        LCHECK(c->timed(DLO_K_CONVERT, 0.0, 6.0 * nx, c->cs,
+                        [&] { return launch_bf16_to_f32(x_in, x, nx, c->cs, &c->st.kernel_launches); }),
+               "input conversion");
+    }
     if (c->resident_pending) {
         LCHECK(cudaStreamWaitEvent(c->cs, c->resident_ev, 0), "wait resident");
         c->resident_pending = false;
     }
     for (int i = 0; i < k; ++i) {
         c->log(1, i, -1);
-        r = run_block(c, c->resident[i], batch, tokens, text_tokens, cond, ctx_tokens);
+        r = run_block(c, c->resident[i], batch, tokens, text_tokens, cond, ctx_tokens, i, x_out);
         if (r != DLO_OK) return r;
     }
     for (int i = k; i < n; ++i) {
@@ -661,7 +679,7 @@ extern "C" dlo_status dlo_forward(dlo_ctx* c, const void* x_in, const void* cond
         LCHECK(cudaStreamWaitEvent(c->cs, c->copy_done[s], 0), "compute waits copy");
         if (c->timing) LCHECK(cudaEventRecord(te.comp0, c->cs), "event");
         c->log(1, i, s);
-        r = run_block(c, c->slot[s], batch, tokens, text_tokens, cond, ctx_tokens);
+        r = run_block(c, c->slot[s], batch, tokens, text_tokens, cond, ctx_tokens, i, x_out);
         if (r != DLO_OK) return r;
         if (c->timing) LCHECK(cudaEventRecord(te.comp1, c->cs), "event");
         LCHECK(cudaEventRecord(c->compute_done[s], c->cs), "event record");
@@ -669,9 +687,11 @@ extern "C" dlo_status dlo_forward(dlo_ctx* c, const void* x_in, const void* cond
         ++c->exec_counter;
         ++c->st.streamed_execs;
     }
-    LCHECK(c->timed(DLO_K_CONVERT, 0.0, 6.0 * nx, c->cs,
-                    [&] { return launch_f32_to_bf16(x, x_out, nx, c->cs, &c->st.kernel_launches); }),
-           "output conversion");
+    if (!bytes_kind) {
+        LCHECK(c->timed(DLO_K_CONVERT, 0.0, 6.0 * nx, c->cs,
+                        [&] { return launch_f32_to_bf16(x, x_out, nx, c->cs, &c->st.kernel_launches); }),
+               "output conversion");
+    }
     ++c->st.forwards;
     return DLO_OK;
 }
@@ -694,6 +714,16 @@ extern "C" dlo_status dlo_forward_host(dlo_ctx* c, const void* x_in, const void*
     if (!c) return DLO_EINVAL;
     if (c->state != kRegistered) return c->fail(DLO_ESTATE, "register host blocks first");
     const dlo_desc& d = c->d;
+    if (d.block_kind == DLO_BLOCK_BYTES) {
+        if (!x_out) return c->fail(DLO_EINVAL, "NULL output");
+        cudaSetDevice(c->device);
+        void* sums = c->wsp + c->ws.in_x;
+        dlo_status r = dlo_forward(c, nullptr, nullptr, nullptr, 1, 1, 0, sums);
+        if (r != DLO_OK) return r;
+        LCHECK(cudaMemcpyAsync(x_out, sums, static_cast<size_t>(d.n_blocks) * 8, cudaMemcpyDeviceToHost, c->cs),
+               "D2H checksums");
+        return dlo_wait(c, timeout_ms);
+    }
     if (batch < 1 || batch > d.max_batch || tokens < 1 || tokens > d.max_tokens)
         return c->fail(DLO_EINVAL, "batch/tokens out of range");
     if (!x_in || !x_out || !cond) return c->fail(DLO_EINVAL, "NULL input/output");

@@ -97,5 +97,8 @@ cudaError_t launch_f32_to_bf16(const float* in, void* out, size_t n, cudaStream_
                                unsigned long long* launches);
 cudaError_t launch_gather(void* dst, const void* src, size_t bytes, cudaStream_t s,
                           unsigned long long* launches);
+// *out += sum of the 64-bit words of src (bytes % 16 == 0), mod 2^64.
+cudaError_t launch_checksum(const void* src, size_t bytes, unsigned long long* out, cudaStream_t s,
+                            unsigned long long* launches);
 
 }  // namespace dlo

@@ -273,6 +273,22 @@ __global__ void __launch_bounds__(1024) gather_kernel(uint4* __restrict__ dst,
     for (; i < n16; i += stride) dst[i] = src[i];
 }
 
+// *out += sum of 64-bit words (mod 2^64): reads every byte of a staged slot,
+// so it is the "compute" of an opaque bytes block.
+__global__ void __launch_bounds__(256) checksum_kernel(const uint4* __restrict__ src, size_t n16,
+                                                       unsigned long long* __restrict__ out) {
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    unsigned long long s = 0;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride) {
+        const uint4 v = src[i];
+        s += (static_cast<unsigned long long>(v.y) << 32) | v.x;
+        s += (static_cast<unsigned long long>(v.w) << 32) | v.z;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    if ((threadIdx.x & 31) == 0) atomicAdd(out, s);
+}
+
 inline unsigned blocks_for(size_t threads, unsigned per) {
     return static_cast<unsigned>((threads + per - 1) / per);
 }
@@ -382,6 +398,21 @@ cudaError_t launch_gather(void* dst, const void* src, size_t bytes, cudaStream_t
     if (need < g) g = static_cast<unsigned>(need);
     gather_kernel<<<g, 1024, 0, s>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src),
                                      n16);
+    ++*launches;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_checksum(const void* src, size_t bytes, unsigned long long* out, cudaStream_t s,
+                            unsigned long long* launches) {
+    const size_t n16 = bytes / 16;
+    if (!n16) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    size_t g = static_cast<size_t>(sms > 0 ? sms : 1) * 8;
+    const size_t need = (n16 + 255) / 256;
+    if (need < g) g = need;
+    checksum_kernel<<<static_cast<unsigned>(g), 256, 0, s>>>(static_cast<const uint4*>(src), n16, out);
     ++*launches;
     return cudaGetLastError();
 }

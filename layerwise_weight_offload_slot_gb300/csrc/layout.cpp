@@ -27,8 +27,17 @@ dlo_status validate_desc(const dlo_desc* d, std::string* msg) {
     };
     if (!d) return fail(DLO_EINVAL, "desc is NULL");
     if (d->abi_version != DLO_ABI_VERSION) return fail(DLO_EINVAL, "abi_version mismatch");
-    if (d->block_kind != DLO_BLOCK_DIT && d->block_kind != DLO_BLOCK_VIDEO)
+    if (d->block_kind != DLO_BLOCK_DIT && d->block_kind != DLO_BLOCK_VIDEO &&
+        d->block_kind != DLO_BLOCK_BYTES)
         return fail(DLO_EINVAL, "unknown block_kind");
+    if (d->block_kind == DLO_BLOCK_BYTES) {
+        if (d->n_blocks < 1) return fail(DLO_EINVAL, "n_blocks < 1");
+        if (d->bytes_block == 0 || d->bytes_block % 256 != 0)
+            return fail(DLO_EINVAL, "bytes_block must be a positive multiple of 256");
+        if (d->staging != DLO_STAGE_MEMCPY && d->staging != DLO_STAGE_GATHER)
+            return fail(DLO_EINVAL, "unknown staging");
+        return DLO_OK;
+    }
     if (d->wdtype != DLO_W_BF16 && d->wdtype != DLO_W_E4M3) return fail(DLO_EINVAL, "unknown wdtype");
     if (d->n_blocks < 1) return fail(DLO_EINVAL, "n_blocks < 1");
     if (d->heads < 1 || d->head_dim < 8 || d->hidden != d->heads * d->head_dim)
@@ -66,7 +75,7 @@ struct Builder {
         e.shape[0] = s0;
         e.shape[1] = s1 < 0 ? 0 : s1;
         size_t n = static_cast<size_t>(s0) * static_cast<size_t>(s1 < 0 ? 1 : s1);
-        size_t es = dtype == DLO_DT_BF16 ? 2 : dtype == DLO_DT_E4M3 ? 1 : 4;
+        size_t es = dtype == DLO_DT_BF16 ? 2 : (dtype == DLO_DT_E4M3 || dtype == DLO_DT_U8) ? 1 : 4;
         e.offset = cur;
         e.bytes = n * es;
         e.source = source;
@@ -79,6 +88,11 @@ struct Builder {
 size_t build_layout(const dlo_desc& d, std::vector<Entry>* out) {
     out->clear();
     Builder b{out};
+    if (d.block_kind == DLO_BLOCK_BYTES) {
+        b.group(); b.add("bytes", DLO_DT_U8, static_cast<long long>(d.bytes_block));
+        b.group();
+        return b.cur;
+    }
     const long long D = d.hidden, F = d.ffn;
     const int W = d.wdtype == DLO_W_E4M3 ? DLO_DT_E4M3 : DLO_DT_BF16;
     const int H = DLO_DT_BF16;
@@ -141,6 +155,13 @@ int find_entry(const std::vector<Entry>& L, const char* name) {
 
 Workspace plan_workspace(const dlo_desc& d) {
     Workspace w;
+    if (d.block_kind == DLO_BLOCK_BYTES) {
+        // error words, then the per-block checksums of dlo_forward_host
+        w.err = 0;
+        w.in_x = 256;
+        w.total = align_up(256 + static_cast<size_t>(d.n_blocks) * 8, 256);
+        return w;
+    }
     const size_t BN = static_cast<size_t>(d.max_batch) * d.max_tokens;
     const size_t D = d.hidden, F = d.ffn;
     size_t cur = 0;
@@ -296,6 +317,8 @@ extern "C" dlo_status dlo_pack_block(const dlo_desc* desc, const float* const* t
         if (e.dtype == DLO_DT_BF16) {
             uint16_t* dst = reinterpret_cast<uint16_t*>(base + e.offset);
             for (size_t j = 0; j < n; ++j) dst[j] = f32_to_bf16_rne(src[j]);
+        } else if (e.dtype == DLO_DT_U8) {
+            return DLO_EINVAL;   // opaque byte blocks are written by the caller, not packed
         } else if (e.dtype == DLO_DT_E4M3) {
             float s = 1.0f;
             st = dlo_quantize_e4m3(src, n, base + e.offset, &s);

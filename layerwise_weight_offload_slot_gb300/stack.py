@@ -15,7 +15,7 @@ from concurrent.futures import ThreadPoolExecutor
 import numpy as np
 import torch
 
-from . import (BLOCK_DIT, BLOCK_VIDEO, HOST_PINNED, HOST_REGISTER, OK, STAGE_MEMCPY, W_BF16,
+from . import (BLOCK_BYTES, BLOCK_DIT, BLOCK_VIDEO, HOST_PINNED, HOST_REGISTER, OK, STAGE_MEMCPY, W_BF16,
                dlo_block_bytes, dlo_block_layout, dlo_create, dlo_destroy, dlo_forward,
                dlo_forward_host, dlo_get_log, dlo_get_stats, dlo_pack_block,
                dlo_register_host_blocks, dlo_reset_log, dlo_set_resident, dlo_set_timing,
@@ -68,16 +68,18 @@ class HostBlocks:
 
 
 class OffloadStack:
-    def __init__(self, *, block_kind: int, n_blocks: int, hidden: int, heads: int, head_dim: int,
-                 ffn: int, cond_dim: int = 0, text_dim: int = 0, max_batch: int = 1,
-                 max_tokens: int = 1, max_text_tokens: int = 0, wdtype: int = W_BF16,
-                 eps: float = 1e-6, staging: int = STAGE_MEMCPY, host_mode: str = "pinned",
-                 register_budget_bytes: int = 0, device: int = 0):
+    def __init__(self, *, block_kind: int, n_blocks: int, hidden: int = 0, heads: int = 0,
+                 head_dim: int = 0, ffn: int = 0, cond_dim: int = 0, text_dim: int = 0,
+                 max_batch: int = 1, max_tokens: int = 1, max_text_tokens: int = 0,
+                 wdtype: int = W_BF16, eps: float = 1e-6, staging: int = STAGE_MEMCPY,
+                 host_mode: str = "pinned", register_budget_bytes: int = 0,
+                 bytes_block: int = 0, device: int = 0):
         self.desc = make_desc(block_kind=block_kind, n_blocks=n_blocks, hidden=hidden, heads=heads,
                               head_dim=head_dim, ffn=ffn, cond_dim=cond_dim, text_dim=text_dim,
                               max_batch=max_batch, max_tokens=max_tokens,
                               max_text_tokens=max_text_tokens, wdtype=wdtype, eps=eps,
-                              staging=staging, register_budget_bytes=register_budget_bytes)
+                              staging=staging, register_budget_bytes=register_budget_bytes,
+                              bytes_block=bytes_block)
         self.block_bytes = dlo_block_bytes(self.desc)
         if self.block_bytes == 0:
             raise ValueError("invalid stack description")
@@ -127,6 +129,16 @@ class OffloadStack:
         dlo_set_resident(self.ctx, [_round(t.data_ptr(), 256) for t in bufs])
 
     # ---------------------------------------------------------------- run
+    def forward_bytes(self, sums: torch.Tensor | None = None) -> torch.Tensor:
+        """One pass over an opaque bytes stack; per-block uint64 checksums (as int64)."""
+        if sums is None:
+            sums = torch.zeros(self.n_blocks, dtype=torch.int64, device=self.dev)
+        cur = torch.cuda.current_stream(self.dev)
+        self.compute_stream.wait_stream(cur)
+        dlo_forward(self.ctx, None, None, None, 1, 1, 0, sums.data_ptr())
+        cur.wait_stream(self.compute_stream)
+        return sums
+
     def forward(self, x: torch.Tensor, cond: torch.Tensor, ctx_tokens: torch.Tensor | None = None,
                 out: torch.Tensor | None = None) -> torch.Tensor:
         B, N, _ = x.shape

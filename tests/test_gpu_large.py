@@ -1,0 +1,118 @@
+"""Full-width and full-size checks: the video stacks at hidden 5120 (bf16 and
+E4M3 weights), sampled query rows at 32760 / 8192 tokens, residency
+invariance at full width, and opaque-byte staging of 16 MB .. 1 GB blocks."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import dit
+from tests import helpers as H
+
+dlo = pytest.importorskip("layerwise_weight_offload_slot_gb300")
+
+pytestmark = pytest.mark.gpu
+
+
+def _rows(cfg, n=256, seed=7):
+    g = np.random.default_rng(seed)
+    r = np.sort(g.choice(cfg.tokens, size=min(n, cfg.tokens), replace=False))
+    # always include the ragged tail of the last 128-row tile
+    return np.unique(np.concatenate([r, [cfg.tokens - 1]]))
+
+
+@pytest.mark.parametrize("base", [synth.CFG_VIDEO, synth.CFG_VIDEO_FP8], ids=["bf16", "e4m3"])
+def test_video_widths_two_block_stack(base):
+    cfg = base.with_(n_blocks=2, tokens=1024)
+    params = [synth.block_params(cfg, i) for i in range(cfg.n_blocks)]
+    st = H.make_stack(cfg, blocks=params)
+    st.attach()
+    x, cond, ctx = H.device_inputs(cfg)
+    out = st.forward(x, cond, ctx)
+    torch.cuda.synchronize()
+    st.wait()
+    ref = H.oracle_forward(cfg, x, cond, ctx, H.oracle_blocks(cfg, params))
+    err = H.rel_l2(out.float().cpu().numpy(), ref)
+    tol = 5e-2 if cfg.wdtype == synth.W_E4M3 else 2e-2
+    print(cfg.name, "n=2 N=1024 rel L2", err)
+    assert err <= tol
+    st.close()
+
+
+@pytest.mark.parametrize("base,block", [(synth.CFG_VIDEO, 0), (synth.CFG_VIDEO, 17),
+                                        (synth.CFG_VIDEO_FP8, 0), (synth.CFG_VIDEO_FP8, 39)],
+                         ids=["bf16-n32760-b0", "bf16-n32760-b17", "e4m3-n8192-b0", "e4m3-n8192-b39"])
+def test_full_size_block_sampled_rows(base, block):
+    """One block of the full-size workload, streamed through a slot, at the
+    workload's token count; 256 seeded query rows (plus the ragged last row)
+    against the oracle with keys/values over every token."""
+    cfg = base.with_(n_blocks=1)
+    params = synth.block_params(base, block)
+    st = H.make_stack(cfg, blocks=[params])
+    st.attach()
+    x, cond, ctx = H.device_inputs(cfg)
+    out = st.forward(x, cond, ctx)
+    torch.cuda.synchronize()
+    st.wait()
+    assert st.verify_slot(1) and st.verify_slot(0)
+    rows = _rows(cfg)
+    P = dit.prepare_block(params, fp8_linears=cfg.wdtype == synth.W_E4M3)
+    ref = dit.block_forward(cfg.kind, x.float().cpu().numpy().astype(np.float64),
+                            cond.float().cpu().numpy().astype(np.float64),
+                            ctx.float().cpu().numpy().astype(np.float64), P, cfg.heads, rows=rows)
+    y = out.float().cpu().numpy()[:, rows]
+    err = H.rel_l2(y, ref)
+    tol = 5e-2 if cfg.wdtype == synth.W_E4M3 else 2e-2
+    print(base.name, "block", block, "sampled rel L2", err)
+    assert err <= tol
+    st.close()
+
+
+def test_residency_invariance_full_width():
+    cfg = synth.CFG_SWEEP.with_(n_blocks=4)
+    params = synth.stack_params(cfg)
+    outs = []
+    for k in (0, 2, 4):
+        st = H.make_stack(cfg, blocks=params)
+        st.attach()
+        st.set_resident(k)
+        x, cond, ctx = H.device_inputs(cfg)
+        outs.append(st.forward(x, cond, ctx).cpu())
+        torch.cuda.synchronize()
+        st.wait()
+        st.close()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
+def _host_sum(a: np.ndarray) -> int:
+    return int(a.view(np.uint64).sum(dtype=np.uint64))
+
+
+@pytest.mark.parametrize("size_mb,n,k", [(16, 5, 0), (16, 5, 2), (256, 3, 1), (1024, 2, 0)])
+@pytest.mark.parametrize("staging,host", [(0, "pinned"), (1, "pinned"), (0, "register"),
+                                          (1, "register")])
+def test_bytes_blocks_stage_and_checksum(size_mb, n, k, staging, host):
+    from layerwise_weight_offload_slot_gb300.stack import OffloadStack
+    size = size_mb << 20
+    st = OffloadStack(block_kind=dlo.BLOCK_BYTES, n_blocks=n, bytes_block=size, staging=staging,
+                      host_mode=host)
+    sums = []
+    for i in range(n):
+        v = st.host.view(i)
+        v[:] = synth.staging_bytes(size, seed=i)
+        sums.append(_host_sum(v))
+    st.attach()
+    st.set_resident(k)
+    for step in range(2):
+        got = st.forward_bytes()
+        torch.cuda.synchronize()
+        st.wait()
+        assert [int(s) % (1 << 64) for s in got.cpu().numpy().view(np.uint64)] == sums
+        for s in (0, 1):
+            if st.stats()["slot_block"][s] >= 0:
+                assert st.verify_slot(s)
+    out = np.zeros(n, dtype=np.uint64)
+    dlo.dlo_forward_host(st.ctx, None, None, None, 1, 1, 0, out.ctypes.data)
+    assert [int(v) for v in out] == sums
+    st.close()
