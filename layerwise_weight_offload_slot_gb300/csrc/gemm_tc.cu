@@ -7,8 +7,14 @@
 //               N=BN, K=16) x 4 per stage into one of two fp32 TMEM
 //               accumulators; tcgen05.commit frees the stage / publishes the
 //               accumulator
-//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, scale (FP8
-//               per-tensor), + bias, GELU or gate * y + residual, store
+//   warps 2..5  epilogue: warp q owns accumulator rows 32q..32q+31; per
+//               column chunk it loads TMEM (tcgen05.ld), applies the
+//               per-tensor scale, bias, GELU or gate, writes a 32-row box
+//               into a 128-byte-swizzled shared-memory staging buffer and
+//               lets TMA store it (bf16 outputs) or add it into the fp32
+//               hidden state (cp.reduce.async.bulk .add: x += gate*(y + b)
+//               without reading x).  Two staging buffers per warp let the
+//               next chunk overlap the previous store.
 // The two accumulators let the epilogue of tile t overlap the mainloop of
 // tile t+1.  With E4M3 weights (FP8 = true) TMA loads the raw codes, four
 // more warps widen them to bf16 in the swizzled layout the MMA reads (exact),
@@ -22,6 +28,7 @@
 #include <cuda_bf16.h>
 
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -37,12 +44,12 @@ constexpr int BM = 128;
 constexpr int BK = 64;             // 64 bf16 = 128 bytes = one swizzle row
 constexpr int A_TILE = BM * BK * 2;
 constexpr int kThreads = 192;
+constexpr int kConvWarps = 4;
+constexpr int STG_BYTES = 32 * 128;   // one 32-row x 128-byte staging box
 
 struct EpiArgs {
     int M, N, K;
     int epi;
-    void* out;
-    int ldo;
     const __nv_bfloat16* bias;
     const float* scales;
     int scale_seg;
@@ -51,7 +58,6 @@ struct EpiArgs {
     int rows_per_batch;
     int* err;
     int num_m, num_n, num_tiles;
-    const uint8_t* w8;   // e4m3 weights (FP8 kernel), [N, K]
 };
 
 // Grouped tile order: groups of 8 M-blocks sweep all N-blocks, so one
@@ -67,32 +73,35 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mb
     nb = r / gsz;
 }
 
+// GELU, tanh approximation; tanh from the hardware approximation
+// (relative error about 2^-11, below the bf16 rounding of the output).
 __device__ __forceinline__ float gelu_tanh(float x) {
     const float k0 = 0.7978845608028654f, k1 = 0.044715f;
-    return 0.5f * x * (1.f + tanhf(k0 * (x + k1 * x * x * x)));
+    return 0.5f * x * (1.f + tanh_approx(k0 * (x + k1 * x * x * x)));
 }
 
-// Epilogue of one 32-column chunk held by this thread (row `row`, columns
-// col0 .. col0 + ncols - 1, ncols in {16, 32}).
-__device__ __forceinline__ void epilogue_chunk(const EpiArgs& a, int row, int col0, int ncols,
-                                               const uint32_t (&r)[32]) {
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+// Byte offset of 16-byte chunk j of row r in a 128-byte-swizzled box.
+__device__ __forceinline__ uint32_t sw128(int r, int j) {
+    return static_cast<uint32_t>(r * 128 + ((j ^ (r & 7)) << 4));
+}
+
+// Scale (per 16-column segment) and bias of a chunk of CW columns.
+template <int CW>
+__device__ __forceinline__ void scale_bias(const EpiArgs& a, int col0, float (&v)[CW]) {
     if (a.scales) {
-        const float s0 = a.scales[col0 / a.scale_seg];
-        const float s1 = ncols > 16 ? a.scales[(col0 + 16) / a.scale_seg] : s0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] *= s0;
+        for (int g = 0; g < CW / 16; ++g) {
+            const int c = col0 + 16 * g;
+            const float s = c < a.N ? a.scales[c / a.scale_seg] : 0.f;
 #pragma unroll
-        for (int i = 16; i < 32; ++i) v[i] *= s1;
+            for (int i = 0; i < 16; ++i) v[16 * g + i] *= s;
+        }
     }
     if (a.bias) {
-        const uint4* bp = reinterpret_cast<const uint4*>(a.bias + col0);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (q * 8 < ncols) {
-                const uint4 bv = bp[q];
+        for (int q = 0; q < CW / 8; ++q) {
+            if (col0 + 8 * q < a.N) {
+                const uint4 bv = *reinterpret_cast<const uint4*>(a.bias + col0 + 8 * q);
                 const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -100,42 +109,6 @@ __device__ __forceinline__ void epilogue_chunk(const EpiArgs& a, int row, int co
                     v[q * 8 + 2 * j] += f.x;
                     v[q * 8 + 2 * j + 1] += f.y;
                 }
-            }
-        }
-    }
-    if (a.epi == DLO_EPI_RESIDUAL) {
-        float* o = static_cast<float*>(a.out) + static_cast<size_t>(row) * a.ldo + col0;
-        const float* g = a.gate
-                             ? a.gate + static_cast<size_t>(row / a.rows_per_batch) * a.gate_ld + col0
-                             : nullptr;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            if (q * 4 < ncols) {
-                float4 x = reinterpret_cast<float4*>(o)[q];
-                float4 gg = g ? reinterpret_cast<const float4*>(g)[q] : make_float4(1.f, 1.f, 1.f, 1.f);
-                x.x += gg.x * v[q * 4 + 0];
-                x.y += gg.y * v[q * 4 + 1];
-                x.z += gg.z * v[q * 4 + 2];
-                x.w += gg.w * v[q * 4 + 3];
-                reinterpret_cast<float4*>(o)[q] = x;
-            }
-        }
-    } else {
-        if (a.epi == DLO_EPI_GELU) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
-        }
-        uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
-                                            static_cast<size_t>(row) * a.ldo + col0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (q * 8 < ncols) {
-                uint4 w;
-                w.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
-                w.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
-                w.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
-                w.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
-                o[q] = w;
             }
         }
     }
@@ -156,12 +129,6 @@ __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t x, uint32_t& out0, uin
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out1) : "r"(w1), "r"(kScale));
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-constexpr int kConvWarps = 4;
-
 template <int BN, int STAGES, bool FP8>
 struct SmemPlan {
     static constexpr int B_TILE = BN * BK * 2;            // bf16 operand tile (MMA reads)
@@ -169,7 +136,8 @@ struct SmemPlan {
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = STAGES * A_TILE;
     static constexpr int RAW_OFF = B_OFF + STAGES * B_TILE;
-    static constexpr int BAR_OFF = RAW_OFF + STAGES * RAW_TILE;
+    static constexpr int STG_OFF = RAW_OFF + STAGES * RAW_TILE;   // 4 warps x 2 boxes
+    static constexpr int BAR_OFF = STG_OFF + 8 * STG_BYTES;
     // full[STAGES], empty[STAGES], conv[STAGES], tfull[2], tempty[2], drain
     static constexpr int TMEM_SLOT_OFF = BAR_OFF + (3 * STAGES + 5) * 8;
     static constexpr int ABORT_OFF = TMEM_SLOT_OFF + 4;
@@ -181,7 +149,7 @@ struct SmemPlan {
 template <int BN, int STAGES, bool FP8>
 __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const EpiArgs args) {
+                const __grid_constant__ CUtensorMap tmO, const EpiArgs args) {
     using P = SmemPlan<BN, STAGES, FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -214,6 +182,7 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8>::THREADS, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmO);
     }
     if (warp == 1) {
         tmem_alloc(sbase + P::TMEM_SLOT_OFF, 2 * BN);
@@ -311,9 +280,13 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8>::THREADS, 1)
             mbar_wait(bar_drain, 0, nullptr);
         }
     } else if (warp >= 2 && warp < 6) {
-        // ---------------- epilogue
-        const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
+        // ---------------- epilogue: warp q owns accumulator rows 32q .. 32q+31
+        const int q = warp & 3;
+        const uint32_t stg0 = sbase + P::STG_OFF + q * 2 * STG_BYTES;
+        uint8_t* stg0p = smem + P::STG_OFF + q * 2 * STG_BYTES;
+        int bi = 0;   // staging buffer toggle
         int t = 0;
+        const bool residual = args.epi == DLO_EPI_RESIDUAL;
         for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++t) {
             const int acc = t & 1;
             const uint32_t aph = (t >> 1) & 1;
@@ -326,21 +299,101 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8>::THREADS, 1)
                 break;
             }
             tc_fence_after();
-            const int row = mb * BM + quarter * 32 + lane;
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+            const int row0 = mb * BM + q * 32;
+            const int row = row0 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+            if (residual) {
+                // 32-column fp32 boxes: delta = gate * (acc * s + b), added into x by TMA
+                const float* grow = args.gate ? args.gate + static_cast<size_t>(min(row, args.M - 1) /
+                                                                                 args.rows_per_batch) *
+                                                                args.gate_ld
+                                              : nullptr;
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr + c0, r);
-                tmem_wait_ld();
-                const int col0 = nb * BN + c0;
-                const int ncols = min(32, args.N - col0);
-                if (row < args.M && ncols > 0) epilogue_chunk(args, row, col0, ncols, r);
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    const int col0 = nb * BN + c0;
+                    if (col0 >= args.N) break;
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + c0, r);
+                    tmem_wait_ld();
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                    scale_bias<32>(args, col0, v);
+                    if (grow) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            if (col0 + 4 * j < args.N) {
+                                const float4 g = *reinterpret_cast<const float4*>(grow + col0 + 4 * j);
+                                v[4 * j] *= g.x;
+                                v[4 * j + 1] *= g.y;
+                                v[4 * j + 2] *= g.z;
+                                v[4 * j + 3] *= g.w;
+                            }
+                        }
+                    }
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    uint8_t* box = stg0p + bi * STG_BYTES;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<float4*>(box + sw128(lane, j)) =
+                            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_reduce_add_2d(&tmO, stg0 + bi * STG_BYTES, col0, row0);
+                        bulk_commit();
+                    }
+                    bi ^= 1;
+                }
+            } else {
+                // 64-column bf16 boxes: y = [GELU](acc * s + b), stored by TMA
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 64) {
+                    const int col0 = nb * BN + c0;
+                    if (col0 >= args.N) break;
+                    uint32_t r0[32], r1[32];
+                    tmem_ld_32x32b_x32(taddr + c0, r0);
+                    tmem_ld_32x32b_x32(taddr + c0 + 32, r1);
+                    tmem_wait_ld();
+                    float v[64];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        v[i] = __uint_as_float(r0[i]);
+                        v[32 + i] = __uint_as_float(r1[i]);
+                    }
+                    scale_bias<64>(args, col0, v);
+                    if (args.epi == DLO_EPI_GELU) {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) v[i] = gelu_tanh(v[i]);
+                    }
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    uint8_t* box = stg0p + bi * STG_BYTES;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint4 w;
+                        w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+                        w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+                        w.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+                        w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+                        *reinterpret_cast<uint4*>(box + sw128(lane, j)) = w;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmO, stg0 + bi * STG_BYTES, col0, row0);
+                        bulk_commit();
+                    }
+                    bi ^= 1;
+                }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_tempty + acc * 8);
         }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     } else if constexpr (FP8) {
         if (warp >= 6) {
             // ---------------- e4m3 -> bf16 converters (4 warps)
@@ -366,7 +419,7 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8>::THREADS, 1)
                         uint4 o;
                         e4m3x4_to_bf16x4(v.x, o.x, o.y);
                         e4m3x4_to_bf16x4(v.y, o.z, o.w);
-                        *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = o;
+                        *reinterpret_cast<uint4*>(dst + sw128(r, c)) = o;
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -410,24 +463,20 @@ EncodeTiledFn get_encode() {
     return fn;
 }
 
-// Row-major [rows, cols] matrix with row pitch ld elements; box of box_rows
-// x 64 elements, zero fill out of bounds.  bf16 tiles use the 128-byte
-// swizzle the MMA descriptors expect; e4m3 tiles (64-byte rows) are loaded
-// unswizzled for the converter warps.
-bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, long long ld,
-              int box_rows, bool e4m3) {
+// Row-major [rows, cols] matrix with row pitch ld elements of es_bytes; box of
+// box_rows x box_cols, zero fill out of bounds on loads, clipping on stores.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int es_bytes,
+              long long rows, long long cols, long long ld, int box_rows, int box_cols,
+              CUtensorMapSwizzle sw) {
     EncodeTiledFn enc = get_encode();
     if (!enc) return false;
-    const int es_bytes = e4m3 ? 1 : 2;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * es_bytes};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t es[2] = {1, 1};
-    return enc(m, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-               const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               e4m3 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
+    return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int g_num_sms = 0;
@@ -443,16 +492,27 @@ cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* la
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    CUtensorMap ta, tb;
-    if (!make_map(&ta, p.A, p.M, p.K, p.K, BM, false)) return cudaErrorInvalidValue;
-    if (!make_map(&tb, p.W, p.N, p.K, p.K, BN, FP8)) return cudaErrorInvalidValue;
+    CUtensorMap ta, tb, to;
+    if (!make_map(&ta, p.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.M, p.K, p.K, BM, BK,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (FP8) {
+        if (!make_map(&tb, p.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.N, p.K, p.K, BN, BK,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    } else if (!make_map(&tb, p.W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.N, p.K, p.K, BN, BK,
+                         CU_TENSOR_MAP_SWIZZLE_128B)) {
+        return cudaErrorInvalidValue;
+    }
+    const bool residual = p.epi == DLO_EPI_RESIDUAL;
+    if (!make_map(&to, p.out, residual ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  residual ? 4 : 2, p.M, p.N, p.ldo, 32, residual ? 32 : 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
     EpiArgs a;
     a.M = p.M;
     a.N = p.N;
     a.K = p.K;
     a.epi = p.epi;
-    a.out = p.out;
-    a.ldo = p.ldo;
     a.bias = static_cast<const __nv_bfloat16*>(p.bias);
     a.scales = p.scales;
     a.scale_seg = p.scale_seg > 0 ? p.scale_seg : p.N;
@@ -463,11 +523,19 @@ cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* la
     a.num_m = (p.M + BM - 1) / BM;
     a.num_n = (p.N + BN - 1) / BN;
     a.num_tiles = a.num_m * a.num_n;
-    a.w8 = nullptr;
     const int grid = a.num_tiles < g_num_sms ? a.num_tiles : g_num_sms;
-    gemm_kernel<BN, STAGES, FP8><<<grid, PL::THREADS, PL::BYTES, s>>>(ta, tb, a);
+    gemm_kernel<BN, STAGES, FP8><<<grid, PL::THREADS, PL::BYTES, s>>>(ta, tb, to, a);
     ++*launches;
     return cudaGetLastError();
+}
+
+int forced_bn() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = std::getenv("DLO_GEMM_BN");
+        v = e ? std::atoi(e) : 0;
+    }
+    return v;
 }
 
 }  // namespace
@@ -485,15 +553,20 @@ int gemm_num_sms() {
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
     if (p.M <= 0) return cudaSuccess;
     gemm_num_sms();
-    // Pick the N tile that minimises (waves x tile width) over the SMs.
+    // N tile: 256-wide tiles need 3/4 of the shared-memory bandwidth per FLOP
+    // of 128-wide ones; pick the smaller (waves x width / efficiency).
+    // DLO_GEMM_BN=128|256 forces one (tuning).
     const long long num_m = (p.M + BM - 1) / BM;
     auto cost = [&](int bn) {
         const long long tiles = num_m * ((p.N + bn - 1) / bn);
-        return ((tiles + g_num_sms - 1) / g_num_sms) * bn;
+        const double eff = bn == 256 ? 1.0 : 0.75;
+        return static_cast<double>((tiles + g_num_sms - 1) / g_num_sms) * bn / eff;
     };
-    const bool wide = cost(256) <= cost(128);
+    bool wide = cost(256) <= cost(128);
+    if (forced_bn() == 128) wide = false;
+    if (forced_bn() == 256) wide = true;
     if (p.w_dtype == DLO_DT_E4M3)
-        return wide ? run_gemm<256, 3, true>(p, s, launches) : run_gemm<128, 5, true>(p, s, launches);
+        return wide ? run_gemm<256, 3, true>(p, s, launches) : run_gemm<128, 4, true>(p, s, launches);
     if (p.w_dtype != DLO_DT_BF16) return cudaErrorNotSupported;
     return wide ? run_gemm<256, 4, false>(p, s, launches) : run_gemm<128, 6, false>(p, s, launches);
 }
