@@ -45,6 +45,9 @@ def parse():
     p.add_argument("--resident", type=int, default=0)
     p.add_argument("--host", default="pinned", choices=["pinned", "register"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--sweep", action="store_true",
+                   help="residency sweep (k = 0,2,4,8) on the 40-block hidden-5120 stack at 8192 "
+                        "tokens and a 16 MB..1 GB staging sweep; prints one JSON line")
     return p.parse_args()
 
 
@@ -409,8 +412,137 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
         dist.destroy_process_group()
 
 
+def link_peak_gbs(torch, dev) -> float:
+    hbuf = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    dbuf = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    best = 0.0
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dbuf.copy_(hbuf, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        best = max(best, (1 << 30) / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    return best
+
+
+def run_sweep(args):
+    """Residency and staging sweep (one JSON line)."""
+    import torch
+    import layerwise_weight_offload_slot_gb300 as dlo
+    from layerwise_weight_offload_slot_gb300.stack import HostBlocks, OffloadStack
+
+    dev = torch.device("cuda", 0)
+    link = link_peak_gbs(torch, dev)
+    out = {"metric": "residency and staging sweep", "link_gbs_measured": link}
+
+    # ---- residency: k = 0, 2, 4, 8 resident leading blocks
+    cfg = synth.CFG_SWEEP
+    bb = None
+    host = None
+    res = []
+    x0 = torch.from_numpy(synth.activations(cfg)).to(torch.bfloat16).to(dev)
+    e = torch.from_numpy(synth.condition(cfg)).float().to(dev)
+    ctx = torch.from_numpy(synth.text_context(cfg)).to(torch.bfloat16).to(dev)
+    ref = None
+    for k in (0, 2, 4, 8):
+        st = OffloadStack(block_kind=cfg.kind, n_blocks=cfg.n_blocks, hidden=cfg.hidden,
+                          heads=cfg.heads, head_dim=cfg.head_dim, ffn=cfg.ffn,
+                          text_dim=cfg.text_dim, max_batch=cfg.batch, max_tokens=cfg.tokens,
+                          max_text_tokens=cfg.text_tokens, host=host)
+        if host is None:
+            host = st.host
+            st._own_host = True
+            st.pack_all(lambda i: synth.block_params(cfg, i))
+        bb = st.block_bytes
+        st.attach()
+        st.set_resident(k)
+        y = st.forward(x0, e, ctx)
+        torch.cuda.synchronize()
+        st.wait()
+        exact = None
+        if ref is None:
+            ref = y.clone()
+        else:
+            exact = bool(torch.equal(y, ref))
+        cs = st.compute_stream
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(cs)
+        for _ in range(args.steps):
+            st.forward(x0, e, ctx, out=y)
+        e1.record(cs)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        st.set_timing(1)
+        s0 = st.stats()
+        st.forward(x0, e, ctx, out=y)
+        torch.cuda.synchronize()
+        st.wait()
+        s1 = st.stats()
+        copy = s1["copy_ms"] - s0["copy_ms"]
+        exposed = s1["exposed_wait_ms"] - s0["exposed_wait_ms"]
+        n_exec = s1["timed_execs"] - s0["timed_execs"]
+        slots_ok = all(st.verify_slot(s) for s in (0, 1) if st.stats()["slot_block"][s] >= 0)
+        res.append({"k": k, "steps_per_s": 1e3 / ms, "ms_per_step": ms,
+                    "streamed_gb_per_step": (cfg.n_blocks - k) * bb / 1e9,
+                    "h2d_gbs": n_exec * bb / (copy * 1e-3) / 1e9 if copy > 0 else None,
+                    "overlap_fraction": 1.0 - exposed / copy if copy > 0 else None,
+                    "output_equals_k0": exact, "slots_bit_exact": slots_ok})
+        st._own_host = False      # the host blocks are shared by the four contexts
+        st.close()
+    host.close()
+    out["residency"] = {"workload": cfg.name, "block_bytes": bb, "runs": res}
+
+    # ---- staging: opaque byte blocks 16 MB .. 1 GB
+    stg = []
+    for mb in (16, 32, 64, 128, 256, 512, 1024):
+        size = mb << 20
+        n = 4 if mb <= 256 else 2
+        for host_mode in ("pinned", "register"):
+            hb = None
+            for staging in (dlo.STAGE_MEMCPY, dlo.STAGE_GATHER):
+                st = OffloadStack(block_kind=dlo.BLOCK_BYTES, n_blocks=n, bytes_block=size,
+                                  staging=staging, host_mode=host_mode,
+                                  host=hb if host_mode == "pinned" else None)
+                if host_mode == "pinned" and hb is None:
+                    hb = st.host
+                sums = []
+                for i in range(n):
+                    v = st.host.view(i)
+                    if staging == dlo.STAGE_MEMCPY or host_mode == "register":
+                        v[:] = synth.staging_bytes(size, seed=i)
+                    sums.append(int(v.view(np.uint64).sum(dtype=np.uint64)))
+                st.attach()
+                st.set_timing(1)
+                ok = True
+                for _ in range(max(2, args.steps // 2)):
+                    got = st.forward_bytes()
+                    torch.cuda.synchronize()
+                    st.wait()
+                    ok &= [int(x) for x in got.cpu().numpy().view(np.uint64)] == sums
+                ok &= all(st.verify_slot(s) for s in (0, 1) if st.stats()["slot_block"][s] >= 0)
+                s1 = st.stats()
+                gbs = s1["timed_execs"] * size / (s1["copy_ms"] * 1e-3) / 1e9
+                stg.append({"block_mb": mb, "host": host_mode,
+                            "staging": "memcpy" if staging == dlo.STAGE_MEMCPY else "gather",
+                            "h2d_gbs": gbs, "frac_of_link": gbs / link,
+                            "overlap_fraction": 1.0 - s1["exposed_wait_ms"] / s1["copy_ms"],
+                            "bit_exact": bool(ok),
+                            "registered_read_only": s1["registered_read_only"]})
+                if host_mode == "pinned":
+                    st._own_host = False
+                st.close()
+            if hb is not None:
+                hb.close()
+    out["staging"] = stg
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
+    if args.sweep:
+        run_sweep(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus else 1)))
     if "WORLD_SIZE" not in os.environ:

@@ -73,7 +73,7 @@ class OffloadStack:
                  max_batch: int = 1, max_tokens: int = 1, max_text_tokens: int = 0,
                  wdtype: int = W_BF16, eps: float = 1e-6, staging: int = STAGE_MEMCPY,
                  host_mode: str = "pinned", register_budget_bytes: int = 0,
-                 bytes_block: int = 0, device: int = 0):
+                 bytes_block: int = 0, device: int = 0, host: "HostBlocks | None" = None):
         self.desc = make_desc(block_kind=block_kind, n_blocks=n_blocks, hidden=hidden, heads=heads,
                               head_dim=head_dim, ffn=ffn, cond_dim=cond_dim, text_dim=text_dim,
                               max_batch=max_batch, max_tokens=max_tokens,
@@ -96,7 +96,9 @@ class OffloadStack:
         self.ws_ptr = _round(self._ws.data_ptr(), 256)
         self.compute_stream = torch.cuda.Stream(device=self.dev)
         self.copy_stream = torch.cuda.Stream(device=self.dev)
-        self.host = HostBlocks(n_blocks, self.block_bytes, host_mode)
+        # host blocks may be shared between contexts (pinned mode only)
+        self._own_host = host is None
+        self.host = host if host is not None else HostBlocks(n_blocks, self.block_bytes, host_mode)
         self.host_mode = host_mode
         self.n_blocks = n_blocks
         self.kind = block_kind
@@ -185,7 +187,8 @@ class OffloadStack:
         if self.ctx:
             st = dlo_destroy(self.ctx)
             self.ctx = 0
-        self.host.close()
+        if self._own_host:
+            self.host.close()
         self._resident = []
         return st
 
