@@ -7,8 +7,13 @@
 // the padded columns add nothing to Q K^T and are dropped from O.  Keys past
 // nk are masked to -inf; query rows past nq are not stored.
 //
-// This version issues mma.sync m16n8k16 (bf16 in, fp32 accumulate).
+// This kernel issues mma.sync m16n8k16 (bf16 in, fp32 accumulate); it serves
+// head dims that are not multiples of 64 (e.g. 72, zero-padded to 80).  Head
+// dims 64 and 128 run on the tcgen05 kernel in attention_tc.cu.
 #include <cuda_bf16.h>
+
+#include <cstdlib>
+#include <string>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -235,9 +240,17 @@ cudaError_t run(const void* Q, const void* K, const void* V, void* O, int batch,
 
 cudaError_t launch_attention(const void* Q, const void* K, const void* V, void* O, int batch,
                              int heads, int hd, int nq, int nk, int ldq, int ldk, int ldv, int ldo,
-                             cudaStream_t s, unsigned long long* launches) {
+                             int* err, cudaStream_t s, unsigned long long* launches) {
     if (nq <= 0 || batch <= 0 || heads <= 0) return cudaSuccess;
     if (nk <= 0) return cudaErrorInvalidValue;
+    static int force_sync = -1;
+    if (force_sync < 0) {
+        const char* e = std::getenv("DLO_ATTN");
+        force_sync = (e && std::string(e) == "sync") ? 1 : 0;
+    }
+    if (!force_sync && attention_tc_supported(hd))
+        return launch_attention_tc(Q, K, V, O, batch, heads, hd, nq, nk, ldq, ldk, ldv, ldo, err, s,
+                                   launches);
     const int hdp = (hd + 15) / 16 * 16;
     switch (hdp) {
         case 16: return run<16>(Q, K, V, O, batch, heads, hd, nq, nk, ldq, ldk, ldv, ldo, s, launches);

@@ -1,0 +1,380 @@
+// Non-causal multi-head attention on the 5th-generation tensor cores, for head
+// dims that are multiples of 64 (64, 128).  O = softmax(Q K^T / sqrt(hd)) V.
+//
+// One CTA per (128 query rows, head, batch); 6 warps:
+//   warp 0      TMA: the Q tile once, then K_j and V_j tiles of 128 keys into
+//               2-stage rings (3-D tensor maps over [batch, rows, columns], so
+//               rows past a batch's end are zero-filled)
+//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM S
+//               buffers (128 fp32 columns each), and O += P_j V_j into the TMEM
+//               O accumulator; issue order S_0, S_1, PV_0, S_2, PV_1, ... so the
+//               tensor core computes S_{j+1} while the softmax warps work on S_j
+//   warps 2..5  softmax, one thread per query row (its TMEM lane): load S_j,
+//               mask keys past nk, running max in the log2 domain, p = 2^(s -
+//               m), row sum, P_j as bf16 into 128-byte-swizzled shared memory
+//               (the K-major A operand of P V).  The reference max only moves
+//               when a row's max grows by more than 8 (a factor 256), and only
+//               then is that row's O rescaled in TMEM (ld, scale, st) -- the
+//               p values stay below 2^8, which bf16 and fp32 hold exactly in
+//               range.  At the end O / l is written as bf16.
+// V is the B operand of P V in its natural [key][dim] layout, i.e. MN-major
+// (dims contiguous): 64-dim blocks of 128-byte rows, one row per key.
+//
+// Every mbarrier wait is bounded; a wait that runs out sets the error word
+// and the abort flag, every role leaves its loop, in-flight TMA loads and
+// MMAs are drained (bounded) and TMEM is freed.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dlo {
+
+namespace {
+
+constexpr int TQ = 128;          // query rows per CTA (MMA M, TMEM lanes)
+constexpr int TK = 128;          // keys per tile
+constexpr int kThreadsA = 192;
+
+template <int HD>
+struct AttnPlan {
+    static constexpr int NB = HD / 64;                  // 64-column blocks per row
+    static constexpr int BLK = 128 * 128;               // one 128-row x 128-byte block
+    static constexpr int Q_BYTES = TQ * HD * 2;
+    static constexpr int KV_BYTES = TK * HD * 2;
+    static constexpr int P_BYTES = TQ * TK * 2;
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = Q_OFF + Q_BYTES;       // 2 stages
+    static constexpr int V_OFF = K_OFF + 2 * KV_BYTES;  // 2 stages
+    static constexpr int P_OFF = V_OFF + 2 * KV_BYTES;
+    static constexpr int BAR_OFF = P_OFF + P_BYTES;
+    // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2],
+    // p_full, pv_done, drain
+    static constexpr int NBARS = 1 + 12 + 3;
+    static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int ABORT_OFF = TMEM_SLOT_OFF + 4;
+    static constexpr int USED = ABORT_OFF + 4 + 1024;
+    // at least 116 KB, so one CTA per SM owns all 512 TMEM columns
+    static constexpr int BYTES = USED > 118784 ? USED : 118784;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t O_COL = 256;             // S buffers at columns 0 and 128
+};
+
+__device__ __forceinline__ uint32_t sw128_off(int r, int j) {
+    return static_cast<uint32_t>(r * 128 + ((j ^ (r & 7)) << 4));
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreadsA, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O, int nq,
+                   int nk, int ldo, float scale_log2, int* err) {
+    using P = AttnPlan<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t bar = sb + P::BAR_OFF;
+    const uint32_t q_full = bar;
+    const uint32_t k_full = bar + 8, k_empty = bar + 24;
+    const uint32_t v_full = bar + 40, v_empty = bar + 56;
+    const uint32_t s_full = bar + 72, s_free = bar + 88;
+    const uint32_t p_full = bar + 104, pv_done = bar + 112, drain = bar + 120;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + P::TMEM_SLOT_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P::ABORT_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int ntiles = (nk + TK - 1) / TK;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(k_full + 8 * i, 1);
+            mbar_init(k_empty + 8 * i, 1);
+            mbar_init(v_full + 8 * i, 1);
+            mbar_init(v_empty + 8 * i, 1);
+            mbar_init(s_full + 8 * i, 1);
+            mbar_init(s_free + 8 * i, 4);
+        }
+        mbar_init(p_full, 4);
+        mbar_init(pv_done, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(sb + P::TMEM_SLOT_OFF, P::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto fail = [&]() {
+        *abort_flag = 1;
+        if (err) atomicExch(err, 1);
+    };
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer
+        bool ok = true;
+        uint32_t issued_k = 0, issued_v = 0;      // stages with a load in flight
+        uint32_t par_k = 0, par_v = 0;            // parity of that load's phase
+        mbar_arrive_expect_tx(q_full, P::Q_BYTES);
+        for (int blk = 0; blk < P::NB; ++blk)
+            tma_load_3d(sb + P::Q_OFF + blk * P::BLK, &tmQ, h * HD + blk * 64, qt * TQ, b, q_full);
+        for (int j = 0; ok && j < ntiles; ++j) {
+            const int st = j & 1;
+            const uint32_t ph = (j >> 1) & 1;
+            if (!mbar_wait(k_empty + 8 * st, ph ^ 1, abort_flag)) { fail(); ok = false; break; }
+            mbar_arrive_expect_tx(k_full + 8 * st, P::KV_BYTES);
+            for (int blk = 0; blk < P::NB; ++blk)
+                tma_load_3d(sb + P::K_OFF + st * P::KV_BYTES + blk * P::BLK, &tmK, h * HD + blk * 64,
+                            j * TK, b, k_full + 8 * st);
+            issued_k |= 1u << st;
+            par_k = (par_k & ~(1u << st)) | (ph << st);
+            if (!mbar_wait(v_empty + 8 * st, ph ^ 1, abort_flag)) { fail(); ok = false; break; }
+            mbar_arrive_expect_tx(v_full + 8 * st, P::KV_BYTES);
+            for (int blk = 0; blk < P::NB; ++blk)
+                tma_load_3d(sb + P::V_OFF + st * P::KV_BYTES + blk * P::BLK, &tmV, h * HD + blk * 64,
+                            j * TK, b, v_full + 8 * st);
+            issued_v |= 1u << st;
+            par_v = (par_v & ~(1u << st)) | (ph << st);
+        }
+        if (!ok || *abort_flag) {
+            mbar_wait(q_full, 0, nullptr);
+            for (int i = 0; i < 2; ++i) {
+                if (issued_k & (1u << i)) mbar_wait(k_full + 8 * i, (par_k >> i) & 1u, nullptr);
+                if (issued_v & (1u << i)) mbar_wait(v_full + 8 * i, (par_v >> i) & 1u, nullptr);
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer
+        constexpr uint32_t idesc_s = idesc_bf16_f32(TQ, TK);
+        constexpr uint32_t idesc_o = idesc_bf16_f32(TQ, HD, true);
+        bool ok = mbar_wait(q_full, 0, abort_flag);
+        auto issue_s = [&](int j) -> bool {
+            const int st = j & 1;
+            const uint32_t ph = (j >> 1) & 1;
+            if (!mbar_wait(k_full + 8 * st, ph, abort_flag)) return false;
+            if (!mbar_wait(s_free + 8 * st, ph ^ 1, abort_flag)) return false;
+            tc_fence_after();
+            const uint32_t d = tmem + st * TK;
+#pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * P::BLK + (kk & 3) * 32;
+                tc_mma_f16(d, sw128_kmajor_desc(sb + P::Q_OFF + off),
+                           sw128_kmajor_desc(sb + P::K_OFF + st * P::KV_BYTES + off), idesc_s, kk > 0);
+            }
+            tc_commit(s_full + 8 * st);
+            tc_commit(k_empty + 8 * st);
+            return true;
+        };
+        auto issue_pv = [&](int j) -> bool {
+            const int st = j & 1;
+            const uint32_t ph = (j >> 1) & 1;
+            if (!mbar_wait(p_full, j & 1, abort_flag)) return false;
+            if (!mbar_wait(v_full + 8 * st, ph, abort_flag)) return false;
+            tc_fence_after();
+            const uint32_t d = tmem + P::O_COL;
+#pragma unroll
+            for (int kk = 0; kk < TK / 16; ++kk) {
+                const uint32_t a_off = (kk >> 2) * P::BLK + (kk & 3) * 32;
+                tc_mma_f16(d, sw128_kmajor_desc(sb + P::P_OFF + a_off),
+                           sw128_mnmajor_desc(sb + P::V_OFF + st * P::KV_BYTES + kk * 2048, P::BLK),
+                           idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(pv_done);
+            tc_commit(v_empty + 8 * st);
+            return true;
+        };
+        if (ok) ok = issue_s(0);
+        for (int j = 1; ok && j < ntiles; ++j) ok = issue_s(j) && issue_pv(j - 1);
+        if (ok) ok = issue_pv(ntiles - 1);
+        if (!ok) fail();
+        if (*abort_flag) {
+            tc_commit(drain);
+            mbar_wait(drain, 0, nullptr);
+        }
+    } else if (warp >= 2) {
+        // ---------------- softmax: thread = query row
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            const int st = j & 1;
+            const uint32_t ph = (j >> 1) & 1;
+            bool got = mbar_wait(s_full + 8 * st, ph, abort_flag);
+            got = __all_sync(0xFFFFFFFFu, got);
+            if (!got) { ok = false; break; }
+            tc_fence_after();
+            float v[TK];
+#pragma unroll
+            for (int c = 0; c < TK / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tl + st * TK + c * 32, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[c * 32 + i] = __uint_as_float(r[i]) * scale_log2;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free + 8 * st);
+            const int kvalid = nk - j * TK;
+            float mt = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < TK; ++i) {
+                if (i >= kvalid) v[i] = -INFINITY;
+                mt = fmaxf(mt, v[i]);
+            }
+            const bool resc = mt > m_ref + 8.f;
+            const float m_new = resc ? mt : m_ref;
+            const float corr = resc ? ex2_approx(m_ref - m_new) : 1.f;
+            float rs = 0.f;
+#pragma unroll
+            for (int i = 0; i < TK; ++i) {
+                v[i] = ex2_approx(v[i] - m_new);
+                rs += v[i];
+            }
+            l = l * corr + rs;
+            m_ref = m_new;
+            if (j > 0) {
+                got = mbar_wait(pv_done, (j - 1) & 1, abort_flag);
+                got = __all_sync(0xFFFFFFFFu, got);
+                if (!got) { ok = false; break; }
+                tc_fence_after();
+            }
+            // P_j row -> shared memory (two 64-key blocks, 8 chunks of 8 keys each)
+#pragma unroll
+            for (int c = 0; c < TK / 8; ++c) {
+                uint4 w;
+                w.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
+                w.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+                w.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+                w.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+                *reinterpret_cast<uint4*>(smem + P::P_OFF + (c >> 3) * P::BLK + sw128_off(row, c & 7)) = w;
+            }
+            if (j > 0 && __any_sync(0xFFFFFFFFu, resc)) {
+#pragma unroll 1
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tl + P::O_COL + c * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+                    tmem_st_32x32b_x32(tl + P::O_COL + c * 32, r);
+                }
+                tmem_wait_st();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        if (ok) {
+            bool got = mbar_wait(pv_done, (ntiles - 1) & 1, abort_flag);
+            got = __all_sync(0xFFFFFFFFu, got);
+            ok = got;
+        }
+        if (!ok) {
+            if (lane == 0) fail();
+        } else {
+            tc_fence_after();
+            const float inv = 1.f / l;
+            const int grow = qt * TQ + row;
+            __nv_bfloat16* orow = O + (static_cast<size_t>(b) * nq + grow) * ldo + h * HD;
+#pragma unroll 1
+            for (int c = 0; c < HD / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tl + P::O_COL + c * 32, r);
+                tmem_wait_ld();
+                if (grow < nq) {
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(r[8 * k4 + 0]) * inv, __uint_as_float(r[8 * k4 + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(r[8 * k4 + 2]) * inv, __uint_as_float(r[8 * k4 + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(r[8 * k4 + 4]) * inv, __uint_as_float(r[8 * k4 + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(r[8 * k4 + 6]) * inv, __uint_as_float(r[8 * k4 + 7]) * inv);
+                        *reinterpret_cast<uint4*>(orow + c * 32 + 8 * k4) = w;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, P::TMEM_COLS);
+    }
+}
+
+// [batch, rows, cols] view of a bf16 matrix whose batch b, row r starts at
+// base + (b * rows + r) * ld; cols = columns that may be read (from base).
+bool make_map3(CUtensorMap* m, const void* base, int batch, int rows, int cols, int ld) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2,
+                             static_cast<cuuint64_t>(ld) * 2 * static_cast<cuuint64_t>(rows)};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+template <int HD>
+cudaError_t run_tc(const void* Q, const void* K, const void* V, void* O, int batch, int heads,
+                   int nq, int nk, int ldq, int ldk, int ldv, int ldo, int* err, cudaStream_t s,
+                   unsigned long long* launches) {
+    using P = AttnPlan<HD>;
+    static_assert(P::BYTES <= 227 * 1024, "attention shared memory plan exceeds 227 KB");
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, P::BYTES);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int D = heads * HD;
+    CUtensorMap tq, tk, tv;
+    if (!make_map3(&tq, Q, batch, nq, D, ldq) || !make_map3(&tk, K, batch, nk, D, ldk) ||
+        !make_map3(&tv, V, batch, nk, D, ldv))
+        return cudaErrorInvalidValue;
+    const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
+    dim3 grid((nq + TQ - 1) / TQ, heads, batch);
+    attn_tc_kernel<HD><<<grid, kThreadsA, P::BYTES, s>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(O),
+                                                        nq, nk, ldo, scale_log2, err);
+    ++*launches;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attention_tc_supported(int hd) { return hd == 64 || hd == 128; }
+
+cudaError_t launch_attention_tc(const void* Q, const void* K, const void* V, void* O, int batch,
+                                int heads, int hd, int nq, int nk, int ldq, int ldk, int ldv,
+                                int ldo, int* err, cudaStream_t s, unsigned long long* launches) {
+    if (hd == 64)
+        return run_tc<64>(Q, K, V, O, batch, heads, nq, nk, ldq, ldk, ldv, ldo, err, s, launches);
+    if (hd == 128)
+        return run_tc<128>(Q, K, V, O, batch, heads, nq, nk, ldq, ldk, ldv, ldo, err, s, launches);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace dlo

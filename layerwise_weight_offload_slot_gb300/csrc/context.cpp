@@ -297,7 +297,7 @@ dlo_status run_block(dlo_ctx* c, const uint8_t* W, int B, int N, int L, const vo
         const double flops = 4.0 * B * H * nq * static_cast<double>(nk) * hd;
         const double bytes = 2.0 * B * (2.0 * nq + 2.0 * nk) * D;
         return c->timed(DLO_K_ATTENTION, flops, bytes, s, [&] {
-            return launch_attention(q, k, v, out, B, H, hd, nq, nk, ldq, ldk, ldv, D, s, nl);
+            return launch_attention(q, k, v, out, B, H, hd, nq, nk, ldq, ldk, ldv, D, c->err_word(), s, nl);
         });
     };
     auto ln = [&](const float* shift, const float* scale, const void* lw, const void* lb) {
@@ -896,7 +896,7 @@ extern "C" dlo_status dlo_op_attention(const void* Q, const void* K, const void*
     if (ldq % 8 || ldk % 8 || ldv % 8 || ldo % 8) return op_inval("ld % 8 != 0");
     if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16)) return op_inval("alignment");
     return op_result(launch_attention(Q, K, V, O, batch, heads, head_dim, nq, nk, ldq, ldk, ldv, ldo,
-                                      static_cast<cudaStream_t>(stream), &g_op_launches));
+                                      nullptr, static_cast<cudaStream_t>(stream), &g_op_launches));
 }
 
 extern "C" dlo_status dlo_op_layernorm(const float* x, int rows, int D, int rows_per_batch,

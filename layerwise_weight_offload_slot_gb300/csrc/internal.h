@@ -1,5 +1,6 @@
 // Internal declarations shared by the host runtime and the kernel files.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -74,9 +75,23 @@ struct GemmParams {
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches);
 int gemm_num_sms();
 
+// cuTensorMapEncodeTiled, resolved once through the runtime's driver entry
+// point (no link-time dependency on libcuda); NULL if unavailable.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
+
+// Attention: the tcgen05 kernel for head dims 64 and 128, the mma.sync
+// kernel otherwise (or when DLO_ATTN=sync).  err: device error word or NULL.
 cudaError_t launch_attention(const void* Q, const void* K, const void* V, void* O, int batch,
                              int heads, int hd, int nq, int nk, int ldq, int ldk, int ldv, int ldo,
-                             cudaStream_t s, unsigned long long* launches);
+                             int* err, cudaStream_t s, unsigned long long* launches);
+bool attention_tc_supported(int hd);
+cudaError_t launch_attention_tc(const void* Q, const void* K, const void* V, void* O, int batch,
+                                int heads, int hd, int nq, int nk, int ldq, int ldk, int ldv,
+                                int ldo, int* err, cudaStream_t s, unsigned long long* launches);
 
 cudaError_t launch_layernorm(const float* x, int rows, int D, int rpb, const float* shift,
                              const float* scale, int mod_ld, const void* w, const void* b,
