@@ -1,6 +1,6 @@
 // Y = A W^T on the 5th-generation tensor cores (tcgen05), sm_103a.
 //
-// Persistent kernel, one CTA per SM, 6 warps (+4 converter warps for E4M3):
+// Persistent kernel, one CTA per SM, 6 warps (+8 converter warps for E4M3):
 //   warp 0      TMA producer: 128x64 A tile and BNx64 W tile per stage,
 //               128-byte swizzle, into a STAGES-deep shared-memory ring
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16 (M=128,
@@ -16,7 +16,7 @@
 //               without reading x).  Two staging buffers per warp let the
 //               next chunk overlap the previous store.
 // The two accumulators let the epilogue of tile t overlap the mainloop of
-// tile t+1.  With E4M3 weights (FP8 = true) TMA loads the raw codes, four
+// tile t+1.  With E4M3 weights (FP8 = true) TMA loads the raw codes, eight
 // more warps widen them to bf16 in the swizzled layout the MMA reads (exact),
 // and the per-tensor scale is applied to the fp32 accumulator in the epilogue.
 //
@@ -44,7 +44,7 @@ constexpr int BM = 128;
 constexpr int BK = 64;             // 64 bf16 = 128 bytes = one swizzle row
 constexpr int A_TILE = BM * BK * 2;
 constexpr int kThreads = 192;
-constexpr int kConvWarps = 4;
+constexpr int kConvWarps = 8;
 constexpr int STG_BYTES = 32 * 128;   // one 32-row x 128-byte staging box
 
 struct EpiArgs {
@@ -114,19 +114,27 @@ __device__ __forceinline__ void scale_bias(const EpiArgs& a, int col0, float (&v
     }
 }
 
-// e4m3 -> bf16, four codes at a time, exactly: each code's sign goes to the
-// bf16 sign bit and its 7 exponent/mantissa bits to bf16 bits 4..10, which is
-// the same number scaled by 2^-120 (bf16 subnormals included); one bf16x2
-// multiply by 2^120 restores it.  out0 holds codes 0,1 and out1 codes 2,3.
-__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t x, uint32_t& out0, uint32_t& out1) {
+// e4m3 -> bf16, eight codes at a time, exactly.  For each code the 7
+// exponent/mantissa bits go to bf16 bits 4..10 and the sign to bit 15, which
+// is the same number scaled by 2^-120 (bf16 subnormals included); one bf16x2
+// multiply by 2^120 restores it.  The magnitude bytes and the sign bits
+// (pre-shifted to bit 3 of each byte) are interleaved into 16-bit lanes by
+// one byte permute per pair of codes, and one shift by 4 places both.
+// o[k] receives codes 2k and 2k+1 (code 0 = lowest byte of x0).
+__device__ __forceinline__ void e4m3x8_to_bf16x8(uint32_t x0, uint32_t x1, uint32_t (&o)[4]) {
     constexpr uint32_t kScale = 0x7B807B80u;   // bf16x2 (2^120, 2^120)
-    uint32_t w0, w1;
-    asm("prmt.b32 %0, %1, 0, 0x4140;" : "=r"(w0) : "r"(x));
-    asm("prmt.b32 %0, %1, 0, 0x4342;" : "=r"(w1) : "r"(x));
-    w0 = ((w0 & 0x00800080u) << 8) | ((w0 & 0x007F007Fu) << 4);
-    w1 = ((w1 & 0x00800080u) << 8) | ((w1 & 0x007F007Fu) << 4);
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out0) : "r"(w0), "r"(kScale));
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out1) : "r"(w1), "r"(kScale));
+    const uint32_t m0 = x0 & 0x7F7F7F7Fu, m1 = x1 & 0x7F7F7F7Fu;
+    const uint32_t s0 = (x0 >> 4) & 0x08080808u, s1 = (x1 >> 4) & 0x08080808u;
+    uint32_t w[4];
+    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(w[0]) : "r"(m0), "r"(s0));
+    asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(w[1]) : "r"(m0), "r"(s0));
+    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(w[2]) : "r"(m1), "r"(s1));
+    asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(w[3]) : "r"(m1), "r"(s1));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t t = w[k] << 4;
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[k]) : "r"(t), "r"(kScale));
+    }
 }
 
 template <int BN, int STAGES, bool FP8>
@@ -347,37 +355,37 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8>::THREADS, 1)
                     bi ^= 1;
                 }
             } else {
-                // 64-column bf16 boxes: y = [GELU](acc * s + b), stored by TMA
+                // 64-column bf16 boxes: y = [GELU](acc * s + b), stored by TMA;
+                // filled 32 columns at a time to keep registers low
 #pragma unroll 1
                 for (int c0 = 0; c0 < BN; c0 += 64) {
                     const int col0 = nb * BN + c0;
                     if (col0 >= args.N) break;
-                    uint32_t r0[32], r1[32];
-                    tmem_ld_32x32b_x32(taddr + c0, r0);
-                    tmem_ld_32x32b_x32(taddr + c0 + 32, r1);
-                    tmem_wait_ld();
-                    float v[64];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        v[i] = __uint_as_float(r0[i]);
-                        v[32 + i] = __uint_as_float(r1[i]);
-                    }
-                    scale_bias<64>(args, col0, v);
-                    if (args.epi == DLO_EPI_GELU) {
-#pragma unroll
-                        for (int i = 0; i < 64; ++i) v[i] = gelu_tanh(v[i]);
-                    }
                     if (lane == 0) bulk_wait_read<1>();
                     __syncwarp();
                     uint8_t* box = stg0p + bi * STG_BYTES;
+#pragma unroll 1
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(taddr + c0 + 32 * half, r);
+                        tmem_wait_ld();
+                        float v[32];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        uint4 w;
-                        w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
-                        w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
-                        w.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
-                        w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
-                        *reinterpret_cast<uint4*>(box + sw128(lane, j)) = w;
+                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                        scale_bias<32>(args, col0 + 32 * half, v);
+                        if (args.epi == DLO_EPI_GELU) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint4 w;
+                            w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+                            w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+                            w.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+                            w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+                            *reinterpret_cast<uint4*>(box + sw128(lane, 4 * half + j)) = w;
+                        }
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -396,8 +404,8 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8>::THREADS, 1)
         __syncwarp();
     } else if constexpr (FP8) {
         if (warp >= 6) {
-            // ---------------- e4m3 -> bf16 converters (4 warps)
-            const int ct = threadIdx.x - 6 * 32;       // 0..127
+            // ---------------- e4m3 -> bf16 converters (kConvWarps warps)
+            const int ct = threadIdx.x - 6 * 32;
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
@@ -416,10 +424,9 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8>::THREADS, 1)
                     for (int i = ct; i < BN * 8; i += kConvWarps * 32) {
                         const int r = i >> 3, c = i & 7;
                         const uint2 v = *reinterpret_cast<const uint2*>(raw + r * 64 + c * 8);
-                        uint4 o;
-                        e4m3x4_to_bf16x4(v.x, o.x, o.y);
-                        e4m3x4_to_bf16x4(v.y, o.z, o.w);
-                        *reinterpret_cast<uint4*>(dst + sw128(r, c)) = o;
+                        uint32_t o[4];
+                        e4m3x8_to_bf16x8(v.x, v.y, o);
+                        *reinterpret_cast<uint4*>(dst + sw128(r, c)) = make_uint4(o[0], o[1], o[2], o[3]);
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
