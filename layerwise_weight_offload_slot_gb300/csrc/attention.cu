@@ -8,8 +8,8 @@
 // nk are masked to -inf; query rows past nq are not stored.
 //
 // This kernel issues mma.sync m16n8k16 (bf16 in, fp32 accumulate); it serves
-// head dims that are not multiples of 64 (e.g. 72, zero-padded to 80).  Head
-// dims 64 and 128 run on the tcgen05 kernel in attention_tc.cu.
+// the head dims the tcgen05 kernel in attention_tc.cu does not (it takes 64,
+// 72, 80 and 128).
 #include <cuda_bf16.h>
 
 #include <cstdlib>

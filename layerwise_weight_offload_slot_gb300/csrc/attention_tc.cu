@@ -1,10 +1,13 @@
-// Non-causal multi-head attention on the 5th-generation tensor cores, for head
-// dims that are multiples of 64 (64, 128).  O = softmax(Q K^T / sqrt(hd)) V.
+// Non-causal multi-head attention on the 5th-generation tensor cores.
+// O = softmax(Q K^T / sqrt(hd)) V.  Head dims 64 and 128 are whole 64-column
+// blocks; a head dim of 64 + t (t <= 16, e.g. 72) adds a 16-column tail block
+// loaded with the 32-byte swizzle, whose columns past hd TMA fills with zeros
+// (a 4-D tensor map [batch, rows, heads, hd] ends each head at hd), so the
+// padded columns add nothing to Q K^T and are dropped from O.
 //
 // One CTA per (128 query rows, head, batch); 6 warps:
 //   warp 0      TMA: the Q tile once, then K_j and V_j tiles of 128 keys into
-//               2-stage rings (3-D tensor maps over [batch, rows, columns], so
-//               rows past a batch's end are zero-filled)
+//               2-stage rings (rows past a batch's end are zero-filled)
 //   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM S
 //               buffers (128 fp32 columns each), and O += P_j V_j into the TMEM
 //               O accumulator; issue order S_0, S_1, PV_0, S_2, PV_1, ... so the
@@ -37,17 +40,17 @@ constexpr int TQ = 128;          // query rows per CTA (MMA M, TMEM lanes)
 constexpr int TK = 128;          // keys per tile
 constexpr int kThreadsA = 192;
 
-template <int HD>
+template <int NB, bool TAIL>
 struct AttnPlan {
-    static constexpr int NB = HD / 64;                  // 64-column blocks per row
-    static constexpr int BLK = 128 * 128;               // one 128-row x 128-byte block
-    static constexpr int Q_BYTES = TQ * HD * 2;
-    static constexpr int KV_BYTES = TK * HD * 2;
+    static constexpr int HDP = NB * 64 + (TAIL ? 16 : 0);   // padded head dim
+    static constexpr int BLK = 128 * 128;                   // 128 rows x 128 B (64 cols)
+    static constexpr int TBLK = TAIL ? 128 * 32 : 0;        // 128 rows x 32 B (16 cols)
+    static constexpr int TILE = NB * BLK + TBLK;            // one Q, K or V tile
     static constexpr int P_BYTES = TQ * TK * 2;
     static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = Q_OFF + Q_BYTES;       // 2 stages
-    static constexpr int V_OFF = K_OFF + 2 * KV_BYTES;  // 2 stages
-    static constexpr int P_OFF = V_OFF + 2 * KV_BYTES;
+    static constexpr int K_OFF = Q_OFF + TILE;              // 2 stages
+    static constexpr int V_OFF = K_OFF + 2 * TILE;          // 2 stages
+    static constexpr int P_OFF = V_OFF + 2 * TILE;
     static constexpr int BAR_OFF = P_OFF + P_BYTES;
     // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2],
     // p_full, pv_done, drain
@@ -65,12 +68,27 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int j) {
     return static_cast<uint32_t>(r * 128 + ((j ^ (r & 7)) << 4));
 }
 
-template <int HD>
+struct AttnMaps {
+    CUtensorMap q, k, v;        // 64-column boxes, 128-byte swizzle
+    CUtensorMap qt, kt, vt;     // 16-column tail boxes, 32-byte swizzle
+};
+
+template <int NB, bool TAIL>
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* main,
+                                          const CUtensorMap* tail, int h, int row0, int b,
+                                          uint32_t bar) {
+    using P = AttnPlan<NB, TAIL>;
+#pragma unroll
+    for (int blk = 0; blk < NB; ++blk) tma_load_4d(dst + blk * P::BLK, main, blk * 64, h, row0, b, bar);
+    if constexpr (TAIL) tma_load_4d(dst + NB * P::BLK, tail, NB * 64, h, row0, b, bar);
+}
+
+template <int NB, bool TAIL>
 __global__ void __launch_bounds__(kThreadsA, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O, int nq,
-                   int nk, int ldo, float scale_log2, int* err) {
-    using P = AttnPlan<HD>;
+    attn_tc_kernel(const __grid_constant__ AttnMaps maps, __nv_bfloat16* __restrict__ O, int hd,
+                   int nq, int nk, int ldo, float scale_log2, int* err) {
+    using P = AttnPlan<NB, TAIL>;
+    constexpr int HDP = P::HDP;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -103,9 +121,9 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmQ);
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&maps.q);
+        tma_prefetch_desc(&maps.k);
+        tma_prefetch_desc(&maps.v);
     }
     if (warp == 1) {
         tmem_alloc(sb + P::TMEM_SLOT_OFF, P::TMEM_COLS);
@@ -126,24 +144,19 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         bool ok = true;
         uint32_t issued_k = 0, issued_v = 0;      // stages with a load in flight
         uint32_t par_k = 0, par_v = 0;            // parity of that load's phase
-        mbar_arrive_expect_tx(q_full, P::Q_BYTES);
-        for (int blk = 0; blk < P::NB; ++blk)
-            tma_load_3d(sb + P::Q_OFF + blk * P::BLK, &tmQ, h * HD + blk * 64, qt * TQ, b, q_full);
+        mbar_arrive_expect_tx(q_full, P::TILE);
+        load_tile<NB, TAIL>(sb + P::Q_OFF, &maps.q, &maps.qt, h, qt * TQ, b, q_full);
         for (int j = 0; ok && j < ntiles; ++j) {
             const int st = j & 1;
             const uint32_t ph = (j >> 1) & 1;
             if (!mbar_wait(k_empty + 8 * st, ph ^ 1, abort_flag)) { fail(); ok = false; break; }
-            mbar_arrive_expect_tx(k_full + 8 * st, P::KV_BYTES);
-            for (int blk = 0; blk < P::NB; ++blk)
-                tma_load_3d(sb + P::K_OFF + st * P::KV_BYTES + blk * P::BLK, &tmK, h * HD + blk * 64,
-                            j * TK, b, k_full + 8 * st);
+            mbar_arrive_expect_tx(k_full + 8 * st, P::TILE);
+            load_tile<NB, TAIL>(sb + P::K_OFF + st * P::TILE, &maps.k, &maps.kt, h, j * TK, b, k_full + 8 * st);
             issued_k |= 1u << st;
             par_k = (par_k & ~(1u << st)) | (ph << st);
             if (!mbar_wait(v_empty + 8 * st, ph ^ 1, abort_flag)) { fail(); ok = false; break; }
-            mbar_arrive_expect_tx(v_full + 8 * st, P::KV_BYTES);
-            for (int blk = 0; blk < P::NB; ++blk)
-                tma_load_3d(sb + P::V_OFF + st * P::KV_BYTES + blk * P::BLK, &tmV, h * HD + blk * 64,
-                            j * TK, b, v_full + 8 * st);
+            mbar_arrive_expect_tx(v_full + 8 * st, P::TILE);
+            load_tile<NB, TAIL>(sb + P::V_OFF + st * P::TILE, &maps.v, &maps.vt, h, j * TK, b, v_full + 8 * st);
             issued_v |= 1u << st;
             par_v = (par_v & ~(1u << st)) | (ph << st);
         }
@@ -157,7 +170,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer
         constexpr uint32_t idesc_s = idesc_bf16_f32(TQ, TK);
-        constexpr uint32_t idesc_o = idesc_bf16_f32(TQ, HD, true);
+        constexpr uint32_t idesc_o = idesc_bf16_f32(TQ, NB * 64, true);
+        constexpr uint32_t idesc_ot = idesc_bf16_f32(TQ, 16, true);
         bool ok = mbar_wait(q_full, 0, abort_flag);
         auto issue_s = [&](int j) -> bool {
             const int st = j & 1;
@@ -166,12 +180,16 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             if (!mbar_wait(s_free + 8 * st, ph ^ 1, abort_flag)) return false;
             tc_fence_after();
             const uint32_t d = tmem + st * TK;
+            const uint32_t kb = sb + P::K_OFF + st * P::TILE;
 #pragma unroll
-            for (int kk = 0; kk < HD / 16; ++kk) {
+            for (int kk = 0; kk < NB * 4; ++kk) {
                 const uint32_t off = (kk >> 2) * P::BLK + (kk & 3) * 32;
-                tc_mma_f16(d, sw128_kmajor_desc(sb + P::Q_OFF + off),
-                           sw128_kmajor_desc(sb + P::K_OFF + st * P::KV_BYTES + off), idesc_s, kk > 0);
+                tc_mma_f16(d, sw128_kmajor_desc(sb + P::Q_OFF + off), sw128_kmajor_desc(kb + off),
+                           idesc_s, kk > 0);
             }
+            if constexpr (TAIL)
+                tc_mma_f16(d, sw32_desc(sb + P::Q_OFF + NB * P::BLK), sw32_desc(kb + NB * P::BLK),
+                           idesc_s, 1u);
             tc_commit(s_full + 8 * st);
             tc_commit(k_empty + 8 * st);
             return true;
@@ -182,13 +200,15 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             if (!mbar_wait(p_full, j & 1, abort_flag)) return false;
             if (!mbar_wait(v_full + 8 * st, ph, abort_flag)) return false;
             tc_fence_after();
-            const uint32_t d = tmem + P::O_COL;
+            const uint32_t vb = sb + P::V_OFF + st * P::TILE;
 #pragma unroll
             for (int kk = 0; kk < TK / 16; ++kk) {
-                const uint32_t a_off = (kk >> 2) * P::BLK + (kk & 3) * 32;
-                tc_mma_f16(d, sw128_kmajor_desc(sb + P::P_OFF + a_off),
-                           sw128_mnmajor_desc(sb + P::V_OFF + st * P::KV_BYTES + kk * 2048, P::BLK),
-                           idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                const uint64_t a = sw128_kmajor_desc(sb + P::P_OFF + (kk >> 2) * P::BLK + (kk & 3) * 32);
+                const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+                tc_mma_f16(tmem + P::O_COL, a, sw128_mnmajor_desc(vb + kk * 2048, P::BLK), idesc_o, acc);
+                if constexpr (TAIL)
+                    tc_mma_f16(tmem + P::O_COL + NB * 64, a, sw32_desc(vb + NB * P::BLK + kk * 512),
+                               idesc_ot, acc);
             }
             tc_commit(pv_done);
             tc_commit(v_empty + 8 * st);
@@ -264,7 +284,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             }
             if (j > 0 && __any_sync(0xFFFFFFFFu, resc)) {
 #pragma unroll 1
-                for (int c = 0; c < HD / 32; ++c) {
+                for (int c = 0; c < (HDP + 31) / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tl + P::O_COL + c * 32, r);
                     tmem_wait_ld();
@@ -290,21 +310,23 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             tc_fence_after();
             const float inv = 1.f / l;
             const int grow = qt * TQ + row;
-            __nv_bfloat16* orow = O + (static_cast<size_t>(b) * nq + grow) * ldo + h * HD;
+            __nv_bfloat16* orow = O + (static_cast<size_t>(b) * nq + grow) * ldo + h * hd;
 #pragma unroll 1
-            for (int c = 0; c < HD / 32; ++c) {
+            for (int c = 0; c < (HDP + 31) / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tl + P::O_COL + c * 32, r);
                 tmem_wait_ld();
                 if (grow < nq) {
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(r[8 * k4 + 0]) * inv, __uint_as_float(r[8 * k4 + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(r[8 * k4 + 2]) * inv, __uint_as_float(r[8 * k4 + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(r[8 * k4 + 4]) * inv, __uint_as_float(r[8 * k4 + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(r[8 * k4 + 6]) * inv, __uint_as_float(r[8 * k4 + 7]) * inv);
-                        *reinterpret_cast<uint4*>(orow + c * 32 + 8 * k4) = w;
+                        if (c * 32 + 8 * k4 < hd) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(r[8 * k4 + 0]) * inv, __uint_as_float(r[8 * k4 + 1]) * inv);
+                            w.y = pack_bf16x2(__uint_as_float(r[8 * k4 + 2]) * inv, __uint_as_float(r[8 * k4 + 3]) * inv);
+                            w.z = pack_bf16x2(__uint_as_float(r[8 * k4 + 4]) * inv, __uint_as_float(r[8 * k4 + 5]) * inv);
+                            w.w = pack_bf16x2(__uint_as_float(r[8 * k4 + 6]) * inv, __uint_as_float(r[8 * k4 + 7]) * inv);
+                            *reinterpret_cast<uint4*>(orow + c * 32 + 8 * k4) = w;
+                        }
                     }
                 }
             }
@@ -320,60 +342,76 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     }
 }
 
-// [batch, rows, cols] view of a bf16 matrix whose batch b, row r starts at
-// base + (b * rows + r) * ld; cols = columns that may be read (from base).
-bool make_map3(CUtensorMap* m, const void* base, int batch, int rows, int cols, int ld) {
+// [batch, rows, heads, hd] view of a bf16 matrix whose batch b, row r, head h
+// starts at base + (b * rows + r) * ld + h * hd; box of box_cols x 1 head x
+// 128 rows, columns past hd zero-filled.
+bool make_map4(CUtensorMap* m, const void* base, int batch, int rows, int heads, int hd, int ld,
+               int box_cols, CUtensorMapSwizzle sw) {
     EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return false;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
-                          static_cast<cuuint64_t>(batch)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2,
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(hd), static_cast<cuuint64_t>(heads),
+                          static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(hd) * 2, static_cast<cuuint64_t>(ld) * 2,
                              static_cast<cuuint64_t>(ld) * 2 * static_cast<cuuint64_t>(rows)};
-    cuuint32_t box[3] = {64, 128, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(box_cols), 1, 128, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int HD>
+template <int NB, bool TAIL>
 cudaError_t run_tc(const void* Q, const void* K, const void* V, void* O, int batch, int heads,
-                   int nq, int nk, int ldq, int ldk, int ldv, int ldo, int* err, cudaStream_t s,
-                   unsigned long long* launches) {
-    using P = AttnPlan<HD>;
+                   int hd, int nq, int nk, int ldq, int ldk, int ldv, int ldo, int* err,
+                   cudaStream_t s, unsigned long long* launches) {
+    using P = AttnPlan<NB, TAIL>;
     static_assert(P::BYTES <= 227 * 1024, "attention shared memory plan exceeds 227 KB");
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>,
+        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NB, TAIL>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, P::BYTES);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    const int D = heads * HD;
-    CUtensorMap tq, tk, tv;
-    if (!make_map3(&tq, Q, batch, nq, D, ldq) || !make_map3(&tk, K, batch, nk, D, ldk) ||
-        !make_map3(&tv, V, batch, nk, D, ldv))
+    AttnMaps maps;
+    const CUtensorMapSwizzle w128 = CU_TENSOR_MAP_SWIZZLE_128B, w32 = CU_TENSOR_MAP_SWIZZLE_32B;
+    if (!make_map4(&maps.q, Q, batch, nq, heads, hd, ldq, 64, w128) ||
+        !make_map4(&maps.k, K, batch, nk, heads, hd, ldk, 64, w128) ||
+        !make_map4(&maps.v, V, batch, nk, heads, hd, ldv, 64, w128))
         return cudaErrorInvalidValue;
-    const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
+    if (TAIL) {
+        if (!make_map4(&maps.qt, Q, batch, nq, heads, hd, ldq, 16, w32) ||
+            !make_map4(&maps.kt, K, batch, nk, heads, hd, ldk, 16, w32) ||
+            !make_map4(&maps.vt, V, batch, nk, heads, hd, ldv, 16, w32))
+            return cudaErrorInvalidValue;
+    } else {
+        maps.qt = maps.q;
+        maps.kt = maps.k;
+        maps.vt = maps.v;
+    }
+    const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(hd));
     dim3 grid((nq + TQ - 1) / TQ, heads, batch);
-    attn_tc_kernel<HD><<<grid, kThreadsA, P::BYTES, s>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(O),
-                                                        nq, nk, ldo, scale_log2, err);
+    attn_tc_kernel<NB, TAIL><<<grid, kThreadsA, P::BYTES, s>>>(
+        maps, static_cast<__nv_bfloat16*>(O), hd, nq, nk, ldo, scale_log2, err);
     ++*launches;
     return cudaGetLastError();
 }
 
 }  // namespace
 
-bool attention_tc_supported(int hd) { return hd == 64 || hd == 128; }
+bool attention_tc_supported(int hd) {
+    return hd == 64 || hd == 128 || (hd > 64 && hd <= 80 && hd % 8 == 0);
+}
 
 cudaError_t launch_attention_tc(const void* Q, const void* K, const void* V, void* O, int batch,
                                 int heads, int hd, int nq, int nk, int ldq, int ldk, int ldv,
                                 int ldo, int* err, cudaStream_t s, unsigned long long* launches) {
     if (hd == 64)
-        return run_tc<64>(Q, K, V, O, batch, heads, nq, nk, ldq, ldk, ldv, ldo, err, s, launches);
+        return run_tc<1, false>(Q, K, V, O, batch, heads, hd, nq, nk, ldq, ldk, ldv, ldo, err, s, launches);
     if (hd == 128)
-        return run_tc<128>(Q, K, V, O, batch, heads, nq, nk, ldq, ldk, ldv, ldo, err, s, launches);
+        return run_tc<2, false>(Q, K, V, O, batch, heads, hd, nq, nk, ldq, ldk, ldv, ldo, err, s, launches);
+    if (hd > 64 && hd <= 80 && hd % 8 == 0)
+        return run_tc<1, true>(Q, K, V, O, batch, heads, hd, nq, nk, ldq, ldk, ldv, ldo, err, s, launches);
     return cudaErrorInvalidValue;
 }
 

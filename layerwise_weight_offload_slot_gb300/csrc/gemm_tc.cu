@@ -152,6 +152,8 @@ struct SmemPlan {
     static constexpr int BYTES = ABORT_OFF + 4 + 1024;  // + alignment slack
     static constexpr int THREADS = kThreads + (FP8 ? kConvWarps * 32 : 0);
     static constexpr uint32_t TX = A_TILE + (FP8 ? RAW_TILE : B_TILE);
+    // two accumulators of BN fp32 columns; TMEM is allocated in powers of two
+    static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256u : 512u;
 };
 
 template <int BN, int STAGES, bool FP8>
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8>::THREADS, 1)
         tma_prefetch_desc(&tmO);
     }
     if (warp == 1) {
-        tmem_alloc(sbase + P::TMEM_SLOT_OFF, 2 * BN);
+        tmem_alloc(sbase + P::TMEM_SLOT_OFF, P::TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -445,7 +447,7 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8>::THREADS, 1)
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, 2 * BN);
+        tmem_dealloc(tmem_base, P::TMEM_COLS);
     }
 }
 
@@ -557,22 +559,29 @@ int gemm_num_sms() {
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
     if (p.M <= 0) return cudaSuccess;
     gemm_num_sms();
-    // N tile: 256-wide tiles need 3/4 of the shared-memory bandwidth per FLOP
-    // of 128-wide ones; pick the smaller (waves x width / efficiency).
-    // DLO_GEMM_BN=128|256 forces one (tuning).
+    // N tile from a small cost model: time ~ waves x tile width / efficiency,
+    // where narrower tiles move more shared-memory bytes per FLOP (128-wide
+    // tiles are limited to about 3/4 of the MMA rate, 192-wide to ~0.95).
+    // DLO_GEMM_BN=128|192|256 forces one (tuning).
     const long long num_m = (p.M + BM - 1) / BM;
     auto cost = [&](int bn) {
         const long long tiles = num_m * ((p.N + bn - 1) / bn);
-        const double eff = bn == 256 ? 1.0 : 0.75;
+        const double eff = bn == 256 ? 1.0 : bn == 192 ? 0.95 : 0.75;
         return static_cast<double>((tiles + g_num_sms - 1) / g_num_sms) * bn / eff;
     };
-    bool wide = cost(256) <= cost(128);
-    if (forced_bn() == 128) wide = false;
-    if (forced_bn() == 256) wide = true;
-    if (p.w_dtype == DLO_DT_E4M3)
-        return wide ? run_gemm<256, 3, true>(p, s, launches) : run_gemm<128, 4, true>(p, s, launches);
+    int bn = 256;
+    if (cost(192) < cost(bn)) bn = 192;
+    if (cost(128) < cost(bn)) bn = 128;
+    if (forced_bn() == 128 || forced_bn() == 192 || forced_bn() == 256) bn = forced_bn();
+    if (p.w_dtype == DLO_DT_E4M3) {
+        if (bn == 256) return run_gemm<256, 3, true>(p, s, launches);
+        if (bn == 192) return run_gemm<192, 3, true>(p, s, launches);
+        return run_gemm<128, 4, true>(p, s, launches);
+    }
     if (p.w_dtype != DLO_DT_BF16) return cudaErrorNotSupported;
-    return wide ? run_gemm<256, 4, false>(p, s, launches) : run_gemm<128, 6, false>(p, s, launches);
+    if (bn == 256) return run_gemm<256, 4, false>(p, s, launches);
+    if (bn == 192) return run_gemm<192, 4, false>(p, s, launches);
+    return run_gemm<128, 6, false>(p, s, launches);
 }
 
 }  // namespace dlo

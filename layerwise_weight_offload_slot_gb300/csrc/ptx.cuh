@@ -238,6 +238,29 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     return d;
 }
 
+// Descriptors of operand tiles TMA wrote with the 32-byte swizzle: rows of
+// 32 bytes (16 bf16), 8-row atoms of 256 bytes (stride byte offset), swizzle
+// mode 6.  K-major: one row per M/N index, its 16 K values contiguous.
+// MN-major: one row per K index, 16 M/N values contiguous.
+__device__ __forceinline__ uint64_t sw32_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1u) << 16;
+    d |= static_cast<uint64_t>(256u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(6u) << 61;
+    return d;
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int c0, int c1, int c2,
+                                            int c3, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
 // Descriptor of an MN-major operand tile (the N index contiguous) written by
 // TMA with the 128-byte swizzle: 64-element MN blocks of 128-byte rows, one
 // row per K index, 8-row atoms 1024 bytes apart (stride byte offset) and MN

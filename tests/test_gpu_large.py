@@ -116,3 +116,24 @@ def test_bytes_blocks_stage_and_checksum(size_mb, n, k, staging, host):
     dlo.dlo_forward_host(st.ctx, None, None, None, 1, 1, 0, out.ctypes.data)
     assert [int(v) for v in out] == sums
     st.close()
+
+
+def test_ditxl_full_stack_one_step():
+    """The benchmarked workload at full size: 28 streamed DiT-XL blocks (hidden
+    1152, 16 heads of 72, batch 2, 1024 tokens), one step, whole stack against
+    the float64 oracle."""
+    cfg = synth.CFG_DITXL
+    params = synth.stack_params(cfg)
+    st = H.make_stack(cfg, blocks=params)
+    st.attach()
+    x, cond, ctx = H.device_inputs(cfg, 0)
+    out = st.forward(x, cond, ctx)
+    torch.cuda.synchronize()
+    st.wait()
+    ref = H.oracle_forward(cfg, x, cond, ctx, H.oracle_blocks(cfg, params))
+    err = H.rel_l2(out.float().cpu().numpy(), ref)
+    print("dit-xl full stack rel L2", err)
+    assert err <= 2e-2
+    for s in (0, 1):
+        assert st.verify_slot(s)
+    st.close()
