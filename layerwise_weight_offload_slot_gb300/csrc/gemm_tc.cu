@@ -1,6 +1,6 @@
 // Y = A W^T on the 5th-generation tensor cores (tcgen05), sm_103a.
 //
-// Persistent kernel, one CTA per SM, 6 warps (+8 converter warps for E4M3):
+// Persistent kernel, one CTA per SM, 6 warps (+12 converter warps for E4M3):
 //   warp 0      TMA producer: 128x64 A tile and BNx64 W tile per stage,
 //               128-byte swizzle, into a STAGES-deep shared-memory ring
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16 (M=128,
@@ -16,7 +16,7 @@
 //               without reading x).  Two staging buffers per warp let the
 //               next chunk overlap the previous store.
 // The two accumulators let the epilogue of tile t overlap the mainloop of
-// tile t+1.  With E4M3 weights (FP8 = true) TMA loads the raw codes, eight
+// tile t+1.  With E4M3 weights (FP8 = true) TMA loads the raw codes, twelve
 // more warps widen them to bf16 in the swizzled layout the MMA reads (exact),
 // and the per-tensor scale is applied to the fp32 accumulator in the epilogue.
 //
@@ -44,7 +44,7 @@ constexpr int BM = 128;
 constexpr int BK = 64;             // 64 bf16 = 128 bytes = one swizzle row
 constexpr int A_TILE = BM * BK * 2;
 constexpr int kThreads = 192;
-constexpr int kConvWarps = 8;
+constexpr int kConvWarps = 12;
 constexpr int STG_BYTES = 32 * 128;   // one 32-row x 128-byte staging box
 
 struct EpiArgs {
@@ -137,12 +137,13 @@ __device__ __forceinline__ void e4m3x8_to_bf16x8(uint32_t x0, uint32_t x1, uint3
     }
 }
 
-template <int BN, int STAGES, bool FP8>
+template <int BN, int STAGES, bool FP8, int MT = 1>
 struct SmemPlan {
+    static constexpr int A_STAGE = MT * A_TILE;           // MT 128-row A boxes per stage
     static constexpr int B_TILE = BN * BK * 2;            // bf16 operand tile (MMA reads)
     static constexpr int RAW_TILE = FP8 ? BN * BK : 0;     // e4m3 tile as loaded by TMA
     static constexpr int A_OFF = 0;
-    static constexpr int B_OFF = STAGES * A_TILE;
+    static constexpr int B_OFF = STAGES * A_STAGE;
     static constexpr int RAW_OFF = B_OFF + STAGES * B_TILE;
     static constexpr int STG_OFF = RAW_OFF + STAGES * RAW_TILE;   // 4 warps x 2 boxes
     static constexpr int BAR_OFF = STG_OFF + 8 * STG_BYTES;
@@ -151,16 +152,19 @@ struct SmemPlan {
     static constexpr int ABORT_OFF = TMEM_SLOT_OFF + 4;
     static constexpr int BYTES = ABORT_OFF + 4 + 1024;  // + alignment slack
     static constexpr int THREADS = kThreads + (FP8 ? kConvWarps * 32 : 0);
-    static constexpr uint32_t TX = A_TILE + (FP8 ? RAW_TILE : B_TILE);
-    // two accumulators of BN fp32 columns; TMEM is allocated in powers of two
-    static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256u : 512u;
+    static constexpr uint32_t TX = A_STAGE + (FP8 ? RAW_TILE : B_TILE);
+    // two accumulator sets of MT x BN fp32 columns; allocated in powers of two
+    static constexpr uint32_t TMEM_COLS = 2 * MT * BN <= 256 ? 256u : 512u;
+    static_assert(2 * MT * BN <= 512, "accumulators exceed TMEM");
 };
 
-template <int BN, int STAGES, bool FP8>
-__global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8>::THREADS, 1)
+// MT > 1: a CTA tile is MT x 128 rows; every weight tile (and, for E4M3,
+// its widening) serves MT row blocks.
+template <int BN, int STAGES, bool FP8, int MT>
+__global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO, const EpiArgs args) {
-    using P = SmemPlan<BN, STAGES, FP8>;
+    using P = SmemPlan<BN, STAGES, FP8, MT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -226,7 +230,10 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8>::THREADS, 1)
                 }
                 const uint32_t fb = bar_full + s * 8;
                 mbar_arrive_expect_tx(fb, P::TX);
-                tma_load_2d(sbase + P::A_OFF + s * A_TILE, &tmA, kb * BK, mb * BM, fb);
+#pragma unroll
+                for (int i = 0; i < MT; ++i)
+                    tma_load_2d(sbase + P::A_OFF + s * P::A_STAGE + i * A_TILE, &tmA, kb * BK,
+                                (mb * MT + i) * BM, fb);
                 if constexpr (FP8)
                     tma_load_2d(sbase + P::RAW_OFF + s * P::RAW_TILE, &tmB, kb * BK, nb * BN, fb);
                 else
@@ -261,7 +268,7 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8>::THREADS, 1)
                 break;
             }
             tc_fence_after();
-            const uint32_t d_tmem = tmem_base + acc * BN;
+            const uint32_t d_tmem = tmem_base + acc * (MT * BN);
             for (int kb = 0; kb < kblocks; ++kb) {
                 if (!mbar_wait(bar_ready + s * 8, ph, abort_flag)) {
                     fail();
@@ -269,12 +276,15 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8>::THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a0 = sbase + P::A_OFF + s * A_TILE;
+                const uint32_t a0 = sbase + P::A_OFF + s * P::A_STAGE;
                 const uint32_t b0 = sbase + P::B_OFF + s * P::B_TILE;
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
-                    tc_mma_f16(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32),
-                               idesc, (kb | kk) != 0);
+                for (int i = 0; i < MT; ++i) {
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        tc_mma_f16(d_tmem + i * BN, sw128_kmajor_desc(a0 + i * A_TILE + kk * 32),
+                                   sw128_kmajor_desc(b0 + kk * 32), idesc, (kb | kk) != 0);
+                    }
                 }
                 tc_commit(bar_empty + s * 8);
                 if (++s == STAGES) {
@@ -309,93 +319,97 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8>::THREADS, 1)
                 break;
             }
             tc_fence_after();
-            const int row0 = mb * BM + q * 32;
-            const int row = row0 + lane;
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-            if (residual) {
-                // 32-column fp32 boxes: delta = gate * (acc * s + b), added into x by TMA
-                const float* grow = args.gate ? args.gate + static_cast<size_t>(min(row, args.M - 1) /
-                                                                                 args.rows_per_batch) *
-                                                                args.gate_ld
-                                              : nullptr;
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 32) {
-                    const int col0 = nb * BN + c0;
-                    if (col0 >= args.N) break;
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(taddr + c0, r);
-                    tmem_wait_ld();
-                    float v[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                    scale_bias<32>(args, col0, v);
-                    if (grow) {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            if (col0 + 4 * j < args.N) {
-                                const float4 g = *reinterpret_cast<const float4*>(grow + col0 + 4 * j);
-                                v[4 * j] *= g.x;
-                                v[4 * j + 1] *= g.y;
-                                v[4 * j + 2] *= g.z;
-                                v[4 * j + 3] *= g.w;
-                            }
-                        }
-                    }
-                    if (lane == 0) bulk_wait_read<1>();
-                    __syncwarp();
-                    uint8_t* box = stg0p + bi * STG_BYTES;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        *reinterpret_cast<float4*>(box + sw128(lane, j)) =
-                            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_reduce_add_2d(&tmO, stg0 + bi * STG_BYTES, col0, row0);
-                        bulk_commit();
-                    }
-                    bi ^= 1;
-                }
-            } else {
-                // 64-column bf16 boxes: y = [GELU](acc * s + b), stored by TMA;
-                // filled 32 columns at a time to keep registers low
-#pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 64) {
-                    const int col0 = nb * BN + c0;
-                    if (col0 >= args.N) break;
-                    if (lane == 0) bulk_wait_read<1>();
-                    __syncwarp();
-                    uint8_t* box = stg0p + bi * STG_BYTES;
-#pragma unroll 1
-                    for (int half = 0; half < 2; ++half) {
+            for (int mi = 0; mi < MT; ++mi) {
+                const int row0 = (mb * MT + mi) * BM + q * 32;
+                const int row = row0 + lane;
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       acc * (MT * BN) + mi * BN;
+                if (residual) {
+                    // 32-column fp32 boxes: delta = gate * (acc * s + b), added into x by TMA
+                    const float* grow = args.gate ? args.gate + static_cast<size_t>(min(row, args.M - 1) /
+                                                                                     args.rows_per_batch) *
+                                                                    args.gate_ld
+                                                  : nullptr;
+    #pragma unroll 1
+                    for (int c0 = 0; c0 < BN; c0 += 32) {
+                        const int col0 = nb * BN + c0;
+                        if (col0 >= args.N) break;
                         uint32_t r[32];
-                        tmem_ld_32x32b_x32(taddr + c0 + 32 * half, r);
+                        tmem_ld_32x32b_x32(taddr + c0, r);
                         tmem_wait_ld();
                         float v[32];
-#pragma unroll
+    #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                        scale_bias<32>(args, col0 + 32 * half, v);
-                        if (args.epi == DLO_EPI_GELU) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+                        scale_bias<32>(args, col0, v);
+                        if (grow) {
+    #pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                if (col0 + 4 * j < args.N) {
+                                    const float4 g = *reinterpret_cast<const float4*>(grow + col0 + 4 * j);
+                                    v[4 * j] *= g.x;
+                                    v[4 * j + 1] *= g.y;
+                                    v[4 * j + 2] *= g.z;
+                                    v[4 * j + 3] *= g.w;
+                                }
+                            }
                         }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            uint4 w;
-                            w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
-                            w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
-                            w.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
-                            w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
-                            *reinterpret_cast<uint4*>(box + sw128(lane, 4 * half + j)) = w;
+                        if (lane == 0) bulk_wait_read<1>();
+                        __syncwarp();
+                        uint8_t* box = stg0p + bi * STG_BYTES;
+    #pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<float4*>(box + sw128(lane, j)) =
+                                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_reduce_add_2d(&tmO, stg0 + bi * STG_BYTES, col0, row0);
+                            bulk_commit();
                         }
+                        bi ^= 1;
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tmO, stg0 + bi * STG_BYTES, col0, row0);
-                        bulk_commit();
+                } else {
+                    // 64-column bf16 boxes: y = [GELU](acc * s + b), stored by TMA;
+                    // filled 32 columns at a time to keep registers low
+    #pragma unroll 1
+                    for (int c0 = 0; c0 < BN; c0 += 64) {
+                        const int col0 = nb * BN + c0;
+                        if (col0 >= args.N) break;
+                        if (lane == 0) bulk_wait_read<1>();
+                        __syncwarp();
+                        uint8_t* box = stg0p + bi * STG_BYTES;
+    #pragma unroll 1
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t r[32];
+                            tmem_ld_32x32b_x32(taddr + c0 + 32 * half, r);
+                            tmem_wait_ld();
+                            float v[32];
+    #pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                            scale_bias<32>(args, col0 + 32 * half, v);
+                            if (args.epi == DLO_EPI_GELU) {
+    #pragma unroll
+                                for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+                            }
+    #pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                uint4 w;
+                                w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+                                w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+                                w.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+                                w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+                                *reinterpret_cast<uint4*>(box + sw128(lane, 4 * half + j)) = w;
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmO, stg0 + bi * STG_BYTES, col0, row0);
+                            bulk_commit();
+                        }
+                        bi ^= 1;
                     }
-                    bi ^= 1;
                 }
             }
             tc_fence_before();
@@ -473,13 +487,13 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int es_b
 
 int g_num_sms = 0;
 
-template <int BN, int STAGES, bool FP8>
+template <int BN, int STAGES, bool FP8, int MT = 1>
 cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
-    using PL = SmemPlan<BN, STAGES, FP8>;
+    using PL = SmemPlan<BN, STAGES, FP8, MT>;
     static_assert(PL::BYTES <= 227 * 1024, "shared memory plan exceeds 227 KB");
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, STAGES, FP8>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, STAGES, FP8, MT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, PL::BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -512,13 +526,22 @@ cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* la
     a.gate_ld = p.gate_ld;
     a.rows_per_batch = p.rows_per_batch > 0 ? p.rows_per_batch : 1;
     a.err = p.err;
-    a.num_m = (p.M + BM - 1) / BM;
+    a.num_m = (p.M + MT * BM - 1) / (MT * BM);
     a.num_n = (p.N + BN - 1) / BN;
     a.num_tiles = a.num_m * a.num_n;
     const int grid = a.num_tiles < g_num_sms ? a.num_tiles : g_num_sms;
-    gemm_kernel<BN, STAGES, FP8><<<grid, PL::THREADS, PL::BYTES, s>>>(ta, tb, to, a);
+    gemm_kernel<BN, STAGES, FP8, MT><<<grid, PL::THREADS, PL::BYTES, s>>>(ta, tb, to, a);
     ++*launches;
     return cudaGetLastError();
+}
+
+int forced_mt() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = std::getenv("DLO_GEMM_MT");
+        v = e ? std::atoi(e) : 0;
+    }
+    return v;
 }
 
 int forced_bn() {
@@ -574,6 +597,13 @@ cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long*
     if (cost(128) < cost(bn)) bn = 128;
     if (forced_bn() == 128 || forced_bn() == 192 || forced_bn() == 256) bn = forced_bn();
     if (p.w_dtype == DLO_DT_E4M3) {
+        // E4M3: 256-row CTA tiles (two 128-row accumulators) share each
+        // widened weight tile, halving the widening work per FLOP, when
+        // there are enough row blocks to fill the SMs.  DLO_GEMM_MT=1 turns
+        // it off (tuning).
+        const long long tiles2 = ((p.M + 255) / 256) * ((p.N + 127) / 128);
+        if (forced_mt() != 1 && (forced_mt() == 2 || tiles2 >= g_num_sms))
+            return run_gemm<128, 3, true, 2>(p, s, launches);
         if (bn == 256) return run_gemm<256, 3, true>(p, s, launches);
         if (bn == 192) return run_gemm<192, 3, true>(p, s, launches);
         return run_gemm<128, 4, true>(p, s, launches);
