@@ -490,8 +490,62 @@ def run_sweep(args):
                     "output_equals_k0": exact, "slots_bit_exact": slots_ok})
         st._own_host = False      # the host blocks are shared by the four contexts
         st.close()
+
+    # ---- staging engines at k = 0: one packed copy, one copy per tensor, the
+    # SM gather kernel, and pageable host blocks packed through pinned slots
+    eng = []
+    page = None
+    for name, staging, mode in (("memcpy", dlo.STAGE_MEMCPY, "pinned"),
+                                ("per_tensor", dlo.STAGE_PER_TENSOR, "pinned"),
+                                ("gather", dlo.STAGE_GATHER, "pinned"),
+                                ("pageable_two_slot", dlo.STAGE_MEMCPY, "pageable")):
+        hb = host
+        if mode == "pageable":
+            page = HostBlocks(cfg.n_blocks, bb, "pageable")
+            for i in range(cfg.n_blocks):
+                page.view(i)[:] = host.view(i)
+            hb = page
+        st = OffloadStack(block_kind=cfg.kind, n_blocks=cfg.n_blocks, hidden=cfg.hidden,
+                          heads=cfg.heads, head_dim=cfg.head_dim, ffn=cfg.ffn,
+                          text_dim=cfg.text_dim, max_batch=cfg.batch, max_tokens=cfg.tokens,
+                          max_text_tokens=cfg.text_tokens, staging=staging, host_mode=mode,
+                          host=hb)
+        st.attach()
+        y = st.forward(x0, e, ctx)
+        torch.cuda.synchronize()
+        st.wait()
+        exact = bool(torch.equal(y, ref))
+        cs = st.compute_stream
+        c0 = st.stats()["h2d_copies"]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(cs)
+        for _ in range(args.steps):
+            st.forward(x0, e, ctx, out=y)
+        e1.record(cs)
+        torch.cuda.synchronize()
+        st.wait()
+        ms = e0.elapsed_time(e1) / args.steps
+        copies = (st.stats()["h2d_copies"] - c0) / args.steps
+        st.set_timing(1)
+        s0 = st.stats()
+        st.forward(x0, e, ctx, out=y)
+        torch.cuda.synchronize()
+        st.wait()
+        s1 = st.stats()
+        copy = s1["copy_ms"] - s0["copy_ms"]
+        n_exec = s1["timed_execs"] - s0["timed_execs"]
+        eng.append({"engine": name, "steps_per_s": 1e3 / ms, "ms_per_step": ms,
+                    "h2d_copies_per_step": copies,
+                    "staging_gbs": n_exec * bb / (copy * 1e-3) / 1e9 if copy > 0 else None,
+                    "overlap_fraction": 1.0 - (s1["exposed_wait_ms"] - s0["exposed_wait_ms"]) / copy
+                    if copy > 0 else None,
+                    "output_equals_memcpy_k0": exact})
+        st._own_host = False
+        st.close()
+    if page is not None:
+        page.close()
     host.close()
-    out["residency"] = {"workload": cfg.name, "block_bytes": bb, "runs": res}
+    out["residency"] = {"workload": cfg.name, "block_bytes": bb, "runs": res, "engines": eng}
 
     # ---- staging: opaque byte blocks 16 MB .. 1 GB
     stg = []

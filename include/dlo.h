@@ -28,7 +28,8 @@
  *  - Streams are cudaStream_t passed as void*.
  *  - The caller owns every buffer it passes and keeps it alive until
  *    dlo_destroy returns.  The library owns only its events, the host ranges
- *    it registered itself and the context object.
+ *    it registered itself, the two pinned host staging slots of
+ *    DLO_HOST_PAGEABLE and the context object.
  *  - Calls are not thread-safe on one context.  Different contexts are
  *    independent.
  *  - Errors return a negative dlo_status; dlo_last_error() gives the message.
@@ -69,10 +70,16 @@ typedef int dlo_status;
 /* slot staging engine */
 #define DLO_STAGE_MEMCPY 0   /* cudaMemcpyAsync on the copy stream (copy engine) */
 #define DLO_STAGE_GATHER 1   /* SM kernel reading mapped host memory, 16-B loads */
+/* one cudaMemcpyAsync per layout tensor, host offset -> the same slot offset
+ * ("Distributed Layerwise Offload", Registered runtime-cache transfer: each
+ * immutable tensor view is copied directly into its offset of the flattened
+ * rotating device buffer; more copy operations than one packed block copy) */
+#define DLO_STAGE_PER_TENSOR 2
 
 /* host block flags for dlo_register_host_blocks */
 #define DLO_HOST_PINNED   1u /* caller's memory is already page-locked           */
 #define DLO_HOST_REGISTER 2u /* library page-locks it (all-or-nothing)           */
+#define DLO_HOST_PAGEABLE 4u /* pageable; packed through two pinned host slots    */
 
 /* tensor dtypes in the flat block layout */
 #define DLO_DT_BF16 0
@@ -190,7 +197,19 @@ dlo_status dlo_create(const dlo_desc* desc, int device, void* slot0, void* slot1
  *                     unregisters the ranges already registered and returns
  *                     DLO_EREGISTER with the context unchanged, so the call can
  *                     be retried ([DLO] Failure and lifecycle boundaries).
- * Exactly one of the two flags.  With DLO_STAGE_GATHER the blocks must be
+ *  DLO_HOST_PAGEABLE: memory stays pageable (e.g. views of a file mapping);
+ *                     the library allocates two pinned host staging slots of
+ *                     block_bytes each (cudaHostAlloc; freed by dlo_destroy)
+ *                     and, for every staging, packs the block into the next
+ *                     host slot with a stream-ordered host function on the
+ *                     copy stream (a synchronous host copy spread over a few
+ *                     library threads) before the pinned host-to-device copy
+ *                     ([DLO] Host backing and transfer composition: "mmap views
+ *                     -> pinned staging slot -> device slot"; the user guide's
+ *                     mmap weight storage: packing into the host slot is
+ *                     synchronous, the pinned copy overlaps computation).
+ *                     Needs DLO_STAGE_MEMCPY.  Allocation failure: DLO_ENOMEM.
+ * Exactly one of the flags.  With DLO_STAGE_GATHER the blocks must be
  * device-accessible (mapped); checked here.  Allowed once, before forward. */
 dlo_status dlo_register_host_blocks(dlo_ctx* ctx, int n, const void* const* host_blocks,
                                     size_t block_bytes, unsigned flags);
@@ -289,6 +308,7 @@ typedef struct dlo_stats {
     double kclass_flops[8];
     double kclass_bytes[8];
     unsigned long long kclass_launches[8];
+    unsigned long long h2d_copies;       /* host-to-device copy calls issued     */
 } dlo_stats;
 
 /* kernel classes of dlo_stats.kclass_* */

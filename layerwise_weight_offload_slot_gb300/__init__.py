@@ -26,8 +26,8 @@ OK, EINVAL, ESTATE, ENOMEM, ECUDA, EREGISTER, ETIMEDOUT, EUNSUPPORTED, EMISMATCH
     0, -1, -2, -3, -4, -5, -6, -7, -8
 BLOCK_DIT, BLOCK_VIDEO, BLOCK_BYTES = 0, 1, 2
 W_BF16, W_E4M3 = 0, 1
-STAGE_MEMCPY, STAGE_GATHER = 0, 1
-HOST_PINNED, HOST_REGISTER = 1, 2
+STAGE_MEMCPY, STAGE_GATHER, STAGE_PER_TENSOR = 0, 1, 2
+HOST_PINNED, HOST_REGISTER, HOST_PAGEABLE = 1, 2, 4
 DT_BF16, DT_E4M3, DT_F32, DT_U8 = 0, 1, 2, 3
 EPI_BIAS, EPI_GELU, EPI_RESIDUAL = 0, 1, 2
 
@@ -67,7 +67,8 @@ class dlo_stats(ctypes.Structure):
                 ("timed_execs", ctypes.c_int), ("copy_ms", ctypes.c_double),
                 ("compute_ms", ctypes.c_double), ("exposed_wait_ms", ctypes.c_double),
                 ("kclass_ms", ctypes.c_double * 8), ("kclass_flops", ctypes.c_double * 8),
-                ("kclass_bytes", ctypes.c_double * 8), ("kclass_launches", ctypes.c_ulonglong * 8)]
+                ("kclass_bytes", ctypes.c_double * 8), ("kclass_launches", ctypes.c_ulonglong * 8),
+                ("h2d_copies", ctypes.c_ulonglong)]
 
     def as_dict(self) -> dict:
         d = {}

@@ -13,6 +13,8 @@
 #include <algorithm>
 #include <atomic>
 #include <chrono>
+#include <condition_variable>
+#include <mutex>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -53,6 +55,83 @@ struct Offsets {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// A few host threads that split one memcpy between them (the pack of a
+// pageable block into a pinned host staging slot).
+class CopyPool {
+  public:
+    explicit CopyPool(int n) {
+        for (int i = 0; i < n; ++i) threads_.emplace_back([this, i] { loop(i); });
+    }
+    ~CopyPool() {
+        {
+            std::lock_guard<std::mutex> g(mu_);
+            stop_ = true;
+        }
+        cv_.notify_all();
+        for (auto& t : threads_) t.join();
+    }
+    void copy(void* dst, const void* src, size_t bytes) {
+        const int n = static_cast<int>(threads_.size());
+        std::unique_lock<std::mutex> g(mu_);
+        dst_ = static_cast<uint8_t*>(dst);
+        src_ = static_cast<const uint8_t*>(src);
+        bytes_ = bytes;
+        pending_ = n;
+        ++gen_;
+        cv_.notify_all();
+        done_cv_.wait(g, [&] { return pending_ == 0; });
+    }
+
+  private:
+    void loop(int i) {
+        unsigned long long seen = 0;
+        for (;;) {
+            uint8_t* d;
+            const uint8_t* s;
+            size_t b;
+            {
+                std::unique_lock<std::mutex> g(mu_);
+                cv_.wait(g, [&] { return stop_ || gen_ != seen; });
+                if (stop_) return;
+                seen = gen_;
+                d = dst_;
+                s = src_;
+                b = bytes_;
+            }
+            const int n = static_cast<int>(threads_.size());
+            const size_t chunk = (b / n + 4095) / 4096 * 4096;
+            const size_t lo = std::min(b, chunk * i), hi = std::min(b, lo + chunk);
+            if (hi > lo) std::memcpy(d + lo, s + lo, hi - lo);
+            {
+                std::lock_guard<std::mutex> g(mu_);
+                if (--pending_ == 0) done_cv_.notify_all();
+            }
+        }
+    }
+    std::vector<std::thread> threads_;
+    std::mutex mu_;
+    std::condition_variable cv_, done_cv_;
+    uint8_t* dst_ = nullptr;
+    const uint8_t* src_ = nullptr;
+    size_t bytes_ = 0;
+    int pending_ = 0;
+    unsigned long long gen_ = 0;
+    bool stop_ = false;
+};
+
+struct PackJob {
+    CopyPool* pool;
+    void* dst;
+    const void* src;
+    size_t bytes;
+};
+
+void CUDART_CB pack_host_fn(void* arg) {
+    PackJob* j = static_cast<PackJob*>(arg);
+    j->pool->copy(j->dst, j->src, j->bytes);
+    delete j;
+}
+
 }  // namespace
 
 struct dlo_ctx {
@@ -79,6 +158,10 @@ struct dlo_ctx {
     std::vector<const uint8_t*> host_dev;
     std::vector<std::pair<void*, size_t>> reg_ranges;
     bool reg_read_only = false;
+    bool pageable = false;
+    uint8_t* hstage[2] = {nullptr, nullptr};   // pinned host staging slots (pageable mode)
+    int hstage_next = 0;
+    std::unique_ptr<CopyPool> pool;
     std::vector<uint8_t*> resident;
     unsigned long long exec_counter = 0;
     int slot_block[2] = {-1, -1};
@@ -212,8 +295,31 @@ dlo_status stage(dlo_ctx* c, int blk, int s) {
         e = c->timed(DLO_K_GATHER, 0.0, 2.0 * c->block_bytes, c->xs, [&] {
             return launch_gather(c->slot[s], c->host_dev[blk], c->block_bytes, c->xs, &c->st.kernel_launches);
         });
+    } else if (c->pageable) {
+        // pack into the next pinned host slot (stream-ordered host function),
+        // then copy that slot to the device slot
+        const int h = c->hstage_next;
+        c->hstage_next ^= 1;
+        PackJob* job = new PackJob{c->pool.get(), c->hstage[h], c->host[blk], c->block_bytes};
+        e = cudaLaunchHostFunc(c->xs, pack_host_fn, job);
+        if (e != cudaSuccess) {
+            delete job;
+        } else {
+            e = cudaMemcpyAsync(c->slot[s], c->hstage[h], c->block_bytes, cudaMemcpyHostToDevice, c->xs);
+            ++c->st.h2d_copies;
+        }
+    } else if (c->d.staging == DLO_STAGE_PER_TENSOR) {
+        e = cudaSuccess;
+        for (const Entry& t : c->L) {
+            if (!t.bytes) continue;
+            e = cudaMemcpyAsync(c->slot[s] + t.offset, c->host[blk] + t.offset, t.bytes,
+                                cudaMemcpyHostToDevice, c->xs);
+            if (e != cudaSuccess) break;
+            ++c->st.h2d_copies;
+        }
     } else {
         e = cudaMemcpyAsync(c->slot[s], c->host[blk], c->block_bytes, cudaMemcpyHostToDevice, c->xs);
+        ++c->st.h2d_copies;
     }
     if (e != cudaSuccess) return c->cuda_fail(e, "slot staging");
     c->slot_block[s] = blk;
@@ -488,12 +594,36 @@ extern "C" dlo_status dlo_register_host_blocks(dlo_ctx* c, int n, const void* co
     if (block_bytes != c->block_bytes)
         return c->fail(DLO_EINVAL, "block_bytes %zu != layout bytes %zu", block_bytes, c->block_bytes);
     const bool pinned = flags == DLO_HOST_PINNED, reg = flags == DLO_HOST_REGISTER;
-    if (!pinned && !reg) return c->fail(DLO_EINVAL, "flags must be DLO_HOST_PINNED or DLO_HOST_REGISTER");
+    const bool pageable = flags == DLO_HOST_PAGEABLE;
+    if (!pinned && !reg && !pageable)
+        return c->fail(DLO_EINVAL, "flags must be one of DLO_HOST_PINNED, DLO_HOST_REGISTER, DLO_HOST_PAGEABLE");
+    if (pageable && c->d.staging != DLO_STAGE_MEMCPY)
+        return c->fail(DLO_EINVAL, "DLO_HOST_PAGEABLE needs DLO_STAGE_MEMCPY");
     for (int i = 0; i < n; ++i) {
         if (!host_blocks[i]) return c->fail(DLO_EINVAL, "host block %d is NULL", i);
         if (!aligned(host_blocks[i], 16)) return c->fail(DLO_EINVAL, "host block %d is not 16-byte aligned", i);
     }
     cudaSetDevice(c->device);
+    if (pageable) {
+        // two bounded pinned host staging slots; nothing else is page-locked
+        for (int i = 0; i < 2; ++i) {
+            cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&c->hstage[i]), block_bytes,
+                                          cudaHostAllocDefault);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                for (int k = 0; k < i; ++k) cudaFreeHost(c->hstage[k]);
+                c->hstage[0] = c->hstage[1] = nullptr;
+                return c->fail(DLO_ENOMEM, "pinned host staging slots: %s", cudaGetErrorString(e));
+            }
+        }
+        c->pool.reset(new CopyPool(8));
+        c->pageable = true;
+        c->host.assign(reinterpret_cast<const uint8_t* const*>(host_blocks),
+                       reinterpret_cast<const uint8_t* const*>(host_blocks) + n);
+        c->host_dev.assign(n, nullptr);
+        c->state = kRegistered;
+        return DLO_OK;
+    }
     std::vector<std::pair<void*, size_t>> done;
     bool ro = false;
     if (reg) {
@@ -777,6 +907,11 @@ extern "C" dlo_status dlo_destroy(dlo_ctx* c) {
         cudaEventDestroy(t.b);
     }
     for (cudaEvent_t ev : c->ev_pool) cudaEventDestroy(ev);
+    if (idle) {
+        for (int i = 0; i < 2; ++i)
+            if (c->hstage[i]) cudaFreeHost(c->hstage[i]);
+    }
+    c->pool.reset();
     delete c;
     return first;
 }

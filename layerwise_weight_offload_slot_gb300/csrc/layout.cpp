@@ -34,7 +34,8 @@ dlo_status validate_desc(const dlo_desc* d, std::string* msg) {
         if (d->n_blocks < 1) return fail(DLO_EINVAL, "n_blocks < 1");
         if (d->bytes_block == 0 || d->bytes_block % 256 != 0)
             return fail(DLO_EINVAL, "bytes_block must be a positive multiple of 256");
-        if (d->staging != DLO_STAGE_MEMCPY && d->staging != DLO_STAGE_GATHER)
+        if (d->staging != DLO_STAGE_MEMCPY && d->staging != DLO_STAGE_GATHER &&
+            d->staging != DLO_STAGE_PER_TENSOR)
             return fail(DLO_EINVAL, "unknown staging");
         return DLO_OK;
     }
@@ -47,7 +48,8 @@ dlo_status validate_desc(const dlo_desc* d, std::string* msg) {
     if (d->ffn < 16 || d->ffn % 16 != 0) return fail(DLO_EINVAL, "ffn % 16 != 0");
     if (d->max_batch < 1 || d->max_tokens < 1) return fail(DLO_EINVAL, "max_batch/max_tokens < 1");
     if (!(d->eps > 0.0f)) return fail(DLO_EINVAL, "eps <= 0");
-    if (d->staging != DLO_STAGE_MEMCPY && d->staging != DLO_STAGE_GATHER)
+    if (d->staging != DLO_STAGE_MEMCPY && d->staging != DLO_STAGE_GATHER &&
+        d->staging != DLO_STAGE_PER_TENSOR)
         return fail(DLO_EINVAL, "unknown staging");
     if (d->block_kind == DLO_BLOCK_DIT) {
         if (d->cond_dim < 8 || d->cond_dim % 16 != 0) return fail(DLO_EINVAL, "cond_dim % 16 != 0");

@@ -15,7 +15,7 @@ from concurrent.futures import ThreadPoolExecutor
 import numpy as np
 import torch
 
-from . import (BLOCK_BYTES, BLOCK_DIT, BLOCK_VIDEO, HOST_PINNED, HOST_REGISTER, OK, STAGE_MEMCPY, W_BF16,
+from . import (BLOCK_BYTES, BLOCK_DIT, BLOCK_VIDEO, HOST_PAGEABLE, HOST_PINNED, HOST_REGISTER, OK, STAGE_MEMCPY, W_BF16,
                dlo_block_bytes, dlo_block_layout, dlo_create, dlo_destroy, dlo_forward,
                dlo_forward_host, dlo_get_log, dlo_get_stats, dlo_pack_block,
                dlo_register_host_blocks, dlo_reset_log, dlo_set_resident, dlo_set_timing,
@@ -32,7 +32,8 @@ class HostBlocks:
     """n flat blocks of `block_bytes`, each page-aligned, in one allocation.
 
     mode "pinned": torch pinned memory (cudaHostAlloc); "register": anonymous
-    mmap (pageable) for the library to register.
+    mmap (pageable) for the library to register; "pageable": anonymous mmap
+    that stays pageable (the library packs it through pinned host slots).
     """
 
     def __init__(self, n: int, block_bytes: int, mode: str):
@@ -45,7 +46,7 @@ class HostBlocks:
             self._t = torch.empty(total, dtype=torch.uint8, pin_memory=True)
             base = self._t.data_ptr()
             self._buf = None
-        elif mode == "register":
+        elif mode in ("register", "pageable"):
             self._buf = mmap.mmap(-1, total)
             self._anchor = ctypes.c_char.from_buffer(self._buf)
             base = ctypes.addressof(self._anchor)
@@ -119,7 +120,8 @@ class OffloadStack:
             list(ex.map(lambda i: self.pack(i, get(i)), range(self.n_blocks)))
 
     def attach(self) -> None:
-        flags = HOST_PINNED if self.host_mode == "pinned" else HOST_REGISTER
+        flags = {"pinned": HOST_PINNED, "register": HOST_REGISTER,
+                 "pageable": HOST_PAGEABLE}[self.host_mode]
         dlo_register_host_blocks(self.ctx, self.host.ptrs, self.block_bytes, flags)
 
     def set_resident(self, k: int) -> None:

@@ -112,14 +112,24 @@ def test_gather_staging_and_registered_memory_bit_exact():
     cfg = SMALL_VID
     outs = []
     for staging, mode in ((dlo.STAGE_MEMCPY, "pinned"), (dlo.STAGE_GATHER, "pinned"),
-                          (dlo.STAGE_MEMCPY, "register"), (dlo.STAGE_GATHER, "register")):
+                          (dlo.STAGE_MEMCPY, "register"), (dlo.STAGE_GATHER, "register"),
+                          (dlo.STAGE_PER_TENSOR, "register"), (dlo.STAGE_PER_TENSOR, "pinned"),
+                          (dlo.STAGE_MEMCPY, "pageable")):
         st = H.make_stack(cfg, staging=staging, host_mode=mode)
         st.attach()
         if mode == "register":
             assert st.stats()["registered_ranges"] >= 1
+        if mode == "pageable":
+            assert st.stats()["registered_ranges"] == 0
         outs.append(run(st, cfg)[3].cpu())
         for s in (0, 1):
             assert st.verify_slot(s)
+        stats = st.stats()
+        per_stage = len(st.layout) if staging == dlo.STAGE_PER_TENSOR else 0
+        if staging == dlo.STAGE_PER_TENSOR:
+            assert stats["h2d_copies"] == per_stage * stats["stagings"]
+        elif staging == dlo.STAGE_MEMCPY:
+            assert stats["h2d_copies"] == stats["stagings"]
         st.close()
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
@@ -207,3 +217,12 @@ def test_lifecycle_errors():
     assert e.value.status == dlo.EINVAL
     run(st, cfg)
     assert st.close() == 0
+
+
+def test_pageable_rejects_gather():
+    cfg = SMALL_DIT
+    st = H.make_stack(cfg, staging=dlo.STAGE_GATHER, host_mode="pageable")
+    with pytest.raises(dlo.DloError) as e:
+        st.attach()
+    assert e.value.status == dlo.EINVAL
+    st.close()
