@@ -243,27 +243,39 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 tmem_ld_32x32b_x32(tl + st * TK + c * 32, r);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[c * 32 + i] = __uint_as_float(r[i]) * scale_log2;
+                for (int i = 0; i < 32; ++i) v[c * 32 + i] = __uint_as_float(r[i]);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free + 8 * st);
+            // raw scores: the row max is taken before scaling (scale > 0), and
+            // keys past nk exist only in the last tile
             const int kvalid = nk - j * TK;
-            float mt = -INFINITY;
+            if (kvalid < TK) {
 #pragma unroll
-            for (int i = 0; i < TK; ++i) {
-                if (i >= kvalid) v[i] = -INFINITY;
-                mt = fmaxf(mt, v[i]);
+                for (int i = 0; i < TK; ++i)
+                    if (i >= kvalid) v[i] = -INFINITY;
             }
+            // 8 independent max / sum chains (ILP instead of one 128-long chain)
+            float mp[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mp[u] = v[u];
+#pragma unroll
+            for (int i = 8; i < TK; ++i) mp[i & 7] = fmaxf(mp[i & 7], v[i]);
+            float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+            mt *= scale_log2;
             const bool resc = mt > m_ref + 8.f;
             const float m_new = resc ? mt : m_ref;
             const float corr = resc ? ex2_approx(m_ref - m_new) : 1.f;
-            float rs = 0.f;
+            const float neg = -m_new;
+            float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int i = 0; i < TK; ++i) {
-                v[i] = ex2_approx(v[i] - m_new);
-                rs += v[i];
+                v[i] = ex2_approx(fmaf(v[i], scale_log2, neg));
+                sp[i & 7] += v[i];
             }
+            const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
             l = l * corr + rs;
             m_ref = m_new;
             if (j > 0) {

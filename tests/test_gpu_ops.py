@@ -91,7 +91,7 @@ def test_gemm_scale_segments():
 
 @pytest.mark.parametrize("B,H,hd,nq,nk", [(1, 1, 64, 64, 64), (2, 3, 72, 100, 300), (1, 2, 128, 257, 129),
                                           (2, 16, 72, 1024, 1024), (1, 4, 64, 1, 5), (1, 2, 32, 70, 512),
-                                          (1, 40, 128, 200, 512)])
+                                          (1, 40, 128, 200, 512), (1, 40, 128, 1024, 8192)])
 def test_attention_matches_oracle(B, H, hd, nq, nk):
     g = np.random.default_rng(B + H + hd + nq + nk)
     D = H * hd
