@@ -274,12 +274,7 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
     clk = clocks.stop()
     st.wait()
     launches = st.stats()["kernel_launches"] - launches0
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    ms_per_step = ms / args.steps
-    value = world * args.steps / (ms * 1e-3)
+    ms_local = ms
 
     # ---------------- overlap pass (events per streamed execution)
     st.set_timing(1)
@@ -341,7 +336,7 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
     t_roof = max(t_compute, t_link)
     step_roof = {"t_roof_ms": t_roof, "compute_ms_at_peak": t_compute, "link_ms_at_peak": t_link,
                  "link_gbs_measured": link, "streamed_bytes_per_step": streamed_bytes,
-                 "flops_per_step": flops_step, "frac": t_roof / ms_per_step,
+                 "flops_per_step": flops_step,
                  "bound": "link" if t_link >= t_compute else "tensor"}
     kernels = {n: {"launches_per_step": v["launches"] / args.steps,
                    "ms_per_step": v["ms"] / args.steps} for n, v in cls.items()}
@@ -371,13 +366,12 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
     for i in range(args.steps):
         host_step(args.warmup + i)
     e2e_s = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    ms, value, e2e_s, e2e_value = aggregate(ms_local, e2e_s, args.steps, world, dist, dev)
+    ms_per_step = ms / args.steps
+    step_roof["frac"] = step_roof["t_roof_ms"] / ms_per_step
     h2d = B * N * D * 2 + hconds[0].numel() * hconds[0].element_size() + \
         (hctxs[0].numel() * 2 if hctxs[0] is not None else 0)
-    e2e = {"value": world * args.steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+    e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": B * N * D * 2}
 
     stats = st.stats()
@@ -410,6 +404,18 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def aggregate(ms: float, e2e_s: float, steps: int, world: int, dist=None, device=None):
+    """Whole-job throughput of independent replicas: each rank ran `steps`
+    steps; the job time is the slowest rank's (max over ranks).  Returns
+    (max ms, steps/s over all ranks, max e2e seconds, e2e steps/s)."""
+    if dist is not None and world > 1:
+        import torch
+        t = torch.tensor([ms, e2e_s], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_s = float(t[0].item()), float(t[1].item())
+    return ms, world * steps / (ms * 1e-3), e2e_s, world * steps / e2e_s
 
 
 def link_peak_gbs(torch, dev) -> float:
