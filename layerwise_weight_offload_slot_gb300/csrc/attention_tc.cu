@@ -14,8 +14,9 @@
 //               tensor core computes S_{j+1} while the softmax warps work on S_j
 //   warps 2..5  softmax, one thread per query row (its TMEM lane): load S_j,
 //               mask keys past nk, running max in the log2 domain, p = 2^(s -
-//               m), row sum, P_j as bf16 into 128-byte-swizzled shared memory
-//               (the K-major A operand of P V).  The reference max only moves
+//               m), row sum, P_j as bf16 pairs over the first 64 columns of
+//               its own S buffer in TMEM (P V reads A from tensor memory).
+//               The reference max only moves
 //               when a row's max grows by more than 8 (a factor 256), and only
 //               then is that row's O rescaled in TMEM (ld, scale, st) -- the
 //               p values stay below 2^8, which bf16 and fp32 hold exactly in
@@ -46,13 +47,11 @@ struct AttnPlan {
     static constexpr int BLK = 128 * 128;                   // 128 rows x 128 B (64 cols)
     static constexpr int TBLK = TAIL ? 128 * 32 : 0;        // 128 rows x 32 B (16 cols)
     static constexpr int TILE = NB * BLK + TBLK;            // one Q, K or V tile
-    static constexpr int P_BYTES = TQ * TK * 2;
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = Q_OFF + TILE;              // 2 stages
     static constexpr int V_OFF = K_OFF + 2 * TILE;          // 2 stages
-    static constexpr int P_OFF = V_OFF + 2 * TILE;
-    static constexpr int BAR_OFF = P_OFF + P_BYTES;
-    // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2],
+    static constexpr int BAR_OFF = V_OFF + 2 * TILE;
+    // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], (2 unused),
     // p_full, pv_done, drain
     static constexpr int NBARS = 1 + 12 + 3;
     static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
@@ -63,10 +62,6 @@ struct AttnPlan {
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t O_COL = 256;             // S buffers at columns 0 and 128
 };
-
-__device__ __forceinline__ uint32_t sw128_off(int r, int j) {
-    return static_cast<uint32_t>(r * 128 + ((j ^ (r & 7)) << 4));
-}
 
 struct AttnMaps {
     CUtensorMap q, k, v;        // 64-column boxes, 128-byte swizzle
@@ -97,7 +92,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     const uint32_t q_full = bar;
     const uint32_t k_full = bar + 8, k_empty = bar + 24;
     const uint32_t v_full = bar + 40, v_empty = bar + 56;
-    const uint32_t s_full = bar + 72, s_free = bar + 88;
+    const uint32_t s_full = bar + 72;
     const uint32_t p_full = bar + 104, pv_done = bar + 112, drain = bar + 120;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + P::TMEM_SLOT_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P::ABORT_OFF);
@@ -114,7 +109,6 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             mbar_init(v_full + 8 * i, 1);
             mbar_init(v_empty + 8 * i, 1);
             mbar_init(s_full + 8 * i, 1);
-            mbar_init(s_free + 8 * i, 4);
         }
         mbar_init(p_full, 4);
         mbar_init(pv_done, 1);
@@ -176,8 +170,11 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         auto issue_s = [&](int j) -> bool {
             const int st = j & 1;
             const uint32_t ph = (j >> 1) & 1;
+            // S_j overwrites the columns of S_{j-2} / P_{j-2}: the softmax
+            // finished with them before p_full(j-2), and PV_{j-2}, issued
+            // earlier by this thread, reads P_{j-2} before this MMA writes
+            // (MMAs of one thread execute in issue order)
             if (!mbar_wait(k_full + 8 * st, ph, abort_flag)) return false;
-            if (!mbar_wait(s_free + 8 * st, ph ^ 1, abort_flag)) return false;
             tc_fence_after();
             const uint32_t d = tmem + st * TK;
             const uint32_t kb = sb + P::K_OFF + st * P::TILE;
@@ -203,12 +200,12 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             const uint32_t vb = sb + P::V_OFF + st * P::TILE;
 #pragma unroll
             for (int kk = 0; kk < TK / 16; ++kk) {
-                const uint64_t a = sw128_kmajor_desc(sb + P::P_OFF + (kk >> 2) * P::BLK + (kk & 3) * 32);
+                const uint32_t a = tmem + st * TK + kk * 8;      // P_j: 16 keys = 8 columns
                 const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-                tc_mma_f16(tmem + P::O_COL, a, sw128_mnmajor_desc(vb + kk * 2048, P::BLK), idesc_o, acc);
+                tc_mma_f16_ts(tmem + P::O_COL, a, sw128_mnmajor_desc(vb + kk * 2048, P::BLK), idesc_o, acc);
                 if constexpr (TAIL)
-                    tc_mma_f16(tmem + P::O_COL + NB * 64, a, sw32_desc(vb + NB * P::BLK + kk * 512),
-                               idesc_ot, acc);
+                    tc_mma_f16_ts(tmem + P::O_COL + NB * 64, a, sw32_desc(vb + NB * P::BLK + kk * 512),
+                                  idesc_ot, acc);
             }
             tc_commit(pv_done);
             tc_commit(v_empty + 8 * st);
@@ -245,9 +242,6 @@ __global__ void __launch_bounds__(kThreadsA, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[c * 32 + i] = __uint_as_float(r[i]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free + 8 * st);
             // raw scores: the row max is taken before scaling (scale > 0), and
             // keys past nk exist only in the last tile
             const int kvalid = nk - j * TK;
@@ -278,21 +272,22 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
             l = l * corr + rs;
             m_ref = m_new;
+            // P_j (bf16 pairs) over the first 64 columns of its own S buffer
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t w[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[64 * c + 2 * i], v[64 * c + 2 * i + 1]);
+                tmem_st_32x32b_x32(tl + st * TK + c * 32, w);
+            }
+            tmem_wait_st();
+            // PV_{j-1} must be done before O is rescaled; every phase is waited
+            // so the parity stays in step with the barrier
             if (j > 0) {
                 got = mbar_wait(pv_done, (j - 1) & 1, abort_flag);
                 got = __all_sync(0xFFFFFFFFu, got);
                 if (!got) { ok = false; break; }
                 tc_fence_after();
-            }
-            // P_j row -> shared memory (two 64-key blocks, 8 chunks of 8 keys each)
-#pragma unroll
-            for (int c = 0; c < TK / 8; ++c) {
-                uint4 w;
-                w.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
-                w.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
-                w.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
-                w.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
-                *reinterpret_cast<uint4*>(smem + P::P_OFF + (c >> 3) * P::BLK + sw128_off(row, c & 7)) = w;
             }
             if (j > 0 && __any_sync(0xFFFFFFFFu, resc)) {
 #pragma unroll 1
@@ -306,7 +301,6 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 }
                 tmem_wait_st();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
