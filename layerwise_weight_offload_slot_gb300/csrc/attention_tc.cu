@@ -47,13 +47,15 @@ struct AttnPlan {
     static constexpr int BLK = 128 * 128;                   // 128 rows x 128 B (64 cols)
     static constexpr int TBLK = TAIL ? 128 * 32 : 0;        // 128 rows x 32 B (16 cols)
     static constexpr int TILE = NB * BLK + TBLK;            // one Q, K or V tile
+    // K/V ring depth: three stages when they fit next to Q in shared memory
+    static constexpr int STAGES = (TILE * 7 + 2048 <= 227 * 1024) ? 3 : 2;
     static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = Q_OFF + TILE;              // 2 stages
-    static constexpr int V_OFF = K_OFF + 2 * TILE;          // 2 stages
-    static constexpr int BAR_OFF = V_OFF + 2 * TILE;
-    // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], (2 unused),
-    // p_full, pv_done, drain
-    static constexpr int NBARS = 1 + 12 + 3;
+    static constexpr int K_OFF = Q_OFF + TILE;              // STAGES stages
+    static constexpr int V_OFF = K_OFF + STAGES * TILE;     // STAGES stages
+    static constexpr int BAR_OFF = V_OFF + STAGES * TILE;
+    // q_full, k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[2], p_full,
+    // pv_done, drain
+    static constexpr int NBARS = 1 + 12 + 2 + 3;
     static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
     static constexpr int ABORT_OFF = TMEM_SLOT_OFF + 4;
     static constexpr int USED = ABORT_OFF + 4 + 1024;
@@ -90,10 +92,11 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     const uint32_t sb = smem_u32(smem);
     const uint32_t bar = sb + P::BAR_OFF;
     const uint32_t q_full = bar;
-    const uint32_t k_full = bar + 8, k_empty = bar + 24;
-    const uint32_t v_full = bar + 40, v_empty = bar + 56;
-    const uint32_t s_full = bar + 72;
-    const uint32_t p_full = bar + 104, pv_done = bar + 112, drain = bar + 120;
+    const uint32_t k_full = bar + 8, k_empty = bar + 32;
+    const uint32_t v_full = bar + 56, v_empty = bar + 80;
+    const uint32_t s_full = bar + 104;
+    const uint32_t p_full = bar + 120, pv_done = bar + 128, drain = bar + 136;
+    constexpr int NS = P::STAGES;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + P::TMEM_SLOT_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P::ABORT_OFF);
 
@@ -103,13 +106,13 @@ __global__ void __launch_bounds__(kThreadsA, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NS; ++i) {
             mbar_init(k_full + 8 * i, 1);
             mbar_init(k_empty + 8 * i, 1);
             mbar_init(v_full + 8 * i, 1);
             mbar_init(v_empty + 8 * i, 1);
-            mbar_init(s_full + 8 * i, 1);
         }
+        for (int i = 0; i < 2; ++i) mbar_init(s_full + 8 * i, 1);
         mbar_init(p_full, 4);
         mbar_init(pv_done, 1);
         mbar_init(drain, 1);
@@ -141,8 +144,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         mbar_arrive_expect_tx(q_full, P::TILE);
         load_tile<NB, TAIL>(sb + P::Q_OFF, &maps.q, &maps.qt, h, qt * TQ, b, q_full);
         for (int j = 0; ok && j < ntiles; ++j) {
-            const int st = j & 1;
-            const uint32_t ph = (j >> 1) & 1;
+            const int st = j % NS;
+            const uint32_t ph = (j / NS) & 1;
             if (!mbar_wait(k_empty + 8 * st, ph ^ 1, abort_flag)) { fail(); ok = false; break; }
             mbar_arrive_expect_tx(k_full + 8 * st, P::TILE);
             load_tile<NB, TAIL>(sb + P::K_OFF + st * P::TILE, &maps.k, &maps.kt, h, j * TK, b, k_full + 8 * st);
@@ -156,7 +159,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         }
         if (!ok || *abort_flag) {
             mbar_wait(q_full, 0, nullptr);
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < NS; ++i) {
                 if (issued_k & (1u << i)) mbar_wait(k_full + 8 * i, (par_k >> i) & 1u, nullptr);
                 if (issued_v & (1u << i)) mbar_wait(v_full + 8 * i, (par_v >> i) & 1u, nullptr);
             }
@@ -168,15 +171,16 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         constexpr uint32_t idesc_ot = idesc_bf16_f32(TQ, 16, true);
         bool ok = mbar_wait(q_full, 0, abort_flag);
         auto issue_s = [&](int j) -> bool {
-            const int st = j & 1;
-            const uint32_t ph = (j >> 1) & 1;
+            const int st = j % NS;                 // K stage
+            const uint32_t ph = (j / NS) & 1;
+            const int sbuf = j & 1;                // S buffer
             // S_j overwrites the columns of S_{j-2} / P_{j-2}: the softmax
             // finished with them before p_full(j-2), and PV_{j-2}, issued
             // earlier by this thread, reads P_{j-2} before this MMA writes
             // (MMAs of one thread execute in issue order)
             if (!mbar_wait(k_full + 8 * st, ph, abort_flag)) return false;
             tc_fence_after();
-            const uint32_t d = tmem + st * TK;
+            const uint32_t d = tmem + sbuf * TK;
             const uint32_t kb = sb + P::K_OFF + st * P::TILE;
 #pragma unroll
             for (int kk = 0; kk < NB * 4; ++kk) {
@@ -187,20 +191,21 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             if constexpr (TAIL)
                 tc_mma_f16(d, sw32_desc(sb + P::Q_OFF + NB * P::BLK), sw32_desc(kb + NB * P::BLK),
                            idesc_s, 1u);
-            tc_commit(s_full + 8 * st);
+            tc_commit(s_full + 8 * sbuf);
             tc_commit(k_empty + 8 * st);
             return true;
         };
         auto issue_pv = [&](int j) -> bool {
-            const int st = j & 1;
-            const uint32_t ph = (j >> 1) & 1;
+            const int st = j % NS;                 // V stage
+            const uint32_t ph = (j / NS) & 1;
+            const int sbuf = j & 1;                // P lives in S buffer sbuf
             if (!mbar_wait(p_full, j & 1, abort_flag)) return false;
             if (!mbar_wait(v_full + 8 * st, ph, abort_flag)) return false;
             tc_fence_after();
             const uint32_t vb = sb + P::V_OFF + st * P::TILE;
 #pragma unroll
             for (int kk = 0; kk < TK / 16; ++kk) {
-                const uint32_t a = tmem + st * TK + kk * 8;      // P_j: 16 keys = 8 columns
+                const uint32_t a = tmem + sbuf * TK + kk * 8;    // P_j: 16 keys = 8 columns
                 const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
                 tc_mma_f16_ts(tmem + P::O_COL, a, sw128_mnmajor_desc(vb + kk * 2048, P::BLK), idesc_o, acc);
                 if constexpr (TAIL)
