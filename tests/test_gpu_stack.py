@@ -226,3 +226,41 @@ def test_pageable_rejects_gather():
         st.attach()
     assert e.value.status == dlo.EINVAL
     st.close()
+
+
+@pytest.mark.parametrize("cfg", [
+    synth.StackConfig("dit-1block-1token", synth.KIND_DIT, 1, 128, 2, 64, 256, 1, 1, cond_dim=128),
+    synth.StackConfig("dit-2blocks-ragged", synth.KIND_DIT, 2, 128, 2, 64, 256, 3, 129, cond_dim=128),
+    synth.StackConfig("video-1token-1text", synth.KIND_VIDEO, 2, 128, 1, 128, 256, 1, 1, text_dim=64,
+                      text_tokens=1),
+    synth.StackConfig("video-hd64-ragged", synth.KIND_VIDEO, 3, 256, 4, 64, 512, 2, 257,
+                      text_dim=128, text_tokens=130),
+], ids=lambda c: c.name)
+def test_degenerate_and_ragged_shapes(cfg):
+    """One streamed block (re-staged into alternating slots every execution),
+    one query token, one text token, ragged token counts past a tile edge."""
+    st = H.make_stack(cfg)
+    st.attach()
+    for step in range(2):
+        x, cond, ctx, out = run(st, cfg, step)
+        ref = H.oracle_forward(cfg, x, cond, ctx, H.oracle_blocks(cfg))
+        assert H.rel_l2(out.float().cpu().numpy(), ref) <= 2e-2
+    log = st.log()
+    assert log == osched.schedule(cfg.n_blocks, 0, 2)
+    for s in (0, 1):
+        assert st.verify_slot(s)
+    st.close()
+
+
+def test_smaller_batch_and_tokens_than_the_maximum():
+    cfg = SMALL_VID
+    st = H.make_stack(cfg)
+    st.attach()
+    small = cfg.with_(batch=1, tokens=77, text_tokens=5)
+    x, cond, ctx = H.device_inputs(small)
+    out = st.forward(x, cond, ctx)
+    torch.cuda.synchronize()
+    st.wait()
+    ref = H.oracle_forward(small, x, cond, ctx, H.oracle_blocks(cfg))
+    assert H.rel_l2(out.float().cpu().numpy(), ref) <= 2e-2
+    st.close()
