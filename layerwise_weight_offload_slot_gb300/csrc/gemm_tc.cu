@@ -32,6 +32,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <unordered_map>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -555,6 +556,70 @@ int forced_bn() {
 
 }  // namespace
 
+namespace {
+
+// A tensor map is a pure function of its encoding arguments, and the same
+// few dozen maps (workspace, slots, resident blocks) recur every forward, so
+// encoded maps are kept in a table keyed by every argument.  Encoding costs
+// microseconds of host time per map; a lookup costs tens of nanoseconds.
+EncodeTiledFn g_encode_raw = nullptr;
+
+struct MapKey {
+    uint64_t w[23];
+    bool operator==(const MapKey& o) const { return std::memcmp(w, o.w, sizeof(w)) == 0; }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey& k) const {
+        uint64_t h = 1469598103934665603ull;   // FNV-1a over the words
+        for (uint64_t v : k.w) {
+            h ^= v;
+            h *= 1099511628211ull;
+        }
+        return static_cast<size_t>(h);
+    }
+};
+constexpr size_t kMapCacheMax = 4096;
+
+CUresult encode_cached(CUtensorMap* m, CUtensorMapDataType dt, cuuint32_t rank, void* base,
+                       const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                       const cuuint32_t* es, CUtensorMapInterleave il, CUtensorMapSwizzle sw,
+                       CUtensorMapL2promotion l2, CUtensorMapFloatOOBfill oob) {
+    if (rank < 1 || rank > 5)
+        return g_encode_raw(m, dt, rank, base, dims, strides, box, es, il, sw, l2, oob);
+    MapKey key;
+    std::memset(key.w, 0, sizeof(key.w));
+    key.w[0] = static_cast<uint64_t>(dt);
+    key.w[1] = rank;
+    key.w[2] = reinterpret_cast<uintptr_t>(base);
+    for (cuuint32_t i = 0; i < rank; ++i) {
+        key.w[3 + i] = dims[i];
+        key.w[12 + i] = box[i];
+        key.w[17 + i] = es[i];
+    }
+    for (cuuint32_t i = 0; i + 1 < rank; ++i) key.w[8 + i] = strides[i];
+    key.w[22] = static_cast<uint64_t>(il) | static_cast<uint64_t>(sw) << 8 |
+                static_cast<uint64_t>(l2) << 16 | static_cast<uint64_t>(oob) << 24;
+    static std::mutex mu;
+    static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> table;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = table.find(key);
+        if (it != table.end()) {
+            *m = it->second;
+            return CUDA_SUCCESS;
+        }
+    }
+    const CUresult r = g_encode_raw(m, dt, rank, base, dims, strides, box, es, il, sw, l2, oob);
+    if (r == CUDA_SUCCESS) {
+        std::lock_guard<std::mutex> g(mu);
+        if (table.size() >= kMapCacheMax) table.clear();
+        table.emplace(key, *m);
+    }
+    return r;
+}
+
+}  // namespace
+
 EncodeTiledFn tensor_map_encoder() {
     static EncodeTiledFn fn = nullptr;
     static std::once_flag once;
@@ -563,8 +628,10 @@ EncodeTiledFn tensor_map_encoder() {
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
                                              cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
+            q == cudaDriverEntryPointSuccess) {
+            g_encode_raw = reinterpret_cast<EncodeTiledFn>(p);
+            fn = encode_cached;
+        }
     });
     return fn;
 }

@@ -76,7 +76,8 @@ cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long*
 int gemm_num_sms();
 
 // cuTensorMapEncodeTiled, resolved once through the runtime's driver entry
-// point (no link-time dependency on libcuda); NULL if unavailable.
+// point (no link-time dependency on libcuda) and wrapped by a table of
+// already-encoded maps keyed by every argument; NULL if unavailable.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
