@@ -46,6 +46,7 @@ extern "C" {
 #endif
 
 #define DLO_ABI_VERSION 1
+#define DLO_MAX_CONTAINERS 64   /* block containers of one stack (dlo_create_multi) */
 
 typedef int dlo_status;
 #define DLO_OK            0
@@ -151,6 +152,11 @@ dlo_status dlo_block_layout(const dlo_desc* desc, dlo_tensor_info* out, int cap,
  * word).  Returns 0 for an invalid desc. */
 size_t dlo_workspace_bytes(const dlo_desc* desc);
 
+/* Workspace bytes of a multi-container stack (dlo_create_multi): one carve-up
+ * that serves every container.  Returns 0 when the descriptions are invalid
+ * as a stack (see dlo_create_multi). */
+size_t dlo_workspace_bytes_multi(const dlo_desc* descs, int n_containers);
+
 /* Fill one flat host block from fp32 source tensors.
  * tensors[i] points at the fp32 values of layout entry i (row-major, the
  * entry's shape) for every entry with source == 1, and is ignored (may be
@@ -183,9 +189,32 @@ dlo_status dlo_create(const dlo_desc* desc, int device, void* slot0, void* slot1
                       size_t slot_bytes, void* workspace, size_t ws_bytes,
                       void* compute_stream, void* copy_stream, dlo_ctx** out);
 
+/* A stack of several ordered block containers ([LW] "For models with multiple
+ * block types": a model lists more than one attribute holding transformer
+ * blocks, e.g. double-stream then single-stream blocks).  descs[c] describes
+ * container c (its own block_kind, wdtype, heads, head_dim, ffn, cond_dim and
+ * n_blocks); the stack runs container 0's blocks, then container 1's, ..., as
+ * one list of sum(n_blocks) blocks, numbered in that order by every other
+ * call (registration, residency, the schedule, logs, dlo_verify_slot).  The
+ * prefetch crosses container boundaries and, after the last block, wraps to
+ * the first streamed block as for one container.  Both slots are shared by
+ * all containers: slot_bytes >= the largest dlo_block_bytes(&descs[c])
+ * ([DLO] Startup and runtime sequence: "two shared device slots sized for the
+ * largest streamed block"); ws_bytes >= dlo_workspace_bytes_multi.
+ * 1 <= n_containers <= DLO_MAX_CONTAINERS.  The containers must agree on
+ * hidden, max_batch, max_tokens, eps, staging and register_budget_bytes;
+ * video containers also on text_dim and max_text_tokens; DLO_BLOCK_BYTES
+ * stacks have a single container.  Else DLO_EINVAL.  Host blocks for such a
+ * stack are registered with block_bytes = 0 (each block holds its own
+ * container's dlo_block_bytes); resident buffer i holds block i's bytes. */
+dlo_status dlo_create_multi(const dlo_desc* descs, int n_containers, int device, void* slot0,
+                            void* slot1, size_t slot_bytes, void* workspace, size_t ws_bytes,
+                            void* compute_stream, void* copy_stream, dlo_ctx** out);
+
 /* Attach the n = desc->n_blocks flat host blocks (host_blocks[i], block_bytes
- * = dlo_block_bytes(desc) each; immutable while attached: [OFF] "a parameter
- * has one authoritative host representation").
+ * = dlo_block_bytes(desc) each, or 0 meaning each block's own layout size --
+ * the only value for multi-container stacks; immutable while attached: [OFF]
+ * "a parameter has one authoritative host representation").
  *  DLO_HOST_PINNED:   memory is already page-locked (cudaHostAlloc or
  *                     registered); verified with cudaPointerGetAttributes.
  *  DLO_HOST_REGISTER: the library page-aligns the block ranges, merges
@@ -257,6 +286,16 @@ dlo_status dlo_set_resident(dlo_ctx* ctx, int k, void* const* device_blocks);
  * dlo_wait / dlo_forward_host / dlo_get_stats as DLO_ETIMEDOUT. */
 dlo_status dlo_forward(dlo_ctx* ctx, const void* x_in, const void* cond, const void* ctx_tokens,
                        int batch, int tokens, int text_tokens, void* x_out);
+
+/* dlo_forward of a multi-container stack: conds[c] (device, layout of that
+ * container's block_kind as for dlo_forward) conditions the blocks of
+ * container c; ctx_tokens serves every video container.  dlo_forward itself
+ * accepts a multi-container stack only when all containers share block_kind
+ * and cond_dim (one cond for all); else DLO_EINVAL.  dlo_forward_host takes
+ * single-container stacks only (DLO_EUNSUPPORTED otherwise). */
+dlo_status dlo_forward_multi(dlo_ctx* ctx, const void* x_in, const void* const* conds,
+                             const void* ctx_tokens, int batch, int tokens, int text_tokens,
+                             void* x_out);
 
 /* dlo_forward with HOST inputs and output: copies x_in, cond and ctx_tokens
  * (same layouts as dlo_forward) into the workspace on the compute stream,

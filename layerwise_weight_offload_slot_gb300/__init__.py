@@ -97,12 +97,16 @@ _c = {
     "dlo_block_bytes": _decl("dlo_block_bytes", _sz, _P(dlo_desc)),
     "dlo_block_layout": _decl("dlo_block_layout", _int, _P(dlo_desc), _P(dlo_tensor_info), _int, _P(_int)),
     "dlo_workspace_bytes": _decl("dlo_workspace_bytes", _sz, _P(dlo_desc)),
+    "dlo_workspace_bytes_multi": _decl("dlo_workspace_bytes_multi", _sz, _P(dlo_desc), _int),
     "dlo_pack_block": _decl("dlo_pack_block", _int, _P(dlo_desc), _P(_vp), _int, _vp, _sz),
     "dlo_quantize_e4m3": _decl("dlo_quantize_e4m3", _int, _vp, _sz, _vp, _P(_f32)),
     "dlo_create": _decl("dlo_create", _int, _P(dlo_desc), _int, _vp, _vp, _sz, _vp, _sz, _vp, _vp, _P(_vp)),
+    "dlo_create_multi": _decl("dlo_create_multi", _int, _P(dlo_desc), _int, _int, _vp, _vp, _sz, _vp, _sz,
+                              _vp, _vp, _P(_vp)),
     "dlo_register_host_blocks": _decl("dlo_register_host_blocks", _int, _vp, _int, _P(_vp), _sz, _uint),
     "dlo_set_resident": _decl("dlo_set_resident", _int, _vp, _int, _P(_vp)),
     "dlo_forward": _decl("dlo_forward", _int, _vp, _vp, _vp, _vp, _int, _int, _int, _vp),
+    "dlo_forward_multi": _decl("dlo_forward_multi", _int, _vp, _vp, _P(_vp), _vp, _int, _int, _int, _vp),
     "dlo_forward_host": _decl("dlo_forward_host", _int, _vp, _vp, _vp, _vp, _int, _int, _int, _vp, _int),
     "dlo_wait": _decl("dlo_wait", _int, _vp, _int),
     "dlo_destroy": _decl("dlo_destroy", _int, _vp),
@@ -157,6 +161,11 @@ def dlo_workspace_bytes(desc: dlo_desc) -> int:
     return int(_c["dlo_workspace_bytes"](ctypes.byref(desc)))
 
 
+def dlo_workspace_bytes_multi(descs) -> int:
+    arr = (dlo_desc * len(descs))(*descs)
+    return int(_c["dlo_workspace_bytes_multi"](arr, len(descs)))
+
+
 def dlo_block_layout(desc: dlo_desc) -> list[dict]:
     n = _int(0)
     _check(_c["dlo_block_layout"](ctypes.byref(desc), None, 0, ctypes.byref(n)))
@@ -208,6 +217,16 @@ def dlo_create(desc: dlo_desc, device: int, slot0: int, slot1: int, slot_bytes: 
     return out.value
 
 
+def dlo_create_multi(descs, device: int, slot0: int, slot1: int, slot_bytes: int, workspace: int,
+                     ws_bytes: int, compute_stream: int, copy_stream: int) -> int:
+    arr = (dlo_desc * len(descs))(*descs)
+    out = _vp(0)
+    st = _c["dlo_create_multi"](arr, len(descs), device, slot0, slot1, slot_bytes, workspace, ws_bytes,
+                                compute_stream, copy_stream, ctypes.byref(out))
+    _check(st, None)
+    return out.value
+
+
 def dlo_register_host_blocks(ctx: int, host_ptrs, block_bytes: int, flags: int) -> None:
     arr = (_vp * len(host_ptrs))(*host_ptrs)
     _check(_c["dlo_register_host_blocks"](ctx, len(host_ptrs), arr, block_bytes, flags), ctx)
@@ -221,6 +240,12 @@ def dlo_set_resident(ctx: int, device_ptrs) -> None:
 def dlo_forward(ctx: int, x_in: int, cond: int, ctx_tokens: int | None, batch: int, tokens: int,
                 text_tokens: int, x_out: int) -> None:
     _check(_c["dlo_forward"](ctx, x_in, cond, ctx_tokens, batch, tokens, text_tokens, x_out), ctx)
+
+
+def dlo_forward_multi(ctx: int, x_in: int, conds, ctx_tokens: int | None, batch: int, tokens: int,
+                      text_tokens: int, x_out: int) -> None:
+    arr = (_vp * len(conds))(*conds)
+    _check(_c["dlo_forward_multi"](ctx, x_in, arr, ctx_tokens, batch, tokens, text_tokens, x_out), ctx)
 
 
 def dlo_forward_host(ctx: int, x_in: int, cond: int, ctx_tokens: int | None, batch: int,

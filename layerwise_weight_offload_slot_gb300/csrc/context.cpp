@@ -53,6 +53,19 @@ struct Offsets {
     bool has_scales;
 };
 
+// One ordered block container: a run of blocks that share one description
+// and so one flat layout.  A stack is one container or several executed in
+// order as a single list of blocks ("CPU Offloading for Diffusion Models",
+// Layerwise Offloading: models with multiple block types), all streamed
+// through the same two slots, sized for the largest block.
+struct Container {
+    dlo_desc d{};
+    std::vector<Entry> L;
+    size_t block_bytes = 0;
+    Offsets off{};
+    int first = 0;
+};
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // A few host threads that split one memcpy between them (the pack of a
@@ -135,12 +148,12 @@ void CUDART_CB pack_host_fn(void* arg) {
 }  // namespace
 
 struct dlo_ctx {
-    dlo_desc d{};
+    dlo_desc d{};                 // stack-wide: shared fields, n_blocks = all blocks
     int device = 0;
-    std::vector<Entry> L;
-    size_t block_bytes = 0;
+    std::vector<Container> conts;
+    std::vector<int> cont_of;     // block index -> container index
+    size_t block_bytes = 0;       // largest block: what a slot must hold
     Workspace ws;
-    Offsets off{};
     uint8_t* slot[2] = {nullptr, nullptr};
     size_t slot_bytes = 0;
     uint8_t* wsp = nullptr;
@@ -194,7 +207,10 @@ struct dlo_ctx {
             log_slot.push_back(slot_);
         }
     }
+    bool any_video = false;
     int* err_word() { return reinterpret_cast<int*>(wsp + ws.err); }
+    const Container& cont(int blk) const { return conts[cont_of[blk]]; }
+    size_t bytes_of(int blk) const { return conts[cont_of[blk]].block_bytes; }
     // Launch through f(); with timing level 2 bracket it with events on `s`
     // and remember its class and algorithmic work.
     template <class Fn>
@@ -226,10 +242,10 @@ size_t off_of(const std::vector<Entry>& L, const char* n) {
     return i < 0 ? 0 : L[i].offset;
 }
 
-void fill_offsets(dlo_ctx* c) {
-    const auto& L = c->L;
-    Offsets& o = c->off;
-    if (c->d.block_kind == DLO_BLOCK_DIT) {
+void fill_offsets(Container* k) {
+    const auto& L = k->L;
+    Offsets& o = k->off;
+    if (k->d.block_kind == DLO_BLOCK_DIT) {
         o.ada_w = off_of(L, "adaLN.weight");
         o.ada_b = off_of(L, "adaLN.bias");
         o.qkv_w = off_of(L, "attn.qkv.weight");
@@ -291,26 +307,27 @@ bool stream_wait(cudaStream_t s, int timeout_ms, cudaError_t* e) {
 // Copy host block `blk` into slot `s` on the copy stream.
 dlo_status stage(dlo_ctx* c, int blk, int s) {
     cudaError_t e;
+    const size_t bytes = c->bytes_of(blk);
     if (c->d.staging == DLO_STAGE_GATHER) {
-        e = c->timed(DLO_K_GATHER, 0.0, 2.0 * c->block_bytes, c->xs, [&] {
-            return launch_gather(c->slot[s], c->host_dev[blk], c->block_bytes, c->xs, &c->st.kernel_launches);
+        e = c->timed(DLO_K_GATHER, 0.0, 2.0 * bytes, c->xs, [&] {
+            return launch_gather(c->slot[s], c->host_dev[blk], bytes, c->xs, &c->st.kernel_launches);
         });
     } else if (c->pageable) {
         // pack into the next pinned host slot (stream-ordered host function),
         // then copy that slot to the device slot
         const int h = c->hstage_next;
         c->hstage_next ^= 1;
-        PackJob* job = new PackJob{c->pool.get(), c->hstage[h], c->host[blk], c->block_bytes};
+        PackJob* job = new PackJob{c->pool.get(), c->hstage[h], c->host[blk], bytes};
         e = cudaLaunchHostFunc(c->xs, pack_host_fn, job);
         if (e != cudaSuccess) {
             delete job;
         } else {
-            e = cudaMemcpyAsync(c->slot[s], c->hstage[h], c->block_bytes, cudaMemcpyHostToDevice, c->xs);
+            e = cudaMemcpyAsync(c->slot[s], c->hstage[h], bytes, cudaMemcpyHostToDevice, c->xs);
             ++c->st.h2d_copies;
         }
     } else if (c->d.staging == DLO_STAGE_PER_TENSOR) {
         e = cudaSuccess;
-        for (const Entry& t : c->L) {
+        for (const Entry& t : c->cont(blk).L) {
             if (!t.bytes) continue;
             e = cudaMemcpyAsync(c->slot[s] + t.offset, c->host[blk] + t.offset, t.bytes,
                                 cudaMemcpyHostToDevice, c->xs);
@@ -318,13 +335,13 @@ dlo_status stage(dlo_ctx* c, int blk, int s) {
             ++c->st.h2d_copies;
         }
     } else {
-        e = cudaMemcpyAsync(c->slot[s], c->host[blk], c->block_bytes, cudaMemcpyHostToDevice, c->xs);
+        e = cudaMemcpyAsync(c->slot[s], c->host[blk], bytes, cudaMemcpyHostToDevice, c->xs);
         ++c->st.h2d_copies;
     }
     if (e != cudaSuccess) return c->cuda_fail(e, "slot staging");
     c->slot_block[s] = blk;
     ++c->st.stagings;
-    c->st.staged_bytes += c->block_bytes;
+    c->st.staged_bytes += bytes;
     c->log(0, blk, s);
     return DLO_OK;
 }
@@ -350,16 +367,17 @@ dlo_status prime(dlo_ctx* c) {
 // One block from weights at `W` (a slot or a resident buffer).
 dlo_status run_block(dlo_ctx* c, const uint8_t* W, int B, int N, int L, const void* cond,
                      const void* ctx_tokens, int block, void* x_out) {
-    const dlo_desc& d = c->d;
+    const Container& K = c->cont(block);
+    const dlo_desc& d = K.d;
     if (d.block_kind == DLO_BLOCK_BYTES) {
         unsigned long long* sums = static_cast<unsigned long long*>(x_out) + block;
-        LCHECK(c->timed(DLO_K_CONVERT, 0.0, static_cast<double>(c->block_bytes), c->cs, [&] {
-                   return launch_checksum(W, c->block_bytes, sums, c->cs, &c->st.kernel_launches);
+        LCHECK(c->timed(DLO_K_CONVERT, 0.0, static_cast<double>(K.block_bytes), c->cs, [&] {
+                   return launch_checksum(W, K.block_bytes, sums, c->cs, &c->st.kernel_launches);
                }),
                "checksum");
         return DLO_OK;
     }
-    const Offsets& o = c->off;
+    const Offsets& o = K.off;
     const int D = d.hidden, F = d.ffn, H = d.heads, hd = d.head_dim;
     const int BN = B * N;
     uint8_t* w = c->wsp;
@@ -516,25 +534,37 @@ extern "C" const char* dlo_last_error(const dlo_ctx* ctx) {
 
 extern "C" void dlo_debug_fail_register(int nth) { g_fail_register_nth.store(nth > 0 ? nth : 0); }
 
-extern "C" dlo_status dlo_create(const dlo_desc* desc, int device, void* slot0, void* slot1,
-                                 size_t slot_bytes, void* workspace, size_t ws_bytes,
-                                 void* compute_stream, void* copy_stream, dlo_ctx** out) {
+namespace {
+
+dlo_status create_stack(const dlo_desc* descs, int n_cont, int device, void* slot0, void* slot1,
+                        size_t slot_bytes, void* workspace, size_t ws_bytes, void* compute_stream,
+                        void* copy_stream, dlo_ctx** out) {
     if (out) *out = nullptr;
     std::string msg;
-    dlo_status st = validate_desc(desc, &msg);
+    dlo_desc whole{};
+    dlo_status st = validate_stack(descs, n_cont, &whole, &msg);
     auto cfail = [&](dlo_status s, const std::string& m) {
         g_create_error = m;
         return s;
     };
     if (!out) return cfail(DLO_EINVAL, "out is NULL");
     if (st != DLO_OK) return cfail(st, msg);
-    std::vector<Entry> L;
-    const size_t bb = build_layout(*desc, &L);
-    const Workspace ws = plan_workspace(*desc);
+    std::vector<Container> conts(n_cont);
+    std::vector<int> cont_of;
+    size_t bb = 0;
+    for (int i = 0; i < n_cont; ++i) {
+        conts[i].d = descs[i];
+        conts[i].block_bytes = build_layout(descs[i], &conts[i].L);
+        conts[i].first = static_cast<int>(cont_of.size());
+        fill_offsets(&conts[i]);
+        cont_of.insert(cont_of.end(), descs[i].n_blocks, i);
+        bb = std::max(bb, conts[i].block_bytes);
+    }
+    const Workspace ws = plan_workspace_stack(descs, n_cont);
     if (!slot0 || !slot1 || slot0 == slot1) return cfail(DLO_EINVAL, "two distinct slots are required");
     if (!aligned(slot0, 256) || !aligned(slot1, 256) || !aligned(workspace, 256))
         return cfail(DLO_EINVAL, "slots and workspace must be 256-byte aligned");
-    if (slot_bytes < bb) return cfail(DLO_ENOMEM, "slot_bytes < block bytes");
+    if (slot_bytes < bb) return cfail(DLO_ENOMEM, "slot_bytes < bytes of the largest block");
     {
         const uintptr_t a0 = reinterpret_cast<uintptr_t>(slot0), a1 = reinterpret_cast<uintptr_t>(slot1);
         if ((a0 < a1 && a0 + slot_bytes > a1) || (a1 < a0 && a1 + slot_bytes > a0))
@@ -551,9 +581,11 @@ extern "C" dlo_status dlo_create(const dlo_desc* desc, int device, void* slot0, 
     if (e != cudaSuccess) return cfail(DLO_ECUDA, std::string("cudaSetDevice: ") + cudaGetErrorString(e));
 
     std::unique_ptr<dlo_ctx> c(new dlo_ctx());
-    c->d = *desc;
+    c->d = whole;
     c->device = device;
-    c->L = std::move(L);
+    c->conts = std::move(conts);
+    c->cont_of = std::move(cont_of);
+    for (const Container& k : c->conts) c->any_video |= k.d.block_kind == DLO_BLOCK_VIDEO;
     c->block_bytes = bb;
     c->ws = ws;
     c->slot[0] = static_cast<uint8_t*>(slot0);
@@ -562,7 +594,6 @@ extern "C" dlo_status dlo_create(const dlo_desc* desc, int device, void* slot0, 
     c->wsp = static_cast<uint8_t*>(workspace);
     c->cs = static_cast<cudaStream_t>(compute_stream);
     c->xs = static_cast<cudaStream_t>(copy_stream);
-    fill_offsets(c.get());
     auto evfail = [&](cudaError_t err) {
         for (int i = 0; i < 2; ++i) {
             if (c->copy_done[i]) cudaEventDestroy(c->copy_done[i]);
@@ -585,14 +616,31 @@ extern "C" dlo_status dlo_create(const dlo_desc* desc, int device, void* slot0, 
     return DLO_OK;
 }
 
+}  // namespace
+
+extern "C" dlo_status dlo_create(const dlo_desc* desc, int device, void* slot0, void* slot1,
+                                 size_t slot_bytes, void* workspace, size_t ws_bytes,
+                                 void* compute_stream, void* copy_stream, dlo_ctx** out) {
+    return create_stack(desc, 1, device, slot0, slot1, slot_bytes, workspace, ws_bytes, compute_stream,
+                        copy_stream, out);
+}
+
+extern "C" dlo_status dlo_create_multi(const dlo_desc* descs, int n_containers, int device, void* slot0,
+                                       void* slot1, size_t slot_bytes, void* workspace, size_t ws_bytes,
+                                       void* compute_stream, void* copy_stream, dlo_ctx** out) {
+    return create_stack(descs, n_containers, device, slot0, slot1, slot_bytes, workspace, ws_bytes,
+                        compute_stream, copy_stream, out);
+}
+
 extern "C" dlo_status dlo_register_host_blocks(dlo_ctx* c, int n, const void* const* host_blocks,
                                                size_t block_bytes, unsigned flags) {
     if (!c) return DLO_EINVAL;
     if (c->state != kCreated) return c->fail(DLO_ESTATE, "host blocks are already attached");
     if (n != c->d.n_blocks) return c->fail(DLO_EINVAL, "n (%d) != n_blocks (%d)", n, c->d.n_blocks);
     if (!host_blocks) return c->fail(DLO_EINVAL, "host_blocks is NULL");
-    if (block_bytes != c->block_bytes)
-        return c->fail(DLO_EINVAL, "block_bytes %zu != layout bytes %zu", block_bytes, c->block_bytes);
+    if (block_bytes != 0 && (c->conts.size() != 1 || block_bytes != c->block_bytes))
+        return c->fail(DLO_EINVAL, "block_bytes %zu != layout bytes %zu (pass 0 to use each block's own size)",
+                       block_bytes, c->block_bytes);
     const bool pinned = flags == DLO_HOST_PINNED, reg = flags == DLO_HOST_REGISTER;
     const bool pageable = flags == DLO_HOST_PAGEABLE;
     if (!pinned && !reg && !pageable)
@@ -607,7 +655,7 @@ extern "C" dlo_status dlo_register_host_blocks(dlo_ctx* c, int n, const void* co
     if (pageable) {
         // two bounded pinned host staging slots; nothing else is page-locked
         for (int i = 0; i < 2; ++i) {
-            cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&c->hstage[i]), block_bytes,
+            cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&c->hstage[i]), c->block_bytes,
                                           cudaHostAllocDefault);
             if (e != cudaSuccess) {
                 cudaGetLastError();
@@ -632,7 +680,7 @@ extern "C" dlo_status dlo_register_host_blocks(dlo_ctx* c, int n, const void* co
         std::vector<std::pair<uintptr_t, uintptr_t>> r;
         for (int i = 0; i < n; ++i) {
             const uintptr_t a = reinterpret_cast<uintptr_t>(host_blocks[i]);
-            r.push_back({a / page * page, (a + block_bytes + page - 1) / page * page});
+            r.push_back({a / page * page, (a + c->bytes_of(i) + page - 1) / page * page});
         }
         std::sort(r.begin(), r.end());
         std::vector<std::pair<uintptr_t, uintptr_t>> merged;
@@ -690,7 +738,7 @@ extern "C" dlo_status dlo_register_host_blocks(dlo_ctx* c, int n, const void* co
     for (int i = 0; i < n; ++i) {
         cudaPointerAttributes at{};
         cudaError_t e = cudaPointerGetAttributes(&at, host_blocks[i]);
-        const uint8_t* last = static_cast<const uint8_t*>(host_blocks[i]) + block_bytes - 1;
+        const uint8_t* last = static_cast<const uint8_t*>(host_blocks[i]) + c->bytes_of(i) - 1;
         cudaPointerAttributes at2{};
         cudaError_t e2 = cudaPointerGetAttributes(&at2, last);
         if (e != cudaSuccess || e2 != cudaSuccess || at.type != cudaMemoryTypeHost ||
@@ -727,7 +775,7 @@ extern "C" dlo_status dlo_set_resident(dlo_ctx* c, int k, void* const* device_bl
             return c->fail(DLO_EINVAL, "resident buffer %d is NULL or not 256-byte aligned", i);
     cudaSetDevice(c->device);
     for (int i = 0; i < k; ++i) {
-        cudaError_t e = cudaMemcpyAsync(device_blocks[i], c->host[i], c->block_bytes, cudaMemcpyHostToDevice, c->xs);
+        cudaError_t e = cudaMemcpyAsync(device_blocks[i], c->host[i], c->bytes_of(i), cudaMemcpyHostToDevice, c->xs);
         if (e != cudaSuccess) return c->cuda_fail(e, "resident copy");
     }
     if (k > 0) {
@@ -743,10 +791,12 @@ extern "C" dlo_status dlo_set_resident(dlo_ctx* c, int k, void* const* device_bl
     return prime(c);
 }
 
-extern "C" dlo_status dlo_forward(dlo_ctx* c, const void* x_in, const void* cond,
-                                  const void* ctx_tokens, int batch, int tokens, int text_tokens,
-                                  void* x_out) {
-    if (!c) return DLO_EINVAL;
+namespace {
+
+// One forward over every container's blocks in order; conds[i] conditions
+// the blocks of container i.
+dlo_status forward_stack(dlo_ctx* c, const void* x_in, const void* const* conds, const void* ctx_tokens,
+                         int batch, int tokens, int text_tokens, void* x_out) {
     if (c->state != kRegistered) return c->fail(DLO_ESTATE, "register host blocks first");
     const dlo_desc& d = c->d;
     const bool bytes_kind = d.block_kind == DLO_BLOCK_BYTES;
@@ -756,10 +806,13 @@ extern "C" dlo_status dlo_forward(dlo_ctx* c, const void* x_in, const void* cond
     } else {
     if (batch < 1 || batch > d.max_batch) return c->fail(DLO_EINVAL, "batch out of range");
     if (tokens < 1 || tokens > d.max_tokens) return c->fail(DLO_EINVAL, "tokens out of range");
-    if (!x_in || !x_out || !cond) return c->fail(DLO_EINVAL, "NULL input/output");
-    if (!aligned(x_in, 16) || !aligned(x_out, 16) || !aligned(cond, 16))
+    if (!x_in || !x_out) return c->fail(DLO_EINVAL, "NULL input/output");
+    if (!aligned(x_in, 16) || !aligned(x_out, 16))
         return c->fail(DLO_EINVAL, "inputs/outputs must be 16-byte aligned");
-    if (d.block_kind == DLO_BLOCK_VIDEO) {
+    for (size_t i = 0; i < c->conts.size(); ++i)
+        if (!conds[i] || !aligned(conds[i], 16))
+            return c->fail(DLO_EINVAL, "conditioning of container %zu is NULL or not 16-byte aligned", i);
+    if (c->any_video) {
         if (text_tokens < 1 || text_tokens > d.max_text_tokens) return c->fail(DLO_EINVAL, "text_tokens out of range");
         if (!ctx_tokens || !aligned(ctx_tokens, 16)) return c->fail(DLO_EINVAL, "ctx_tokens NULL or misaligned");
     }
@@ -783,7 +836,7 @@ extern "C" dlo_status dlo_forward(dlo_ctx* c, const void* x_in, const void* cond
     }
     for (int i = 0; i < k; ++i) {
         c->log(1, i, -1);
-        r = run_block(c, c->resident[i], batch, tokens, text_tokens, cond, ctx_tokens, i, x_out);
+        r = run_block(c, c->resident[i], batch, tokens, text_tokens, conds[c->cont_of[i]], ctx_tokens, i, x_out);
         if (r != DLO_OK) return r;
     }
     for (int i = k; i < n; ++i) {
@@ -809,7 +862,7 @@ extern "C" dlo_status dlo_forward(dlo_ctx* c, const void* x_in, const void* cond
         LCHECK(cudaStreamWaitEvent(c->cs, c->copy_done[s], 0), "compute waits copy");
         if (c->timing) LCHECK(cudaEventRecord(te.comp0, c->cs), "event");
         c->log(1, i, s);
-        r = run_block(c, c->slot[s], batch, tokens, text_tokens, cond, ctx_tokens, i, x_out);
+        r = run_block(c, c->slot[s], batch, tokens, text_tokens, conds[c->cont_of[i]], ctx_tokens, i, x_out);
         if (r != DLO_OK) return r;
         if (c->timing) LCHECK(cudaEventRecord(te.comp1, c->cs), "event");
         LCHECK(cudaEventRecord(c->compute_done[s], c->cs), "event record");
@@ -824,6 +877,28 @@ extern "C" dlo_status dlo_forward(dlo_ctx* c, const void* x_in, const void* cond
     }
     ++c->st.forwards;
     return DLO_OK;
+}
+
+}  // namespace
+
+extern "C" dlo_status dlo_forward(dlo_ctx* c, const void* x_in, const void* cond,
+                                  const void* ctx_tokens, int batch, int tokens, int text_tokens,
+                                  void* x_out) {
+    if (!c) return DLO_EINVAL;
+    const Container& z = c->conts[0];
+    for (const Container& k : c->conts)
+        if (k.d.block_kind != z.d.block_kind || k.d.cond_dim != z.d.cond_dim)
+            return c->fail(DLO_EINVAL, "containers take different conditionings: use dlo_forward_multi");
+    std::vector<const void*> conds(c->conts.size(), cond);
+    return forward_stack(c, x_in, conds.data(), ctx_tokens, batch, tokens, text_tokens, x_out);
+}
+
+extern "C" dlo_status dlo_forward_multi(dlo_ctx* c, const void* x_in, const void* const* conds,
+                                        const void* ctx_tokens, int batch, int tokens, int text_tokens,
+                                        void* x_out) {
+    if (!c) return DLO_EINVAL;
+    if (!conds) return c->fail(DLO_EINVAL, "conds is NULL");
+    return forward_stack(c, x_in, conds, ctx_tokens, batch, tokens, text_tokens, x_out);
 }
 
 extern "C" dlo_status dlo_wait(dlo_ctx* c, int timeout_ms) {
@@ -843,6 +918,8 @@ extern "C" dlo_status dlo_forward_host(dlo_ctx* c, const void* x_in, const void*
                                        int text_tokens, void* x_out, int timeout_ms) {
     if (!c) return DLO_EINVAL;
     if (c->state != kRegistered) return c->fail(DLO_ESTATE, "register host blocks first");
+    if (c->conts.size() != 1)
+        return c->fail(DLO_EUNSUPPORTED, "host-buffer forward takes single-container stacks");
     const dlo_desc& d = c->d;
     if (d.block_kind == DLO_BLOCK_BYTES) {
         if (!x_out) return c->fail(DLO_EINVAL, "NULL output");
@@ -965,10 +1042,11 @@ extern "C" dlo_status dlo_verify_slot(dlo_ctx* c, int slot, int block) {
     cudaSetDevice(c->device);
     cudaError_t e = cudaSuccess;
     if (!stream_wait(c->xs, 60000, &e)) return c->fail(DLO_ETIMEDOUT, "copy stream busy");
-    std::vector<uint8_t> tmp(c->block_bytes);
-    e = cudaMemcpy(tmp.data(), c->slot[slot], c->block_bytes, cudaMemcpyDeviceToHost);
+    const size_t nb = c->bytes_of(block);
+    std::vector<uint8_t> tmp(nb);
+    e = cudaMemcpy(tmp.data(), c->slot[slot], nb, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return c->cuda_fail(e, "slot read-back");
-    if (std::memcmp(tmp.data(), c->host[block], c->block_bytes) != 0)
+    if (std::memcmp(tmp.data(), c->host[block], nb) != 0)
         return c->fail(DLO_EMISMATCH, "slot %d differs from host block %d", slot, block);
     return DLO_OK;
 }

@@ -28,6 +28,11 @@ dlo_status validate_desc(const dlo_desc* d, std::string* msg);
 // Builds the flat block layout (groups start 256-B aligned; members of a
 // group are contiguous).  Returns total bytes (multiple of 256).
 size_t build_layout(const dlo_desc& d, std::vector<Entry>* out);
+// Validates an ordered list of n container descriptions: each valid, the
+// shared fields equal, bytes blocks alone.  *stack (may be NULL) receives the
+// stack-wide description: container 0's fields, n_blocks = all blocks, the
+// text fields of the video containers.
+dlo_status validate_stack(const dlo_desc* ds, int n, dlo_desc* stack, std::string* msg);
 int find_entry(const std::vector<Entry>& L, const char* name);
 
 // Device workspace carve-up for max_batch x max_tokens activations.
@@ -46,6 +51,8 @@ struct Workspace {
     size_t total = 0;
 };
 Workspace plan_workspace(const dlo_desc& d);
+// One workspace that serves every container of a stack.
+Workspace plan_workspace_stack(const dlo_desc* ds, int n);
 
 // ------------------------------------------------------------------ host math
 

@@ -64,6 +64,63 @@ dlo_status validate_desc(const dlo_desc* d, std::string* msg) {
     return DLO_OK;
 }
 
+dlo_status validate_stack(const dlo_desc* ds, int n, dlo_desc* stack, std::string* msg) {
+    auto fail = [&](dlo_status st, const char* m) {
+        if (msg) *msg = m;
+        return st;
+    };
+    if (!ds) return fail(DLO_EINVAL, "descs is NULL");
+    if (n < 1 || n > DLO_MAX_CONTAINERS) return fail(DLO_EINVAL, "n_containers out of range");
+    long long total = 0;
+    int video = -1;
+    for (int i = 0; i < n; ++i) {
+        dlo_status st = validate_desc(&ds[i], msg);
+        if (st != DLO_OK) return st;
+        const dlo_desc& a = ds[i];
+        const dlo_desc& z = ds[0];
+        if (n > 1 && a.block_kind == DLO_BLOCK_BYTES)
+            return fail(DLO_EINVAL, "bytes blocks cannot share a stack with other containers");
+        if (a.hidden != z.hidden || a.max_batch != z.max_batch || a.max_tokens != z.max_tokens ||
+            a.eps != z.eps || a.staging != z.staging || a.register_budget_bytes != z.register_budget_bytes)
+            return fail(DLO_EINVAL,
+                        "containers must share hidden, max_batch, max_tokens, eps, staging and "
+                        "register_budget_bytes");
+        if (a.block_kind == DLO_BLOCK_VIDEO) {
+            if (video >= 0 && (a.text_dim != ds[video].text_dim ||
+                               a.max_text_tokens != ds[video].max_text_tokens))
+                return fail(DLO_EINVAL, "video containers must share text_dim and max_text_tokens");
+            if (video < 0) video = i;
+        }
+        total += a.n_blocks;
+    }
+    if (total > (1LL << 24)) return fail(DLO_EINVAL, "too many blocks");
+    if (stack) {
+        *stack = ds[0];
+        stack->n_blocks = static_cast<int>(total);
+        if (video >= 0) {
+            stack->text_dim = ds[video].text_dim;
+            stack->max_text_tokens = ds[video].max_text_tokens;
+        }
+    }
+    return DLO_OK;
+}
+
+Workspace plan_workspace_stack(const dlo_desc* ds, int n) {
+    // one carve-up that serves every container: the widest FFN, and the
+    // cross-attention buffers when any container is a video one
+    dlo_desc u = ds[0];
+    for (int i = 0; i < n; ++i) {
+        u.ffn = std::max(u.ffn, ds[i].ffn);
+        u.cond_dim = std::max(u.cond_dim, ds[i].cond_dim);
+        if (ds[i].block_kind == DLO_BLOCK_VIDEO) {
+            u.block_kind = DLO_BLOCK_VIDEO;
+            u.text_dim = ds[i].text_dim;
+            u.max_text_tokens = ds[i].max_text_tokens;
+        }
+    }
+    return plan_workspace(u);
+}
+
 namespace {
 struct Builder {
     std::vector<Entry>* out;
@@ -278,6 +335,11 @@ extern "C" dlo_status dlo_block_layout(const dlo_desc* desc, dlo_tensor_info* ou
 extern "C" size_t dlo_workspace_bytes(const dlo_desc* desc) {
     if (validate_desc(desc, nullptr) != DLO_OK) return 0;
     return plan_workspace(*desc).total;
+}
+
+extern "C" size_t dlo_workspace_bytes_multi(const dlo_desc* descs, int n_containers) {
+    if (validate_stack(descs, n_containers, nullptr, nullptr) != DLO_OK) return 0;
+    return plan_workspace_stack(descs, n_containers).total;
 }
 
 extern "C" dlo_status dlo_quantize_e4m3(const float* w, size_t n, uint8_t* codes, float* scale) {

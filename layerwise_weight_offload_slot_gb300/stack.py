@@ -16,10 +16,11 @@ import numpy as np
 import torch
 
 from . import (BLOCK_BYTES, BLOCK_DIT, BLOCK_VIDEO, HOST_PAGEABLE, HOST_PINNED, HOST_REGISTER, OK, STAGE_MEMCPY, W_BF16,
-               dlo_block_bytes, dlo_block_layout, dlo_create, dlo_destroy, dlo_forward,
-               dlo_forward_host, dlo_get_log, dlo_get_stats, dlo_pack_block,
-               dlo_register_host_blocks, dlo_reset_log, dlo_set_resident, dlo_set_timing,
-               dlo_verify_slot, dlo_wait, dlo_workspace_bytes, make_desc)
+               dlo_block_bytes, dlo_block_layout, dlo_create, dlo_create_multi, dlo_destroy,
+               dlo_forward, dlo_forward_host, dlo_forward_multi, dlo_get_log, dlo_get_stats,
+               dlo_pack_block, dlo_register_host_blocks, dlo_reset_log, dlo_set_resident,
+               dlo_set_timing, dlo_verify_slot, dlo_wait, dlo_workspace_bytes,
+               dlo_workspace_bytes_multi, make_desc)
 
 PAGE = 4096
 
@@ -29,16 +30,18 @@ def _round(n: int, a: int) -> int:
 
 
 class HostBlocks:
-    """n flat blocks of `block_bytes`, each page-aligned, in one allocation.
+    """n flat blocks of `block_bytes` (or sizes[i] <= block_bytes each), each
+    page-aligned, in one allocation.
 
     mode "pinned": torch pinned memory (cudaHostAlloc); "register": anonymous
     mmap (pageable) for the library to register; "pageable": anonymous mmap
     that stays pageable (the library packs it through pinned host slots).
     """
 
-    def __init__(self, n: int, block_bytes: int, mode: str):
+    def __init__(self, n: int, block_bytes: int, mode: str, sizes=None):
         self.n = n
         self.block_bytes = block_bytes
+        self.sizes = list(sizes) if sizes is not None else [block_bytes] * n
         self.stride = _round(block_bytes, PAGE)
         total = self.stride * n + PAGE
         self.mode = mode
@@ -58,7 +61,7 @@ class HostBlocks:
 
     def view(self, i: int) -> np.ndarray:
         """numpy uint8 view of block i (host memory)."""
-        return np.ctypeslib.as_array((ctypes.c_uint8 * self.block_bytes).from_address(self.ptrs[i]))
+        return np.ctypeslib.as_array((ctypes.c_uint8 * self.sizes[i]).from_address(self.ptrs[i]))
 
     def close(self):
         self._t = None
@@ -69,23 +72,45 @@ class HostBlocks:
 
 
 class OffloadStack:
-    def __init__(self, *, block_kind: int, n_blocks: int, hidden: int = 0, heads: int = 0,
-                 head_dim: int = 0, ffn: int = 0, cond_dim: int = 0, text_dim: int = 0,
-                 max_batch: int = 1, max_tokens: int = 1, max_text_tokens: int = 0,
-                 wdtype: int = W_BF16, eps: float = 1e-6, staging: int = STAGE_MEMCPY,
-                 host_mode: str = "pinned", register_budget_bytes: int = 0,
-                 bytes_block: int = 0, device: int = 0, host: "HostBlocks | None" = None):
-        self.desc = make_desc(block_kind=block_kind, n_blocks=n_blocks, hidden=hidden, heads=heads,
-                              head_dim=head_dim, ffn=ffn, cond_dim=cond_dim, text_dim=text_dim,
-                              max_batch=max_batch, max_tokens=max_tokens,
-                              max_text_tokens=max_text_tokens, wdtype=wdtype, eps=eps,
-                              staging=staging, register_budget_bytes=register_budget_bytes,
-                              bytes_block=bytes_block)
-        self.block_bytes = dlo_block_bytes(self.desc)
-        if self.block_bytes == 0:
+    """One block stack.  Either one container (block_kind, n_blocks and the
+    per-block fields as keywords) or several ordered containers:
+    containers = [dict(block_kind=..., n_blocks=..., heads=..., head_dim=...,
+    ffn=..., cond_dim=..., text_dim=..., max_text_tokens=..., wdtype=...), ...]
+    with the shared fields (hidden, max_batch, max_tokens, eps, staging,
+    register_budget_bytes) given once.  Blocks are numbered across containers
+    in order."""
+
+    def __init__(self, *, block_kind: int = BLOCK_DIT, n_blocks: int = 0, hidden: int = 0,
+                 heads: int = 0, head_dim: int = 0, ffn: int = 0, cond_dim: int = 0,
+                 text_dim: int = 0, max_batch: int = 1, max_tokens: int = 1,
+                 max_text_tokens: int = 0, wdtype: int = W_BF16, eps: float = 1e-6,
+                 staging: int = STAGE_MEMCPY, host_mode: str = "pinned",
+                 register_budget_bytes: int = 0, bytes_block: int = 0, device: int = 0,
+                 host: "HostBlocks | None" = None, containers=None):
+        shared = dict(hidden=hidden, max_batch=max_batch, max_tokens=max_tokens, eps=eps,
+                      staging=staging, register_budget_bytes=register_budget_bytes)
+        if containers is None:
+            containers = [dict(block_kind=block_kind, n_blocks=n_blocks, heads=heads,
+                               head_dim=head_dim, ffn=ffn, cond_dim=cond_dim, text_dim=text_dim,
+                               max_text_tokens=max_text_tokens, wdtype=wdtype,
+                               bytes_block=bytes_block)]
+        self.descs = [make_desc(**{**shared, **ct}) for ct in containers]
+        self.multi = len(self.descs) > 1
+        self.desc = self.descs[0]
+        self.container_bytes = [dlo_block_bytes(d) for d in self.descs]
+        if not all(self.container_bytes):
             raise ValueError("invalid stack description")
-        self.layout = dlo_block_layout(self.desc)
-        self.ws_bytes = dlo_workspace_bytes(self.desc)
+        self.container_of = [ci for ci, d in enumerate(self.descs) for _ in range(d.n_blocks)]
+        self.block_sizes = [self.container_bytes[ci] for ci in self.container_of]
+        self.block_bytes = max(self.container_bytes)
+        self.layouts = [dlo_block_layout(d) for d in self.descs]
+        self.layout = self.layouts[0]
+        self.ws_bytes = (dlo_workspace_bytes_multi(self.descs) if self.multi
+                         else dlo_workspace_bytes(self.desc))
+        if self.ws_bytes == 0:
+            raise ValueError("invalid stack description")
+        n_blocks = len(self.container_of)
+        block_kind = self.desc.block_kind
         self.device = device
         self.dev = torch.device("cuda", device)
         sb = _round(self.block_bytes, 256)
@@ -99,19 +124,22 @@ class OffloadStack:
         self.copy_stream = torch.cuda.Stream(device=self.dev)
         # host blocks may be shared between contexts (pinned mode only)
         self._own_host = host is None
-        self.host = host if host is not None else HostBlocks(n_blocks, self.block_bytes, host_mode)
+        self.host = host if host is not None else HostBlocks(n_blocks, self.block_bytes, host_mode,
+                                                             sizes=self.block_sizes)
         self.host_mode = host_mode
         self.n_blocks = n_blocks
         self.kind = block_kind
         self._resident = []
         torch.cuda.synchronize(self.dev)
-        self.ctx = dlo_create(self.desc, device, self.slot_ptrs[0], self.slot_ptrs[1], sb,
-                              self.ws_ptr, self.ws_bytes, self.compute_stream.cuda_stream,
-                              self.copy_stream.cuda_stream)
+        create = dlo_create_multi if self.multi else dlo_create
+        self.ctx = create(self.descs if self.multi else self.desc, device, self.slot_ptrs[0],
+                          self.slot_ptrs[1], sb, self.ws_ptr, self.ws_bytes,
+                          self.compute_stream.cuda_stream, self.copy_stream.cuda_stream)
 
     # ---------------------------------------------------------------- setup
     def pack(self, i: int, params: dict) -> None:
-        dlo_pack_block(self.desc, params, self.host.ptrs[i], self.block_bytes)
+        dlo_pack_block(self.descs[self.container_of[i]], params, self.host.ptrs[i],
+                       self.block_sizes[i])
 
     def pack_all(self, blocks, threads: int = 8) -> None:
         """blocks: list of param dicts, or a callable i -> param dict."""
@@ -122,12 +150,13 @@ class OffloadStack:
     def attach(self) -> None:
         flags = {"pinned": HOST_PINNED, "register": HOST_REGISTER,
                  "pageable": HOST_PAGEABLE}[self.host_mode]
-        dlo_register_host_blocks(self.ctx, self.host.ptrs, self.block_bytes, flags)
+        dlo_register_host_blocks(self.ctx, self.host.ptrs, 0 if self.multi else self.block_bytes,
+                                 flags)
 
     def set_resident(self, k: int) -> None:
         bufs = []
-        for _ in range(k):
-            t = torch.empty(self.block_bytes + 256, dtype=torch.uint8, device=self.dev)
+        for i in range(k):
+            t = torch.empty(self.block_sizes[i] + 256, dtype=torch.uint8, device=self.dev)
             bufs.append(t)
         self._resident = bufs
         dlo_set_resident(self.ctx, [_round(t.data_ptr(), 256) for t in bufs])
@@ -143,17 +172,21 @@ class OffloadStack:
         cur.wait_stream(self.compute_stream)
         return sums
 
-    def forward(self, x: torch.Tensor, cond: torch.Tensor, ctx_tokens: torch.Tensor | None = None,
+    def forward(self, x: torch.Tensor, cond, ctx_tokens: torch.Tensor | None = None,
                 out: torch.Tensor | None = None) -> torch.Tensor:
+        """cond: one tensor for all containers, or a list with one per container."""
         B, N, _ = x.shape
         L = ctx_tokens.shape[1] if ctx_tokens is not None else 0
         if out is None:
             out = torch.empty_like(x)
         cur = torch.cuda.current_stream(self.dev)
         self.compute_stream.wait_stream(cur)
-        dlo_forward(self.ctx, x.data_ptr(), cond.data_ptr(),
-                    ctx_tokens.data_ptr() if ctx_tokens is not None else None, B, N, L,
-                    out.data_ptr())
+        tok = ctx_tokens.data_ptr() if ctx_tokens is not None else None
+        if isinstance(cond, (list, tuple)):
+            dlo_forward_multi(self.ctx, x.data_ptr(), [c.data_ptr() for c in cond], tok, B, N, L,
+                              out.data_ptr())
+        else:
+            dlo_forward(self.ctx, x.data_ptr(), cond.data_ptr(), tok, B, N, L, out.data_ptr())
         cur.wait_stream(self.compute_stream)
         return out
 

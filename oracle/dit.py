@@ -198,6 +198,17 @@ def stack_forward(kind, x, cond, ctx, blocks, heads, eps=EPS):
     return x
 
 
+def multi_stack_forward(parts, x, ctx, eps=EPS):
+    """A stack of several ordered block containers ("CPU Offloading for
+    Diffusion Models", Layerwise (Blockwise) Offloading: a model may list more
+    than one attribute holding transformer blocks, offloaded as one ordered
+    sequence).  parts = [(kind, cond, blocks, heads), ...]: the containers run
+    in order on the one hidden state; ctx feeds every video container."""
+    for kind, cond, blocks, heads in parts:
+        x = stack_forward(kind, x, cond, ctx if kind == KIND_VIDEO else None, blocks, heads, eps)
+    return x
+
+
 def max_rel_l2(y, ref):
     """max over batch b of ||y_b - ref_b||_2 / ||ref_b||_2 over all other axes."""
     y = np.asarray(y, dtype=np.float64)

@@ -75,6 +75,66 @@ CFG_SWEEP = StackConfig("video-sweep-40x5120-n8192", KIND_VIDEO, 40, 5120, 40, 1
 CONFIGS = {c.name: c for c in (CFG_TINY, CFG_DITXL, CFG_VIDEO, CFG_VIDEO_FP8, CFG_SWEEP)}
 
 
+@dataclasses.dataclass(frozen=True)
+class MultiConfig:
+    """A stack of several ordered block containers (e.g. double-stream blocks
+    followed by single-stream blocks).  The parts share hidden, batch and
+    tokens; part c draws its weights with its own seed, and its block j is
+    block `first(c) + j` of the stack."""
+    name: str
+    parts: tuple
+    steps: int = 1
+
+    @property
+    def n_blocks(self) -> int:
+        return sum(p.n_blocks for p in self.parts)
+
+    @property
+    def hidden(self) -> int:
+        return self.parts[0].hidden
+
+    @property
+    def batch(self) -> int:
+        return self.parts[0].batch
+
+    @property
+    def tokens(self) -> int:
+        return self.parts[0].tokens
+
+    @property
+    def video(self) -> "StackConfig | None":
+        return next((p for p in self.parts if p.kind == KIND_VIDEO), None)
+
+    def part_of(self, block: int) -> tuple[int, int]:
+        for c, p in enumerate(self.parts):
+            if block < p.n_blocks:
+                return c, block
+            block -= p.n_blocks
+        raise IndexError("block out of range")
+
+
+# Mixed stacks: video (cross-attention) blocks, then DiT adaLN blocks.
+MULTI_TINY = MultiConfig("mixed-video2-dit3-d128", (
+    StackConfig("mixed-tiny-video", KIND_VIDEO, 2, 128, 2, 64, 256, 2, 40, text_dim=64,
+                text_tokens=9, seed=0),
+    StackConfig("mixed-tiny-dit", KIND_DIT, 3, 128, 2, 64, 512, 2, 40, cond_dim=128, seed=7)))
+MULTI_FP8_TINY = MultiConfig("mixed-video2fp8-dit2-d256", (
+    StackConfig("mixed-fp8-video", KIND_VIDEO, 2, 256, 4, 64, 512, 1, 130, text_dim=128,
+                text_tokens=17, wdtype=W_E4M3, master_fp32=True, seed=3),
+    StackConfig("mixed-fp8-dit", KIND_DIT, 2, 256, 2, 128, 768, 1, 130, cond_dim=256, seed=5)))
+MULTI_DITXL = MultiConfig("mixed-video8-dit20-d1152-b2-n1024", (
+    StackConfig("mixed-xl-video", KIND_VIDEO, 8, 1152, 16, 72, 4608, 2, 1024, text_dim=4096,
+                text_tokens=256, seed=0),
+    StackConfig("mixed-xl-dit", KIND_DIT, 20, 1152, 16, 72, 4608, 2, 1024, cond_dim=1152,
+                seed=11)), steps=10)
+MULTI_CONFIGS = {c.name: c for c in (MULTI_TINY, MULTI_FP8_TINY, MULTI_DITXL)}
+
+
+def multi_block_params(mc: MultiConfig, block: int) -> dict[str, np.ndarray]:
+    c, j = mc.part_of(block)
+    return block_params(mc.parts[c], j)
+
+
 def param_specs(cfg: StackConfig):
     """Ordered (name, shape, role) of one block's tensors.
 

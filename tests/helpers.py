@@ -52,3 +52,40 @@ def rel_l2(y, ref):
 
 def bf16(a) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).cuda()
+
+
+# ---------------------------------------------------------------- multi-container stacks
+
+def make_multi_stack(mc: synth.MultiConfig, *, staging=0, host_mode="pinned"):
+    from layerwise_weight_offload_slot_gb300.stack import OffloadStack
+    v = mc.video
+    conts = [dict(block_kind=p.kind, n_blocks=p.n_blocks, heads=p.heads, head_dim=p.head_dim,
+                  ffn=p.ffn, cond_dim=p.cond_dim, text_dim=p.text_dim,
+                  max_text_tokens=p.text_tokens, wdtype=p.wdtype) for p in mc.parts]
+    st = OffloadStack(containers=conts, hidden=mc.hidden, max_batch=mc.batch, max_tokens=mc.tokens,
+                      staging=staging, host_mode=host_mode)
+    st.pack_all(lambda i: synth.multi_block_params(mc, i))
+    return st
+
+
+def multi_inputs(mc: synth.MultiConfig, step: int = 0):
+    """x, one conditioning tensor per container, the text context (or None)."""
+    x = torch.from_numpy(synth.activations(mc.parts[0], step)).to(torch.bfloat16).cuda()
+    conds = []
+    for p in mc.parts:
+        c = synth.condition(p, step)
+        conds.append(torch.from_numpy(c).to(torch.bfloat16 if p.kind == synth.KIND_DIT
+                                            else torch.float32).cuda())
+    v = mc.video
+    ctx = torch.from_numpy(synth.text_context(v, step)).to(torch.bfloat16).cuda() if v else None
+    return x, conds, ctx
+
+
+def oracle_multi(mc: synth.MultiConfig, x_bf16, conds, ctx):
+    parts = []
+    for p, c in zip(mc.parts, conds):
+        blocks = oracle_blocks(p)
+        parts.append((p.kind, c.float().cpu().numpy().astype(np.float64), blocks, p.heads))
+    x = x_bf16.float().cpu().numpy().astype(np.float64)
+    t = ctx.float().cpu().numpy().astype(np.float64) if ctx is not None else None
+    return dit.multi_stack_forward(parts, x, t)

@@ -140,3 +140,67 @@ def test_pack_fp8_block_matches_oracle():
         assert sc[i] == s
     e = lay["ffn.fc1.bias"]
     assert e["dtype"] == dlo.DT_BF16
+
+
+def _multi_descs(mc, **kw):
+    return [dlo.make_desc(block_kind=p.kind, n_blocks=p.n_blocks, hidden=p.hidden, heads=p.heads,
+                          head_dim=p.head_dim, ffn=p.ffn, cond_dim=p.cond_dim, text_dim=p.text_dim,
+                          max_batch=p.batch, max_tokens=p.tokens, max_text_tokens=p.text_tokens,
+                          wdtype=p.wdtype, **kw) for p in mc.parts]
+
+
+@pytest.mark.parametrize("mc", list(synth.MULTI_CONFIGS.values()), ids=lambda c: c.name)
+def test_multi_container_workspace_serves_every_container(mc):
+    ds = _multi_descs(mc)
+    ws = dlo.dlo_workspace_bytes_multi(ds)
+    assert ws > 0 and ws % 256 == 0
+    for d in ds:
+        assert ws >= dlo.dlo_workspace_bytes(d)
+    # one container through the multi entry point is the plain workspace
+    assert dlo.dlo_workspace_bytes_multi(ds[:1]) == dlo.dlo_workspace_bytes(ds[0])
+
+
+def test_multi_container_stacks_are_validated():
+    mc = synth.MULTI_TINY
+    ds = _multi_descs(mc)
+    assert dlo.dlo_workspace_bytes_multi(ds) > 0
+    assert dlo.dlo_workspace_bytes_multi([]) == 0
+    def bad(i, **kw):
+        out = list(ds)
+        f = {name: getattr(out[i], name) for name, _ in dlo.dlo_desc._fields_}
+        f.update(kw)
+        out[i] = dlo.dlo_desc(**f)
+        return out
+    # shared fields must agree
+    for kw in (dict(hidden=256, heads=4), dict(max_batch=3), dict(max_tokens=41), dict(eps=1e-5),
+               dict(staging=dlo.STAGE_GATHER), dict(register_budget_bytes=1 << 20)):
+        assert dlo.dlo_workspace_bytes_multi(bad(1, **kw)) == 0, kw
+    # an invalid container invalidates the stack
+    assert dlo.dlo_workspace_bytes_multi(bad(1, ffn=100)) == 0
+    # video containers share the text fields
+    v2 = bad(1, block_kind=dlo.BLOCK_VIDEO, text_dim=128, max_text_tokens=9)
+    assert dlo.dlo_workspace_bytes_multi(v2) == 0
+    v3 = bad(1, block_kind=dlo.BLOCK_VIDEO, text_dim=64, max_text_tokens=9)
+    assert dlo.dlo_workspace_bytes_multi(v3) > 0
+    # bytes blocks stand alone
+    b = dlo.make_desc(block_kind=dlo.BLOCK_BYTES, n_blocks=2, hidden=0, heads=0, head_dim=0, ffn=0,
+                      bytes_block=4096)
+    assert dlo.dlo_workspace_bytes_multi([b]) > 0
+    assert dlo.dlo_workspace_bytes_multi([b, b]) == 0
+
+
+def test_multi_container_create_rejects_small_slots_before_touching_the_device():
+    mc = synth.MULTI_TINY
+    ds = _multi_descs(mc)
+    sizes = [dlo.dlo_block_bytes(d) for d in ds]
+    assert sizes[0] != sizes[1]
+    ws = dlo.dlo_workspace_bytes_multi(ds)
+    fake = 1 << 40
+    with pytest.raises(dlo.DloError) as e:
+        dlo.dlo_create_multi(ds, 0, fake, fake + (1 << 30), min(sizes), fake + (2 << 30), ws,
+                             fake + 8, fake + 16)
+    assert e.value.status == dlo.ENOMEM and "largest" in str(e.value)
+    with pytest.raises(dlo.DloError) as e:
+        dlo.dlo_create_multi(ds + [ds[0]] * 64, 0, fake, fake + (1 << 30), max(sizes),
+                             fake + (2 << 30), ws, fake + 8, fake + 16)
+    assert e.value.status == dlo.EINVAL

@@ -219,3 +219,56 @@ def test_max_rel_l2():
     y[1] *= 1.1
     assert abs(dit.max_rel_l2(y, ref) - 0.1) < 1e-12
     assert dit.max_rel_l2(ref, ref) == 0.0
+
+
+def _multi_parts(mc, step=0):
+    parts = []
+    for p in mc.parts:
+        blocks = [dit.prepare_block(synth.block_params(p, j), fp8_linears=p.wdtype == synth.W_E4M3)
+                  for j in range(p.n_blocks)]
+        parts.append((p.kind, synth.condition(p, step).astype(np.float64), blocks, p.heads))
+    x = synth.activations(mc.parts[0], step).astype(np.float64)
+    v = mc.video
+    ctx = synth.text_context(v, step).astype(np.float64) if v else None
+    return parts, x, ctx
+
+
+def test_multi_stack_split_of_one_container_is_the_same_stack():
+    # one DiT container of 3 blocks == containers of 1 + 2 of the same blocks
+    mc = synth.MULTI_TINY
+    parts, x, ctx = _multi_parts(mc)
+    kind, c, blocks, heads = parts[1]
+    whole = dit.stack_forward(kind, x, c, None, blocks, heads)
+    split = dit.multi_stack_forward([(kind, c, blocks[:1], heads), (kind, c, blocks[1:], heads)], x, ctx)
+    np.testing.assert_array_equal(split, whole)
+
+
+def test_multi_stack_identity_container_and_order():
+    # a trailing DiT container whose gates are all zero leaves the video
+    # container's output unchanged; swapping the order of two non-identity
+    # containers changes the result (they do not commute)
+    mc = synth.MULTI_TINY
+    parts, x, ctx = _multi_parts(mc)
+    kv, e, bv, hv = parts[0]
+    kd, c, bd, hd = parts[1]
+    D = mc.hidden
+    ident = []
+    for P in bd:
+        Q = dict(P)
+        Q["adaLN.weight"] = P["adaLN.weight"].copy()
+        Q["adaLN.bias"] = P["adaLN.bias"].copy()
+        for chunk in (2, 5):
+            Q["adaLN.weight"][chunk * D:(chunk + 1) * D] = 0
+            Q["adaLN.bias"][chunk * D:(chunk + 1) * D] = 0
+        ident.append(Q)
+    video_only = dit.stack_forward(kv, x, e, ctx, bv, hv)
+    np.testing.assert_array_equal(dit.multi_stack_forward([parts[0], (kd, c, ident, hd)], x, ctx),
+                                  video_only)
+    fwd = dit.multi_stack_forward(parts, x, ctx)
+    rev = dit.multi_stack_forward([parts[1], parts[0]], x, ctx)
+    assert dit.max_rel_l2(rev, fwd) > 1e-7
+    # each container sees its own conditioning: feeding the DiT container a
+    # different c changes only what follows it
+    c2 = c + 0.5
+    other = dit.multi_stack_forward([parts[0], (kd, c2, bd, hd)], x, ctx)
+    assert dit.max_rel_l2(other, fwd) > 1e-7
