@@ -40,7 +40,8 @@ def parse():
     p.add_argument("--steps", type=int, default=30)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default=synth.CFG_DITXL.name, choices=list(synth.CONFIGS))
+    p.add_argument("--workload", default=synth.CFG_DITXL.name,
+                   choices=list(synth.CONFIGS) + list(synth.MULTI_CONFIGS))
     p.add_argument("--staging", default="memcpy", choices=["memcpy", "gather"])
     p.add_argument("--resident", type=int, default=0)
     p.add_argument("--host", default="pinned", choices=["pinned", "register"])
@@ -120,6 +121,25 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- oracle timing
 
+def parts_of(cfg):
+    """The block containers of a workload (one for a plain stack)."""
+    return list(cfg.parts) if isinstance(cfg, synth.MultiConfig) else [cfg]
+
+
+def oracle_step_seconds(cfg, budget_s: float):
+    """CPU oracle seconds of one whole step, extrapolated from a timed sample
+    of each container's blocks (their share of the budget by block count),
+    and a description of the sample."""
+    total, desc = 0.0, []
+    for p in parts_of(cfg):
+        times = oracle_block_seconds(p, budget_s * p.n_blocks / cfg.n_blocks)
+        per = statistics.mean(times)
+        total += per * p.n_blocks
+        desc.append(f"{len(times)} of {p.n_blocks} {'video' if p.kind else 'DiT'} blocks, "
+                    f"{per:.2f} s per block")
+    return total, desc
+
+
 def oracle_block_seconds(cfg, budget_s: float, max_blocks: int | None = None):
     """Time the CPU oracle (float64 numpy, as it stands) on blocks of the workload."""
     from oracle import dit
@@ -153,14 +173,16 @@ def run_reference(args, cfg, rank: int, world: int):
         return
     # each reference "step": one block of the stack's step on the host cores,
     # the steps/s figure extrapolated to the whole stack (n_blocks blocks)
+    parts = parts_of(cfg)
     if args.warmup:
-        oracle_block_seconds(cfg, 0.0, max_blocks=1)
-    times = []
+        oracle_block_seconds(parts[0], 0.0, max_blocks=1)
+    step_s = []
     for s in range(args.steps):
-        times += oracle_block_seconds(cfg, 0.0, max_blocks=1)
-    per_block = statistics.mean(times)
-    value = 1.0 / (per_block * cfg.n_blocks)
-    sample = f"1 of {cfg.n_blocks} blocks per step, float64 numpy oracle, extrapolated x{cfg.n_blocks}"
+        # one block of every container per step, weighted by its block count
+        step_s.append(sum(oracle_block_seconds(p, 0.0, max_blocks=1)[0] * p.n_blocks for p in parts))
+    value = 1.0 / statistics.mean(step_s)
+    sample = (f"1 block of each of the {len(parts)} container(s) per step, float64 numpy oracle, "
+              f"extrapolated to the {cfg.n_blocks}-block step")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / value,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -210,15 +232,20 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
             dist.barrier()
 
     staging = dlo.STAGE_MEMCPY if args.staging == "memcpy" else dlo.STAGE_GATHER
-    st = OffloadStack(block_kind=cfg.kind, n_blocks=cfg.n_blocks, hidden=cfg.hidden,
-                      heads=cfg.heads, head_dim=cfg.head_dim, ffn=cfg.ffn, cond_dim=cfg.cond_dim,
-                      text_dim=cfg.text_dim, max_batch=cfg.batch, max_tokens=cfg.tokens,
-                      max_text_tokens=cfg.text_tokens, wdtype=cfg.wdtype, staging=staging,
-                      host_mode=args.host, device=local_rank)
-    st.pack_all(lambda i: synth.block_params(cfg, i))
+    parts = parts_of(cfg)
+    multi = len(parts) > 1
+    video = next((p for p in parts if p.kind == synth.KIND_VIDEO), None)
+    conts = [dict(block_kind=p.kind, n_blocks=p.n_blocks, heads=p.heads, head_dim=p.head_dim,
+                  ffn=p.ffn, cond_dim=p.cond_dim, text_dim=p.text_dim,
+                  max_text_tokens=p.text_tokens, wdtype=p.wdtype) for p in parts]
+    st = OffloadStack(containers=conts, hidden=cfg.hidden, max_batch=cfg.batch,
+                      max_tokens=cfg.tokens, staging=staging, host_mode=args.host,
+                      device=local_rank)
+    st.pack_all((lambda i: synth.multi_block_params(cfg, i)) if multi
+                else (lambda i: synth.block_params(cfg, i)))
     st.attach()
     st.set_resident(args.resident)
-    streamed_bytes = (cfg.n_blocks - args.resident) * st.block_bytes
+    streamed_bytes = sum(st.block_sizes[args.resident:])
 
     # link peak: best pinned 1 GiB host->device copy (copy engine), this run
     hbuf = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
@@ -234,14 +261,14 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
     del hbuf, dbuf
 
     steps_total = args.warmup + args.steps
-    x0 = torch.from_numpy(synth.activations(cfg)).to(torch.bfloat16).to(dev)
+    x0 = torch.from_numpy(synth.activations(parts[0])).to(torch.bfloat16).to(dev)
     conds, ctxs = [], []
     for s in range(max(steps_total, 1)):
-        c = synth.condition(cfg, s % max(cfg.steps, 1))
-        conds.append(torch.from_numpy(c).to(torch.bfloat16 if cfg.kind == synth.KIND_DIT
-                                            else torch.float32).to(dev))
-        ctxs.append(torch.from_numpy(synth.text_context(cfg)).to(torch.bfloat16).to(dev)
-                    if cfg.kind == synth.KIND_VIDEO else None)
+        cs_ = [torch.from_numpy(synth.condition(p, s % max(cfg.steps, 1))).to(
+            torch.bfloat16 if p.kind == synth.KIND_DIT else torch.float32).to(dev) for p in parts]
+        conds.append(cs_ if multi else cs_[0])
+        ctxs.append(torch.from_numpy(synth.text_context(video)).to(torch.bfloat16).to(dev)
+                    if video is not None else None)
     xa = x0.clone()
     xb = torch.empty_like(x0)
     cs = st.compute_stream
@@ -292,7 +319,7 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
                "copy_ms_per_step": copy_ms / args.steps,
                "exposed_wait_ms_per_step": exposed / args.steps,
                "compute_ms_per_step": (s1["compute_ms"] - s0["compute_ms"]) / args.steps,
-               "h2d_gbs": (st.block_bytes * n_exec) / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else None,
+               "h2d_gbs": (streamed_bytes * args.steps) / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else None,
                "timed_execs": n_exec}
 
     # ---------------- per-kernel-class pass (event pair around every launch)
@@ -342,18 +369,36 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
                    "ms_per_step": v["ms"] / args.steps} for n, v in cls.items()}
 
     # ---------------- end to end through the public host-buffer call
+    # (a multi-container stack: pinned host copies in, dlo_forward_multi, the
+    # result copied back and waited for, all in the timed loop)
     B, N, D = cfg.batch, cfg.tokens, cfg.hidden
     hx = torch.empty((B, N, D), dtype=torch.bfloat16).pin_memory()
     hx.copy_(x0.cpu())
     hout = torch.empty_like(hx).pin_memory()
-    hconds = [c.cpu().pin_memory() for c in conds]
+    as_list = (lambda c: c) if multi else (lambda c: [c])
+    hconds = [[c.cpu().pin_memory() for c in as_list(cc)] for cc in conds]
     hctxs = [c.cpu().pin_memory() if c is not None else None for c in ctxs]
     xin = hx.view(torch.int16).numpy()
     xout = hout.view(torch.int16).numpy()
+    dx = torch.empty_like(x0)
+    dconds = [torch.empty_like(c, device=dev) for c in hconds[0]]
+    dctx = torch.empty_like(hctxs[0], device=dev) if hctxs[0] is not None else None
 
     def host_step(i):
-        nonlocal xin, xout
-        c = hconds[i]
+        nonlocal xin, xout, hx, hout
+        if multi:
+            dx.copy_(hx, non_blocking=True)
+            for d_, h_ in zip(dconds, hconds[i]):
+                d_.copy_(h_, non_blocking=True)
+            if dctx is not None:
+                dctx.copy_(hctxs[i], non_blocking=True)
+            st.forward(dx, dconds, dctx, out=dx)
+            hout.copy_(dx, non_blocking=True)
+            torch.cuda.current_stream(dev).synchronize()
+            st.wait()
+            hx, hout = hout, hx
+            return
+        c = hconds[i][0]
         cn = c.view(torch.int16).numpy() if c.dtype == torch.bfloat16 else c.numpy()
         t = hctxs[i].view(torch.int16).numpy() if hctxs[i] is not None else None
         st.forward_host(xin, cn, t, xout)
@@ -369,7 +414,7 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
     ms, value, e2e_s, e2e_value = aggregate(ms_local, e2e_s, args.steps, world, dist, dev)
     ms_per_step = ms / args.steps
     step_roof["frac"] = step_roof["t_roof_ms"] / ms_per_step
-    h2d = B * N * D * 2 + hconds[0].numel() * hconds[0].element_size() + \
+    h2d = B * N * D * 2 + sum(c.numel() * c.element_size() for c in hconds[0]) + \
         (hctxs[0].numel() * 2 if hctxs[0] is not None else 0)
     e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": B * N * D * 2}
@@ -379,12 +424,10 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        times = oracle_block_seconds(cfg, 15.0)
-        per_block = statistics.mean(times)
-        cpu = {"value": 1.0 / (per_block * cfg.n_blocks), "unit": UNIT, "cores": cores(),
-               "kind": "oracle",
-               "sample": f"{len(times)} of {cfg.n_blocks} blocks of one step (float64 numpy), "
-                         f"{per_block:.2f} s per block, extrapolated to the {cfg.n_blocks}-block step"}
+        step_s, desc = oracle_step_seconds(cfg, 15.0)
+        cpu = {"value": 1.0 / step_s, "unit": UNIT, "cores": cores(), "kind": "oracle",
+               "sample": "float64 numpy oracle on " + "; ".join(desc) +
+                         f"; extrapolated to the {cfg.n_blocks}-block step"}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -392,8 +435,12 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations)",
                 "config": {"workload": cfg.name, "blocks": cfg.n_blocks, "hidden": cfg.hidden,
-                           "heads": cfg.heads, "ffn": cfg.ffn, "batch": cfg.batch,
-                           "tokens": cfg.tokens, "resident": args.resident,
+                           "containers": [{"kind": "video" if p.kind else "dit",
+                                           "blocks": p.n_blocks, "heads": p.heads,
+                                           "ffn": p.ffn, "block_bytes": b,
+                                           "weights": "e4m3" if p.wdtype else "bf16"}
+                                          for p, b in zip(parts, st.container_bytes)],
+                           "batch": cfg.batch, "tokens": cfg.tokens, "resident": args.resident,
                            "staging": args.staging, "host": args.host,
                            "parallelism": "replicas" if world > 1 else "single",
                            "l2": f"inputs larger than L2: {streamed_bytes / 1e9:.2f} GB of weights "
@@ -608,7 +655,7 @@ def main():
     if "WORLD_SIZE" not in os.environ:
         world = 1
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    cfg = synth.CONFIGS[args.workload]
+    cfg = synth.CONFIGS.get(args.workload) or synth.MULTI_CONFIGS[args.workload]
     if args.impl == "reference":
         run_reference(args, cfg, rank, world)
         return
