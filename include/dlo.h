@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define DLO_ABI_VERSION 1
+#define DLO_ABI_VERSION 2
 #define DLO_MAX_CONTAINERS 64   /* block containers of one stack (dlo_create_multi) */
 
 typedef int dlo_status;
@@ -67,6 +67,11 @@ typedef int dlo_status;
 /* weight storage of the linears in a block */
 #define DLO_W_BF16       0
 #define DLO_W_E4M3       1   /* e4m3 weight + one fp32 scale per linear tensor   */
+/* W8A8: the DLO_W_E4M3 weights (same layout and bytes), and every linear's
+ * input activation quantised to E4M3 on the fly with one dynamic per-tensor
+ * scale (dlo_op_quantize_act); the product runs on the 8-bit tensor cores:
+ * y = s_x * s_w * (q_x q_w^T) + b, fp32 accumulation. */
+#define DLO_W_E4M3_A8    2
 
 /* slot staging engine */
 #define DLO_STAGE_MEMCPY 0   /* cudaMemcpyAsync on the copy stream (copy engine) */
@@ -82,6 +87,9 @@ typedef int dlo_status;
 #define DLO_HOST_REGISTER 2u /* library page-locks it (all-or-nothing)           */
 #define DLO_HOST_PAGEABLE 4u /* pageable; packed through two pinned host slots    */
 
+/* number of kernel classes counted in dlo_stats (DLO_K_* below) */
+#define DLO_K_COUNT 16
+
 /* tensor dtypes in the flat block layout */
 #define DLO_DT_BF16 0
 #define DLO_DT_E4M3 1
@@ -92,8 +100,8 @@ typedef int dlo_status;
  * DLO_ABI_VERSION; n_blocks >= 1; hidden == heads * head_dim; hidden % 16 == 0;
  * head_dim % 8 == 0 and head_dim <= 128; ffn % 16 == 0; max_batch >= 1;
  * max_tokens >= 1; DiT: cond_dim % 8 == 0; video: text_dim % 16 == 0 and
- * max_text_tokens >= 1; eps > 0.  DLO_W_E4M3 requires DLO_BLOCK_VIDEO
- * (else DLO_EUNSUPPORTED).
+ * max_text_tokens >= 1; eps > 0.  DLO_W_E4M3 and DLO_W_E4M3_A8 require
+ * DLO_BLOCK_VIDEO (else DLO_EUNSUPPORTED).
  * DLO_BLOCK_BYTES streams opaque blocks of bytes_block bytes (a multiple of
  * 256) through the same slots and schedule; only n_blocks, staging,
  * register_budget_bytes and bytes_block are read.  Its "compute" reads the
@@ -343,10 +351,10 @@ typedef struct dlo_stats {
      * of each launch on its own stream, launches, and the algorithmic work of
      * those launches: 2*M*N*K per GEMM, 4*B*H*nq*nk*hd per attention, bytes
      * read + written once per element for the bandwidth-bound kernels. */
-    double kclass_ms[8];
-    double kclass_flops[8];
-    double kclass_bytes[8];
-    unsigned long long kclass_launches[8];
+    double kclass_ms[DLO_K_COUNT];
+    double kclass_flops[DLO_K_COUNT];
+    double kclass_bytes[DLO_K_COUNT];
+    unsigned long long kclass_launches[DLO_K_COUNT];
     unsigned long long h2d_copies;       /* host-to-device copy calls issued     */
 } dlo_stats;
 
@@ -360,6 +368,8 @@ typedef struct dlo_stats {
 #define DLO_K_CONVERT    6   /* bf16 <-> fp32 of the hidden state; bytes-block
                                 checksum                                       */
 #define DLO_K_GATHER     7   /* zero-copy slot staging kernel                  */
+#define DLO_K_GEMM_FP8   8   /* W8A8 GEMM (kind::f8f6f4, both operands E4M3)   */
+#define DLO_K_QUANT      9   /* dynamic per-tensor E4M3 activation quantiser  */
 
 /* Counters and timing.  Timing sums need the timed work finished (call
  * dlo_wait first); they are read from CUDA events. */
@@ -410,6 +420,29 @@ dlo_status dlo_op_gemm(const void* A, const void* W, int w_dtype, const float* s
                        int scale_seg, const void* bias, int M, int N, int K, int epilogue,
                        void* out, int ldo, const float* gate, int gate_ld, int rows_per_batch,
                        int* err, void* stream);
+
+/* Dynamic per-tensor E4M3 quantisation of an activation (DLO_W_E4M3_A8):
+ * x bf16 [rows, cols] with row stride ld (elements); q receives E4M3 codes
+ * [rows, cols], contiguous; *scale (device fp32) receives s = amax|x| / 448
+ * (1 when amax = 0) -- the weights' scale rule (dlo_quantize_e4m3) -- and
+ * q = E4M3(x * r) with r = 1 / s rounded to fp32 and the product rounded to
+ * fp32, then round to nearest even, saturating at +-448 (the inverted-scale
+ * form of dynamic FP8 activation quantisers: one multiply per element).  scratch: device
+ * buffer of DLO_QUANT_SCRATCH floats (partial maxima; no allocation here).
+ * cols % 8 == 0, ld % 8 == 0, x and q 16-B aligned.  Two kernel launches. */
+#define DLO_QUANT_SCRATCH 1024
+dlo_status dlo_op_quantize_act(const void* x, int rows, int cols, int ld, void* q, float* scale,
+                               float* scratch, void* stream);
+
+/* Y = s_x s_w (A W^T) + bias with A E4M3 codes [M, K] (lda = K) and its scale
+ * *a_scale (device fp32, e.g. from dlo_op_quantize_act), W E4M3 codes [N, K]
+ * with per-tensor scales as dlo_op_gemm (scales required); kind::f8f6f4 on
+ * the tensor cores, fp32 accumulation, then the epilogues of dlo_op_gemm.
+ * M >= 1, N % 16 == 0, K % 16 == 0; pointers 16-B aligned, ldo % 8 == 0. */
+dlo_status dlo_op_gemm_w8a8(const void* A, const float* a_scale, const void* W, const float* scales,
+                            int scale_seg, const void* bias, int M, int N, int K, int epilogue,
+                            void* out, int ldo, const float* gate, int gate_ld, int rows_per_batch,
+                            int* err, void* stream);
 
 /* dlo_op_gemm for callers that cannot allocate device memory (for example code
  * running where the CUDA allocator is unavailable or forbidden, such as inside

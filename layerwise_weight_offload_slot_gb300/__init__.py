@@ -21,11 +21,13 @@ if not os.path.exists(LIB_PATH):
 
 _lib = ctypes.CDLL(LIB_PATH)
 
-ABI_VERSION = 1
+ABI_VERSION = 2
+K_COUNT = 16
+QUANT_SCRATCH = 1024
 OK, EINVAL, ESTATE, ENOMEM, ECUDA, EREGISTER, ETIMEDOUT, EUNSUPPORTED, EMISMATCH = \
     0, -1, -2, -3, -4, -5, -6, -7, -8
 BLOCK_DIT, BLOCK_VIDEO, BLOCK_BYTES = 0, 1, 2
-W_BF16, W_E4M3 = 0, 1
+W_BF16, W_E4M3, W_E4M3_A8 = 0, 1, 2
 STAGE_MEMCPY, STAGE_GATHER, STAGE_PER_TENSOR = 0, 1, 2
 HOST_PINNED, HOST_REGISTER, HOST_PAGEABLE = 1, 2, 4
 DT_BF16, DT_E4M3, DT_F32, DT_U8 = 0, 1, 2, 3
@@ -66,8 +68,9 @@ class dlo_stats(ctypes.Structure):
                 ("registered_read_only", ctypes.c_int), ("device_error", ctypes.c_int),
                 ("timed_execs", ctypes.c_int), ("copy_ms", ctypes.c_double),
                 ("compute_ms", ctypes.c_double), ("exposed_wait_ms", ctypes.c_double),
-                ("kclass_ms", ctypes.c_double * 8), ("kclass_flops", ctypes.c_double * 8),
-                ("kclass_bytes", ctypes.c_double * 8), ("kclass_launches", ctypes.c_ulonglong * 8),
+                ("kclass_ms", ctypes.c_double * K_COUNT), ("kclass_flops", ctypes.c_double * K_COUNT),
+                ("kclass_bytes", ctypes.c_double * K_COUNT),
+                ("kclass_launches", ctypes.c_ulonglong * K_COUNT),
                 ("h2d_copies", ctypes.c_ulonglong)]
 
     def as_dict(self) -> dict:
@@ -79,7 +82,7 @@ class dlo_stats(ctypes.Structure):
 
 
 KCLASS_NAMES = ("gemm_bf16", "gemm_e4m3", "attention", "layernorm", "rmsnorm", "modulation",
-                "convert", "gather")
+                "convert", "gather", "gemm_fp8", "quant")
 
 
 _vp, _sz, _int, _uint, _f32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint, ctypes.c_float
@@ -121,6 +124,9 @@ _c = {
                          _vp, _int, _vp, _int, _int, _vp, _vp),
     "dlo_op_gemm_noalloc": _decl("dlo_op_gemm_noalloc", _int, _vp, _vp, _int, _vp, _int, _vp, _int, _int,
                                  _int, _int, _vp, _int, _vp, _int, _int, _vp),
+    "dlo_op_quantize_act": _decl("dlo_op_quantize_act", _int, _vp, _int, _int, _int, _vp, _vp, _vp, _vp),
+    "dlo_op_gemm_w8a8": _decl("dlo_op_gemm_w8a8", _int, _vp, _vp, _vp, _vp, _int, _vp, _int, _int, _int,
+                              _int, _vp, _int, _vp, _int, _int, _vp, _vp),
     "dlo_op_attention": _decl("dlo_op_attention", _int, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int,
                               _int, _int, _int, _int, _vp),
     "dlo_op_layernorm": _decl("dlo_op_layernorm", _int, _vp, _int, _int, _int, _vp, _vp, _int, _vp, _vp,
@@ -316,6 +322,16 @@ def dlo_op_gemm_noalloc(A, W, w_dtype, scales, scale_seg, bias, M, N, K, epilogu
                                    ldo, gate, gate_ld, rows_per_batch, stream)
     if st != OK:
         raise DloError(st, "dlo_op_gemm_noalloc rejected the call (see stderr)")
+
+
+def dlo_op_quantize_act(x, rows, cols, ld, q, scale, scratch, stream) -> None:
+    _check(_c["dlo_op_quantize_act"](x, rows, cols, ld, q, scale, scratch, stream))
+
+
+def dlo_op_gemm_w8a8(A, a_scale, W, scales, scale_seg, bias, M, N, K, epilogue, out, ldo, gate,
+                     gate_ld, rows_per_batch, err, stream) -> None:
+    _check(_c["dlo_op_gemm_w8a8"](A, a_scale, W, scales, scale_seg, bias, M, N, K, epilogue, out, ldo,
+                                  gate, gate_ld, rows_per_batch, err, stream))
 
 
 def dlo_op_attention(Q, K, V, O, batch, heads, head_dim, nq, nk, ldq, ldk, ldv, ldo, stream) -> None:

@@ -389,12 +389,27 @@ dlo_status run_block(dlo_ctx* c, const uint8_t* W, int B, int N, int L, const vo
     unsigned long long* nl = &c->st.kernel_launches;
     cudaStream_t s = c->cs;
     const int D6 = 6 * D;
-    const bool e4m3 = d.wdtype == DLO_W_E4M3;
+    const bool e4m3 = e4m3_weights(d.wdtype);
+    const bool w8a8 = d.wdtype == DLO_W_E4M3_A8;
     const int wsize = e4m3 ? 1 : 2;
     auto gemm = [&](const void* A, size_t woff, size_t boff, int M, int Nn, int K, int epi,
                     void* out, int ldo, const float* gate, int rpb, int scale_idx, int seg) {
         GemmParams p;
         p.A = A;
+        if (w8a8) {
+            // quantise this linear's input (dynamic per-tensor scale), then
+            // multiply E4M3 by E4M3
+            uint8_t* qa = w + c->ws.qa;
+            float* part = reinterpret_cast<float*>(w + c->ws.qs);
+            float* sx = part + kQuantScratch;
+            cudaError_t e = c->timed(DLO_K_QUANT, 0.0, 5.0 * M * K, s, [&] {
+                return launch_quantize_e4m3(A, M, K, K, qa, sx, part, s, nl);
+            });
+            if (e != cudaSuccess) return e;
+            p.A = qa;
+            p.a_dtype = DLO_DT_E4M3;
+            p.a_scale = sx;
+        }
         p.W = W + woff;
         p.w_dtype = e4m3 ? DLO_DT_E4M3 : DLO_DT_BF16;
         p.scales = o.has_scales ? reinterpret_cast<const float*>(W + o.scales) + scale_idx : nullptr;
@@ -411,10 +426,10 @@ dlo_status run_block(dlo_ctx* c, const uint8_t* W, int B, int N, int L, const vo
         p.rows_per_batch = rpb;
         p.err = c->err_word();
         const double flops = 2.0 * M * Nn * K;
-        const double bytes = 1.0 * M * K * 2 + 1.0 * Nn * K * wsize +
+        const double bytes = 1.0 * M * K * (w8a8 ? 1 : 2) + 1.0 * Nn * K * wsize +
                              1.0 * M * Nn * (epi == DLO_EPI_RESIDUAL ? 8 : 2);
-        return c->timed(e4m3 ? DLO_K_GEMM_E4M3 : DLO_K_GEMM_BF16, flops, bytes, s,
-                        [&] { return launch_gemm(p, s, nl); });
+        return c->timed(w8a8 ? DLO_K_GEMM_FP8 : e4m3 ? DLO_K_GEMM_E4M3 : DLO_K_GEMM_BF16, flops,
+                        bytes, s, [&] { return launch_gemm(p, s, nl); });
     };
     auto attn = [&](const void* q, const void* k, const void* v, void* out, int nq, int nk, int ldq, int ldk,
                     int ldv) {
@@ -1067,10 +1082,44 @@ dlo_status op_inval(const char* m) {
 }
 }  // namespace
 
+namespace {
+dlo_status gemm_op(const void* A, const void* W, int w_dtype, const float* scales, int scale_seg,
+                   const void* bias, int M, int N, int K, int epilogue, void* out, int ldo, const float* gate,
+                   int gate_ld, int rows_per_batch, int* err, void* stream, int a_dtype, const float* a_scale);
+}  // namespace
+
+extern "C" dlo_status dlo_op_quantize_act(const void* x, int rows, int cols, int ld, void* q, float* scale,
+                                          float* scratch, void* stream) {
+    if (!x || !q || !scale || !scratch) return op_inval("NULL argument");
+    if (rows < 1 || cols < 8 || cols % 8 || ld < cols || ld % 8) return op_inval("need cols % 8 == 0, ld >= cols, ld % 8 == 0");
+    if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 4) || !aligned(scratch, 4))
+        return op_inval("x and q must be 16-byte aligned");
+    return op_result(launch_quantize_e4m3(x, rows, cols, ld, q, scale, scratch, static_cast<cudaStream_t>(stream),
+                                          &g_op_launches));
+}
+
+extern "C" dlo_status dlo_op_gemm_w8a8(const void* A, const float* a_scale, const void* W, const float* scales,
+                                       int scale_seg, const void* bias, int M, int N, int K, int epilogue,
+                                       void* out, int ldo, const float* gate, int gate_ld, int rows_per_batch,
+                                       int* err, void* stream) {
+    if (!a_scale || !scales) return op_inval("W8A8 needs the activation scale and the weight scales");
+    if (!aligned(a_scale, 4)) return op_inval("a_scale misaligned");
+    return gemm_op(A, W, DLO_DT_E4M3, scales, scale_seg, bias, M, N, K, epilogue, out, ldo, gate, gate_ld,
+                   rows_per_batch, err, stream, DLO_DT_E4M3, a_scale);
+}
+
 extern "C" dlo_status dlo_op_gemm(const void* A, const void* W, int w_dtype, const float* scales,
                                   int scale_seg, const void* bias, int M, int N, int K, int epilogue,
                                   void* out, int ldo, const float* gate, int gate_ld,
                                   int rows_per_batch, int* err, void* stream) {
+    return gemm_op(A, W, w_dtype, scales, scale_seg, bias, M, N, K, epilogue, out, ldo, gate, gate_ld,
+                   rows_per_batch, err, stream, DLO_DT_BF16, nullptr);
+}
+
+namespace {
+dlo_status gemm_op(const void* A, const void* W, int w_dtype, const float* scales, int scale_seg,
+                   const void* bias, int M, int N, int K, int epilogue, void* out, int ldo, const float* gate,
+                   int gate_ld, int rows_per_batch, int* err, void* stream, int a_dtype, const float* a_scale) {
     if (!A || !W || !out) return op_inval("NULL operand");
     if (M < 1 || N < 16 || N % 16 || K < 16 || K % 16) return op_inval("need M >= 1, N % 16 == 0, K % 16 == 0");
     if (!aligned(A, 16) || !aligned(W, 16) || !aligned(out, 16) || ldo % 8 || ldo < N)
@@ -1097,8 +1146,11 @@ extern "C" dlo_status dlo_op_gemm(const void* A, const void* W, int w_dtype, con
     p.gate_ld = gate_ld;
     p.rows_per_batch = rows_per_batch > 0 ? rows_per_batch : 1;
     p.err = err;
+    p.a_dtype = a_dtype;
+    p.a_scale = a_scale;
     return op_result(launch_gemm(p, static_cast<cudaStream_t>(stream), &g_op_launches));
 }
+}  // namespace
 
 extern "C" dlo_status dlo_op_attention(const void* Q, const void* K, const void* V, void* O, int batch,
                                        int heads, int head_dim, int nq, int nk, int ldq, int ldk, int ldv,

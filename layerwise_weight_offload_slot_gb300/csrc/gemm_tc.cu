@@ -54,6 +54,7 @@ struct EpiArgs {
     const __nv_bfloat16* bias;
     const float* scales;
     int scale_seg;
+    const float* act_scale;   // W8A8: per-tensor activation scale (device), else NULL
     const float* gate;
     int gate_ld;
     int rows_per_batch;
@@ -90,10 +91,11 @@ __device__ __forceinline__ uint32_t sw128(int r, int j) {
 template <int CW>
 __device__ __forceinline__ void scale_bias(const EpiArgs& a, int col0, float (&v)[CW]) {
     if (a.scales) {
+        const float sa = a.act_scale ? *a.act_scale : 1.0f;
 #pragma unroll
         for (int g = 0; g < CW / 16; ++g) {
             const int c = col0 + 16 * g;
-            const float s = c < a.N ? a.scales[c / a.scale_seg] : 0.f;
+            const float s = c < a.N ? a.scales[c / a.scale_seg] * sa : 0.f;
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[16 * g + i] *= s;
         }
@@ -160,12 +162,16 @@ struct SmemPlan {
 };
 
 // MT > 1: a CTA tile is MT x 128 rows; every weight tile (and, for E4M3,
-// its widening) serves MT row blocks.
-template <int BN, int STAGES, bool FP8, int MT>
+// its widening) serves MT row blocks.  A8: A and W are both E4M3 codes
+// (W8A8), multiplied by kind::f8f6f4 at 128 K per stage (the same 128-byte
+// swizzled rows as bf16 at 64 K); no widening.
+template <int BN, int STAGES, bool FP8, int MT, bool A8>
 __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO, const EpiArgs args) {
+    static_assert(!(A8 && FP8), "W8A8 loads 8-bit codes for both operands, nothing to widen");
     using P = SmemPlan<BN, STAGES, FP8, MT>;
+    constexpr int KS = A8 ? 128 : BK;   // K elements per stage (128 bytes of a row either way)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -207,7 +213,7 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int kblocks = (args.K + BK - 1) / BK;
+    const int kblocks = (args.K + KS - 1) / KS;
 
     auto fail = [&]() {
         *abort_flag = 1;
@@ -233,12 +239,12 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
                 mbar_arrive_expect_tx(fb, P::TX);
 #pragma unroll
                 for (int i = 0; i < MT; ++i)
-                    tma_load_2d(sbase + P::A_OFF + s * P::A_STAGE + i * A_TILE, &tmA, kb * BK,
+                    tma_load_2d(sbase + P::A_OFF + s * P::A_STAGE + i * A_TILE, &tmA, kb * KS,
                                 (mb * MT + i) * BM, fb);
                 if constexpr (FP8)
-                    tma_load_2d(sbase + P::RAW_OFF + s * P::RAW_TILE, &tmB, kb * BK, nb * BN, fb);
+                    tma_load_2d(sbase + P::RAW_OFF + s * P::RAW_TILE, &tmB, kb * KS, nb * BN, fb);
                 else
-                    tma_load_2d(sbase + P::B_OFF + s * P::B_TILE, &tmB, kb * BK, nb * BN, fb);
+                    tma_load_2d(sbase + P::B_OFF + s * P::B_TILE, &tmB, kb * KS, nb * BN, fb);
                 issued |= 1u << s;
                 last_par = (last_par & ~(1u << s)) | (ph << s);
                 if (++s == STAGES) {
@@ -255,7 +261,7 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer
-        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+        constexpr uint32_t idesc = A8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN);
         const uint32_t bar_ready = FP8 ? bar_conv : bar_full;
         int s = 0;
         uint32_t ph = 0;
@@ -282,9 +288,13 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < MT; ++i) {
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        tc_mma_f16(d_tmem + i * BN, sw128_kmajor_desc(a0 + i * A_TILE + kk * 32),
-                                   sw128_kmajor_desc(b0 + kk * 32), idesc, (kb | kk) != 0);
+                    for (int kk = 0; kk < 4; ++kk) {   // 4 x 32 bytes of K per stage
+                        const uint64_t ad = sw128_kmajor_desc(a0 + i * A_TILE + kk * 32);
+                        const uint64_t bd = sw128_kmajor_desc(b0 + kk * 32);
+                        if constexpr (A8)
+                            tc_mma_f8(d_tmem + i * BN, ad, bd, idesc, (kb | kk) != 0);
+                        else
+                            tc_mma_f16(d_tmem + i * BN, ad, bd, idesc, (kb | kk) != 0);
                     }
                 }
                 tc_commit(bar_empty + s * 8);
@@ -488,22 +498,31 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int es_b
 
 int g_num_sms = 0;
 
-template <int BN, int STAGES, bool FP8, int MT = 1>
+template <int BN, int STAGES, bool FP8, int MT = 1, bool A8 = false>
 cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
     using PL = SmemPlan<BN, STAGES, FP8, MT>;
     static_assert(PL::BYTES <= 227 * 1024, "shared memory plan exceeds 227 KB");
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, STAGES, FP8, MT>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, STAGES, FP8, MT, A8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, PL::BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     CUtensorMap ta, tb, to;
-    if (!make_map(&ta, p.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.M, p.K, p.K, BM, BK,
-                  CU_TENSOR_MAP_SWIZZLE_128B))
+    if (A8) {
+        // E4M3 codes of both operands, 128 K per box (128-byte rows)
+        if (!make_map(&ta, p.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.M, p.K, p.K, BM, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map(&tb, p.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.N, p.K, p.K, BN, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    } else if (!make_map(&ta, p.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.M, p.K, p.K, BM, BK,
+                         CU_TENSOR_MAP_SWIZZLE_128B)) {
         return cudaErrorInvalidValue;
-    if (FP8) {
+    }
+    if (A8) {
+    } else if (FP8) {
         if (!make_map(&tb, p.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.N, p.K, p.K, BN, BK,
                       CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
@@ -523,6 +542,7 @@ cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* la
     a.bias = static_cast<const __nv_bfloat16*>(p.bias);
     a.scales = p.scales;
     a.scale_seg = p.scale_seg > 0 ? p.scale_seg : p.N;
+    a.act_scale = A8 ? p.a_scale : nullptr;
     a.gate = p.gate;
     a.gate_ld = p.gate_ld;
     a.rows_per_batch = p.rows_per_batch > 0 ? p.rows_per_batch : 1;
@@ -531,7 +551,7 @@ cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* la
     a.num_n = (p.N + BN - 1) / BN;
     a.num_tiles = a.num_m * a.num_n;
     const int grid = a.num_tiles < g_num_sms ? a.num_tiles : g_num_sms;
-    gemm_kernel<BN, STAGES, FP8, MT><<<grid, PL::THREADS, PL::BYTES, s>>>(ta, tb, to, a);
+    gemm_kernel<BN, STAGES, FP8, MT, A8><<<grid, PL::THREADS, PL::BYTES, s>>>(ta, tb, to, a);
     ++*launches;
     return cudaGetLastError();
 }
@@ -663,7 +683,7 @@ cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long*
     if (cost(192) < cost(bn)) bn = 192;
     if (cost(128) < cost(bn)) bn = 128;
     if (forced_bn() == 128 || forced_bn() == 192 || forced_bn() == 256) bn = forced_bn();
-    if (p.w_dtype == DLO_DT_E4M3) {
+    if (p.w_dtype == DLO_DT_E4M3 && p.a_dtype != DLO_DT_E4M3) {
         // E4M3: 256-row CTA tiles (two 128-row accumulators) share each
         // widened weight tile, halving the widening work per FLOP, when
         // there are enough row blocks to fill the SMs.  DLO_GEMM_MT=1 turns
@@ -674,6 +694,13 @@ cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long*
         if (bn == 256) return run_gemm<256, 3, true>(p, s, launches);
         if (bn == 192) return run_gemm<192, 3, true>(p, s, launches);
         return run_gemm<128, 4, true>(p, s, launches);
+    }
+    if (p.a_dtype == DLO_DT_E4M3) {
+        // W8A8: both operands E4M3; same stage bytes as bf16
+        if (p.w_dtype != DLO_DT_E4M3 || !p.a_scale || !p.scales) return cudaErrorInvalidValue;
+        if (bn == 256) return run_gemm<256, 4, false, 1, true>(p, s, launches);
+        if (bn == 192) return run_gemm<192, 4, false, 1, true>(p, s, launches);
+        return run_gemm<128, 6, false, 1, true>(p, s, launches);
     }
     if (p.w_dtype != DLO_DT_BF16) return cudaErrorNotSupported;
     if (bn == 256) return run_gemm<256, 4, false>(p, s, launches);

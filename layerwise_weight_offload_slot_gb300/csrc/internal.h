@@ -13,6 +13,9 @@ namespace dlo {
 
 // ------------------------------------------------------------------ layout
 
+// Linear weights stored as E4M3 codes (W8A16 or W8A8).
+inline bool e4m3_weights(int wdtype) { return wdtype == DLO_W_E4M3 || wdtype == DLO_W_E4M3_A8; }
+
 struct Entry {
     std::string name;
     size_t offset = 0;
@@ -47,6 +50,8 @@ struct Workspace {
     size_t in_x = 0;     // bf16 [BN, D]   staging of host inputs (forward_host)
     size_t in_cond = 0;  // cond staging (forward_host)
     size_t in_ctx = 0;   // bf16 [B*L, Dt] (forward_host)
+    size_t qa = 0;       // W8A8: E4M3 codes of the current linear's input
+    size_t qs = 0;       // W8A8: kQuantScratch partial maxima, then the scale
     size_t err = 0;      // int[64] kernels' error words
     size_t total = 0;
 };
@@ -69,6 +74,8 @@ struct GemmParams {
     int w_dtype = DLO_DT_BF16;
     const float* scales = nullptr;
     int scale_seg = 0;
+    int a_dtype = DLO_DT_BF16;        // DLO_DT_E4M3: A holds E4M3 codes [M, K] (W8A8)
+    const float* a_scale = nullptr;   // W8A8: device fp32 activation scale
     const void* bias = nullptr;   // bf16 [N]
     int M = 0, N = 0, K = 0;
     int epi = DLO_EPI_BIAS;
@@ -120,6 +127,13 @@ cudaError_t launch_f32_to_bf16(const float* in, void* out, size_t n, cudaStream_
                                unsigned long long* launches);
 cudaError_t launch_gather(void* dst, const void* src, size_t bytes, cudaStream_t s,
                           unsigned long long* launches);
+// Dynamic per-tensor E4M3 quantisation of a bf16 [rows, cols] activation
+// (row stride ld, cols % 8 == 0, 16-B aligned rows) into contiguous codes q
+// [rows, cols] and the fp32 scale *scale (device); scratch holds
+// kQuantScratch floats of partial maxima.
+constexpr int kQuantScratch = DLO_QUANT_SCRATCH;
+cudaError_t launch_quantize_e4m3(const void* x, int rows, int cols, int ld, void* q, float* scale,
+                                 float* scratch, cudaStream_t s, unsigned long long* launches);
 // *out += sum of the 64-bit words of src (bytes % 16 == 0), mod 2^64.
 cudaError_t launch_checksum(const void* src, size_t bytes, unsigned long long* out, cudaStream_t s,
                             unsigned long long* launches);

@@ -256,6 +256,86 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* 
 
 // dst[i] = src[i] over 16-byte words; src may be mapped host memory.  Four
 // independent loads per thread are in flight before the stores.
+// ---- dynamic per-tensor E4M3 quantisation of an activation (W8A8 linears)
+//
+// s = amax|x| / 448 in fp32 (1 when amax = 0), r = 1 / s rounded to fp32;
+// code = E4M3_rn_satfinite(x * r) with the product rounded to fp32 (the
+// inverted-scale form: one multiply per element).  Two launches: partial maxima per CTA,
+// then every CTA of the quantiser reduces the partials itself (no atomics,
+// no memset, deterministic) before it converts its share of the tensor.
+
+// max over the 16-bit halves of |bf16| bit patterns: for non-negative values
+// the bit order is the numeric order, and NaN patterns sort above infinity.
+__device__ __forceinline__ uint32_t absmax_bf16x8(uint32_t m, const uint4& v) {
+    m = __vmaxu2(m, v.x & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.y & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.w & 0x7FFF7FFFu);
+    return m;
+}
+
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t m, uint32_t* sh) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        m = threadIdx.x < (blockDim.x >> 5) ? sh[threadIdx.x] : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        if (threadIdx.x == 0) sh[0] = m;
+    }
+    __syncthreads();
+    return sh[0];
+}
+
+__global__ void __launch_bounds__(256) amax_partial_kernel(const __nv_bfloat16* __restrict__ x,
+                                                           int rows, int c8, int ld,
+                                                           float* __restrict__ part) {
+    __shared__ uint32_t sh[32];
+    uint32_t m = 0;
+    const long long n = 1LL * rows * c8;
+    for (long long i = blockIdx.x * 256LL + threadIdx.x; i < n; i += gridDim.x * 256LL) {
+        const long long r = i / c8, c = i - r * c8;
+        const uint4 v = *reinterpret_cast<const uint4*>(x + r * ld + c * 8);
+        m = absmax_bf16x8(m, v);
+    }
+    m = max(m & 0xFFFFu, m >> 16);
+    m = block_max_u32(m, sh);
+    if (threadIdx.x == 0) part[blockIdx.x] = __uint_as_float(m << 16);
+}
+
+__global__ void __launch_bounds__(256) quant_e4m3_kernel(const __nv_bfloat16* __restrict__ x,
+                                                         int rows, int c8, int ld,
+                                                         const float* __restrict__ part, int nparts,
+                                                         uint8_t* __restrict__ q,
+                                                         float* __restrict__ scale_out) {
+    __shared__ uint32_t sh[32];
+    uint32_t m = 0;
+    for (int i = threadIdx.x; i < nparts; i += 256) m = max(m, __float_as_uint(part[i]));
+    m = block_max_u32(m, sh);
+    const float amax = __uint_as_float(m);
+    const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+    const float inv = __frcp_rn(s);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s;
+    const long long n = 1LL * rows * c8;
+    for (long long i = blockIdx.x * 256LL + threadIdx.x; i < n; i += gridDim.x * 256LL) {
+        const long long r = i / c8, c = i - r * c8;
+        const uint4 v = *reinterpret_cast<const uint4*>(x + r * ld + c * 8);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float f0 = __uint_as_float(w[2 * h] << 16), f1 = __uint_as_float(w[2 * h] & 0xFFFF0000u);
+            const float f2 = __uint_as_float(w[2 * h + 1] << 16),
+                        f3 = __uint_as_float(w[2 * h + 1] & 0xFFFF0000u);
+            o[h] = e4m3x2_rn_sat(__fmul_rn(f0, inv), __fmul_rn(f1, inv)) |
+                   (e4m3x2_rn_sat(__fmul_rn(f2, inv), __fmul_rn(f3, inv)) << 16);
+        }
+        *reinterpret_cast<uint2*>(q + r * (8LL * c8) + c * 8) = make_uint2(o[0], o[1]);
+    }
+}
+
 __global__ void __launch_bounds__(1024) gather_kernel(uint4* __restrict__ dst,
                                                       const uint4* __restrict__ src, size_t n16) {
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
@@ -379,6 +459,28 @@ cudaError_t launch_f32_to_bf16(const float* in, void* out, size_t n, cudaStream_
     f32_to_bf16_kernel<<<blocks_for(n8, 256), 256, 0, s>>>(in, static_cast<__nv_bfloat16*>(out),
                                                            n8);
     ++*launches;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_e4m3(const void* x, int rows, int cols, int ld, void* q, float* scale,
+                                 float* scratch, cudaStream_t s, unsigned long long* launches) {
+    if (rows <= 0) return cudaSuccess;
+    static int grid = 0;
+    if (!grid) {
+        int dev = 0, sms = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        grid = sms > 0 ? 4 * sms : 128;
+        if (grid > kQuantScratch) grid = kQuantScratch;
+    }
+    const int c8 = cols / 8;
+    const long long chunks = 1LL * rows * c8;
+    long long need = (chunks + 255) / 256;
+    const int g = static_cast<int>(need < grid ? (need > 0 ? need : 1) : grid);
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+    amax_partial_kernel<<<g, 256, 0, s>>>(xb, rows, c8, ld, scratch);
+    quant_e4m3_kernel<<<g, 256, 0, s>>>(xb, rows, c8, ld, scratch, g, static_cast<uint8_t*>(q), scale);
+    *launches += 2;
     return cudaGetLastError();
 }
 

@@ -39,7 +39,7 @@ dlo_status validate_desc(const dlo_desc* d, std::string* msg) {
             return fail(DLO_EINVAL, "unknown staging");
         return DLO_OK;
     }
-    if (d->wdtype != DLO_W_BF16 && d->wdtype != DLO_W_E4M3) return fail(DLO_EINVAL, "unknown wdtype");
+    if (d->wdtype != DLO_W_BF16 && !e4m3_weights(d->wdtype)) return fail(DLO_EINVAL, "unknown wdtype");
     if (d->n_blocks < 1) return fail(DLO_EINVAL, "n_blocks < 1");
     if (d->heads < 1 || d->head_dim < 8 || d->hidden != d->heads * d->head_dim)
         return fail(DLO_EINVAL, "hidden must equal heads * head_dim");
@@ -53,7 +53,7 @@ dlo_status validate_desc(const dlo_desc* d, std::string* msg) {
         return fail(DLO_EINVAL, "unknown staging");
     if (d->block_kind == DLO_BLOCK_DIT) {
         if (d->cond_dim < 8 || d->cond_dim % 16 != 0) return fail(DLO_EINVAL, "cond_dim % 16 != 0");
-        if (d->wdtype == DLO_W_E4M3)
+        if (e4m3_weights(d->wdtype))
             return fail(DLO_EUNSUPPORTED, "E4M3 weights are implemented for video blocks only");
     } else {
         if (d->text_dim < 16 || d->text_dim % 16 != 0) return fail(DLO_EINVAL, "text_dim % 16 != 0");
@@ -112,6 +112,7 @@ Workspace plan_workspace_stack(const dlo_desc* ds, int n) {
     for (int i = 0; i < n; ++i) {
         u.ffn = std::max(u.ffn, ds[i].ffn);
         u.cond_dim = std::max(u.cond_dim, ds[i].cond_dim);
+        if (ds[i].wdtype == DLO_W_E4M3_A8) u.wdtype = DLO_W_E4M3_A8;
         if (ds[i].block_kind == DLO_BLOCK_VIDEO) {
             u.block_kind = DLO_BLOCK_VIDEO;
             u.text_dim = ds[i].text_dim;
@@ -153,7 +154,7 @@ size_t build_layout(const dlo_desc& d, std::vector<Entry>* out) {
         return b.cur;
     }
     const long long D = d.hidden, F = d.ffn;
-    const int W = d.wdtype == DLO_W_E4M3 ? DLO_DT_E4M3 : DLO_DT_BF16;
+    const int W = e4m3_weights(d.wdtype) ? DLO_DT_E4M3 : DLO_DT_BF16;
     const int H = DLO_DT_BF16;
     if (d.block_kind == DLO_BLOCK_DIT) {
         const long long C = d.cond_dim;
@@ -197,7 +198,7 @@ size_t build_layout(const dlo_desc& d, std::vector<Entry>* out) {
         b.group(); b.add("ffn.fc1.bias", H, F);
         b.group(); b.add("ffn.fc2.weight", W, D, F);
         b.group(); b.add("ffn.fc2.bias", H, D);
-        if (d.wdtype == DLO_W_E4M3) {
+        if (e4m3_weights(d.wdtype)) {
             // one fp32 scale per linear: self q,k,v,o, cross q,k,v,o, fc1, fc2
             b.group(); b.add("linear_scales", DLO_DT_F32, 16, -1, 0);
         }
@@ -245,6 +246,12 @@ Workspace plan_workspace(const dlo_desc& d) {
     }
     w.mod = take(static_cast<size_t>(d.max_batch) * 6 * D * 4);
     w.in_x = take(BN * D * 2);
+    if (d.wdtype == DLO_W_E4M3_A8) {
+        // codes of the widest linear input: fc2's [BN, F], or the text context
+        const size_t BL = static_cast<size_t>(d.max_batch) * d.max_text_tokens;
+        w.qa = take(std::max(BN * std::max(D, F), BL * static_cast<size_t>(d.text_dim)));
+        w.qs = take((kQuantScratch + 64) * sizeof(float));
+    }
     w.err = take(64 * sizeof(int));
     w.total = align_up(cur, 256);
     return w;

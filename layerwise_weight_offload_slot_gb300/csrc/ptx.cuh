@@ -298,6 +298,34 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn = 
            | (static_cast<uint32_t>(M >> 4) << 24);   // M
 }
 
+// Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format code 0 for
+// both), fp32 D, both operands K-major; N >> 3 at bits 17-22, M >> 4 at 24-28.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+    return (1u << 4)                                  // D format: f32
+           | (static_cast<uint32_t>(N >> 3) << 17)    // N
+           | (static_cast<uint32_t>(M >> 4) << 24);   // M
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f8f6f4 (8-bit operands, K = 32 per
+// instruction: 32 bytes of each operand row, the same 32-byte step of a
+// 128-byte-swizzled row as kind::f16).
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Two fp32 values to two E4M3 codes (round to nearest even, saturating to
+// +-448, NaN stays NaN); `lo` lands in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2_rn_sat(float lo, float hi) {
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
 // ------------------------------------------------------------------ cp.async / mma.sync
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {

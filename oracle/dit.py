@@ -101,14 +101,20 @@ _LINEARS_VIDEO = ("self_attn.q", "self_attn.k", "self_attn.v", "self_attn.o",
 _LINEARS_DIT = ("adaLN", "attn.qkv", "attn.proj", "mlp.fc1", "mlp.fc2")
 
 
-def prepare_block(params, fp8_linears=False):
+def prepare_block(params, fp8_linears=False, fp8_activations=False):
     """float64 copies of one block's tensors.
 
     With fp8_linears every linear weight W is replaced by s * decode(q) where
     (q, s) = quantize_per_tensor(W); the codes and scales are also returned
     under "<name>.codes" / "<name>.scale" for byte-level comparisons.
+    With fp8_activations as well (W8A8, video blocks), every linear's input is
+    quantised the same way, per tensor, when the block runs (`_linear`).
     """
+    if fp8_activations and not fp8_linears:
+        raise ValueError("W8A8 quantises the weights too")
     out = {k: np.asarray(v, dtype=np.float64) for k, v in params.items()}
+    if fp8_activations:
+        out["act_e4m3"] = True
     if fp8_linears:
         names = _LINEARS_VIDEO if "modulation" in params else _LINEARS_DIT
         for n in names:
@@ -149,40 +155,55 @@ def dit_block(x, c, P, heads, eps=EPS, rows=None):
     return out
 
 
+def _linear(P, name, x, rows=None):
+    """x w^T + b of the named linear on a whole activation x [B, M, K]
+    (rows: keep only those rows of the result, [B, len(rows), out]).
+
+    W8A8 (P["act_e4m3"]): the input is first replaced by s_x * decode(q_x),
+    (q_x, s_x) = fp8.quantize_activation(x) over the WHOLE tensor, all batch
+    elements and rows, in float32 -- one dynamic scale per linear input, as
+    the weights have one per tensor ("Distributed Layerwise Offload", Feature
+    compatibility, row "Per-tensor online FP8 linears", extended to the
+    inputs).  Then y = s_x s_w (q_x q_w^T) + b up to float64 rounding.
+    """
+    if P.get("act_e4m3"):
+        q, s = fp8.quantize_activation(x)
+        x = fp8.dequantize(q, s)
+    if rows is not None:
+        x = x[:, rows]
+    return linear(x, P[name + ".weight"], P[name + ".bias"])
+
+
 def video_block(x, e, ctx, P, heads, eps=EPS, rows=None):
     """Video-DiT block.  x [B, N, D], e [B, 6, D], ctx [B, L, Dt].
 
-    rows: as in `dit_block`.
+    rows: as in `dit_block` (not with W8A8: the output projection's input
+    scale needs every row of the attention output).
     """
     x = np.asarray(x, dtype=np.float64)
     e = np.asarray(e, dtype=np.float64)
     ctx = np.asarray(ctx, dtype=np.float64)
     B, N, D = x.shape
+    if rows is not None and P.get("act_e4m3"):
+        raise ValueError("W8A8 blocks are computed for all rows")
     m = e + P["modulation"][None]                                        # [B, 6, D]
+    shift1, scale1, gate1, shift2, scale2, gate2 = (m[:, i][:, None, :] for i in range(6))
     sel = np.arange(N) if rows is None else np.asarray(rows)
-    out = np.empty((B, len(sel), D))
-    for b in range(B):
-        shift1, scale1, gate1, shift2, scale2, gate2 = m[b]
-        h = layernorm(x[b], eps) * (1.0 + scale1) + shift1
-        q = rmsnorm(linear(h[sel], P["self_attn.q.weight"], P["self_attn.q.bias"]),
-                    P["self_attn.norm_q.weight"], eps)
-        k = rmsnorm(linear(h, P["self_attn.k.weight"], P["self_attn.k.bias"]),
-                    P["self_attn.norm_k.weight"], eps)
-        v = linear(h, P["self_attn.v.weight"], P["self_attn.v.bias"])
-        a = attention(q, k, v, heads)
-        xb = x[b, sel] + gate1 * linear(a, P["self_attn.o.weight"], P["self_attn.o.bias"])
-        hc = layernorm(xb, eps) * P["norm_cross.weight"] + P["norm_cross.bias"]
-        qc = rmsnorm(linear(hc, P["cross_attn.q.weight"], P["cross_attn.q.bias"]),
-                     P["cross_attn.norm_q.weight"], eps)
-        kc = rmsnorm(linear(ctx[b], P["cross_attn.k.weight"], P["cross_attn.k.bias"]),
-                     P["cross_attn.norm_k.weight"], eps)
-        vc = linear(ctx[b], P["cross_attn.v.weight"], P["cross_attn.v.bias"])
-        ac = attention(qc, kc, vc, heads)
-        xb = xb + linear(ac, P["cross_attn.o.weight"], P["cross_attn.o.bias"])
-        h2 = layernorm(xb, eps) * (1.0 + scale2) + shift2
-        f = gelu_tanh(linear(h2, P["ffn.fc1.weight"], P["ffn.fc1.bias"]))
-        out[b] = xb + gate2 * linear(f, P["ffn.fc2.weight"], P["ffn.fc2.bias"])
-    return out
+    h = layernorm(x, eps) * (1.0 + scale1) + shift1
+    q = rmsnorm(_linear(P, "self_attn.q", h, sel), P["self_attn.norm_q.weight"], eps)
+    k = rmsnorm(_linear(P, "self_attn.k", h), P["self_attn.norm_k.weight"], eps)
+    v = _linear(P, "self_attn.v", h)
+    a = np.stack([attention(q[b], k[b], v[b], heads) for b in range(B)])
+    xb = x[:, sel] + gate1 * _linear(P, "self_attn.o", a)
+    hc = layernorm(xb, eps) * P["norm_cross.weight"] + P["norm_cross.bias"]
+    qc = rmsnorm(_linear(P, "cross_attn.q", hc), P["cross_attn.norm_q.weight"], eps)
+    kc = rmsnorm(_linear(P, "cross_attn.k", ctx), P["cross_attn.norm_k.weight"], eps)
+    vc = _linear(P, "cross_attn.v", ctx)
+    ac = np.stack([attention(qc[b], kc[b], vc[b], heads) for b in range(B)])
+    xb = xb + _linear(P, "cross_attn.o", ac)
+    h2 = layernorm(xb, eps) * (1.0 + scale2) + shift2
+    f = gelu_tanh(_linear(P, "ffn.fc1", h2))
+    return xb + gate2 * _linear(P, "ffn.fc2", f)
 
 
 def block_forward(kind, x, cond, ctx, P, heads, eps=EPS, rows=None):

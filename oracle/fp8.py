@@ -8,6 +8,11 @@ per-tensor one:
   s = amax(|W|) / 448   (float32; s = 1 when amax = 0)
   q = e4m3(W / s)       (W / s in float32, then round-to-nearest-even to
                          E4M3 with saturation to +-448)
+Activations of the W8A8 linears (an extension the pages do not describe)
+are quantised per tensor with the same scale rule and the inverted-scale
+form of dynamic FP8 activation quantisers:
+  s = amax(|x|) / 448   (float32; 1 when amax = 0),  r = 1 / s  (float32)
+  q = e4m3(x * r)       (x * r in float32, then as above)
 E4M3 per the OCP 8-bit floating point specification: 1 sign bit, 4 exponent
 bits with bias 7, 3 mantissa bits, subnormals, no infinities, S.1111.111 is
 NaN, largest finite magnitude 448.
@@ -71,6 +76,17 @@ def quantize_per_tensor(w: np.ndarray):
     amax = np.float32(np.max(np.abs(w32))) if w32.size else np.float32(0.0)
     s = np.float32(1.0) if amax == 0 else np.float32(amax / np.float32(E4M3_MAX))
     v = (w32 / s).astype(np.float32)
+    return encode_e4m3(v), s
+
+
+def quantize_activation(x: np.ndarray):
+    """(codes uint8, scale float32) of one activation tensor (W8A8 inputs):
+    the weight quantiser's scale, codes of x times the float32 reciprocal."""
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.float32(np.max(np.abs(x32))) if x32.size else np.float32(0.0)
+    s = np.float32(1.0) if amax == 0 else np.float32(amax / np.float32(E4M3_MAX))
+    r = np.float32(np.float32(1.0) / s)
+    v = (x32 * r).astype(np.float32)
     return encode_e4m3(v), s
 
 

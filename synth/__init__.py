@@ -33,6 +33,11 @@ KIND_VIDEO = 1    # video-DiT block (self-attn, cross-attn to text, FFN)
 
 W_BF16 = 0
 W_E4M3 = 1
+W_E4M3_A8 = 2     # E4M3 weights and dynamically quantised E4M3 linear inputs (W8A8)
+
+
+def fp8_weights(wdtype: int) -> bool:
+    return wdtype in (W_E4M3, W_E4M3_A8)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -69,10 +74,14 @@ CFG_VIDEO = StackConfig("video-40x5120-n32760", KIND_VIDEO, 40, 5120, 40, 128, 1
 CFG_VIDEO_FP8 = StackConfig("video-fp8-40x5120-n8192", KIND_VIDEO, 40, 5120, 40, 128, 13824,
                             1, 8192, text_dim=4096, text_tokens=512, wdtype=W_E4M3,
                             master_fp32=True)
+CFG_VIDEO_W8A8 = StackConfig("video-w8a8-40x5120-n8192", KIND_VIDEO, 40, 5120, 40, 128, 13824,
+                             1, 8192, text_dim=4096, text_tokens=512, wdtype=W_E4M3_A8,
+                             master_fp32=True)
 CFG_SWEEP = StackConfig("video-sweep-40x5120-n8192", KIND_VIDEO, 40, 5120, 40, 128, 13824, 1,
                         8192, text_dim=4096, text_tokens=512)
 
-CONFIGS = {c.name: c for c in (CFG_TINY, CFG_DITXL, CFG_VIDEO, CFG_VIDEO_FP8, CFG_SWEEP)}
+CONFIGS = {c.name: c for c in (CFG_TINY, CFG_DITXL, CFG_VIDEO, CFG_VIDEO_FP8, CFG_VIDEO_W8A8,
+                               CFG_SWEEP)}
 
 
 @dataclasses.dataclass(frozen=True)

@@ -33,9 +33,10 @@ def device_inputs(cfg: synth.StackConfig, step: int = 0):
 
 
 def oracle_blocks(cfg: synth.StackConfig, params=None):
-    fp8_lin = cfg.wdtype == synth.W_E4M3
+    fp8_lin = synth.fp8_weights(cfg.wdtype)
+    fp8_act = cfg.wdtype == synth.W_E4M3_A8
     ps = params if params is not None else [synth.block_params(cfg, i) for i in range(cfg.n_blocks)]
-    return [dit.prepare_block(p, fp8_linears=fp8_lin) for p in ps]
+    return [dit.prepare_block(p, fp8_linears=fp8_lin, fp8_activations=fp8_act) for p in ps]
 
 
 def oracle_forward(cfg: synth.StackConfig, x_bf16: torch.Tensor, cond, ctx, blocks):

@@ -66,7 +66,7 @@ def test_layout_matches_param_specs(cfg):
         if all(g in by for g in grp):
             for a, b in zip(grp, grp[1:]):
                 assert by[a]["offset"] + by[a]["bytes"] == by[b]["offset"]
-    if cfg.wdtype == synth.W_E4M3:
+    if synth.fp8_weights(cfg.wdtype):
         assert not by["linear_scales"]["source"]
     assert dlo.dlo_workspace_bytes(d) > 0
 

@@ -21,7 +21,8 @@ def _rows(cfg, n=256, seed=7):
     return np.unique(np.concatenate([r, [cfg.tokens - 1]]))
 
 
-@pytest.mark.parametrize("base", [synth.CFG_VIDEO, synth.CFG_VIDEO_FP8], ids=["bf16", "e4m3"])
+@pytest.mark.parametrize("base", [synth.CFG_VIDEO, synth.CFG_VIDEO_FP8, synth.CFG_VIDEO_W8A8],
+                         ids=["bf16", "e4m3", "w8a8"])
 def test_video_widths_two_block_stack(base):
     cfg = base.with_(n_blocks=2, tokens=1024)
     params = [synth.block_params(cfg, i) for i in range(cfg.n_blocks)]
@@ -33,7 +34,7 @@ def test_video_widths_two_block_stack(base):
     st.wait()
     ref = H.oracle_forward(cfg, x, cond, ctx, H.oracle_blocks(cfg, params))
     err = H.rel_l2(out.float().cpu().numpy(), ref)
-    tol = 5e-2 if cfg.wdtype == synth.W_E4M3 else 2e-2
+    tol = 5e-2 if synth.fp8_weights(cfg.wdtype) else 2e-2
     print(cfg.name, "n=2 N=1024 rel L2", err)
     assert err <= tol
     st.close()
@@ -56,13 +57,14 @@ def test_full_size_block_sampled_rows(base, block):
     st.wait()
     assert st.verify_slot(1) and st.verify_slot(0)
     rows = _rows(cfg)
-    P = dit.prepare_block(params, fp8_linears=cfg.wdtype == synth.W_E4M3)
+    P = dit.prepare_block(params, fp8_linears=synth.fp8_weights(cfg.wdtype),
+                          fp8_activations=cfg.wdtype == synth.W_E4M3_A8)
     ref = dit.block_forward(cfg.kind, x.float().cpu().numpy().astype(np.float64),
                             cond.float().cpu().numpy().astype(np.float64),
                             ctx.float().cpu().numpy().astype(np.float64), P, cfg.heads, rows=rows)
     y = out.float().cpu().numpy()[:, rows]
     err = H.rel_l2(y, ref)
-    tol = 5e-2 if cfg.wdtype == synth.W_E4M3 else 2e-2
+    tol = 5e-2 if synth.fp8_weights(cfg.wdtype) else 2e-2
     print(base.name, "block", block, "sampled rel L2", err)
     assert err <= tol
     st.close()

@@ -29,7 +29,7 @@ def test_mixed_stack_matches_oracle(mc):
     assert st.multi and len(set(st.container_bytes)) == 2
     assert st.slot_bytes >= max(st.container_bytes)
     st.attach()
-    tol = 5e-2 if any(p.wdtype == synth.W_E4M3 for p in mc.parts) else 2e-2
+    tol = 5e-2 if any(synth.fp8_weights(p.wdtype) for p in mc.parts) else 2e-2
     for step in range(2):
         x, conds, ctx, out = run(st, mc, step)
         ref = H.oracle_multi(mc, x, conds, ctx)

@@ -243,3 +243,125 @@ def test_gemm_e4m3_decodes_every_code_exactly():
                     dlo.EPI_RESIDUAL, out.data_ptr(), N, None, 0, K, None, stream())
     torch.cuda.synchronize()
     np.testing.assert_array_equal(out.cpu().numpy().astype(np.float64), fp8.decode_e4m3(codes).T)
+
+
+# ---------------------------------------------------------------- W8A8
+
+def _quantize_act(x, cols=None):
+    """Device E4M3 codes [rows, cols] and scale of the first `cols` columns
+    (default all) of a bf16 [rows, full] tensor."""
+    rows, full = x.shape
+    cols = full if cols is None else cols
+    q = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+    s = torch.empty(1, dtype=torch.float32, device="cuda")
+    scratch = torch.empty(dlo.QUANT_SCRATCH, dtype=torch.float32, device="cuda")
+    dlo.dlo_op_quantize_act(x.data_ptr(), rows, cols, full, q.data_ptr(), s.data_ptr(),
+                            scratch.data_ptr(), stream())
+    torch.cuda.synchronize()
+    return q, s
+
+
+@pytest.mark.parametrize("rows,cols,pad", [(1, 8, 0), (7, 40, 8), (300, 1152, 0), (2048, 4608, 0),
+                                           (1000, 5120, 64), (8192, 5120, 0)])
+def test_activation_quantiser_matches_oracle_bit_exactly(rows, cols, pad):
+    from oracle import fp8
+    g = np.random.default_rng(rows + cols)
+    a = g.standard_normal((rows, cols + pad)) * np.exp(g.uniform(-12, 4, size=(rows, cols + pad)))
+    a[0, 0] = 1e-12                       # far below the smallest code: flushes to 0
+    x = bf16(a)
+    q, s = _quantize_act(x, cols if pad else None)
+    xr = f64(x)[:, :cols]
+    oq, os_ = fp8.quantize_activation(xr)   # same fp32 decisions as the device
+    assert float(s.item()) == float(os_)
+    np.testing.assert_array_equal(q.cpu().numpy(), oq)
+
+
+def test_activation_quantiser_special_tensors():
+    from oracle import fp8
+    z = torch.zeros((33, 64), dtype=torch.bfloat16, device="cuda")
+    q, s = _quantize_act(z)
+    assert float(s.item()) == 1.0 and int(q.sum().item()) == 0
+    # one value per code: x = 2^-4 * decode(code); amax = 448 * 2^-4
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    codes = np.concatenate([codes, codes[:2]]).reshape(16, 16)
+    x = bf16(fp8.decode_e4m3(codes) * 2.0 ** -4)
+    q, s = _quantize_act(x)
+    assert float(s.item()) == 2.0 ** -4
+    got = q.cpu().numpy()
+    # -0 (0x80) and +0 are both zero; every other code is returned unchanged
+    ok = (got == codes) | ((codes & 0x7F) == 0) & ((got & 0x7F) == 0)
+    assert ok.all()
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (300, 272, 1152), (2048, 3456, 1152),
+                                   (777, 1152, 4608), (129, 512, 4096), (1, 16, 16), (100, 48, 80)])
+@pytest.mark.parametrize("epi", [0, 1, 2])
+def test_gemm_w8a8_matches_oracle(M, N, K, epi):
+    """E4M3 x E4M3 on kind::f8f6f4: products of two codes are exact in fp32,
+    so only the fp32 accumulation and the epilogue round."""
+    from oracle import fp8
+    g = np.random.default_rng(M + 3 * N + 7 * K + epi)
+    A = bf16(g.standard_normal((M, K)))
+    qa, sa = _quantize_act(A)
+    codes = g.integers(0, 256, size=(N, K), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] &= 0xFE
+    Wq = torch.from_numpy(codes).cuda()
+    seg = N // 2 if (N // 2) % 16 == 0 else N
+    sc = (0.02 / 448.0) * (1.0 + np.arange(N // seg, dtype=np.float32))
+    scales = torch.from_numpy(sc.astype(np.float32)).cuda()
+    b = bf16(g.standard_normal(N) * 0.1)
+    adeq = fp8.decode_e4m3(qa.cpu().numpy()) * float(sa.item())
+    wdeq = fp8.decode_e4m3(codes) * np.repeat(sc.astype(np.float64), seg)[:, None]
+    ref = dit.linear(adeq, wdeq, f64(b))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if epi == dlo.EPI_RESIDUAL:
+        gate = torch.from_numpy(g.standard_normal((1, N)).astype(np.float32)).cuda()
+        x0 = torch.from_numpy(g.standard_normal((M, N)).astype(np.float32)).cuda()
+        out = x0.clone()
+        dlo.dlo_op_gemm_w8a8(qa.data_ptr(), sa.data_ptr(), Wq.data_ptr(), scales.data_ptr(), seg,
+                             b.data_ptr(), M, N, K, epi, out.data_ptr(), N, gate.data_ptr(), N, M,
+                             err.data_ptr(), stream())
+        ref = f64(x0) + f64(gate) * ref
+        tol = 1e-5
+    else:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        dlo.dlo_op_gemm_w8a8(qa.data_ptr(), sa.data_ptr(), Wq.data_ptr(), scales.data_ptr(), seg,
+                             b.data_ptr(), M, N, K, epi, out.data_ptr(), N, None, 0, 1,
+                             err.data_ptr(), stream())
+        if epi == dlo.EPI_GELU:
+            ref = dit.gelu_tanh(ref)
+        tol = 6e-3
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert rel(f64(out), ref) < tol
+
+
+def test_gemm_w8a8_multiplies_every_code_pair_exactly():
+    """A = one-hot rows of code 0x38 (1.0) pick weight columns; then A's own
+    codes against a weight column of ones: Y = decode exactly, both ways."""
+    from oracle import fp8
+    K, N = 256, 16
+    allc = np.array([c for c in range(256) if c not in (0x7F, 0xFF)] + [0, 0], dtype=np.uint8)
+    W = np.zeros((N, K), dtype=np.uint8)
+    W[:] = allc[None, :]
+    W[1] = allc[::-1]
+    A = np.zeros((K, K), dtype=np.uint8)
+    A[np.arange(K), np.arange(K)] = 0x38                   # 1.0
+    one = torch.ones(1, dtype=torch.float32, device="cuda")
+    sc = torch.ones(1, dtype=torch.float32, device="cuda")
+    out = torch.zeros((K, N), dtype=torch.float32, device="cuda")
+    dA, dW = torch.from_numpy(A).cuda(), torch.from_numpy(W).cuda()    # alive until synchronised
+    dlo.dlo_op_gemm_w8a8(dA.data_ptr(), one.data_ptr(), dW.data_ptr(), sc.data_ptr(), N, None, K, N, K,
+                         dlo.EPI_RESIDUAL, out.data_ptr(), N, None, 0, K, None, stream())
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.cpu().numpy().astype(np.float64), fp8.decode_e4m3(W).T)
+    Wone = np.zeros((N, K), dtype=np.uint8)
+    Wone[np.arange(N), np.arange(N)] = 0x38
+    Acodes = np.zeros((K, K), dtype=np.uint8)
+    Acodes[:, :N] = np.stack([allc] * N, axis=1)
+    out.zero_()
+    dA, dW = torch.from_numpy(Acodes).cuda(), torch.from_numpy(Wone).cuda()
+    dlo.dlo_op_gemm_w8a8(dA.data_ptr(), one.data_ptr(), dW.data_ptr(), sc.data_ptr(), N, None, K, N, K,
+                         dlo.EPI_RESIDUAL, out.data_ptr(), N, None, 0, K, None, stream())
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.cpu().numpy().astype(np.float64), fp8.decode_e4m3(Acodes[:, :N]))

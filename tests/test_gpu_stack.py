@@ -18,6 +18,7 @@ SMALL_DIT = synth.StackConfig("dit-small", synth.KIND_DIT, 6, 256, 4, 64, 512, 2
 SMALL_VID = synth.StackConfig("video-small", synth.KIND_VIDEO, 4, 256, 2, 128, 512, 2, 300,
                               text_dim=192, text_tokens=77)
 SMALL_VID_FP8 = SMALL_VID.with_(name="video-small-fp8", wdtype=synth.W_E4M3, master_fp32=True)
+SMALL_VID_W8A8 = SMALL_VID.with_(name="video-small-w8a8", wdtype=synth.W_E4M3_A8, master_fp32=True)
 
 
 def run(st, cfg, step=0):
@@ -40,7 +41,7 @@ def test_tiny_stack_matches_oracle():
     st.close()
 
 
-@pytest.mark.parametrize("cfg", [SMALL_DIT, SMALL_VID, SMALL_VID_FP8], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [SMALL_DIT, SMALL_VID, SMALL_VID_FP8, SMALL_VID_W8A8], ids=lambda c: c.name)
 def test_small_stacks_match_oracle(cfg):
     st = H.make_stack(cfg)
     st.attach()
@@ -54,7 +55,7 @@ def test_small_stacks_match_oracle(cfg):
     derr = H.rel_l2(y - x0, ref - x0)
     rounding = H.rel_l2(synth.round_bf16(ref.astype(np.float32)) - x0, ref - x0)
     print(cfg.name, "rel L2", err, "update rel L2", derr, "of which output rounding", rounding)
-    tol = 5e-2 if cfg.wdtype == synth.W_E4M3 else 2e-2
+    tol = 5e-2 if synth.fp8_weights(cfg.wdtype) else 2e-2
     assert err <= tol and derr <= tol + 2 * rounding
     st.close()
 

@@ -272,3 +272,83 @@ def test_multi_stack_identity_container_and_order():
     c2 = c + 0.5
     other = dit.multi_stack_forward([parts[0], (kd, c2, bd, hd)], x, ctx)
     assert dit.max_rel_l2(other, fwd) > 1e-7
+
+
+# ---------------------------------------------------------------- W8A8 linears
+
+def _w8a8_linear_params(out_f=24, in_f=40, seed=3):
+    g = np.random.default_rng(seed)
+    w = g.standard_normal((out_f, in_f)).astype(np.float32) * 0.05
+    b = g.standard_normal(out_f).astype(np.float32) * 0.01
+    q, s = fp8.quantize_per_tensor(w)
+    P = {"l.weight": fp8.dequantize(q, s), "l.bias": b.astype(np.float64), "act_e4m3": True}
+    return P
+
+
+def test_w8a8_linear_is_exact_on_representable_inputs():
+    # x = 2^-3 * decode(codes) with a code of magnitude 448 present: the
+    # per-tensor scale is exactly 2^-3 and the codes come back unchanged, so
+    # the W8A8 product equals the product with the unquantised input
+    P = _w8a8_linear_params()
+    g = np.random.default_rng(0)
+    codes = g.integers(0, 0x7F, size=(2, 7, 40)).astype(np.uint8)
+    codes[0, 0, 0] = 0x7E                                   # 448
+    codes |= (g.integers(0, 2, size=codes.shape) << 7).astype(np.uint8)
+    x = fp8.decode_e4m3(codes) * 2.0 ** -3
+    q, s = fp8.quantize_activation(x)
+    assert s == np.float32(2.0 ** -3)
+    np.testing.assert_array_equal(q, codes)
+    y = dit._linear(P, "l", x)
+    np.testing.assert_array_equal(y, dit.linear(x, P["l.weight"], P["l.bias"]))
+
+
+def test_w8a8_linear_scale_invariance_and_error_bound():
+    P = _w8a8_linear_params()
+    P0 = dict(P, **{"l.bias": np.zeros_like(P["l.bias"])})
+    g = np.random.default_rng(1)
+    x = g.standard_normal((2, 9, 40)) * np.array([1.0, 3.0])[:, None, None]
+    y = dit._linear(P0, "l", x)
+    # powers of two move the scale, not the codes
+    np.testing.assert_array_equal(dit._linear(P0, "l", x * 8.0), y * 8.0)
+    # error against the exact input: at most half a quantum per element,
+    # relative 2^-4 in the normal range, 2^-10 s among the subnormals
+    x32 = x.astype(np.float32).astype(np.float64)
+    _, s = fp8.quantize_activation(x)
+    per = np.maximum(np.abs(x32) * 2.0 ** -4, float(s) * 2.0 ** -10) + np.abs(x32) * 2.0 ** -21
+    bound = per @ np.abs(P0["l.weight"]).T
+    ref = dit.linear(x32, P0["l.weight"], P0["l.bias"])
+    assert np.all(np.abs(y - ref) <= bound * (1 + 1e-9))
+    assert np.abs(y - ref).max() > 0                        # it does quantise
+
+
+def test_w8a8_scale_spans_the_whole_tensor():
+    # one scale for all batch elements and rows: enlarging batch element 1
+    # changes the codes, hence the result, of batch element 0
+    P = _w8a8_linear_params()
+    g = np.random.default_rng(2)
+    x = g.standard_normal((2, 9, 40))
+    y = dit._linear(P, "l", x)
+    x2 = x.copy()
+    x2[1] *= 5.0
+    y2 = dit._linear(P, "l", x2)
+    assert not np.array_equal(y2[0], y[0])
+    # ... while the W8A16 linear keeps batch elements independent
+    Pw = {k: v for k, v in P.items() if k != "act_e4m3"}
+    np.testing.assert_array_equal(dit._linear(Pw, "l", x2)[0], dit._linear(Pw, "l", x)[0])
+    # rows are taken after quantising the whole tensor
+    rows = [0, 4, 8]
+    np.testing.assert_array_equal(dit._linear(P, "l", x, rows), y[:, rows])
+
+
+def test_w8a8_video_block_near_w8a16():
+    cfg = _tiny(synth.KIND_VIDEO)
+    prm = synth.block_params(cfg, 0)
+    P16 = dit.prepare_block(prm, fp8_linears=True)
+    P8 = dit.prepare_block(prm, fp8_linears=True, fp8_activations=True)
+    x, e, ctx = _inputs(cfg)
+    y16 = dit.video_block(x, e, ctx, P16, cfg.heads)
+    y8 = dit.video_block(x, e, ctx, P8, cfg.heads)
+    d = dit.max_rel_l2(y8 - x, y16 - x)        # the block's update, not the residual
+    assert 1e-4 < d < 0.1
+    with pytest.raises(ValueError):
+        dit.video_block(x, e, ctx, P8, cfg.heads, rows=[0, 1])

@@ -81,3 +81,29 @@ def test_quantize_per_tensor():
     assert np.all(np.abs(deq - w) <= bound)
     z, sz = fp8.quantize_per_tensor(np.zeros((4, 4), np.float32))
     assert sz == 1.0 and not z.any()
+
+
+def test_quantize_activation_inverted_scale():
+    g = np.random.default_rng(4)
+    x = (g.standard_normal((2, 50, 96)) * np.exp(g.uniform(-6, 3, (2, 50, 96)))).astype(np.float32)
+    q, s = fp8.quantize_activation(x)
+    # same scale rule as the weights
+    assert s == fp8.quantize_per_tensor(x)[1]
+    # codes of x * (1/s), both rounded to fp32, against torch's E4M3 cast
+    r = np.float32(1.0) / s
+    v = torch.from_numpy(x) * torch.tensor(r, dtype=torch.float32)
+    ref = v.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(q, ref)
+    # with a power-of-two scale the product is the quotient: the weights' codes
+    y = x / np.float32(np.max(np.abs(x))) * np.float32(448.0 * 2.0 ** -5)
+    y = y.astype(np.float32)
+    qa, sa = fp8.quantize_activation(y)
+    qw, sw = fp8.quantize_per_tensor(y)
+    assert sa == sw == np.float32(2.0 ** -5)
+    np.testing.assert_array_equal(qa, qw)
+    # half a quantum of error, plus the reciprocal's rounding
+    deq = fp8.dequantize(q, s)
+    a = np.abs(x.astype(np.float64) / s)
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -6)))
+    bound = (0.5 * 2.0 ** (e - 3) + a * 2.0 ** -21) * s
+    assert np.all(np.abs(deq - x) <= bound)
