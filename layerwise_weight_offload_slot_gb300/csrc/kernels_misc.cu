@@ -289,20 +289,51 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t m, uint32_t* sh) {
     return sh[0];
 }
 
+// Element chunk i (8 bf16) of a [rows, 8 * c8] tensor with row stride ld:
+// contiguous tensors (ld == 8 * c8) are addressed flat, without a division.
+__device__ __forceinline__ const uint4* chunk_ptr(const __nv_bfloat16* x, long long i, int c8, int ld,
+                                                  bool flat) {
+    if (flat) return reinterpret_cast<const uint4*>(x) + i;
+    const long long r = i / c8;
+    return reinterpret_cast<const uint4*>(x + r * ld + (i - r * c8) * 8);
+}
+
+constexpr int kQU = 4;   // chunks in flight per thread
+
 __global__ void __launch_bounds__(256) amax_partial_kernel(const __nv_bfloat16* __restrict__ x,
                                                            int rows, int c8, int ld,
                                                            float* __restrict__ part) {
     __shared__ uint32_t sh[32];
     uint32_t m = 0;
     const long long n = 1LL * rows * c8;
-    for (long long i = blockIdx.x * 256LL + threadIdx.x; i < n; i += gridDim.x * 256LL) {
-        const long long r = i / c8, c = i - r * c8;
-        const uint4 v = *reinterpret_cast<const uint4*>(x + r * ld + c * 8);
-        m = absmax_bf16x8(m, v);
+    const bool flat = ld == 8 * c8;
+    const long long stride = gridDim.x * 256LL;
+    long long i = blockIdx.x * 256LL + threadIdx.x;
+    for (; i + (kQU - 1) * stride < n; i += kQU * stride) {
+        uint4 v[kQU];
+#pragma unroll
+        for (int u = 0; u < kQU; ++u) v[u] = *chunk_ptr(x, i + u * stride, c8, ld, flat);
+#pragma unroll
+        for (int u = 0; u < kQU; ++u) m = absmax_bf16x8(m, v[u]);
     }
+    for (; i < n; i += stride) m = absmax_bf16x8(m, *chunk_ptr(x, i, c8, ld, flat));
     m = max(m & 0xFFFFu, m >> 16);
     m = block_max_u32(m, sh);
     if (threadIdx.x == 0) part[blockIdx.x] = __uint_as_float(m << 16);
+}
+
+__device__ __forceinline__ uint2 e4m3x8(const uint4& v, float inv) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float f0 = __uint_as_float(w[2 * h] << 16), f1 = __uint_as_float(w[2 * h] & 0xFFFF0000u);
+        const float f2 = __uint_as_float(w[2 * h + 1] << 16),
+                    f3 = __uint_as_float(w[2 * h + 1] & 0xFFFF0000u);
+        o[h] = e4m3x2_rn_sat(__fmul_rn(f0, inv), __fmul_rn(f1, inv)) |
+               (e4m3x2_rn_sat(__fmul_rn(f2, inv), __fmul_rn(f3, inv)) << 16);
+    }
+    return make_uint2(o[0], o[1]);
 }
 
 __global__ void __launch_bounds__(256) quant_e4m3_kernel(const __nv_bfloat16* __restrict__ x,
@@ -319,21 +350,18 @@ __global__ void __launch_bounds__(256) quant_e4m3_kernel(const __nv_bfloat16* __
     const float inv = __frcp_rn(s);
     if (blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s;
     const long long n = 1LL * rows * c8;
-    for (long long i = blockIdx.x * 256LL + threadIdx.x; i < n; i += gridDim.x * 256LL) {
-        const long long r = i / c8, c = i - r * c8;
-        const uint4 v = *reinterpret_cast<const uint4*>(x + r * ld + c * 8);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[2];
+    const bool flat = ld == 8 * c8;
+    const long long stride = gridDim.x * 256LL;
+    uint2* qo = reinterpret_cast<uint2*>(q);   // codes are contiguous: chunk i -> 8 bytes at 8 i
+    long long i = blockIdx.x * 256LL + threadIdx.x;
+    for (; i + (kQU - 1) * stride < n; i += kQU * stride) {
+        uint4 v[kQU];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float f0 = __uint_as_float(w[2 * h] << 16), f1 = __uint_as_float(w[2 * h] & 0xFFFF0000u);
-            const float f2 = __uint_as_float(w[2 * h + 1] << 16),
-                        f3 = __uint_as_float(w[2 * h + 1] & 0xFFFF0000u);
-            o[h] = e4m3x2_rn_sat(__fmul_rn(f0, inv), __fmul_rn(f1, inv)) |
-                   (e4m3x2_rn_sat(__fmul_rn(f2, inv), __fmul_rn(f3, inv)) << 16);
-        }
-        *reinterpret_cast<uint2*>(q + r * (8LL * c8) + c * 8) = make_uint2(o[0], o[1]);
+        for (int u = 0; u < kQU; ++u) v[u] = *chunk_ptr(x, i + u * stride, c8, ld, flat);
+#pragma unroll
+        for (int u = 0; u < kQU; ++u) qo[i + u * stride] = e4m3x8(v[u], inv);
     }
+    for (; i < n; i += stride) qo[i] = e4m3x8(*chunk_ptr(x, i, c8, ld, flat), inv);
 }
 
 __global__ void __launch_bounds__(1024) gather_kernel(uint4* __restrict__ dst,
