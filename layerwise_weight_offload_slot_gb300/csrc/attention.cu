@@ -54,6 +54,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     attn_fwd_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
                     const __nv_bfloat16* __restrict__ V, __nv_bfloat16* __restrict__ O, int hd,
                     int nq, int nk, int ldq, int ldk, int ldv, int ldo, float scale_log2) {
+    pdl_wait();
+    pdl_launch_dependents();
     using S = AttnSmem<HDP>;
     constexpr int PITCH = S::PITCH;
     constexpr int KSTEPS = HDP / 16;     // k-steps of Q K^T
@@ -228,12 +230,11 @@ cudaError_t run(const void* Q, const void* K, const void* V, void* O, int batch,
     }
     const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(hd));
     dim3 grid((nq + BQ - 1) / BQ, heads, batch);
-    attn_fwd_kernel<HDP><<<grid, kWarps * 32, bytes, s>>>(
-        static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
+    cudaError_t le_ = launch_k(attn_fwd_kernel<HDP>, grid, kWarps * 32, bytes, s, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
         static_cast<const __nv_bfloat16*>(V), static_cast<__nv_bfloat16*>(O), hd, nq, nk, ldq, ldk,
         ldv, ldo, scale_log2);
     ++*launches;
-    return cudaGetLastError();
+    return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
 
 }  // namespace

@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();                 // predecessor's outputs complete and visible
+    pdl_launch_dependents();
 
     auto fail = [&]() {
         *abort_flag = 1;
@@ -402,10 +404,9 @@ cudaError_t run_tc(const void* Q, const void* K, const void* V, void* O, int bat
     }
     const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(hd));
     dim3 grid((nq + TQ - 1) / TQ, heads, batch);
-    attn_tc_kernel<NB, TAIL><<<grid, kThreadsA, P::BYTES, s>>>(
-        maps, static_cast<__nv_bfloat16*>(O), hd, nq, nk, ldo, scale_log2, err);
+    cudaError_t le_ = launch_k(attn_tc_kernel<NB, TAIL>, grid, kThreadsA, P::BYTES, s, maps, static_cast<__nv_bfloat16*>(O), hd, nq, nk, ldo, scale_log2, err);
     ++*launches;
-    return cudaGetLastError();
+    return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
 
 }  // namespace

@@ -213,6 +213,8 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();                 // predecessor's outputs complete and visible
+    pdl_launch_dependents();
     const int kblocks = (args.K + KS - 1) / KS;
 
     auto fail = [&]() {
@@ -551,9 +553,9 @@ cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* la
     a.num_n = (p.N + BN - 1) / BN;
     a.num_tiles = a.num_m * a.num_n;
     const int grid = a.num_tiles < g_num_sms ? a.num_tiles : g_num_sms;
-    gemm_kernel<BN, STAGES, FP8, MT, A8><<<grid, PL::THREADS, PL::BYTES, s>>>(ta, tb, to, a);
+    cudaError_t le_ = launch_k(gemm_kernel<BN, STAGES, FP8, MT, A8>, grid, PL::THREADS, PL::BYTES, s, ta, tb, to, a);
     ++*launches;
-    return cudaGetLastError();
+    return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
 
 int forced_mt() {

@@ -11,6 +11,27 @@
 
 namespace dlo {
 
+// Programmatic dependent launch: on unless DLO_PDL=0 (diagnosis).
+bool pdl_enabled();
+
+// Launch `kernel` on `s` allowing programmatic stream serialisation (the
+// kernel must run pdl_wait() before touching global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ------------------------------------------------------------------ layout
 
 // Linear weights stored as E4M3 codes (W8A16 or W8A8).

@@ -6,10 +6,21 @@
 // One warp per row for the row-wise kernels.
 #include <cuda_bf16.h>
 
+#include <cstdlib>
+
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace dlo {
+
+bool pdl_enabled() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = std::getenv("DLO_PDL");
+        v = (e && e[0] == '0') ? 0 : 1;
+    }
+    return v != 0;
+}
 
 namespace {
 
@@ -35,6 +46,8 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const float* __restrict_
                                                         const __nv_bfloat16* __restrict__ b,
                                                         float eps,
                                                         __nv_bfloat16* __restrict__ out) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -103,6 +116,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(__nv_bfloat16* __restrict_
                                                       int col0b,
                                                       const __nv_bfloat16* __restrict__ wb,
                                                       float eps) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int nseg = wb ? 2 : 1;
@@ -152,6 +167,8 @@ __global__ void __launch_bounds__(256) adaln_kernel(const __nv_bfloat16* __restr
                                                     int C, const __nv_bfloat16* __restrict__ W,
                                                     const __nv_bfloat16* __restrict__ bias,
                                                     int N, float* __restrict__ m) {
+    pdl_wait();
+    pdl_launch_dependents();
     __shared__ float sc[ADALN_BCHUNK * ADALN_CCHUNK];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = (blockIdx.x * 8 + warp) * ADALN_ROWS;
@@ -220,6 +237,8 @@ __global__ void __launch_bounds__(256) adaln_kernel(const __nv_bfloat16* __restr
 // m[b, r] = e[b, r] + table[r] over r < 6D
 __global__ void mod_add_kernel(const float* __restrict__ e, const __nv_bfloat16* __restrict__ t,
                                int B, int n6d, float* __restrict__ m) {
+    pdl_wait();
+    pdl_launch_dependents();
     const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= static_cast<size_t>(B) * n6d) return;
     m[i] = e[i] + bf(t[i % n6d]);
@@ -227,6 +246,8 @@ __global__ void mod_add_kernel(const float* __restrict__ e, const __nv_bfloat16*
 
 __global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ in, float* __restrict__ out,
                                    size_t n8) {
+    pdl_wait();
+    pdl_launch_dependents();
     const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= n8) return;
     const uint4 v = reinterpret_cast<const uint4*>(in)[i];
@@ -242,6 +263,8 @@ __global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ in, float* 
 
 __global__ void f32_to_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* __restrict__ out,
                                    size_t n8) {
+    pdl_wait();
+    pdl_launch_dependents();
     const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= n8) return;
     const float4 a = reinterpret_cast<const float4*>(in)[2 * i];
@@ -303,6 +326,8 @@ constexpr int kQU = 4;   // chunks in flight per thread
 __global__ void __launch_bounds__(256) amax_partial_kernel(const __nv_bfloat16* __restrict__ x,
                                                            int rows, int c8, int ld,
                                                            float* __restrict__ part) {
+    pdl_wait();
+    pdl_launch_dependents();
     __shared__ uint32_t sh[32];
     uint32_t m = 0;
     const long long n = 1LL * rows * c8;
@@ -341,6 +366,8 @@ __global__ void __launch_bounds__(256) quant_e4m3_kernel(const __nv_bfloat16* __
                                                          const float* __restrict__ part, int nparts,
                                                          uint8_t* __restrict__ q,
                                                          float* __restrict__ scale_out) {
+    pdl_wait();
+    pdl_launch_dependents();
     __shared__ uint32_t sh[32];
     uint32_t m = 0;
     for (int i = threadIdx.x; i < nparts; i += 256) m = max(m, __float_as_uint(part[i]));
@@ -385,6 +412,8 @@ __global__ void __launch_bounds__(1024) gather_kernel(uint4* __restrict__ dst,
 // so it is the "compute" of an opaque bytes block.
 __global__ void __launch_bounds__(256) checksum_kernel(const uint4* __restrict__ src, size_t n16,
                                                        unsigned long long* __restrict__ out) {
+    pdl_wait();
+    pdl_launch_dependents();
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
     unsigned long long s = 0;
     for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride) {
@@ -412,8 +441,9 @@ cudaError_t launch_layernorm(const float* x, int rows, int D, int rpb, const flo
     const __nv_bfloat16* bb = static_cast<const __nv_bfloat16*>(b);
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
     const int v4 = (D / 4 + 31) / 32;   // float4 per lane
-#define DLO_LN(V)                                                                          \
-    layernorm_kernel<V><<<g, 256, 0, s>>>(x, rows, D, rpb, shift, scale, mod_ld, wb, bb, eps, o)
+    cudaError_t le_ = cudaSuccess;
+#define DLO_LN(V) \
+    le_ = launch_k(layernorm_kernel<V>, g, 256, 0, s, x, rows, D, rpb, shift, scale, mod_ld, wb, bb, eps, o)
     if (v4 <= 2) DLO_LN(2);
     else if (v4 <= 4) DLO_LN(4);
     else if (v4 <= 8) DLO_LN(8);
@@ -425,69 +455,66 @@ cudaError_t launch_layernorm(const float* x, int rows, int D, int rpb, const flo
     else return cudaErrorInvalidValue;
 #undef DLO_LN
     ++*launches;
-    return cudaGetLastError();
+    return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm(void* x, int rows, int D, int ld, int col0, const void* w, float eps,
                            cudaStream_t s, unsigned long long* launches) {
     if (rows <= 0) return cudaSuccess;
-    rmsnorm_kernel<<<blocks_for(static_cast<size_t>(rows) * 32, 256), 256, 0, s>>>(
-        static_cast<__nv_bfloat16*>(x), rows, D, ld, col0, static_cast<const __nv_bfloat16*>(w),
+    cudaError_t le_ = launch_k(rmsnorm_kernel, blocks_for(static_cast<size_t>(rows) * 32, 256), 256, 0, s, static_cast<__nv_bfloat16*>(x), rows, D, ld, col0, static_cast<const __nv_bfloat16*>(w),
         0, nullptr, eps);
     ++*launches;
-    return cudaGetLastError();
+    return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm2(void* x, int rows, int D, int ld, int col0a, const void* wa,
                             int col0b, const void* wb, float eps, cudaStream_t s,
                             unsigned long long* launches) {
     if (rows <= 0) return cudaSuccess;
-    rmsnorm_kernel<<<blocks_for(static_cast<size_t>(rows) * 64, 256), 256, 0, s>>>(
-        static_cast<__nv_bfloat16*>(x), rows, D, ld, col0a,
+    cudaError_t le_ = launch_k(rmsnorm_kernel, blocks_for(static_cast<size_t>(rows) * 64, 256), 256, 0, s, static_cast<__nv_bfloat16*>(x), rows, D, ld, col0a,
         static_cast<const __nv_bfloat16*>(wa), col0b, static_cast<const __nv_bfloat16*>(wb), eps);
     ++*launches;
-    return cudaGetLastError();
+    return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
 
 cudaError_t launch_adaln(const void* c, int B, int C, const void* W, const void* bias, int N,
                          float* m, cudaStream_t s, unsigned long long* launches) {
     if (N <= 0 || B <= 0) return cudaSuccess;
     const unsigned g = static_cast<unsigned>((N + 8 * ADALN_ROWS - 1) / (8 * ADALN_ROWS));
-    adaln_kernel<<<g, 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(c), B, C, static_cast<const __nv_bfloat16*>(W),
+    cudaError_t le_ = launch_k(adaln_kernel, g, 256, 0, s, static_cast<const __nv_bfloat16*>(c), B, C, static_cast<const __nv_bfloat16*>(W),
         static_cast<const __nv_bfloat16*>(bias), N, m);
     ++*launches;
-    return cudaGetLastError();
+    return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
 
 cudaError_t launch_mod_add(const float* e, const void* table, int B, int n6d, float* m,
                            cudaStream_t s, unsigned long long* launches) {
     const size_t n = static_cast<size_t>(B) * n6d;
     if (!n) return cudaSuccess;
-    mod_add_kernel<<<blocks_for(n, 256), 256, 0, s>>>(e, static_cast<const __nv_bfloat16*>(table),
+    cudaError_t le_ = launch_k(mod_add_kernel, blocks_for(n, 256), 256, 0, s, e, static_cast<const __nv_bfloat16*>(table),
                                                       B, n6d, m);
     ++*launches;
-    return cudaGetLastError();
+    return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
 
 cudaError_t launch_bf16_to_f32(const void* in, float* out, size_t n, cudaStream_t s,
                                unsigned long long* launches) {
     const size_t n8 = n / 8;
     if (!n8) return cudaSuccess;
-    bf16_to_f32_kernel<<<blocks_for(n8, 256), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(in),
+    cudaError_t le_ = launch_k(bf16_to_f32_kernel, blocks_for(n8, 256), 256, 0, s, static_cast<const __nv_bfloat16*>(in),
                                                            out, n8);
     ++*launches;
-    return cudaGetLastError();
+    return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
 
 cudaError_t launch_f32_to_bf16(const float* in, void* out, size_t n, cudaStream_t s,
                                unsigned long long* launches) {
     const size_t n8 = n / 8;
     if (!n8) return cudaSuccess;
-    f32_to_bf16_kernel<<<blocks_for(n8, 256), 256, 0, s>>>(in, static_cast<__nv_bfloat16*>(out),
+    cudaError_t le_ = launch_k(f32_to_bf16_kernel, blocks_for(n8, 256), 256, 0, s, in, static_cast<__nv_bfloat16*>(out),
                                                            n8);
     ++*launches;
-    return cudaGetLastError();
+    return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
 
 cudaError_t launch_quantize_e4m3(const void* x, int rows, int cols, int ld, void* q, float* scale,
@@ -506,10 +533,11 @@ cudaError_t launch_quantize_e4m3(const void* x, int rows, int cols, int ld, void
     long long need = (chunks + 255) / 256;
     const int g = static_cast<int>(need < grid ? (need > 0 ? need : 1) : grid);
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-    amax_partial_kernel<<<g, 256, 0, s>>>(xb, rows, c8, ld, scratch);
-    quant_e4m3_kernel<<<g, 256, 0, s>>>(xb, rows, c8, ld, scratch, g, static_cast<uint8_t*>(q), scale);
+    cudaError_t le_ = launch_k(amax_partial_kernel, g, 256, 0, s, xb, rows, c8, ld, scratch);
+    if (le_ == cudaSuccess)
+        le_ = launch_k(quant_e4m3_kernel, g, 256, 0, s, xb, rows, c8, ld, scratch, g, static_cast<uint8_t*>(q), scale);
     *launches += 2;
-    return cudaGetLastError();
+    return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
 
 cudaError_t launch_gather(void* dst, const void* src, size_t bytes, cudaStream_t s,
@@ -542,9 +570,9 @@ cudaError_t launch_checksum(const void* src, size_t bytes, unsigned long long* o
     size_t g = static_cast<size_t>(sms > 0 ? sms : 1) * 8;
     const size_t need = (n16 + 255) / 256;
     if (need < g) g = need;
-    checksum_kernel<<<static_cast<unsigned>(g), 256, 0, s>>>(static_cast<const uint4*>(src), n16, out);
+    cudaError_t le_ = launch_k(checksum_kernel, static_cast<unsigned>(g), 256, 0, s, static_cast<const uint4*>(src), n16, out);
     ++*launches;
-    return cudaGetLastError();
+    return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
 
 }  // namespace dlo

@@ -21,6 +21,20 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
     return t;
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Every kernel of this library runs pdl_wait() before its first global memory
+// access (read or write), so a kernel launched with programmatic stream
+// serialisation may be scheduled -- and run its set-up -- while its
+// predecessor on the stream finishes; pdl_wait returns once every
+// prerequisite grid has completed and its memory is visible (immediately when
+// there is none).  pdl_launch_dependents lets the next kernel be scheduled as
+// soon as every CTA of this grid has issued it or exited.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
