@@ -50,6 +50,10 @@ def parse():
     p.add_argument("--sweep", action="store_true",
                    help="residency sweep (k = 0,2,4,8) on the 40-block hidden-5120 stack at 8192 "
                         "tokens and a 16 MB..1 GB staging sweep; prints one JSON line")
+    p.add_argument("--ops", action="store_true",
+                   help="time every unit op of one block of --workload at its shapes (CUDA "
+                        "events over --steps back-to-back launches after --warmup); prints one "
+                        "JSON line")
     return p.parse_args()
 
 
@@ -653,10 +657,141 @@ def run_sweep(args):
     print(json.dumps(out), flush=True)
 
 
+def run_ops(args, cfg):
+    """Each kernel of one block of `cfg`, launched through the unit-op C ABI on
+    synthetic device tensors of the block's shapes, timed back to back."""
+    import torch
+    import layerwise_weight_offload_slot_gb300 as dlo
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    st = torch.cuda.current_stream().cuda_stream
+    g = torch.Generator(device=dev).manual_seed(0)
+    B, N, D, F, H, hd = cfg.batch, cfg.tokens, cfg.hidden, cfg.ffn, cfg.heads, cfg.head_dim
+    BN = B * N
+    video = cfg.kind == synth.KIND_VIDEO
+    L, Dt = cfg.text_tokens, cfg.text_dim
+    w8a16, w8a8 = cfg.wdtype == synth.W_E4M3, cfg.wdtype == synth.W_E4M3_A8
+
+    def rnd(*shape, dtype=torch.bfloat16, scale=1.0):
+        return (torch.randn(*shape, device=dev, generator=g) * scale).to(dtype)
+
+    x = rnd(BN, D, dtype=torch.float32)
+    h = rnd(BN, D)
+    big = rnd(BN, max(3 * D, F))
+    a = rnd(BN, D)
+    mod = rnd(B, 6 * D, dtype=torch.float32, scale=0.1)
+    ones = torch.ones(max(3 * D, F, 2 * D), dtype=torch.bfloat16, device=dev)
+    zeros = torch.zeros_like(ones)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    qa = torch.empty(max(BN * max(D, F), B * max(L, 1) * max(Dt, 1)), dtype=torch.uint8, device=dev)
+    qsc = torch.empty(dlo.QUANT_SCRATCH + 64, dtype=torch.float32, device=dev)
+    ops = []
+
+    def gemm(name, A, M, Nn, K, epi, out, ldo):
+        if w8a16 or w8a8:
+            Wt = torch.randint(0, 0x7E, (Nn, K), dtype=torch.uint8, device=dev, generator=g)
+            sc = torch.full((1,), 0.02 / 448.0, dtype=torch.float32, device=dev)
+        else:
+            Wt = rnd(Nn, K, scale=0.02)
+            sc = None
+        gate = mod[:, 2 * D:] if epi == dlo.EPI_RESIDUAL else None
+        flops, nbytes = 2.0 * M * Nn * K, 0.0
+
+        def run():
+            if w8a8:
+                dlo.dlo_op_quantize_act(A.data_ptr(), M, K, K, qa.data_ptr(), qsc[-1:].data_ptr(),
+                                        qsc.data_ptr(), st)
+                dlo.dlo_op_gemm_w8a8(qa.data_ptr(), qsc[-1:].data_ptr(), Wt.data_ptr(), sc.data_ptr(),
+                                     Nn, zeros.data_ptr(), M, Nn, K, epi, out.data_ptr(), ldo,
+                                     gate.data_ptr() if gate is not None else None, 6 * D,
+                                     max(1, M // B), err.data_ptr(), st)
+            else:
+                dlo.dlo_op_gemm(A.data_ptr(), Wt.data_ptr(), dlo.DT_E4M3 if w8a16 else dlo.DT_BF16,
+                                sc.data_ptr() if sc is not None else None, Nn, zeros.data_ptr(), M, Nn,
+                                K, epi, out.data_ptr(), ldo,
+                                gate.data_ptr() if gate is not None else None, 6 * D,
+                                max(1, M // B), err.data_ptr(), st)
+        ops.append((name, run, flops, nbytes, Wt))
+
+    def ln(name, affine):
+        def run():
+            if affine:
+                dlo.dlo_op_layernorm(x.data_ptr(), BN, D, N, None, None, 0, ones.data_ptr(),
+                                     zeros.data_ptr(), 1e-6, h.data_ptr(), st)
+            else:
+                dlo.dlo_op_layernorm(x.data_ptr(), BN, D, N, mod.data_ptr(), mod[:, D:].data_ptr(),
+                                     6 * D, None, None, 1e-6, h.data_ptr(), st)
+        ops.append((name, run, 0.0, 6.0 * BN * D, None))
+
+    def attn(name, q, k, v, nq, nk, ldq, ldk, ldv):
+        def run():
+            dlo.dlo_op_attention(q, k, v, a.data_ptr(), B, H, hd, nq, nk, ldq, ldk, ldv, D, st)
+        ops.append((name, run, 4.0 * B * H * nq * nk * hd, 0.0, None))
+
+    bp = big.data_ptr()
+    es = big.element_size()
+    if not video:
+        cvec = rnd(B, cfg.cond_dim)
+        Wada = rnd(6 * D, cfg.cond_dim, scale=0.02)
+        ops.append(("adaln", lambda: dlo.dlo_op_adaln(cvec.data_ptr(), B, cfg.cond_dim, Wada.data_ptr(),
+                                                       zeros.data_ptr(), 6 * D, mod.data_ptr(), st),
+                    0.0, 2.0 * 6 * D * cfg.cond_dim, Wada))
+        ln("layernorm", False)
+        gemm("gemm_qkv", h, BN, 3 * D, D, dlo.EPI_BIAS, big, 3 * D)
+        attn("attention", bp, bp + 2 * D * es, bp + 4 * D * es, N, N, 3 * D, 3 * D, 3 * D)
+        gemm("gemm_proj", a, BN, D, D, dlo.EPI_RESIDUAL, x, D)
+        gemm("gemm_fc1", h, BN, F, D, dlo.EPI_GELU, big, F)
+        gemm("gemm_fc2", big, BN, D, F, dlo.EPI_RESIDUAL, x, D)
+    else:
+        ctx = rnd(B * L, Dt)
+        kv2 = rnd(B * L, 2 * D)
+        ln("layernorm", False)
+        gemm("gemm_qkv", h, BN, 3 * D, D, dlo.EPI_BIAS, big, 3 * D)
+        ops.append(("rmsnorm_qk", lambda: dlo.dlo_op_rmsnorm(big.data_ptr(), BN, D, 3 * D, 0,
+                                                              ones.data_ptr(), 1e-6, st),
+                    0.0, 4.0 * BN * D, None))
+        attn("attention_self", bp, bp + 2 * D * es, bp + 4 * D * es, N, N, 3 * D, 3 * D, 3 * D)
+        gemm("gemm_o", a, BN, D, D, dlo.EPI_RESIDUAL, x, D)
+        gemm("gemm_cross_q", h, BN, D, D, dlo.EPI_BIAS, a, D)
+        gemm("gemm_cross_kv", ctx, B * L, 2 * D, Dt, dlo.EPI_BIAS, kv2, 2 * D)
+        kp = kv2.data_ptr()
+        attn("attention_cross", h.data_ptr(), kp, kp + D * 2, N, L, D, 2 * D, 2 * D)
+        gemm("gemm_fc1", h, BN, F, D, dlo.EPI_GELU, big, F)
+        gemm("gemm_fc2", big, BN, D, F, dlo.EPI_RESIDUAL, x, D)
+    peaks = measured_peaks()
+    res = {}
+    for name, run, flops, nbytes, _keep in ops:
+        for _ in range(args.warmup):
+            run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            run()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / args.steps
+        r = {"us": us}
+        if flops:
+            r["tflops"] = flops / us / 1e6
+        if nbytes:
+            r["gbs"] = nbytes / us / 1e3
+        res[name] = r
+    assert int(err.item()) == 0
+    fp8_peak = peaks["bf16_tflops_sustained"] * (FP8_OVER_BF16 if w8a8 else 1.0)
+    print(json.dumps({"mode": "ops", "workload": cfg.name, "steps": args.steps, "warmup": args.warmup,
+                      "weights": {0: "bf16", 1: "e4m3 (W8A16)", 2: "e4m3 x e4m3 (W8A8)"}[cfg.wdtype],
+                      "gemm_peak_tflops": fp8_peak, "peak_source": peaks["source"],
+                      "ops": res}), flush=True)
+
+
 def main():
     args = parse()
     if args.sweep:
         run_sweep(args)
+        return
+    if args.ops:
+        run_ops(args, synth.CONFIGS[args.workload])
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus else 1)))

@@ -60,19 +60,24 @@ struct EpiArgs {
     int rows_per_batch;
     int* err;
     int num_m, num_n, num_tiles;
+    int n_major;   // tile order: groups of N blocks sweep all M blocks (else the reverse)
 };
 
 // Grouped tile order: groups of 8 M-blocks sweep all N-blocks, so one
-// group's A rows stay in L2 while the weights stream.
-__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mb, int& nb) {
+// group's A rows stay in L2 while the weights stream -- or, with n_major,
+// groups of 8 N-blocks sweep all M-blocks so the weight panel stays while A
+// streams.  The host picks the order that re-reads the smaller operand.
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int n_major, int& mb, int& nb) {
     constexpr int G = 8;
-    const int per_group = G * num_n;
+    const int outer = n_major ? num_n : num_m, inner = n_major ? num_m : num_n;
+    const int per_group = G * inner;
     const int g = t / per_group;
     const int first = g * G;
-    const int gsz = min(num_m - first, G);
+    const int gsz = min(outer - first, G);
     const int r = t - g * per_group;
-    mb = first + r % gsz;
-    nb = r / gsz;
+    const int o = first + r % gsz, i = r / gsz;
+    mb = n_major ? i : o;
+    nb = n_major ? o : i;
 }
 
 // GELU, tanh approximation; tanh from the hardware approximation
@@ -230,7 +235,7 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
         uint32_t issued = 0, last_par = 0;   // per-stage bit masks
         for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
             int mb, nb;
-            tile_coords(tile, args.num_m, args.num_n, mb, nb);
+            tile_coords(tile, args.num_m, args.num_n, args.n_major, mb, nb);
             for (int kb = 0; kb < kblocks; ++kb) {
                 if (!mbar_wait(bar_empty + s * 8, ph ^ 1, abort_flag)) {
                     fail();
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
             const int acc = t & 1;
             const uint32_t aph = (t >> 1) & 1;
             int mb, nb;
-            tile_coords(tile, args.num_m, args.num_n, mb, nb);
+            tile_coords(tile, args.num_m, args.num_n, args.n_major, mb, nb);
             bool ok = mbar_wait(bar_tfull + acc * 8, aph, abort_flag);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) {
@@ -552,6 +557,13 @@ cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* la
     a.num_m = (p.M + MT * BM - 1) / (MT * BM);
     a.num_n = (p.N + BN - 1) / BN;
     a.num_tiles = a.num_m * a.num_n;
+    // bytes the sweep re-reads: groups of 8 M blocks read all of W once per
+    // group; groups of 8 N blocks read all of A once per group
+    const double a_bytes = static_cast<double>(p.M) * p.K * (A8 ? 1 : 2);
+    const double w_bytes = static_cast<double>(p.N) * p.K * (FP8 || A8 ? 1 : 2);
+    const double m_sweep = a_bytes + w_bytes * ((a.num_m + 7) / 8);
+    const double n_sweep = w_bytes + a_bytes * ((a.num_n + 7) / 8);
+    a.n_major = n_sweep < m_sweep ? 1 : 0;
     const int grid = a.num_tiles < g_num_sms ? a.num_tiles : g_num_sms;
     cudaError_t le_ = launch_k(gemm_kernel<BN, STAGES, FP8, MT, A8>, grid, PL::THREADS, PL::BYTES, s, ta, tb, to, a);
     ++*launches;
