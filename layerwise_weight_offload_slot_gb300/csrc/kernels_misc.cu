@@ -33,10 +33,12 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ float bf(const __nv_bfloat16 v) { return __bfloat162float(v); }
 
 // out = LN(x) * (1 + scale) + shift | LN(x) * w + b | LN(x)
-// One warp per row; the row (up to 32 * 4 * V4 floats) is read once into
-// registers, mean and variance come from the registers (two passes), so HBM
-// sees one read of x and one write of the bf16 output.
-template <int V4>
+// WPR warps per row (a row group); each thread holds V4 float4 of the row in
+// registers, mean and variance come from the registers (two passes, warp
+// shuffles then shared memory across the row group), so HBM sees one read of
+// x and one write of the bf16 output.  Short stacks (few rows) use more
+// warps per row so that enough loads are in flight per SM.
+template <int V4, int WPR>
 __global__ void __launch_bounds__(256) layernorm_kernel(const float* __restrict__ x, int rows,
                                                         int D, int rpb,
                                                         const float* __restrict__ shift,
@@ -48,43 +50,84 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const float* __restrict_
                                                         __nv_bfloat16* __restrict__ out) {
     pdl_wait();
     pdl_launch_dependents();
-    const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(row) * D);
+    constexpr int RPC = 8 / WPR;                  // rows per 256-thread CTA
+    constexpr bool kPre = V4 <= 16;               // modulation prefetched into registers
+    __shared__ float red[2][8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = warp % WPR;
+    const int row = blockIdx.x * RPC + warp / WPR;
+    const bool live = row < rows;
     const int n4 = D >> 2;
+    const int t0 = sub * 32 + lane;               // first float4 of this thread
+    const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(live ? row : 0) * D);
     float4 v[V4];
 #pragma unroll
     for (int j = 0; j < V4; ++j) {
-        const int i = lane + 32 * j;
-        v[j] = i < n4 ? xr[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int i = t0 + 32 * WPR * j;
+        v[j] = (live && i < n4) ? xr[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    float s = 0.f;
+    const int bt = (live ? row : 0) / rpb;
+    float4 sc4[kPre ? V4 : 1], sh4[kPre ? V4 : 1];
+    if constexpr (kPre) {
 #pragma unroll
-    for (int j = 0; j < V4; ++j) s += (v[j].x + v[j].y) + (v[j].z + v[j].w);
-    const float mean = warp_sum(s) / static_cast<float>(D);
+        for (int j = 0; j < V4; ++j) {
+            const int i = t0 + 32 * WPR * j;
+            sc4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            sh4[j] = sc4[j];
+            if (live && i < n4 && scale) {
+                sc4[j] = *reinterpret_cast<const float4*>(scale + static_cast<size_t>(bt) * mod_ld + i * 4);
+                sh4[j] = *reinterpret_cast<const float4*>(shift + static_cast<size_t>(bt) * mod_ld + i * 4);
+            }
+        }
+    }
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < V4; ++j) sum += (v[j].x + v[j].y) + (v[j].z + v[j].w);
+    sum = warp_sum(sum);
+    if constexpr (WPR > 1) {
+        if (lane == 0) red[0][warp] = sum;
+        __syncthreads();
+        sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < WPR; ++k) sum += red[0][warp - sub + k];
+    }
+    const float mean = sum / static_cast<float>(D);
     float q = 0.f;
 #pragma unroll
     for (int j = 0; j < V4; ++j) {
-        if (lane + 32 * j < n4) {
+        if (t0 + 32 * WPR * j < n4) {
             const float a = v[j].x - mean, bb = v[j].y - mean, c = v[j].z - mean, d = v[j].w - mean;
             q += (a * a + bb * bb) + (c * c + d * d);
         }
     }
-    const float var = warp_sum(q) / static_cast<float>(D);
+    q = warp_sum(q);
+    if constexpr (WPR > 1) {
+        if (lane == 0) red[1][warp] = q;
+        __syncthreads();
+        q = 0.f;
+#pragma unroll
+        for (int k = 0; k < WPR; ++k) q += red[1][warp - sub + k];
+    }
+    if (!live) return;
+    const float var = q / static_cast<float>(D);
     const float rstd = rsqrtf(var + eps);
-    const int bt = row / rpb;
     uint2* orow = reinterpret_cast<uint2*>(out + static_cast<size_t>(row) * D);
 #pragma unroll
     for (int j = 0; j < V4; ++j) {
-        const int i = lane + 32 * j;
-        if (i >= n4) break;
+        const int i = t0 + 32 * WPR * j;
+        if (i >= n4) continue;
         float y0 = (v[j].x - mean) * rstd, y1 = (v[j].y - mean) * rstd;
         float y2 = (v[j].z - mean) * rstd, y3 = (v[j].w - mean) * rstd;
         const int d = i * 4;
         if (scale) {
-            const float4 sc = *reinterpret_cast<const float4*>(scale + static_cast<size_t>(bt) * mod_ld + d);
-            const float4 sh = *reinterpret_cast<const float4*>(shift + static_cast<size_t>(bt) * mod_ld + d);
+            float4 sc, sh;
+            if constexpr (kPre) {
+                sc = sc4[j];
+                sh = sh4[j];
+            } else {
+                sc = *reinterpret_cast<const float4*>(scale + static_cast<size_t>(bt) * mod_ld + d);
+                sh = *reinterpret_cast<const float4*>(shift + static_cast<size_t>(bt) * mod_ld + d);
+            }
             y0 = y0 * (1.f + sc.x) + sh.x;
             y1 = y1 * (1.f + sc.y) + sh.y;
             y2 = y2 * (1.f + sc.z) + sh.z;
@@ -155,76 +198,84 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(__nv_bfloat16* __restrict_
 }
 
 // m[b, n] = sum_i SiLU(c[b, i]) W[n, i] + bias[n].
-// SiLU(c) is computed once per CTA into shared memory (fp32, up to 8 batch
-// rows x 1024 columns per pass); each warp owns ADALN_ROWS output rows and
-// issues all of its 16-byte W loads for a column chunk before the FMAs, so
-// enough bytes are in flight to stream W (a third of a DiT block) at HBM rate.
-constexpr int ADALN_ROWS = 2;
-constexpr int ADALN_CCHUNK = 1024;
-constexpr int ADALN_BCHUNK = 8;
+// SiLU(c) of up to BC batch rows x ADALN_CCH columns is computed once per CTA
+// into shared memory; each warp owns ROWS consecutive output rows and, per
+// step, issues ROWS x ADALN_U 16-byte W loads (streaming, evict-first) before
+// their FMAs, so the bytes in flight stream W (a third of a DiT block) at HBM
+// rate.  ROWS is chosen on the host so that the whole grid is resident at
+// once (one wave).
+constexpr int ADALN_CCH = 2048;   // columns of SiLU(c) held in shared memory
+constexpr int ADALN_U = 3;        // 256-column steps unrolled per iteration
 
+template <int BC, int ROWS>
 __global__ void __launch_bounds__(256) adaln_kernel(const __nv_bfloat16* __restrict__ c, int B,
                                                     int C, const __nv_bfloat16* __restrict__ W,
                                                     const __nv_bfloat16* __restrict__ bias,
                                                     int N, float* __restrict__ m) {
     pdl_wait();
     pdl_launch_dependents();
-    __shared__ float sc[ADALN_BCHUNK * ADALN_CCHUNK];
+    extern __shared__ float sc[];   // [BC][ADALN_CCH]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = (blockIdx.x * 8 + warp) * ADALN_ROWS;
-    for (int b0 = 0; b0 < B; b0 += ADALN_BCHUNK) {
-        const int nb = min(ADALN_BCHUNK, B - b0);
-        float acc[ADALN_ROWS][ADALN_BCHUNK];
+    const int n0 = (blockIdx.x * 8 + warp) * ROWS;
+    for (int b0 = 0; b0 < B; b0 += BC) {
+        const int nb = min(BC, B - b0);
+        float acc[ROWS][BC];
 #pragma unroll
-        for (int r = 0; r < ADALN_ROWS; ++r)
+        for (int r = 0; r < ROWS; ++r)
 #pragma unroll
-            for (int j = 0; j < ADALN_BCHUNK; ++j) acc[r][j] = 0.f;
-        for (int c0 = 0; c0 < C; c0 += ADALN_CCHUNK) {
-            const int cn = min(ADALN_CCHUNK, C - c0);
+            for (int j = 0; j < BC; ++j) acc[r][j] = 0.f;
+        for (int c0 = 0; c0 < C; c0 += ADALN_CCH) {
+            const int cn = min(ADALN_CCH, C - c0);
             __syncthreads();
-            for (int i = threadIdx.x; i < nb * cn; i += blockDim.x) {
-                const int bb = i / cn, cc = i % cn;
-                const float v = __bfloat162float(c[static_cast<size_t>(b0 + bb) * C + c0 + cc]);
-                sc[bb * ADALN_CCHUNK + cc] = v / (1.f + __expf(-v));
-            }
-            __syncthreads();
-            const int n8 = cn >> 3;
-            // up to 4 uint4 per lane per row per chunk (1024 columns)
-            uint4 wv[ADALN_ROWS][4];
-#pragma unroll
-            for (int r = 0; r < ADALN_ROWS; ++r) {
-                const int n = n0 + r;
-                const uint4* wr = reinterpret_cast<const uint4*>(W + static_cast<size_t>(min(n, N - 1)) * C + c0);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int i = lane + 32 * k;
-                    wv[r][k] = (i < n8 && n < N) ? __ldcs(wr + i) : make_uint4(0, 0, 0, 0);
+            for (int i = threadIdx.x; i < BC * cn; i += blockDim.x) {
+                const int bb = i / cn, cc = i - bb * cn;
+                float v = 0.f;
+                if (bb < nb) {
+                    v = __bfloat162float(c[static_cast<size_t>(b0 + bb) * C + c0 + cc]);
+                    v = v / (1.f + __expf(-v));
                 }
+                sc[bb * ADALN_CCH + cc] = v;
             }
+            __syncthreads();
+            const int n8 = cn >> 3;   // 16-byte W chunks per row in this column chunk
+            for (int i0 = lane; i0 < n8; i0 += 32 * ADALN_U) {
+                uint4 wv[ADALN_U][ROWS];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int i = lane + 32 * k;
-                if (i >= n8) break;
+                for (int u = 0; u < ADALN_U; ++u) {
+                    const int i = i0 + 32 * u;
 #pragma unroll
-                for (int bb = 0; bb < ADALN_BCHUNK; ++bb) {
-                    if (bb >= nb) break;
-                    const float4 s0 = *reinterpret_cast<const float4*>(&sc[bb * ADALN_CCHUNK + i * 8]);
-                    const float4 s1 = *reinterpret_cast<const float4*>(&sc[bb * ADALN_CCHUNK + i * 8 + 4]);
+                    for (int r = 0; r < ROWS; ++r) {
+                        const int n = n0 + r;
+                        wv[u][r] = (i < n8 && n < N)
+                                       ? __ldcs(reinterpret_cast<const uint4*>(W + static_cast<size_t>(n) * C + c0) + i)
+                                       : make_uint4(0, 0, 0, 0);
+                    }
+                }
 #pragma unroll
-                    for (int r = 0; r < ADALN_ROWS; ++r) {
-                        const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wv[r][k]);
-                        const float2 w0 = __bfloat1622float2(wp[0]), w1 = __bfloat1622float2(wp[1]);
-                        const float2 w2 = __bfloat1622float2(wp[2]), w3 = __bfloat1622float2(wp[3]);
-                        acc[r][bb] += s0.x * w0.x + s0.y * w0.y + s0.z * w1.x + s0.w * w1.y +
-                                      s1.x * w2.x + s1.y * w2.y + s1.z * w3.x + s1.w * w3.y;
+                for (int u = 0; u < ADALN_U; ++u) {
+                    const int i = i0 + 32 * u;
+                    if (i < n8) {
+#pragma unroll
+                        for (int bb = 0; bb < BC; ++bb) {
+                            const float4 s0 = *reinterpret_cast<const float4*>(&sc[bb * ADALN_CCH + i * 8]);
+                            const float4 s1 = *reinterpret_cast<const float4*>(&sc[bb * ADALN_CCH + i * 8 + 4]);
+#pragma unroll
+                            for (int r = 0; r < ROWS; ++r) {
+                                const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wv[u][r]);
+                                const float2 w0 = __bfloat1622float2(wp[0]), w1 = __bfloat1622float2(wp[1]);
+                                const float2 w2 = __bfloat1622float2(wp[2]), w3 = __bfloat1622float2(wp[3]);
+                                acc[r][bb] += s0.x * w0.x + s0.y * w0.y + s0.z * w1.x + s0.w * w1.y +
+                                              s1.x * w2.x + s1.y * w2.y + s1.z * w3.x + s1.w * w3.y;
+                            }
+                        }
                     }
                 }
             }
         }
 #pragma unroll
-        for (int r = 0; r < ADALN_ROWS; ++r) {
+        for (int r = 0; r < ROWS; ++r) {
 #pragma unroll
-            for (int bb = 0; bb < ADALN_BCHUNK; ++bb) {
+            for (int bb = 0; bb < BC; ++bb) {
                 const float v = warp_sum(acc[r][bb]);
                 const int n = n0 + r;
                 if (lane == 0 && bb < nb && n < N)
@@ -436,23 +487,60 @@ cudaError_t launch_layernorm(const float* x, int rows, int D, int rpb, const flo
                              const float* scale, int mod_ld, const void* w, const void* b,
                              float eps, void* out, cudaStream_t s, unsigned long long* launches) {
     if (rows <= 0) return cudaSuccess;
-    const unsigned g = blocks_for(static_cast<size_t>(rows) * 32, 256);
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 1;
+    }
+    // warps per row: enough row groups for ~32 warps per SM, at most 8;
+    // DLO_LN_WPR=1|2|4|8 forces it (tuning)
+    static int forced = -1;
+    if (forced < 0) {
+        const char* e = std::getenv("DLO_LN_WPR");
+        forced = e ? std::atoi(e) : 0;
+    }
+    const long long want = 32LL * sms;
+    const int n4 = D / 4;
+    int wpr = 1;
+    while (wpr < 8 && 1LL * rows * wpr < want) wpr *= 2;
+    // wide rows: at most 20 float4 per thread (registers decide occupancy)
+    while (wpr < 8 && (n4 + 32 * wpr - 1) / (32 * wpr) > 20) wpr *= 2;
+    if (forced == 1 || forced == 2 || forced == 4 || forced == 8) wpr = forced;
+    if ((n4 + 32 * wpr - 1) / (32 * wpr) > (wpr == 1 ? 40 : 20)) return cudaErrorInvalidValue;
+    const int v4 = (n4 + 32 * wpr - 1) / (32 * wpr);   // float4 per thread
+    const unsigned g = static_cast<unsigned>((rows + 8 / wpr - 1) / (8 / wpr));
     const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w);
     const __nv_bfloat16* bb = static_cast<const __nv_bfloat16*>(b);
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
-    const int v4 = (D / 4 + 31) / 32;   // float4 per lane
-    cudaError_t le_ = cudaSuccess;
-#define DLO_LN(V) \
-    le_ = launch_k(layernorm_kernel<V>, g, 256, 0, s, x, rows, D, rpb, shift, scale, mod_ld, wb, bb, eps, o)
-    if (v4 <= 2) DLO_LN(2);
-    else if (v4 <= 4) DLO_LN(4);
-    else if (v4 <= 8) DLO_LN(8);
-    else if (v4 <= 10) DLO_LN(10);
-    else if (v4 <= 16) DLO_LN(16);
-    else if (v4 <= 24) DLO_LN(24);
-    else if (v4 <= 32) DLO_LN(32);
-    else if (v4 <= 40) DLO_LN(40);
+    cudaError_t le_ = cudaErrorInvalidValue;
+#define DLO_LN(V, W) \
+    le_ = launch_k(layernorm_kernel<V, W>, g, 256, 0, s, x, rows, D, rpb, shift, scale, mod_ld, wb, bb, eps, o)
+    if (wpr == 1) {
+        if (v4 <= 2) DLO_LN(2, 1);
+        else if (v4 <= 4) DLO_LN(4, 1);
+        else if (v4 <= 8) DLO_LN(8, 1);
+        else if (v4 <= 10) DLO_LN(10, 1);
+        else if (v4 <= 16) DLO_LN(16, 1);
+        else if (v4 <= 24) DLO_LN(24, 1);
+        else if (v4 <= 32) DLO_LN(32, 1);
+        else if (v4 <= 40) DLO_LN(40, 1);
+        else return cudaErrorInvalidValue;
+    } else {
+#define DLO_LN_V(W)                   \
+    if (v4 <= 1) DLO_LN(1, W);        \
+    else if (v4 <= 2) DLO_LN(2, W);   \
+    else if (v4 <= 3) DLO_LN(3, W);   \
+    else if (v4 <= 5) DLO_LN(5, W);   \
+    else if (v4 <= 10) DLO_LN(10, W); \
+    else if (v4 <= 20) DLO_LN(20, W); \
     else return cudaErrorInvalidValue;
+        if (wpr == 2) { DLO_LN_V(2) }
+        else if (wpr == 4) { DLO_LN_V(4) }
+        else { DLO_LN_V(8) }
+#undef DLO_LN_V
+    }
 #undef DLO_LN
     ++*launches;
     return le_ != cudaSuccess ? le_ : cudaGetLastError();
@@ -480,9 +568,35 @@ cudaError_t launch_rmsnorm2(void* x, int rows, int D, int ld, int col0a, const v
 cudaError_t launch_adaln(const void* c, int B, int C, const void* W, const void* bias, int N,
                          float* m, cudaStream_t s, unsigned long long* launches) {
     if (N <= 0 || B <= 0) return cudaSuccess;
-    const unsigned g = static_cast<unsigned>((N + 8 * ADALN_ROWS - 1) / (8 * ADALN_ROWS));
-    cudaError_t le_ = launch_k(adaln_kernel, g, 256, 0, s, static_cast<const __nv_bfloat16*>(c), B, C, static_cast<const __nv_bfloat16*>(W),
-        static_cast<const __nv_bfloat16*>(bias), N, m);
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 1;
+    }
+    // rows per warp: the fewest that keep the grid within one wave of two
+    // 256-thread CTAs per SM
+    const long long warps = 2LL * sms * 8;
+    const int rows = N <= warps ? 1 : N <= 2 * warps ? 2 : N <= 3 * warps ? 3 : 4;
+    const unsigned g = static_cast<unsigned>((N + 8 * rows - 1) / (8 * rows));
+    const __nv_bfloat16* cb = static_cast<const __nv_bfloat16*>(c);
+    const __nv_bfloat16* Wb = static_cast<const __nv_bfloat16*>(W);
+    const __nv_bfloat16* bb = static_cast<const __nv_bfloat16*>(bias);
+    cudaError_t le_ = cudaSuccess;
+#define DLO_ADALN(BC, R)                                                                            \
+    le_ = launch_k(adaln_kernel<BC, R>, g, 256, (BC) * ADALN_CCH * sizeof(float), s, cb, B, C, Wb, bb, \
+                   N, m)
+#define DLO_ADALN_R(BC)           \
+    if (rows == 1) DLO_ADALN(BC, 1); \
+    else if (rows == 2) DLO_ADALN(BC, 2); \
+    else if (rows == 3) DLO_ADALN(BC, 3); \
+    else DLO_ADALN(BC, 4)
+    if (B <= 1) { DLO_ADALN_R(1); }
+    else if (B <= 2) { DLO_ADALN_R(2); }
+    else { DLO_ADALN_R(4); }
+#undef DLO_ADALN_R
+#undef DLO_ADALN
     ++*launches;
     return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }

@@ -96,10 +96,10 @@ def test_verify_slot_detects_wrong_block():
     st.close()
 
 
-def test_residency_invariance_bit_exact():
-    cfg = SMALL_DIT
+@pytest.mark.parametrize("cfg", [SMALL_DIT, SMALL_VID_W8A8], ids=lambda c: c.name)
+def test_residency_invariance_bit_exact(cfg):
     outs = []
-    for k in (0, 2, 4, 6):
+    for k in sorted({0, 2, cfg.n_blocks // 2 + 1, cfg.n_blocks}):
         st = H.make_stack(cfg)
         st.attach()
         st.set_resident(k)
@@ -265,3 +265,31 @@ def test_smaller_batch_and_tokens_than_the_maximum():
     ref = H.oracle_forward(small, x, cond, ctx, H.oracle_blocks(cfg))
     assert H.rel_l2(out.float().cpu().numpy(), ref) <= 2e-2
     st.close()
+
+
+def _stack_output_digest(env_pdl: str) -> str:
+    """sha256 of one small video stack's output, computed in a fresh process
+    with DLO_PDL set as given (the switch is read once per process)."""
+    import os
+    import subprocess
+    import sys
+    code = (
+        "import hashlib, torch, synth\n"
+        "from tests import helpers as H\n"
+        "cfg = synth.StackConfig('pdl', synth.KIND_VIDEO, 3, 256, 2, 128, 512, 2, 300,"
+        " text_dim=192, text_tokens=77)\n"
+        "st = H.make_stack(cfg); st.attach()\n"
+        "x, c, t = H.device_inputs(cfg)\n"
+        "y = st.forward(x, c, t); torch.cuda.synchronize(); st.wait()\n"
+        "y = st.forward(y.clone(), c, t); torch.cuda.synchronize(); st.wait()\n"
+        "print(hashlib.sha256(y.view(torch.int16).cpu().numpy().tobytes()).hexdigest())\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, DLO_PDL=env_pdl, PYTHONPATH=root)
+    out = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
+                         text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    return out.stdout.strip().splitlines()[-1]
+
+
+def test_programmatic_dependent_launch_changes_no_bit():
+    assert _stack_output_digest("1") == _stack_output_digest("0")
