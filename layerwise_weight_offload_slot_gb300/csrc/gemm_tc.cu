@@ -92,32 +92,38 @@ __device__ __forceinline__ uint32_t sw128(int r, int j) {
     return static_cast<uint32_t>(r * 128 + ((j ^ (r & 7)) << 4));
 }
 
-// Scale (per 16-column segment) and bias of a chunk of CW columns.
-template <int CW>
-__device__ __forceinline__ void scale_bias(const EpiArgs& a, int col0, float (&v)[CW]) {
-    if (a.scales) {
-        const float sa = a.act_scale ? *a.act_scale : 1.0f;
+// Scale (per 16-column segment) and bias of a 32-column chunk, loaded before
+// the chunk's accumulator so their global-load latency overlaps the TMEM load.
+struct EpiBS {
+    float s[2];   // scale of each 16-column half
+    uint4 b[4];   // bias, 8 bf16 per vector (zero without bias)
+};
+
+__device__ __forceinline__ void epi_load(const EpiArgs& a, float sa, int col0, EpiBS& e) {
 #pragma unroll
-        for (int g = 0; g < CW / 16; ++g) {
-            const int c = col0 + 16 * g;
-            const float s = c < a.N ? a.scales[c / a.scale_seg] * sa : 0.f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[16 * g + i] *= s;
-        }
+    for (int g = 0; g < 2; ++g) {
+        const int c = col0 + 16 * g;
+        e.s[g] = a.scales ? (c < a.N ? a.scales[c / a.scale_seg] * sa : 0.f) : 1.f;
     }
-    if (a.bias) {
 #pragma unroll
-        for (int q = 0; q < CW / 8; ++q) {
-            if (col0 + 8 * q < a.N) {
-                const uint4 bv = *reinterpret_cast<const uint4*>(a.bias + col0 + 8 * q);
-                const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv);
+    for (int q = 0; q < 4; ++q)
+        e.b[q] = (a.bias && col0 + 8 * q < a.N) ? *reinterpret_cast<const uint4*>(a.bias + col0 + 8 * q)
+                                                 : make_uint4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ void epi_apply(const EpiBS& e, float (&v)[32]) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 f = __bfloat1622float2(b2[j]);
-                    v[q * 8 + 2 * j] += f.x;
-                    v[q * 8 + 2 * j + 1] += f.y;
-                }
-            }
+    for (int g = 0; g < 2; ++g)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[16 * g + i] *= e.s[g];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&e.b[q]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(b2[j]);
+            v[q * 8 + 2 * j] += f.x;
+            v[q * 8 + 2 * j + 1] += f.y;
         }
     }
 }
@@ -330,6 +336,7 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
             const uint32_t aph = (t >> 1) & 1;
             int mb, nb;
             tile_coords(tile, args.num_m, args.num_n, args.n_major, mb, nb);
+            const float sa = (args.scales && args.act_scale) ? *args.act_scale : 1.0f;
             bool ok = mbar_wait(bar_tfull + acc * 8, aph, abort_flag);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) {
@@ -353,24 +360,27 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
                     for (int c0 = 0; c0 < BN; c0 += 32) {
                         const int col0 = nb * BN + c0;
                         if (col0 >= args.N) break;
+                        EpiBS e;
+                        epi_load(args, sa, col0, e);
+                        float4 gv[8];
+    #pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            gv[j] = (grow && col0 + 4 * j < args.N)
+                                        ? *reinterpret_cast<const float4*>(grow + col0 + 4 * j)
+                                        : make_float4(1.f, 1.f, 1.f, 1.f);
                         uint32_t r[32];
-                        tmem_ld_32x32b_x32(taddr + c0, r);
-                        tmem_wait_ld();
+                        tmem_ld_32x32b_x32_nc(taddr + c0, r);
+                        tmem_wait_ld_r(r);
                         float v[32];
     #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                        scale_bias<32>(args, col0, v);
-                        if (grow) {
+                        epi_apply(e, v);
     #pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                if (col0 + 4 * j < args.N) {
-                                    const float4 g = *reinterpret_cast<const float4*>(grow + col0 + 4 * j);
-                                    v[4 * j] *= g.x;
-                                    v[4 * j + 1] *= g.y;
-                                    v[4 * j + 2] *= g.z;
-                                    v[4 * j + 3] *= g.w;
-                                }
-                            }
+                        for (int j = 0; j < 8; ++j) {
+                            v[4 * j] *= gv[j].x;
+                            v[4 * j + 1] *= gv[j].y;
+                            v[4 * j + 2] *= gv[j].z;
+                            v[4 * j + 3] *= gv[j].w;
                         }
                         if (lane == 0) bulk_wait_read<1>();
                         __syncwarp();
@@ -397,15 +407,18 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
                         if (lane == 0) bulk_wait_read<1>();
                         __syncwarp();
                         uint8_t* box = stg0p + bi * STG_BYTES;
-    #pragma unroll 1
+                        EpiBS e2[2];
+                        epi_load(args, sa, col0, e2[0]);
+                        epi_load(args, sa, col0 + 32, e2[1]);
+    #pragma unroll
                         for (int half = 0; half < 2; ++half) {
                             uint32_t r[32];
-                            tmem_ld_32x32b_x32(taddr + c0 + 32 * half, r);
-                            tmem_wait_ld();
+                            tmem_ld_32x32b_x32_nc(taddr + c0 + 32 * half, r);
+                            tmem_wait_ld_r(r);
                             float v[32];
     #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                            scale_bias<32>(args, col0 + 32 * half, v);
+                            epi_apply(e2[half], v);
                             if (args.epi == DLO_EPI_GELU) {
     #pragma unroll
                                 for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
