@@ -291,7 +291,8 @@ dlo_status dlo_set_resident(dlo_ctx* ctx, int k, void* const* device_blocks);
  *   ctx W_k^T + b_k), v = ctx W_v^T + b_v, x += o; FFN as DiT with gate2.
  * The hidden state is carried in fp32 between kernels; x_out is its bf16
  * rounding.  Device-side bounded waits that run out are reported by the next
- * dlo_wait / dlo_forward_host / dlo_get_stats as DLO_ETIMEDOUT. */
+ * dlo_wait / dlo_forward_host as DLO_ETIMEDOUT (dlo_stats.device_error keeps
+ * the word read). */
 dlo_status dlo_forward(dlo_ctx* ctx, const void* x_in, const void* cond, const void* ctx_tokens,
                        int batch, int tokens, int text_tokens, void* x_out);
 
@@ -420,6 +421,19 @@ dlo_status dlo_op_gemm(const void* A, const void* W, int w_dtype, const float* s
                        int scale_seg, const void* bias, int M, int N, int K, int epilogue,
                        void* out, int ldo, const float* gate, int gate_ld, int rows_per_batch,
                        int* err, void* stream);
+
+/* Time-out path of the kernels' bounded waits, without a fault ([DLO]
+ * Failure and lifecycle boundaries: a failure is reported, not hidden, and
+ * leaves the process usable).  One thread waits on an mbarrier that nothing
+ * completes; after the library's wait limit (2 s) it writes 1 to *err (a
+ * device int) and the kernel exits normally, as every kernel of this library
+ * does when one of its waits runs out.  For tests. */
+dlo_status dlo_op_wait_selftest(int* err, void* stream);
+
+/* Enqueue the same waiting kernel on ctx's compute stream with ctx's error
+ * word, so the next dlo_wait / dlo_forward_host reports DLO_ETIMEDOUT (and
+ * clears the word; the context stays usable).  For tests. */
+dlo_status dlo_debug_device_timeout(dlo_ctx* ctx);
 
 /* Dynamic per-tensor E4M3 quantisation of an activation (DLO_W_E4M3_A8):
  * x bf16 [rows, cols] with row stride ld (elements); q receives E4M3 codes

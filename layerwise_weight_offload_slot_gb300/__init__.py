@@ -124,6 +124,8 @@ _c = {
                          _vp, _int, _vp, _int, _int, _vp, _vp),
     "dlo_op_gemm_noalloc": _decl("dlo_op_gemm_noalloc", _int, _vp, _vp, _int, _vp, _int, _vp, _int, _int,
                                  _int, _int, _vp, _int, _vp, _int, _int, _vp),
+    "dlo_op_wait_selftest": _decl("dlo_op_wait_selftest", _int, _vp, _vp),
+    "dlo_debug_device_timeout": _decl("dlo_debug_device_timeout", _int, _vp),
     "dlo_op_quantize_act": _decl("dlo_op_quantize_act", _int, _vp, _int, _int, _int, _vp, _vp, _vp, _vp),
     "dlo_op_gemm_w8a8": _decl("dlo_op_gemm_w8a8", _int, _vp, _vp, _vp, _vp, _int, _vp, _int, _int, _int,
                               _int, _vp, _int, _vp, _int, _int, _vp, _vp),
@@ -322,6 +324,14 @@ def dlo_op_gemm_noalloc(A, W, w_dtype, scales, scale_seg, bias, M, N, K, epilogu
                                    ldo, gate, gate_ld, rows_per_batch, stream)
     if st != OK:
         raise DloError(st, "dlo_op_gemm_noalloc rejected the call (see stderr)")
+
+
+def dlo_op_wait_selftest(err, stream) -> None:
+    _check(_c["dlo_op_wait_selftest"](err, stream))
+
+
+def dlo_debug_device_timeout(ctx: int) -> None:
+    _check(_c["dlo_debug_device_timeout"](ctx), ctx)
 
 
 def dlo_op_quantize_act(x, rows, cols, ld, q, scale, scratch, stream) -> None:

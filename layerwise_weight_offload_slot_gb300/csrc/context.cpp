@@ -1088,6 +1088,21 @@ dlo_status gemm_op(const void* A, const void* W, int w_dtype, const float* scale
                    int gate_ld, int rows_per_batch, int* err, void* stream, int a_dtype, const float* a_scale);
 }  // namespace
 
+extern "C" dlo_status dlo_op_wait_selftest(int* err, void* stream) {
+    if (!err || !aligned(err, 4)) return op_inval("err must be a 4-byte aligned device int");
+    return op_result(launch_wait_selftest(err, static_cast<cudaStream_t>(stream), &g_op_launches));
+}
+
+extern "C" dlo_status dlo_debug_device_timeout(dlo_ctx* c) {
+    if (!c) return DLO_EINVAL;
+    cudaSetDevice(c->device);
+    return c->timed(DLO_K_CONVERT, 0.0, 0.0, c->cs, [&] {
+               return launch_wait_selftest(c->err_word(), c->cs, &c->st.kernel_launches);
+           }) == cudaSuccess
+               ? DLO_OK
+               : c->fail(DLO_ECUDA, "launch of the wait self-test failed");
+}
+
 extern "C" dlo_status dlo_op_quantize_act(const void* x, int rows, int cols, int ld, void* q, float* scale,
                                           float* scratch, void* stream) {
     if (!x || !q || !scale || !scratch) return op_inval("NULL argument");

@@ -148,6 +148,9 @@ cudaError_t launch_f32_to_bf16(const float* in, void* out, size_t n, cudaStream_
                                unsigned long long* launches);
 cudaError_t launch_gather(void* dst, const void* src, size_t bytes, cudaStream_t s,
                           unsigned long long* launches);
+// One thread waits on an mbarrier nothing completes; when the bounded wait
+// runs out it sets *err = 1 (device) and the kernel exits.
+cudaError_t launch_wait_selftest(int* err, cudaStream_t s, unsigned long long* launches);
 // Dynamic per-tensor E4M3 quantisation of a bf16 [rows, cols] activation
 // (row stride ld, cols % 8 == 0, 16-B aligned rows) into contiguous codes q
 // [rows, cols] and the fp32 scale *scale (device); scratch holds

@@ -442,6 +442,21 @@ __global__ void __launch_bounds__(256) quant_e4m3_kernel(const __nv_bfloat16* __
     for (; i < n; i += stride) qo[i] = e4m3x8(*chunk_ptr(x, i, c8, ld, flat), inv);
 }
 
+// A wait that nothing completes: one thread waits (bounded, with the limit
+// every kernel of this library uses) on an mbarrier that never receives its
+// arrival, then records the time-out in the error word and exits -- the path
+// any kernel takes when one of its waits runs out, exercised without a fault.
+__global__ void wait_selftest_kernel(int* __restrict__ err) {
+    pdl_wait();
+    pdl_launch_dependents();
+    __shared__ __align__(8) unsigned long long bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    fence_mbar_init();
+    if (!mbar_wait(b, 0, nullptr)) atomicExch(err, 1);
+}
+
 __global__ void __launch_bounds__(1024) gather_kernel(uint4* __restrict__ dst,
                                                       const uint4* __restrict__ src, size_t n16) {
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
@@ -651,6 +666,12 @@ cudaError_t launch_quantize_e4m3(const void* x, int rows, int cols, int ld, void
     if (le_ == cudaSuccess)
         le_ = launch_k(quant_e4m3_kernel, g, 256, 0, s, xb, rows, c8, ld, scratch, g, static_cast<uint8_t*>(q), scale);
     *launches += 2;
+    return le_ != cudaSuccess ? le_ : cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(int* err, cudaStream_t s, unsigned long long* launches) {
+    cudaError_t le_ = launch_k(wait_selftest_kernel, 1, 32, 0, s, err);
+    ++*launches;
     return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
 

@@ -365,3 +365,28 @@ def test_gemm_w8a8_multiplies_every_code_pair_exactly():
                          dlo.EPI_RESIDUAL, out.data_ptr(), N, None, 0, K, None, stream())
     torch.cuda.synchronize()
     np.testing.assert_array_equal(out.cpu().numpy().astype(np.float64), fp8.decode_e4m3(Acodes[:, :N]))
+
+
+def test_bounded_wait_times_out_without_a_fault():
+    """A kernel whose mbarrier wait nothing completes gives up after the
+    library's limit, records it in the error word and exits; the context
+    stays usable."""
+    import time
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    dlo.dlo_op_wait_selftest(err.data_ptr(), stream())
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert int(err.item()) == 1
+    assert 1.5 < dt < 30.0
+    # the device still computes correctly afterwards
+    g = np.random.default_rng(3)
+    A = bf16(g.standard_normal((256, 128)))
+    W = bf16(g.standard_normal((64, 128)) * 0.05)
+    out = torch.empty((256, 64), dtype=torch.bfloat16, device="cuda")
+    err2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dlo.dlo_op_gemm(A.data_ptr(), W.data_ptr(), dlo.DT_BF16, None, 0, None, 256, 64, 128, dlo.EPI_BIAS,
+                    out.data_ptr(), 64, None, 0, 1, err2.data_ptr(), stream())
+    torch.cuda.synchronize()
+    assert int(err2.item()) == 0
+    assert rel(f64(out), f64(A) @ f64(W).T) < 6e-3

@@ -293,3 +293,20 @@ def _stack_output_digest(env_pdl: str) -> str:
 
 def test_programmatic_dependent_launch_changes_no_bit():
     assert _stack_output_digest("1") == _stack_output_digest("0")
+
+
+def test_device_wait_timeout_is_reported_and_the_context_survives():
+    cfg = synth.CFG_TINY
+    st = H.make_stack(cfg)
+    st.attach()
+    x, cond, ctx, out = run(st, cfg)
+    dlo.dlo_debug_device_timeout(st.ctx)
+    with pytest.raises(dlo.DloError) as e:
+        st.wait(30000)
+    assert e.value.status == dlo.ETIMEDOUT
+    assert st.stats()["device_error"] == 1
+    # the word was cleared; the next forward runs and matches the oracle
+    x, cond, ctx, out = run(st, cfg)
+    ref = H.oracle_forward(cfg, x, cond, ctx, H.oracle_blocks(cfg))
+    assert H.rel_l2(out.float().cpu().numpy(), ref) <= 2e-2
+    st.close()
