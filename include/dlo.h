@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define DLO_ABI_VERSION 2
+#define DLO_ABI_VERSION 3
 #define DLO_MAX_CONTAINERS 64   /* block containers of one stack (dlo_create_multi) */
 
 typedef int dlo_status;
@@ -357,6 +357,8 @@ typedef struct dlo_stats {
     double kclass_bytes[DLO_K_COUNT];
     unsigned long long kclass_launches[DLO_K_COUNT];
     unsigned long long h2d_copies;       /* host-to-device copy calls issued     */
+    unsigned long long graph_captures;   /* forwards captured as CUDA graphs     */
+    unsigned long long graph_launches;   /* forwards run as a CUDA graph launch  */
 } dlo_stats;
 
 /* kernel classes of dlo_stats.kclass_* */
@@ -387,6 +389,25 @@ dlo_status dlo_reset_log(dlo_ctx* ctx);
  * (copy, wait and compute intervals); 2 also an event pair around every
  * kernel launch (per-class stats).  Timing adds event records to the streams. */
 dlo_status dlo_set_timing(dlo_ctx* ctx, int on);
+
+/* Whole-forward CUDA graphs: 0 off (default), 1 on.  With graphs on and
+ * timing 0, dlo_forward / dlo_forward_multi / dlo_forward_host capture the
+ * forward's work on both streams (staging copies, event dependencies and
+ * every kernel, with their programmatic-launch edges) into a CUDA graph the
+ * first time they see a set of arguments (pointers, batch, tokens, text
+ * tokens) at a slot parity (which slot holds the first streamed block: the
+ * parity of the streamed executions so far), and launch that graph on later
+ * calls with the same arguments and parity -- up to four graphs per context
+ * (e.g. ping-pong input/output buffers at both parities), the least recently
+ * used one replaced by a new capture.  A context's first forward is always
+ * enqueued directly (kernels' one-time set-up stays outside captures).  Results, staging order, slot contents,
+ * log and counters are the same as without graphs; the graph's launch waits
+ * for all earlier work of both streams.  The pageable host mode and timing
+ * levels >= 1 enqueue directly.  If a capture fails, nothing of it has run:
+ * graphs are turned off for the context, the forward is enqueued directly
+ * and dlo_last_error keeps the reason.  Turning graphs off frees the
+ * captured graphs.  Not thread-safe with concurrent calls on one context. */
+dlo_status dlo_set_graphs(dlo_ctx* ctx, int on);
 
 /* Debug: wait for the copy that last wrote `slot`, copy the slot back and
  * compare it byte for byte with host block `block` (-1: the block the library

@@ -21,7 +21,7 @@ if not os.path.exists(LIB_PATH):
 
 _lib = ctypes.CDLL(LIB_PATH)
 
-ABI_VERSION = 2
+ABI_VERSION = 3
 K_COUNT = 16
 QUANT_SCRATCH = 1024
 OK, EINVAL, ESTATE, ENOMEM, ECUDA, EREGISTER, ETIMEDOUT, EUNSUPPORTED, EMISMATCH = \
@@ -71,7 +71,8 @@ class dlo_stats(ctypes.Structure):
                 ("kclass_ms", ctypes.c_double * K_COUNT), ("kclass_flops", ctypes.c_double * K_COUNT),
                 ("kclass_bytes", ctypes.c_double * K_COUNT),
                 ("kclass_launches", ctypes.c_ulonglong * K_COUNT),
-                ("h2d_copies", ctypes.c_ulonglong)]
+                ("h2d_copies", ctypes.c_ulonglong), ("graph_captures", ctypes.c_ulonglong),
+                ("graph_launches", ctypes.c_ulonglong)]
 
     def as_dict(self) -> dict:
         d = {}
@@ -118,6 +119,7 @@ _c = {
     "dlo_get_log": _decl("dlo_get_log", _int, _vp, _P(_int), _P(_int), _P(_int), _int, _P(_int)),
     "dlo_reset_log": _decl("dlo_reset_log", _int, _vp),
     "dlo_set_timing": _decl("dlo_set_timing", _int, _vp, _int),
+    "dlo_set_graphs": _decl("dlo_set_graphs", _int, _vp, _int),
     "dlo_verify_slot": _decl("dlo_verify_slot", _int, _vp, _int, _int),
     "dlo_debug_fail_register": _decl("dlo_debug_fail_register", None, _int),
     "dlo_op_gemm": _decl("dlo_op_gemm", _int, _vp, _vp, _int, _vp, _int, _vp, _int, _int, _int, _int,
@@ -296,6 +298,10 @@ def dlo_reset_log(ctx: int) -> None:
 
 def dlo_set_timing(ctx: int, level: int) -> None:
     _check(_c["dlo_set_timing"](ctx, int(level)), ctx)
+
+
+def dlo_set_graphs(ctx: int, on: bool) -> None:
+    _check(_c["dlo_set_graphs"](ctx, 1 if on else 0), ctx)
 
 
 def dlo_verify_slot(ctx: int, slot: int, block: int = -1) -> int:

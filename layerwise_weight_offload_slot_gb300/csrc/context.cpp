@@ -187,6 +187,40 @@ struct dlo_ctx {
     std::vector<cudaEvent_t> ev_pool;
     std::string err;
 
+    // Whole-forward CUDA graphs (dlo_set_graphs): executable graphs keyed by
+    // the forward's arguments and the parity of exec_counter at its start
+    // (the slot that holds the first streamed block), each with the host-side
+    // effects of that forward (counters, log entries, slot contents) that are
+    // replayed on each launch.  Up to kGraphs, least recently used replaced.
+    static constexpr int kGraphs = 4;
+    struct GraphRec {
+        cudaGraphExec_t exec = nullptr;
+        int par = 0;
+        unsigned long long last_use = 0;
+        const void* x_in = nullptr;
+        std::vector<const void*> conds;
+        const void* ctx = nullptr;
+        void* x_out = nullptr;
+        int B = 0, N = 0, L = 0;
+        unsigned long long d_stagings = 0, d_staged_bytes = 0, d_streamed = 0, d_launches = 0,
+                           d_h2d = 0, d_exec = 0;
+        std::vector<int> lk, lb, ls;
+        int slot_block_after[2] = {-1, -1};
+    };
+    int graphs = 0;
+    bool capturing = false;
+    bool cap_copy[2] = {false, false};    // copy_done[i] recorded inside the capture
+    bool cap_comp[2] = {false, false};    // compute_done[i] recorded inside the capture
+    GraphRec gr[kGraphs];
+    unsigned long long graph_uses = 0;
+    cudaEvent_t g_ev[2] = {nullptr, nullptr};
+    void drop_graphs() {
+        for (GraphRec& g : gr) {
+            if (g.exec) cudaGraphExecDestroy(g.exec);
+            g = GraphRec();
+        }
+    }
+
     dlo_status fail(dlo_status s, const char* fmt, ...) {
         char buf[512];
         va_list ap;
@@ -284,10 +318,11 @@ void fill_offsets(Container* k) {
     }
 }
 
-// Poll a stream until idle or the limit runs out.
+// Poll a stream until idle or the limit runs out: yielding between queries
+// for the first 20 ms (a step's result is noticed within microseconds), then
+// sleeping 50 us between them.
 bool stream_wait(cudaStream_t s, int timeout_ms, cudaError_t* e) {
     const auto t0 = std::chrono::steady_clock::now();
-    int spins = 0;
     for (;;) {
         cudaError_t q = cudaStreamQuery(s);
         if (q == cudaSuccess) return true;
@@ -295,12 +330,16 @@ bool stream_wait(cudaStream_t s, int timeout_ms, cudaError_t* e) {
             *e = q;
             return false;
         }
-        const auto el = std::chrono::steady_clock::now() - t0;
-        if (std::chrono::duration_cast<std::chrono::milliseconds>(el).count() > timeout_ms) {
+        const auto us = std::chrono::duration_cast<std::chrono::microseconds>(
+                            std::chrono::steady_clock::now() - t0).count();
+        if (us > static_cast<long long>(timeout_ms) * 1000) {
             *e = cudaErrorNotReady;
             return false;
         }
-        if (++spins > 64) std::this_thread::sleep_for(std::chrono::microseconds(50));
+        if (us < 20000)
+            std::this_thread::yield();
+        else
+            std::this_thread::sleep_for(std::chrono::microseconds(50));
     }
 }
 
@@ -810,6 +849,11 @@ namespace {
 
 // One forward over every container's blocks in order; conds[i] conditions
 // the blocks of container i.
+dlo_status enqueue_forward(dlo_ctx* c, const void* x_in, const void* const* conds, const void* ctx_tokens,
+                           int batch, int tokens, int text_tokens, void* x_out);
+dlo_status forward_graph(dlo_ctx* c, const void* x_in, const void* const* conds, const void* ctx_tokens,
+                         int batch, int tokens, int text_tokens, void* x_out);
+
 dlo_status forward_stack(dlo_ctx* c, const void* x_in, const void* const* conds, const void* ctx_tokens,
                          int batch, int tokens, int text_tokens, void* x_out) {
     if (c->state != kRegistered) return c->fail(DLO_ESTATE, "register host blocks first");
@@ -835,6 +879,29 @@ dlo_status forward_stack(dlo_ctx* c, const void* x_in, const void* const* conds,
     cudaSetDevice(c->device);
     dlo_status r = prime(c);
     if (r != DLO_OK) return r;
+    if (c->resident_pending) {
+        LCHECK(cudaStreamWaitEvent(c->cs, c->resident_ev, 0), "wait resident");
+        c->resident_pending = false;
+    }
+    // the first forward is enqueued directly: kernels' one-time set-up
+    // (attributes, tensor-map encoders) runs outside any capture
+    if (c->graphs && c->timing == 0 && !c->pageable && c->st.forwards > 0)
+        r = forward_graph(c, x_in, conds, ctx_tokens, batch, tokens, text_tokens, x_out);
+    else
+        r = enqueue_forward(c, x_in, conds, ctx_tokens, batch, tokens, text_tokens, x_out);
+    if (r == DLO_OK) ++c->st.forwards;
+    return r;
+}
+
+// The stream work of one forward on the compute and copy streams.  While a
+// graph is being captured, waits on events recorded before the capture are
+// left out: the graph's launch is ordered after all earlier work of both
+// streams (forward_graph).
+dlo_status enqueue_forward(dlo_ctx* c, const void* x_in, const void* const* conds, const void* ctx_tokens,
+                           int batch, int tokens, int text_tokens, void* x_out) {
+    const dlo_desc& d = c->d;
+    const bool bytes_kind = d.block_kind == DLO_BLOCK_BYTES;
+    dlo_status r = DLO_OK;
     const int n = d.n_blocks, k = c->k;
     const size_t nx = bytes_kind ? 0 : static_cast<size_t>(batch) * tokens * d.hidden;
     float* x = reinterpret_cast<float*>(c->wsp + c->ws.x);
@@ -844,10 +911,6 @@ dlo_status forward_stack(dlo_ctx* c, const void* x_in, const void* const* conds,
         LCHECK(c->timed(DLO_K_CONVERT, 0.0, 6.0 * nx, c->cs,
                         [&] { return launch_bf16_to_f32(x_in, x, nx, c->cs, &c->st.kernel_launches); }),
                "input conversion");
-    }
-    if (c->resident_pending) {
-        LCHECK(cudaStreamWaitEvent(c->cs, c->resident_ev, 0), "wait resident");
-        c->resident_pending = false;
     }
     for (int i = 0; i < k; ++i) {
         c->log(1, i, -1);
@@ -866,21 +929,25 @@ dlo_status forward_stack(dlo_ctx* c, const void* x_in, const void* const* conds,
             te.comp1 = c->get_event();
         }
         // prefetch the next block into the other slot once its last reader is done
-        LCHECK(cudaStreamWaitEvent(c->xs, c->compute_done[t], 0), "copy waits compute");
+        if (!c->capturing || c->cap_comp[t])
+            LCHECK(cudaStreamWaitEvent(c->xs, c->compute_done[t], 0), "copy waits compute");
         if (c->timing) LCHECK(cudaEventRecord(te.copy0, c->xs), "event");
         r = stage(c, nb, t);
         if (r != DLO_OK) return r;
         if (c->timing) LCHECK(cudaEventRecord(te.copy1, c->xs), "event");
         LCHECK(cudaEventRecord(c->copy_done[t], c->xs), "event record");
+        c->cap_copy[t] = c->capturing;
         // compute block i from slot s once its copy landed
         if (c->timing) LCHECK(cudaEventRecord(te.wait0, c->cs), "event");
-        LCHECK(cudaStreamWaitEvent(c->cs, c->copy_done[s], 0), "compute waits copy");
+        if (!c->capturing || c->cap_copy[s])
+            LCHECK(cudaStreamWaitEvent(c->cs, c->copy_done[s], 0), "compute waits copy");
         if (c->timing) LCHECK(cudaEventRecord(te.comp0, c->cs), "event");
         c->log(1, i, s);
         r = run_block(c, c->slot[s], batch, tokens, text_tokens, conds[c->cont_of[i]], ctx_tokens, i, x_out);
         if (r != DLO_OK) return r;
         if (c->timing) LCHECK(cudaEventRecord(te.comp1, c->cs), "event");
         LCHECK(cudaEventRecord(c->compute_done[s], c->cs), "event record");
+        c->cap_comp[s] = c->capturing;
         if (c->timing) c->timed_pending.push_back(te);
         ++c->exec_counter;
         ++c->st.streamed_execs;
@@ -890,7 +957,142 @@ dlo_status forward_stack(dlo_ctx* c, const void* x_in, const void* const* conds,
                         [&] { return launch_f32_to_bf16(x, x_out, nx, c->cs, &c->st.kernel_launches); }),
                "output conversion");
     }
-    ++c->st.forwards;
+    return DLO_OK;
+}
+
+// Host-side state a capture changes; restored when a capture fails (the
+// captured work never ran).
+struct HostSnap {
+    dlo_stats st;
+    size_t log_n, log_total;
+    unsigned long long exec;
+    int slot_block[2];
+};
+
+HostSnap snap(const dlo_ctx* c) {
+    return HostSnap{c->st, c->log_kind.size(), c->log_total, c->exec_counter,
+                    {c->slot_block[0], c->slot_block[1]}};
+}
+
+void restore(dlo_ctx* c, const HostSnap& h) {
+    c->st = h.st;
+    c->log_kind.resize(h.log_n);
+    c->log_block.resize(h.log_n);
+    c->log_slot.resize(h.log_n);
+    c->log_total = h.log_total;
+    c->exec_counter = h.exec;
+    c->slot_block[0] = h.slot_block[0];
+    c->slot_block[1] = h.slot_block[1];
+}
+
+// One forward as a CUDA graph: captured on first use for these arguments and
+// this slot parity, then launched.  All earlier copy-stream work is joined
+// into the compute stream before the launch; after it, the slot events are
+// re-recorded on the compute stream so direct forwards and dlo_verify_slot
+// see the graph's copies and computes as done.
+dlo_status forward_graph(dlo_ctx* c, const void* x_in, const void* const* conds, const void* ctx_tokens,
+                         int batch, int tokens, int text_tokens, void* x_out) {
+    for (int i = 0; i < 2; ++i)
+        if (!c->g_ev[i]) LCHECK(cudaEventCreateWithFlags(&c->g_ev[i], cudaEventDisableTiming), "event create");
+    const size_t nc = c->conts.size();
+    const int par = static_cast<int>(c->exec_counter & 1);
+    dlo_ctx::GraphRec* found = nullptr;
+    dlo_ctx::GraphRec* victim = nullptr;    // the first free entry, else the least recently used
+    for (dlo_ctx::GraphRec& r : c->gr) {
+        if (r.exec && r.par == par && r.x_in == x_in && r.ctx == ctx_tokens && r.x_out == x_out &&
+            r.B == batch && r.N == tokens && r.L == text_tokens &&
+            std::equal(r.conds.begin(), r.conds.end(), conds, conds + nc)) {
+            found = &r;
+            break;
+        }
+        if (!r.exec) {
+            if (!victim || victim->exec) victim = &r;
+        } else if (!victim || (victim->exec && r.last_use < victim->last_use)) {
+            victim = &r;
+        }
+    }
+    const bool hit = found != nullptr;
+    dlo_ctx::GraphRec& g = hit ? *found : *victim;
+    g.last_use = ++c->graph_uses;
+    LCHECK(cudaEventRecord(c->g_ev[0], c->xs), "event record");
+    LCHECK(cudaStreamWaitEvent(c->cs, c->g_ev[0], 0), "join copy stream");
+    if (hit) {
+        LCHECK(cudaGraphLaunch(g.exec, c->cs), "graph launch");
+        c->st.stagings += g.d_stagings;
+        c->st.staged_bytes += g.d_staged_bytes;
+        c->st.streamed_execs += g.d_streamed;
+        c->st.kernel_launches += g.d_launches;
+        c->st.h2d_copies += g.d_h2d;
+        c->exec_counter += g.d_exec;
+        for (size_t i = 0; i < g.lk.size(); ++i) c->log(g.lk[i], g.lb[i], g.ls[i]);
+        c->slot_block[0] = g.slot_block_after[0];
+        c->slot_block[1] = g.slot_block_after[1];
+        ++c->st.graph_launches;
+    } else {
+        if (g.exec) cudaGraphExecDestroy(g.exec);
+        g = dlo_ctx::GraphRec();
+        g.last_use = c->graph_uses;
+        g.par = par;
+        const HostSnap h0 = snap(c);
+        cudaError_t e = cudaStreamBeginCapture(c->cs, cudaStreamCaptureModeThreadLocal);
+        if (e != cudaSuccess) return c->cuda_fail(e, "begin capture");
+        c->capturing = true;
+        c->cap_copy[0] = c->cap_copy[1] = c->cap_comp[0] = c->cap_comp[1] = false;
+        // the copy stream joins the capture, and is joined back at its end
+        e = cudaEventRecord(c->g_ev[1], c->cs);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(c->xs, c->g_ev[1], 0);
+        dlo_status r = DLO_OK;
+        if (e == cudaSuccess) {
+            r = enqueue_forward(c, x_in, conds, ctx_tokens, batch, tokens, text_tokens, x_out);
+            if (r == DLO_OK) {
+                e = cudaEventRecord(c->g_ev[1], c->xs);
+                if (e == cudaSuccess) e = cudaStreamWaitEvent(c->cs, c->g_ev[1], 0);
+            }
+        }
+        c->capturing = false;
+        cudaGraph_t graph = nullptr;
+        const cudaError_t ee = cudaStreamEndCapture(c->cs, &graph);
+        if (e == cudaSuccess) e = ee;
+        cudaGraphExec_t exec = nullptr;
+        if (r == DLO_OK && e == cudaSuccess) e = cudaGraphInstantiate(&exec, graph, 0);
+        if (graph) cudaGraphDestroy(graph);
+        if (r != DLO_OK || e != cudaSuccess) {
+            // nothing captured ran: undo its host-side effects, turn graphs
+            // off for this context and enqueue the forward directly
+            cudaGetLastError();
+            restore(c, h0);
+            if (r == DLO_OK) c->cuda_fail(e, "graph capture failed; graphs turned off");
+            c->graphs = 0;
+            c->drop_graphs();
+            return enqueue_forward(c, x_in, conds, ctx_tokens, batch, tokens, text_tokens, x_out);
+        }
+        g.exec = exec;
+        g.x_in = x_in;
+        g.conds.assign(conds, conds + nc);
+        g.ctx = ctx_tokens;
+        g.x_out = x_out;
+        g.B = batch;
+        g.N = tokens;
+        g.L = text_tokens;
+        g.d_stagings = c->st.stagings - h0.st.stagings;
+        g.d_staged_bytes = c->st.staged_bytes - h0.st.staged_bytes;
+        g.d_streamed = c->st.streamed_execs - h0.st.streamed_execs;
+        g.d_launches = c->st.kernel_launches - h0.st.kernel_launches;
+        g.d_h2d = c->st.h2d_copies - h0.st.h2d_copies;
+        g.d_exec = c->exec_counter - h0.exec;
+        g.lk.assign(c->log_kind.begin() + h0.log_n, c->log_kind.end());
+        g.lb.assign(c->log_block.begin() + h0.log_n, c->log_block.end());
+        g.ls.assign(c->log_slot.begin() + h0.log_n, c->log_slot.end());
+        g.slot_block_after[0] = c->slot_block[0];
+        g.slot_block_after[1] = c->slot_block[1];
+        ++c->st.graph_captures;
+        LCHECK(cudaGraphLaunch(g.exec, c->cs), "graph launch");
+        ++c->st.graph_launches;
+    }
+    for (int i = 0; i < 2; ++i) {
+        LCHECK(cudaEventRecord(c->copy_done[i], c->cs), "event record");
+        LCHECK(cudaEventRecord(c->compute_done[i], c->cs), "event record");
+    }
     return DLO_OK;
 }
 
@@ -992,6 +1194,9 @@ extern "C" dlo_status dlo_destroy(dlo_ctx* c) {
         if (c->compute_done[i]) cudaEventDestroy(c->compute_done[i]);
     }
     if (c->resident_ev) cudaEventDestroy(c->resident_ev);
+    c->drop_graphs();
+    for (int i = 0; i < 2; ++i)
+        if (c->g_ev[i]) cudaEventDestroy(c->g_ev[i]);
     for (auto& t : c->timed_pending)
         for (cudaEvent_t ev : {t.copy0, t.copy1, t.wait0, t.comp0, t.comp1}) cudaEventDestroy(ev);
     for (auto& t : c->kernels_pending) {
@@ -1038,6 +1243,15 @@ extern "C" dlo_status dlo_reset_log(dlo_ctx* c) {
     c->log_block.clear();
     c->log_slot.clear();
     c->log_total = 0;
+    return DLO_OK;
+}
+
+extern "C" dlo_status dlo_set_graphs(dlo_ctx* c, int on) {
+    if (!c) return DLO_EINVAL;
+    if (on != 0 && on != 1) return c->fail(DLO_EINVAL, "graphs must be 0 or 1");
+    cudaSetDevice(c->device);
+    if (!on) c->drop_graphs();
+    c->graphs = on;
     return DLO_OK;
 }
 

@@ -19,7 +19,7 @@ from . import (BLOCK_BYTES, BLOCK_DIT, BLOCK_VIDEO, HOST_PAGEABLE, HOST_PINNED, 
                dlo_block_bytes, dlo_block_layout, dlo_create, dlo_create_multi, dlo_destroy,
                dlo_forward, dlo_forward_host, dlo_forward_multi, dlo_get_log, dlo_get_stats,
                dlo_pack_block, dlo_register_host_blocks, dlo_reset_log, dlo_set_resident,
-               dlo_set_timing, dlo_verify_slot, dlo_wait, dlo_workspace_bytes,
+               dlo_set_graphs, dlo_set_timing, dlo_verify_slot, dlo_wait, dlo_workspace_bytes,
                dlo_workspace_bytes_multi, make_desc)
 
 PAGE = 4096
@@ -213,6 +213,9 @@ class OffloadStack:
 
     def set_timing(self, level: int) -> None:
         dlo_set_timing(self.ctx, level)
+
+    def set_graphs(self, on: bool) -> None:
+        dlo_set_graphs(self.ctx, on)
 
     def verify_slot(self, slot: int, block: int = -1) -> bool:
         return dlo_verify_slot(self.ctx, slot, block) == OK
