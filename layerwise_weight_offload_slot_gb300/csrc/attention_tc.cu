@@ -171,6 +171,17 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         constexpr uint32_t idesc_s = idesc_bf16_f32(TQ, TK);
         constexpr uint32_t idesc_o = idesc_bf16_f32(TQ, NB * 64, true);
         constexpr uint32_t idesc_ot = idesc_bf16_f32(TQ, 16, true);
+        // Descriptors formed once; a descriptor's start-address field holds
+        // (address >> 4) and shared addresses stay below 256 KB, so an offset
+        // within shared memory adds (offset >> 4).  Every instruction this
+        // thread spends between MMAs costs tensor throughput (N=128 MMAs are
+        // shorter than the issue path).
+        const uint64_t q_desc = sw128_kmajor_desc(sb + P::Q_OFF);
+        const uint64_t k_desc0 = sw128_kmajor_desc(sb + P::K_OFF);
+        const uint64_t v_desc0 = sw128_mnmajor_desc(sb + P::V_OFF, P::BLK);
+        const uint64_t qt_desc = sw32_desc(sb + P::Q_OFF + NB * P::BLK);
+        const uint64_t kt_desc0 = sw32_desc(sb + P::K_OFF + NB * P::BLK);
+        const uint64_t vt_desc0 = sw32_desc(sb + P::V_OFF + NB * P::BLK);
         bool ok = mbar_wait(q_full, 0, abort_flag);
         auto issue_s = [&](int j) -> bool {
             const int st = j % NS;                 // K stage
@@ -183,16 +194,13 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             if (!mbar_wait(k_full + 8 * st, ph, abort_flag)) return false;
             tc_fence_after();
             const uint32_t d = tmem + sbuf * TK;
-            const uint32_t kb = sb + P::K_OFF + st * P::TILE;
+            const uint32_t so = (st * P::TILE) >> 4;
 #pragma unroll
             for (int kk = 0; kk < NB * 4; ++kk) {
-                const uint32_t off = (kk >> 2) * P::BLK + (kk & 3) * 32;
-                tc_mma_f16(d, sw128_kmajor_desc(sb + P::Q_OFF + off), sw128_kmajor_desc(kb + off),
-                           idesc_s, kk > 0);
+                const uint32_t off = ((kk >> 2) * P::BLK + (kk & 3) * 32) >> 4;
+                tc_mma_f16(d, q_desc + off, k_desc0 + so + off, idesc_s, kk > 0);
             }
-            if constexpr (TAIL)
-                tc_mma_f16(d, sw32_desc(sb + P::Q_OFF + NB * P::BLK), sw32_desc(kb + NB * P::BLK),
-                           idesc_s, 1u);
+            if constexpr (TAIL) tc_mma_f16(d, qt_desc, kt_desc0 + so, idesc_s, 1u);
             tc_commit(s_full + 8 * sbuf);
             tc_commit(k_empty + 8 * st);
             return true;
@@ -204,15 +212,15 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             if (!mbar_wait(p_full, j & 1, abort_flag)) return false;
             if (!mbar_wait(v_full + 8 * st, ph, abort_flag)) return false;
             tc_fence_after();
-            const uint32_t vb = sb + P::V_OFF + st * P::TILE;
+            const uint32_t so = (st * P::TILE) >> 4;
 #pragma unroll
             for (int kk = 0; kk < TK / 16; ++kk) {
                 const uint32_t a = tmem + sbuf * TK + kk * 8;    // P_j: 16 keys = 8 columns
                 const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-                tc_mma_f16_ts(tmem + P::O_COL, a, sw128_mnmajor_desc(vb + kk * 2048, P::BLK), idesc_o, acc);
+                tc_mma_f16_ts(tmem + P::O_COL, a, v_desc0 + so + ((kk * 2048) >> 4), idesc_o, acc);
                 if constexpr (TAIL)
-                    tc_mma_f16_ts(tmem + P::O_COL + NB * 64, a, sw32_desc(vb + NB * P::BLK + kk * 512),
-                                  idesc_ot, acc);
+                    tc_mma_f16_ts(tmem + P::O_COL + NB * 64, a, vt_desc0 + so + ((kk * 512) >> 4), idesc_ot,
+                                  acc);
             }
             tc_commit(pv_done);
             tc_commit(v_empty + 8 * st);

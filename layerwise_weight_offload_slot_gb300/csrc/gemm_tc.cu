@@ -276,6 +276,15 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
         // ---------------- MMA issuer
         constexpr uint32_t idesc = A8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN);
         const uint32_t bar_ready = FP8 ? bar_conv : bar_full;
+        // Operand descriptors are formed once: a descriptor's start-address
+        // field holds (address >> 4) and shared addresses stay below 256 KB,
+        // so moving within shared memory adds (offset >> 4).  The issuing
+        // thread's instructions between MMAs cost tensor throughput for
+        // MMAs shorter than the issue path (N <= 192), so the stage loop
+        // only adds constants.
+        const uint64_t a_desc0 = sw128_kmajor_desc(sbase + P::A_OFF);
+        const uint64_t b_desc0 = sw128_kmajor_desc(sbase + P::B_OFF);
+        uint64_t a_desc = a_desc0, b_desc = b_desc0;
         int s = 0;
         uint32_t ph = 0;
         int t = 0;
@@ -296,14 +305,12 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a0 = sbase + P::A_OFF + s * P::A_STAGE;
-                const uint32_t b0 = sbase + P::B_OFF + s * P::B_TILE;
 #pragma unroll
                 for (int i = 0; i < MT; ++i) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {   // 4 x 32 bytes of K per stage
-                        const uint64_t ad = sw128_kmajor_desc(a0 + i * A_TILE + kk * 32);
-                        const uint64_t bd = sw128_kmajor_desc(b0 + kk * 32);
+                        const uint64_t ad = a_desc + ((i * A_TILE + kk * 32) >> 4);
+                        const uint64_t bd = b_desc + ((kk * 32) >> 4);
                         if constexpr (A8)
                             tc_mma_f8(d_tmem + i * BN, ad, bd, idesc, (kb | kk) != 0);
                         else
@@ -314,6 +321,11 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
                 if (++s == STAGES) {
                     s = 0;
                     ph ^= 1;
+                    a_desc = a_desc0;
+                    b_desc = b_desc0;
+                } else {
+                    a_desc += P::A_STAGE >> 4;
+                    b_desc += P::B_TILE >> 4;
                 }
             }
             if (ok) tc_commit(bar_tfull + acc * 8);
