@@ -7,7 +7,8 @@
 //
 // One CTA per (128 query rows, head, batch); 6 warps:
 //   warp 0      TMA: the Q tile once, then K_j and V_j tiles of 128 keys into
-//               2-stage rings (rows past a batch's end are zero-filled)
+//               one ring stage, both completing one barrier (the MMA issuer
+//               waits once per tile); rows past a batch's end are zero-filled
 //   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM S
 //               buffers (128 fp32 columns each), and O += P_j V_j into the TMEM
 //               O accumulator; issue order S_0, S_1, PV_0, S_2, PV_1, ... so the
@@ -53,7 +54,7 @@ struct AttnPlan {
     static constexpr int K_OFF = Q_OFF + TILE;              // STAGES stages
     static constexpr int V_OFF = K_OFF + STAGES * TILE;     // STAGES stages
     static constexpr int BAR_OFF = V_OFF + STAGES * TILE;
-    // q_full, k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[2], p_full,
+    // q_full, kv_full[3], k_empty[3], 3 spare, v_empty[3], s_full[2], p_full,
     // pv_done, drain
     static constexpr int NBARS = 1 + 12 + 2 + 3;
     static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
@@ -92,8 +93,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     const uint32_t sb = smem_u32(smem);
     const uint32_t bar = sb + P::BAR_OFF;
     const uint32_t q_full = bar;
-    const uint32_t k_full = bar + 8, k_empty = bar + 32;
-    const uint32_t v_full = bar + 56, v_empty = bar + 80;
+    const uint32_t kv_full = bar + 8, k_empty = bar + 32;
+    const uint32_t v_empty = bar + 80;
     const uint32_t s_full = bar + 104;
     const uint32_t p_full = bar + 120, pv_done = bar + 128, drain = bar + 136;
     constexpr int NS = P::STAGES;
@@ -107,9 +108,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         for (int i = 0; i < NS; ++i) {
-            mbar_init(k_full + 8 * i, 1);
+            mbar_init(kv_full + 8 * i, 1);
             mbar_init(k_empty + 8 * i, 1);
-            mbar_init(v_full + 8 * i, 1);
             mbar_init(v_empty + 8 * i, 1);
         }
         for (int i = 0; i < 2; ++i) mbar_init(s_full + 8 * i, 1);
@@ -141,30 +141,30 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer
         bool ok = true;
-        uint32_t issued_k = 0, issued_v = 0;      // stages with a load in flight
-        uint32_t par_k = 0, par_v = 0;            // parity of that load's phase
+        uint32_t issued = 0;      // stages with a load in flight
+        uint32_t par = 0;         // parity of that load's phase
         mbar_arrive_expect_tx(q_full, P::TILE);
         load_tile<NB, TAIL>(sb + P::Q_OFF, &maps.q, &maps.qt, h, qt * TQ, b, q_full);
         for (int j = 0; ok && j < ntiles; ++j) {
             const int st = j % NS;
             const uint32_t ph = (j / NS) & 1;
-            if (!mbar_wait(k_empty + 8 * st, ph ^ 1, abort_flag)) { fail(); ok = false; break; }
-            mbar_arrive_expect_tx(k_full + 8 * st, P::TILE);
-            load_tile<NB, TAIL>(sb + P::K_OFF + st * P::TILE, &maps.k, &maps.kt, h, j * TK, b, k_full + 8 * st);
-            issued_k |= 1u << st;
-            par_k = (par_k & ~(1u << st)) | (ph << st);
-            if (!mbar_wait(v_empty + 8 * st, ph ^ 1, abort_flag)) { fail(); ok = false; break; }
-            mbar_arrive_expect_tx(v_full + 8 * st, P::TILE);
-            load_tile<NB, TAIL>(sb + P::V_OFF + st * P::TILE, &maps.v, &maps.vt, h, j * TK, b, v_full + 8 * st);
-            issued_v |= 1u << st;
-            par_v = (par_v & ~(1u << st)) | (ph << st);
+            // the stage's K is free after S_{j-NS}, its V after PV_{j-NS}
+            if (!mbar_wait(k_empty + 8 * st, ph ^ 1, abort_flag) ||
+                !mbar_wait(v_empty + 8 * st, ph ^ 1, abort_flag)) {
+                fail();
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(kv_full + 8 * st, 2 * P::TILE);
+            load_tile<NB, TAIL>(sb + P::K_OFF + st * P::TILE, &maps.k, &maps.kt, h, j * TK, b, kv_full + 8 * st);
+            load_tile<NB, TAIL>(sb + P::V_OFF + st * P::TILE, &maps.v, &maps.vt, h, j * TK, b, kv_full + 8 * st);
+            issued |= 1u << st;
+            par = (par & ~(1u << st)) | (ph << st);
         }
         if (!ok || *abort_flag) {
             mbar_wait(q_full, 0, nullptr);
-            for (int i = 0; i < NS; ++i) {
-                if (issued_k & (1u << i)) mbar_wait(k_full + 8 * i, (par_k >> i) & 1u, nullptr);
-                if (issued_v & (1u << i)) mbar_wait(v_full + 8 * i, (par_v >> i) & 1u, nullptr);
-            }
+            for (int i = 0; i < NS; ++i)
+                if (issued & (1u << i)) mbar_wait(kv_full + 8 * i, (par >> i) & 1u, nullptr);
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             // finished with them before p_full(j-2), and PV_{j-2}, issued
             // earlier by this thread, reads P_{j-2} before this MMA writes
             // (MMAs of one thread execute in issue order)
-            if (!mbar_wait(k_full + 8 * st, ph, abort_flag)) return false;
+            if (!mbar_wait(kv_full + 8 * st, ph, abort_flag)) return false;
             tc_fence_after();
             const uint32_t d = tmem + sbuf * TK;
             const uint32_t so = (st * P::TILE) >> 4;
@@ -206,11 +206,9 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             return true;
         };
         auto issue_pv = [&](int j) -> bool {
-            const int st = j % NS;                 // V stage
-            const uint32_t ph = (j / NS) & 1;
+            const int st = j % NS;                 // V stage: landed with K_j (waited in issue_s)
             const int sbuf = j & 1;                // P lives in S buffer sbuf
             if (!mbar_wait(p_full, j & 1, abort_flag)) return false;
-            if (!mbar_wait(v_full + 8 * st, ph, abort_flag)) return false;
             tc_fence_after();
             const uint32_t so = (st * P::TILE) >> 4;
 #pragma unroll
