@@ -464,6 +464,7 @@ dlo_status run_block(dlo_ctx* c, const uint8_t* W, int B, int N, int L, const vo
         p.gate_ld = D6;
         p.rows_per_batch = rpb;
         p.err = c->err_word();
+        p.w_ready = true;   // weights live in a slot or resident buffer, never a kernel's output
         const double flops = 2.0 * M * Nn * K;
         const double bytes = 1.0 * M * K * (w8a8 ? 1 : 2) + 1.0 * Nn * K * wsize +
                              1.0 * M * Nn * (epi == DLO_EPI_RESIDUAL ? 8 : 2);
@@ -486,7 +487,7 @@ dlo_status run_block(dlo_ctx* c, const uint8_t* W, int B, int N, int L, const vo
     char* bigc = static_cast<char*>(big);
     if (d.block_kind == DLO_BLOCK_DIT) {
         LCHECK(c->timed(DLO_K_MODULATION, 2.0 * B * D6 * d.cond_dim, 2.0 * D6 * d.cond_dim, s,
-                        [&] { return launch_adaln(cond, B, d.cond_dim, W + o.ada_w, W + o.ada_b, D6, m, s, nl); }),
+                        [&] { return launch_adaln(cond, B, d.cond_dim, W + o.ada_w, W + o.ada_b, D6, m, s, nl, true); }),
                "adaLN");
         LCHECK(ln(m, m + D, nullptr, nullptr), "LN1");
         LCHECK(gemm(h, o.qkv_w, o.qkv_b, BN, 3 * D, D, DLO_EPI_BIAS, big, 3 * D, nullptr, N, 0, 3 * D), "qkv");

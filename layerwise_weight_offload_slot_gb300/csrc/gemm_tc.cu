@@ -61,6 +61,7 @@ struct EpiArgs {
     int* err;
     int num_m, num_n, num_tiles;
     int n_major;   // tile order: groups of N blocks sweep all M blocks (else the reverse)
+    int w_ready;   // W is not the preceding kernel's output (see GemmParams::w_ready)
 };
 
 // Grouped tile order: groups of 8 M-blocks sweep all N-blocks, so one
@@ -224,9 +225,14 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    pdl_wait();                 // predecessor's outputs complete and visible
-    pdl_launch_dependents();
     const int kblocks = (args.K + KS - 1) / KS;
+    // predecessor's outputs complete and visible; the producer waits after
+    // its weight prefetch when the weights are not a predecessor's output
+    const bool prefetch_w = args.w_ready && warp == 0 && lane == 0;
+    if (!prefetch_w) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
 
     auto fail = [&]() {
         *abort_flag = 1;
@@ -239,6 +245,29 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
         uint32_t ph = 0;
         bool ok = true;
         uint32_t issued = 0, last_par = 0;   // per-stage bit masks
+        auto load_w = [&](int st, int kb, int nb) {
+            if constexpr (FP8)
+                tma_load_2d(sbase + P::RAW_OFF + st * P::RAW_TILE, &tmB, kb * KS, nb * BN, bar_full + st * 8);
+            else
+                tma_load_2d(sbase + P::B_OFF + st * P::B_TILE, &tmB, kb * KS, nb * BN, bar_full + st * 8);
+        };
+        // weight tiles of the first tile's first stages (the stages start
+        // empty), before the programmatic-launch wait
+        int pre = 0;
+        if (prefetch_w) {
+            if (static_cast<int>(blockIdx.x) < args.num_tiles) {
+                int mb0, nb0;
+                tile_coords(blockIdx.x, args.num_m, args.num_n, args.n_major, mb0, nb0);
+                pre = kblocks < STAGES ? kblocks : STAGES;
+                for (int st = 0; st < pre; ++st) {
+                    mbar_arrive_expect_tx(bar_full + st * 8, P::TX);
+                    load_w(st, st, nb0);
+                    issued |= 1u << st;   // phase 0 (the drain on abort waits for it)
+                }
+            }
+            pdl_wait();
+            pdl_launch_dependents();
+        }
         for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
             int mb, nb;
             tile_coords(tile, args.num_m, args.num_n, args.n_major, mb, nb);
@@ -249,15 +278,13 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
                     break;
                 }
                 const uint32_t fb = bar_full + s * 8;
-                mbar_arrive_expect_tx(fb, P::TX);
+                const bool w_done = tile == static_cast<int>(blockIdx.x) && kb < pre;
+                if (!w_done) mbar_arrive_expect_tx(fb, P::TX);
 #pragma unroll
                 for (int i = 0; i < MT; ++i)
                     tma_load_2d(sbase + P::A_OFF + s * P::A_STAGE + i * A_TILE, &tmA, kb * KS,
                                 (mb * MT + i) * BM, fb);
-                if constexpr (FP8)
-                    tma_load_2d(sbase + P::RAW_OFF + s * P::RAW_TILE, &tmB, kb * KS, nb * BN, fb);
-                else
-                    tma_load_2d(sbase + P::B_OFF + s * P::B_TILE, &tmB, kb * KS, nb * BN, fb);
+                if (!w_done) load_w(s, kb, nb);
                 issued |= 1u << s;
                 last_par = (last_par & ~(1u << s)) | (ph << s);
                 if (++s == STAGES) {
@@ -578,6 +605,7 @@ cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* la
     a.gate = p.gate;
     a.gate_ld = p.gate_ld;
     a.rows_per_batch = p.rows_per_batch > 0 ? p.rows_per_batch : 1;
+    a.w_ready = p.w_ready ? 1 : 0;
     a.err = p.err;
     a.num_m = (p.M + MT * BM - 1) / (MT * BM);
     a.num_n = (p.N + BN - 1) / BN;

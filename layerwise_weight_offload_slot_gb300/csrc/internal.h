@@ -106,6 +106,11 @@ struct GemmParams {
     int gate_ld = 0;
     int rows_per_batch = 1;
     int* err = nullptr;
+    // W is not written by the kernel before this one in the stream (block
+    // weights staged, and waited for, before the block's first kernel): the
+    // producer then loads the first stages' weight tiles before the
+    // programmatic-launch wait, overlapping the predecessor's tail.
+    bool w_ready = false;
 };
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches);
 int gemm_num_sms();
@@ -138,8 +143,10 @@ cudaError_t launch_rmsnorm(void* x, int rows, int D, int ld, int col0, const voi
 cudaError_t launch_rmsnorm2(void* x, int rows, int D, int ld, int col0a, const void* wa,
                             int col0b, const void* wb, float eps, cudaStream_t s,
                             unsigned long long* launches);
+// w_ready: W is not written by the kernel before this one in the stream (the
+// first W loads may then start before the programmatic-launch wait).
 cudaError_t launch_adaln(const void* c, int B, int C, const void* W, const void* bias, int N,
-                         float* m, cudaStream_t s, unsigned long long* launches);
+                         float* m, cudaStream_t s, unsigned long long* launches, bool w_ready = false);
 cudaError_t launch_mod_add(const float* e, const void* table, int B, int n6d, float* m,
                            cudaStream_t s, unsigned long long* launches);
 cudaError_t launch_bf16_to_f32(const void* in, float* out, size_t n, cudaStream_t s,

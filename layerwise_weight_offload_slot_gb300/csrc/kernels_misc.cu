@@ -202,21 +202,44 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(__nv_bfloat16* __restrict_
 // into shared memory; each warp owns ROWS consecutive output rows and, per
 // step, issues ROWS x ADALN_U 16-byte W loads (streaming, evict-first) before
 // their FMAs, so the bytes in flight stream W (a third of a DiT block) at HBM
-// rate.  ROWS is chosen on the host so that the whole grid is resident at
-// once (one wave).
+// rate; 5 x 256 columns per step cover a 1152-wide conditioning in one step.
+// ROWS is chosen on the host so that the whole grid is resident at once (one
+// wave).  W_READY: W is not written by the preceding kernel in the stream
+// (block weights staged, and waited for, before the block's first kernel),
+// so the first step's W loads are issued before the programmatic-launch wait
+// and overlap the predecessor's tail; c and m are touched only after it.
 constexpr int ADALN_CCH = 2048;   // columns of SiLU(c) held in shared memory
-constexpr int ADALN_U = 3;        // 256-column steps unrolled per iteration
+constexpr int ADALN_U = 5;        // 256-column steps unrolled per iteration
 
-template <int BC, int ROWS>
+template <int ROWS>
+__device__ __forceinline__ void adaln_load_w(const __nv_bfloat16* __restrict__ W, int C, int N, int n0,
+                                             int c0, int n8, int i0, uint4 (&wv)[ADALN_U][ROWS]) {
+#pragma unroll
+    for (int u = 0; u < ADALN_U; ++u) {
+        const int i = i0 + 32 * u;
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            const int n = n0 + r;
+            wv[u][r] = (i < n8 && n < N)
+                           ? __ldcs(reinterpret_cast<const uint4*>(W + static_cast<size_t>(n) * C + c0) + i)
+                           : make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+template <int BC, int ROWS, bool W_READY>
 __global__ void __launch_bounds__(256) adaln_kernel(const __nv_bfloat16* __restrict__ c, int B,
                                                     int C, const __nv_bfloat16* __restrict__ W,
                                                     const __nv_bfloat16* __restrict__ bias,
                                                     int N, float* __restrict__ m) {
-    pdl_wait();
-    pdl_launch_dependents();
+    if (!W_READY) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
     extern __shared__ float sc[];   // [BC][ADALN_CCH]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = (blockIdx.x * 8 + warp) * ROWS;
+    bool waited = !W_READY;
     for (int b0 = 0; b0 < B; b0 += BC) {
         const int nb = min(BC, B - b0);
         float acc[ROWS][BC];
@@ -226,6 +249,14 @@ __global__ void __launch_bounds__(256) adaln_kernel(const __nv_bfloat16* __restr
             for (int j = 0; j < BC; ++j) acc[r][j] = 0.f;
         for (int c0 = 0; c0 < C; c0 += ADALN_CCH) {
             const int cn = min(ADALN_CCH, C - c0);
+            const int n8 = cn >> 3;   // 16-byte W chunks per row in this column chunk
+            uint4 wv[ADALN_U][ROWS];
+            adaln_load_w<ROWS>(W, C, N, n0, c0, n8, lane, wv);
+            if (!waited) {
+                pdl_wait();             // c may come from, and m is read by, neighbours
+                pdl_launch_dependents();
+                waited = true;
+            }
             __syncthreads();
             for (int i = threadIdx.x; i < BC * cn; i += blockDim.x) {
                 const int bb = i / cn, cc = i - bb * cn;
@@ -237,20 +268,8 @@ __global__ void __launch_bounds__(256) adaln_kernel(const __nv_bfloat16* __restr
                 sc[bb * ADALN_CCH + cc] = v;
             }
             __syncthreads();
-            const int n8 = cn >> 3;   // 16-byte W chunks per row in this column chunk
             for (int i0 = lane; i0 < n8; i0 += 32 * ADALN_U) {
-                uint4 wv[ADALN_U][ROWS];
-#pragma unroll
-                for (int u = 0; u < ADALN_U; ++u) {
-                    const int i = i0 + 32 * u;
-#pragma unroll
-                    for (int r = 0; r < ROWS; ++r) {
-                        const int n = n0 + r;
-                        wv[u][r] = (i < n8 && n < N)
-                                       ? __ldcs(reinterpret_cast<const uint4*>(W + static_cast<size_t>(n) * C + c0) + i)
-                                       : make_uint4(0, 0, 0, 0);
-                    }
-                }
+                if (i0 != lane) adaln_load_w<ROWS>(W, C, N, n0, c0, n8, i0, wv);
 #pragma unroll
                 for (int u = 0; u < ADALN_U; ++u) {
                     const int i = i0 + 32 * u;
@@ -271,6 +290,11 @@ __global__ void __launch_bounds__(256) adaln_kernel(const __nv_bfloat16* __restr
                     }
                 }
             }
+        }
+        if (!waited) {
+            pdl_wait();
+            pdl_launch_dependents();
+            waited = true;
         }
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) {
@@ -581,7 +605,7 @@ cudaError_t launch_rmsnorm2(void* x, int rows, int D, int ld, int col0a, const v
 }
 
 cudaError_t launch_adaln(const void* c, int B, int C, const void* W, const void* bias, int N,
-                         float* m, cudaStream_t s, unsigned long long* launches) {
+                         float* m, cudaStream_t s, unsigned long long* launches, bool w_ready) {
     if (N <= 0 || B <= 0) return cudaSuccess;
     static int sms = 0;
     if (!sms) {
@@ -600,8 +624,10 @@ cudaError_t launch_adaln(const void* c, int B, int C, const void* W, const void*
     const __nv_bfloat16* bb = static_cast<const __nv_bfloat16*>(bias);
     cudaError_t le_ = cudaSuccess;
 #define DLO_ADALN(BC, R)                                                                            \
-    le_ = launch_k(adaln_kernel<BC, R>, g, 256, (BC) * ADALN_CCH * sizeof(float), s, cb, B, C, Wb, bb, \
-                   N, m)
+    le_ = w_ready ? launch_k(adaln_kernel<BC, R, true>, g, 256, (BC) * ADALN_CCH * sizeof(float), s, cb, B, C, \
+                             Wb, bb, N, m)                                                            \
+                  : launch_k(adaln_kernel<BC, R, false>, g, 256, (BC) * ADALN_CCH * sizeof(float), s, cb, B, \
+                             C, Wb, bb, N, m)
 #define DLO_ADALN_R(BC)           \
     if (rows == 1) DLO_ADALN(BC, 1); \
     else if (rows == 2) DLO_ADALN(BC, 2); \
