@@ -6,8 +6,10 @@ the two device slots, the next step's input being this step's output.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--staging memcpy|gather] [--resident k]
-                    [--host pinned|register] [--no-cpu-baseline]
+                    [--host pinned|register] [--no-cpu-baseline] [--no-graphs]
+                    [--sweep | --ops]
 
+The timed forwards replay whole-forward CUDA graphs unless --no-graphs.
 Prints ONE JSON line (rank 0).  With N > 1 (torchrun) every rank runs an
 independent replica (the path has no exchange step) and `value` is the sum of
 the steps all ranks completed over the slowest rank's time.
