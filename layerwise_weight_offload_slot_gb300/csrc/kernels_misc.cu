@@ -208,10 +208,12 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(__nv_bfloat16* __restrict_
 // (block weights staged, and waited for, before the block's first kernel),
 // so the first step's W loads are issued before the programmatic-launch wait
 // and overlap the predecessor's tail; c and m are touched only after it.
+// Those early loads read L2 (.cg): the slot held other weights two blocks
+// ago and this SM's L1 may still hold lines of them.
 constexpr int ADALN_CCH = 2048;   // columns of SiLU(c) held in shared memory
 constexpr int ADALN_U = 5;        // 256-column steps unrolled per iteration
 
-template <int ROWS>
+template <int ROWS, bool L2ONLY>
 __device__ __forceinline__ void adaln_load_w(const __nv_bfloat16* __restrict__ W, int C, int N, int n0,
                                              int c0, int n8, int i0, uint4 (&wv)[ADALN_U][ROWS]) {
 #pragma unroll
@@ -220,9 +222,8 @@ __device__ __forceinline__ void adaln_load_w(const __nv_bfloat16* __restrict__ W
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) {
             const int n = n0 + r;
-            wv[u][r] = (i < n8 && n < N)
-                           ? __ldcs(reinterpret_cast<const uint4*>(W + static_cast<size_t>(n) * C + c0) + i)
-                           : make_uint4(0, 0, 0, 0);
+            const uint4* src = reinterpret_cast<const uint4*>(W + static_cast<size_t>(n) * C + c0) + i;
+            wv[u][r] = (i < n8 && n < N) ? (L2ONLY ? __ldcg(src) : __ldcs(src)) : make_uint4(0, 0, 0, 0);
         }
     }
 }
@@ -251,7 +252,10 @@ __global__ void __launch_bounds__(256) adaln_kernel(const __nv_bfloat16* __restr
             const int cn = min(ADALN_CCH, C - c0);
             const int n8 = cn >> 3;   // 16-byte W chunks per row in this column chunk
             uint4 wv[ADALN_U][ROWS];
-            adaln_load_w<ROWS>(W, C, N, n0, c0, n8, lane, wv);
+            if (!waited)
+                adaln_load_w<ROWS, true>(W, C, N, n0, c0, n8, lane, wv);
+            else
+                adaln_load_w<ROWS, false>(W, C, N, n0, c0, n8, lane, wv);
             if (!waited) {
                 pdl_wait();             // c may come from, and m is read by, neighbours
                 pdl_launch_dependents();
@@ -269,7 +273,7 @@ __global__ void __launch_bounds__(256) adaln_kernel(const __nv_bfloat16* __restr
             }
             __syncthreads();
             for (int i0 = lane; i0 < n8; i0 += 32 * ADALN_U) {
-                if (i0 != lane) adaln_load_w<ROWS>(W, C, N, n0, c0, n8, i0, wv);
+                if (i0 != lane) adaln_load_w<ROWS, false>(W, C, N, n0, c0, n8, i0, wv);
 #pragma unroll
                 for (int u = 0; u < ADALN_U; ++u) {
                     const int i = i0 + 32 * u;
