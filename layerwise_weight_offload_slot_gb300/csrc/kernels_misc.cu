@@ -36,8 +36,8 @@ __device__ __forceinline__ float bf(const __nv_bfloat16 v) { return __bfloat162f
 // WPR warps per row (a row group); each thread holds V4 float4 of the row in
 // registers, mean and variance come from the registers (two passes, warp
 // shuffles then shared memory across the row group), so HBM sees one read of
-// x and one write of the bf16 output.  Short stacks (few rows) use more
-// warps per row so that enough loads are in flight per SM.
+// x and one write of the bf16 output.  The launcher uses two warps per row,
+// more only for rows too wide for 20 float4 per thread.
 template <int V4, int WPR>
 __global__ void __launch_bounds__(256) layernorm_kernel(const float* __restrict__ x, int rows,
                                                         int D, int rpb,
@@ -530,25 +530,19 @@ cudaError_t launch_layernorm(const float* x, int rows, int D, int rpb, const flo
                              const float* scale, int mod_ld, const void* w, const void* b,
                              float eps, void* out, cudaStream_t s, unsigned long long* launches) {
     if (rows <= 0) return cudaSuccess;
-    static int sms = 0;
-    if (!sms) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (sms <= 0) sms = 1;
-    }
-    // warps per row: enough row groups for ~32 warps per SM, at most 8;
-    // DLO_LN_WPR=1|2|4|8 forces it (tuning)
+    // DLO_LN_WPR=1|2|4|8 forces the warps per row (tuning)
     static int forced = -1;
     if (forced < 0) {
         const char* e = std::getenv("DLO_LN_WPR");
         forced = e ? std::atoi(e) : 0;
     }
-    const long long want = 32LL * sms;
+    // Two warps per row, more only for rows wider than 20 float4 per thread
+    // (registers decide occupancy).  Measured on GB300, back to back: 2048 x
+    // 1152 rows take 6.9 us with two warps per row against 9.0 / 11.6 / 10.5
+    // with one / four / eight, 256 x 256 8.6 against 10.3-10.9, and 8192 or
+    // 32760 x 5120 are fastest at two as well.
     const int n4 = D / 4;
-    int wpr = 1;
-    while (wpr < 8 && 1LL * rows * wpr < want) wpr *= 2;
-    // wide rows: at most 20 float4 per thread (registers decide occupancy)
+    int wpr = 2;
     while (wpr < 8 && (n4 + 32 * wpr - 1) / (32 * wpr) > 20) wpr *= 2;
     if (forced == 1 || forced == 2 || forced == 4 || forced == 8) wpr = forced;
     if ((n4 + 32 * wpr - 1) / (32 * wpr) > (wpr == 1 ? 40 : 20)) return cudaErrorInvalidValue;
