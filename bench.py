@@ -178,6 +178,37 @@ def cores() -> int:
         return os.cpu_count() or 1
 
 
+L2_BYTES = 129 * 1000 * 1000   # GB300 L2
+
+
+def run_config(args, cfg, parts, container_bytes, world: int) -> dict:
+    """The `config` object of both arms' JSON lines."""
+    blocks = [b for p, b in zip(parts, container_bytes) for _ in range(p.n_blocks)]
+    streamed = sum(blocks[args.resident:])
+    weights = {synth.W_BF16: "bf16", synth.W_E4M3: "e4m3", synth.W_E4M3_A8: "e4m3 (W8A8)"}
+    return {"workload": cfg.name, "blocks": cfg.n_blocks, "hidden": cfg.hidden,
+            "containers": [{"kind": "video" if p.kind else "dit", "blocks": p.n_blocks, "heads": p.heads,
+                            "ffn": p.ffn, "block_bytes": b, "weights": weights[p.wdtype]}
+                           for p, b in zip(parts, container_bytes)],
+            "batch": cfg.batch, "tokens": cfg.tokens, "resident": args.resident,
+            "staging": args.staging, "host": args.host, "graphs": not args.no_graphs,
+            "parallelism": "replicas" if world > 1 else "single",
+            "l2": (f"inputs larger than L2: {streamed / 1e9:.2f} GB of weights streamed from host per step"
+                   if streamed > L2_BYTES else
+                   f"inputs smaller than L2 ({streamed / 1e6:.1f} MB streamed per step), L2 not flushed")}
+
+
+def container_bytes_of(parts):
+    """Flat block sizes from the library's layout table (a host function)."""
+    import layerwise_weight_offload_slot_gb300 as dlo
+    return [dlo.dlo_block_bytes(dlo.make_desc(block_kind=p.kind, n_blocks=p.n_blocks, hidden=p.hidden,
+                                              heads=p.heads, head_dim=p.head_dim, ffn=p.ffn,
+                                              cond_dim=p.cond_dim, text_dim=p.text_dim,
+                                              max_batch=p.batch, max_tokens=p.tokens,
+                                              max_text_tokens=p.text_tokens, wdtype=p.wdtype))
+            for p in parts]
+
+
 def run_reference(args, cfg, rank: int, world: int):
     if rank != 0:
         return
@@ -191,12 +222,16 @@ def run_reference(args, cfg, rank: int, world: int):
         # one block of every container per step, weighted by its block count
         step_s.append(sum(oracle_block_seconds(p, 0.0, max_blocks=1)[0] * p.n_blocks for p in parts))
     value = 1.0 / statistics.mean(step_s)
+    try:
+        config = run_config(args, cfg, parts, container_bytes_of(parts), world)
+    except ImportError:   # library not built: the fields that need no layout table
+        config = {"workload": cfg.name, "parallelism": "replicas" if world > 1 else "single"}
     sample = (f"1 block of each of the {len(parts)} container(s) per step, float64 numpy oracle, "
               f"extrapolated to the {cfg.n_blocks}-block step")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / value,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": cfg.name, "parallelism": "replicas"},
+            "data": "synthetic", "config": config,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -462,18 +497,7 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": {synth.W_E4M3: "bf16 (e4m3 weights)", synth.W_E4M3_A8: "e4m3 x e4m3 (W8A8)"}.get(
                     parts[0].wdtype, "bf16"), "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations)",
-                "config": {"workload": cfg.name, "blocks": cfg.n_blocks, "hidden": cfg.hidden,
-                           "containers": [{"kind": "video" if p.kind else "dit",
-                                           "blocks": p.n_blocks, "heads": p.heads,
-                                           "ffn": p.ffn, "block_bytes": b,
-                                           "weights": "e4m3" if p.wdtype else "bf16"}
-                                          for p, b in zip(parts, st.container_bytes)],
-                           "batch": cfg.batch, "tokens": cfg.tokens, "resident": args.resident,
-                           "staging": args.staging, "host": args.host,
-                           "graphs": not args.no_graphs,
-                           "parallelism": "replicas" if world > 1 else "single",
-                           "l2": f"inputs larger than L2: {streamed_bytes / 1e9:.2f} GB of weights "
-                                 "streamed from host per step"},
+                "config": run_config(args, cfg, parts, st.container_bytes, world),
                 "roofline": roof, "step_roofline": step_roof, "overlap": overlap,
                 "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "graph_launches": graph_launches,
