@@ -19,6 +19,8 @@
 // tile t+1.  With E4M3 weights (FP8 = true) TMA loads the raw codes, twelve
 // more warps widen them to bf16 in the swizzled layout the MMA reads (exact),
 // and the per-tensor scale is applied to the fp32 accumulator in the epilogue.
+// The widened tiles live in CB buffers of their own (conv / conv_empty
+// barriers), so the ring of A tiles and raw codes is four stages deep.
 //
 // Every mbarrier wait is bounded (2 s); a wait that runs out sets the
 // kernel's error word and a CTA-wide abort flag, after which every role
@@ -152,18 +154,22 @@ __device__ __forceinline__ void e4m3x8_to_bf16x8(uint32_t x0, uint32_t x1, uint3
     }
 }
 
-template <int BN, int STAGES, bool FP8, int MT = 1>
+template <int BN, int STAGES, bool FP8, int MT = 1, int CB = 0>
 struct SmemPlan {
     static constexpr int A_STAGE = MT * A_TILE;           // MT 128-row A boxes per stage
     static constexpr int B_TILE = BN * BK * 2;            // bf16 operand tile (MMA reads)
     static constexpr int RAW_TILE = FP8 ? BN * BK : 0;     // e4m3 tile as loaded by TMA
+    // bf16 B buffers: one per stage, or (E4M3, CB > 0) CB widened tiles that
+    // cycle on their own, so the A / raw-code ring can be deeper than the
+    // shared memory for a widened tile per stage would allow
+    static constexpr int NBUF = (FP8 && CB) ? CB : STAGES;
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = STAGES * A_STAGE;
-    static constexpr int RAW_OFF = B_OFF + STAGES * B_TILE;
+    static constexpr int RAW_OFF = B_OFF + NBUF * B_TILE;
     static constexpr int STG_OFF = RAW_OFF + STAGES * RAW_TILE;   // 4 warps x 2 boxes
     static constexpr int BAR_OFF = STG_OFF + 8 * STG_BYTES;
-    // full[STAGES], empty[STAGES], conv[STAGES], tfull[2], tempty[2], drain
-    static constexpr int TMEM_SLOT_OFF = BAR_OFF + (3 * STAGES + 5) * 8;
+    // full[STAGES], empty[STAGES], conv[NBUF], conv_empty[NBUF], tfull[2], tempty[2], drain
+    static constexpr int TMEM_SLOT_OFF = BAR_OFF + (2 * STAGES + 2 * NBUF + 5) * 8;
     static constexpr int ABORT_OFF = TMEM_SLOT_OFF + 4;
     static constexpr int BYTES = ABORT_OFF + 4 + 1024;  // + alignment slack
     static constexpr int THREADS = kThreads + (FP8 ? kConvWarps * 32 : 0);
@@ -177,12 +183,13 @@ struct SmemPlan {
 // its widening) serves MT row blocks.  A8: A and W are both E4M3 codes
 // (W8A8), multiplied by kind::f8f6f4 at 128 K per stage (the same 128-byte
 // swizzled rows as bf16 at 64 K); no widening.
-template <int BN, int STAGES, bool FP8, int MT, bool A8>
-__global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
+template <int BN, int STAGES, bool FP8, int MT, bool A8, int CB = 0>
+__global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT, CB>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO, const EpiArgs args) {
     static_assert(!(A8 && FP8), "W8A8 loads 8-bit codes for both operands, nothing to widen");
-    using P = SmemPlan<BN, STAGES, FP8, MT>;
+    using P = SmemPlan<BN, STAGES, FP8, MT, CB>;
+    constexpr bool DEC = FP8 && CB > 0;   // widened tiles decoupled from the stages
     constexpr int KS = A8 ? 128 : BK;   // K elements per stage (128 bytes of a row either way)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -191,7 +198,8 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
     const uint32_t bar_full = sbase + P::BAR_OFF;
     const uint32_t bar_empty = bar_full + STAGES * 8;
     const uint32_t bar_conv = bar_empty + STAGES * 8;
-    const uint32_t bar_tfull = bar_conv + STAGES * 8;
+    const uint32_t bar_cempty = bar_conv + P::NBUF * 8;
+    const uint32_t bar_tfull = bar_cempty + P::NBUF * 8;
     const uint32_t bar_tempty = bar_tfull + 2 * 8;
     const uint32_t bar_drain = bar_tempty + 2 * 8;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + P::TMEM_SLOT_OFF);
@@ -204,7 +212,10 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + s * 8, 1);
             mbar_init(bar_empty + s * 8, 1);
-            mbar_init(bar_conv + s * 8, kConvWarps);
+        }
+        for (int c = 0; c < P::NBUF; ++c) {
+            mbar_init(bar_conv + c * 8, kConvWarps);
+            mbar_init(bar_cempty + c * 8, 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar_tfull + a * 8, 1);
@@ -314,6 +325,8 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
         uint64_t a_desc = a_desc0, b_desc = b_desc0;
         int s = 0;
         uint32_t ph = 0;
+        int cb = 0;          // DEC: widened buffer and its phase
+        uint32_t cph = 0;
         int t = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x, ++t) {
@@ -326,7 +339,7 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * (MT * BN);
             for (int kb = 0; kb < kblocks; ++kb) {
-                if (!mbar_wait(bar_ready + s * 8, ph, abort_flag)) {
+                if (!mbar_wait(DEC ? bar_conv + cb * 8 : bar_ready + s * 8, DEC ? cph : ph, abort_flag)) {
                     fail();
                     ok = false;
                     break;
@@ -345,7 +358,23 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
                     }
                 }
                 tc_commit(bar_empty + s * 8);
-                if (++s == STAGES) {
+                if constexpr (DEC) {
+                    tc_commit(bar_cempty + cb * 8);
+                    if (++cb == P::NBUF) {
+                        cb = 0;
+                        cph ^= 1;
+                        b_desc = b_desc0;
+                    } else {
+                        b_desc += P::B_TILE >> 4;
+                    }
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1;
+                        a_desc = a_desc0;
+                    } else {
+                        a_desc += P::A_STAGE >> 4;
+                    }
+                } else if (++s == STAGES) {
                     s = 0;
                     ph ^= 1;
                     a_desc = a_desc0;
@@ -494,10 +523,13 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
             const int ct = threadIdx.x - 6 * 32;
             int s = 0;
             uint32_t ph = 0;
+            int cb = 0;
+            uint32_t cph = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
                 for (int kb = 0; kb < kblocks; ++kb) {
                     bool got = mbar_wait(bar_full + s * 8, ph, abort_flag);
+                    if (DEC && got) got = mbar_wait(bar_cempty + cb * 8, cph ^ 1, abort_flag);
                     got = __all_sync(0xFFFFFFFFu, got);
                     if (!got) {
                         if (lane == 0) fail();
@@ -505,7 +537,7 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
                         break;
                     }
                     const uint8_t* raw = smem + P::RAW_OFF + s * P::RAW_TILE;
-                    uint8_t* dst = smem + P::B_OFF + s * P::B_TILE;
+                    uint8_t* dst = smem + P::B_OFF + (DEC ? cb : s) * P::B_TILE;
 #pragma unroll 4
                     for (int i = ct; i < BN * 8; i += kConvWarps * 32) {
                         const int r = i >> 3, c = i & 7;
@@ -516,10 +548,14 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT>::THREADS, 1)
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_conv + s * 8);
+                    if (lane == 0) mbar_arrive(bar_conv + (DEC ? cb : s) * 8);
                     if (++s == STAGES) {
                         s = 0;
                         ph ^= 1;
+                    }
+                    if (DEC && ++cb == P::NBUF) {
+                        cb = 0;
+                        cph ^= 1;
                     }
                 }
             }
@@ -557,13 +593,13 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int es_b
 
 int g_num_sms = 0;
 
-template <int BN, int STAGES, bool FP8, int MT = 1, bool A8 = false>
+template <int BN, int STAGES, bool FP8, int MT = 1, bool A8 = false, int CB = 0>
 cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
-    using PL = SmemPlan<BN, STAGES, FP8, MT>;
+    using PL = SmemPlan<BN, STAGES, FP8, MT, CB>;
     static_assert(PL::BYTES <= 227 * 1024, "shared memory plan exceeds 227 KB");
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, STAGES, FP8, MT, A8>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, STAGES, FP8, MT, A8, CB>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, PL::BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -618,7 +654,7 @@ cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* la
     const double n_sweep = w_bytes + a_bytes * ((a.num_n + 7) / 8);
     a.n_major = n_sweep < m_sweep ? 1 : 0;
     const int grid = a.num_tiles < g_num_sms ? a.num_tiles : g_num_sms;
-    cudaError_t le_ = launch_k(gemm_kernel<BN, STAGES, FP8, MT, A8>, grid, PL::THREADS, PL::BYTES, s, ta, tb, to, a);
+    cudaError_t le_ = launch_k(gemm_kernel<BN, STAGES, FP8, MT, A8, CB>, grid, PL::THREADS, PL::BYTES, s, ta, tb, to, a);
     ++*launches;
     return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
@@ -757,7 +793,7 @@ cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long*
         // it off (tuning).
         const long long tiles2 = ((p.M + 255) / 256) * ((p.N + 127) / 128);
         if (forced_mt() != 1 && (forced_mt() == 2 || tiles2 >= g_num_sms))
-            return run_gemm<128, 3, true, 2>(p, s, launches);
+            return run_gemm<128, 4, true, 2, false, 2>(p, s, launches);
         if (bn == 256) return run_gemm<256, 3, true>(p, s, launches);
         if (bn == 192) return run_gemm<192, 3, true>(p, s, launches);
         return run_gemm<128, 4, true>(p, s, launches);
