@@ -41,3 +41,16 @@ def test_c_program_drives_a_stack(tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "c abi ok" in r.stdout
+
+
+def test_header_is_self_contained_in_c_and_cxx(tmp_path):
+    """dlo.h compiles on its own (no CUDA or torch headers) as C99 and C++17."""
+    src = tmp_path / "only_header.c"
+    src.write_text('#include "dlo.h"\nint main(void) { dlo_desc d; (void)d; return DLO_OK; }\n')
+    for compiler, flags in (("gcc", ["-std=c99", "-x", "c"]), ("g++", ["-std=c++17", "-x", "c++"])):
+        cc = shutil.which(compiler)
+        if cc is None:
+            continue
+        r = subprocess.run([cc, *flags, "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-I",
+                            os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+        assert r.returncode == 0, (compiler, r.stderr)
