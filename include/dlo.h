@@ -479,22 +479,26 @@ dlo_status dlo_op_gemm_w8a8(const void* A, const float* a_scale, const void* W, 
                             void* out, int ldo, const float* gate, int gate_ld, int rows_per_batch,
                             int* err, void* stream);
 
-/* dlo_op_gemm for callers that cannot allocate device memory (for example code
- * running where the CUDA allocator is unavailable or forbidden, such as inside
- * another framework's memory pool or a host callback).  The pages have no
- * counterpart; this is an addition of this library.
- * Same arguments and results as dlo_op_gemm minus `err`: the kernel's scratch
- * (its device error word) lives in a static device array of at most 256 bytes
- * that every GPU which loads this library holds until the process exits; this
- * entry uses 4 bytes of it and clears them before each launch.  It calls no
- * cudaMalloc, cudaFree or allocating library routine.
+/* dlo_op_gemm for callers that cannot allocate device memory.  Some code may
+ * not call cudaMalloc at all: a plugin running inside another framework whose
+ * caching allocator owns the device's memory (a direct allocation would
+ * bypass its accounting, or find no memory left), or a serving process whose
+ * memory plan is fixed at start-up.  Such a caller still owns its inputs and
+ * outputs; it has no buffer to hand over for the kernel's scratch.
+ * The pages have no counterpart; this is an addition of this library.
+ * Same arguments, checks and results as dlo_op_gemm minus `err`: the kernel's
+ * scratch (its device error word) lives in a static device array of at most
+ * 256 bytes that every GPU which loads this library holds until the process
+ * exits; this entry uses 4 bytes of it and clears them before each launch.
+ * It calls no cudaMalloc, cudaFree or allocating library routine.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  All calls share the one array, so calls that
  * overlap on the GPU race on the error word; a bounded wait that runs out
  * leaves `out` incomplete and is not reported (use dlo_op_gemm with your own
  * error word when you need that report).  Argument errors return DLO_EINVAL
- * (message on stderr) before anything is enqueued. */
+ * before anything is enqueued, launch errors DLO_ECUDA; the message is in
+ * dlo_last_error(NULL). */
 dlo_status dlo_op_gemm_noalloc(const void* A, const void* W, int w_dtype, const float* scales,
                                int scale_seg, const void* bias, int M, int N, int K,
                                int epilogue, void* out, int ldo, const float* gate, int gate_ld,

@@ -326,10 +326,8 @@ def dlo_op_gemm(A, W, w_dtype, scales, scale_seg, bias, M, N, K, epilogue, out, 
 
 def dlo_op_gemm_noalloc(A, W, w_dtype, scales, scale_seg, bias, M, N, K, epilogue, out, ldo, gate,
                         gate_ld, rows_per_batch, stream) -> None:
-    st = _c["dlo_op_gemm_noalloc"](A, W, w_dtype, scales, scale_seg, bias, M, N, K, epilogue, out,
-                                   ldo, gate, gate_ld, rows_per_batch, stream)
-    if st != OK:
-        raise DloError(st, "dlo_op_gemm_noalloc rejected the call (see stderr)")
+    _check(_c["dlo_op_gemm_noalloc"](A, W, w_dtype, scales, scale_seg, bias, M, N, K, epilogue, out,
+                                     ldo, gate, gate_ld, rows_per_batch, stream))
 
 
 def dlo_op_wait_selftest(err, stream) -> None:

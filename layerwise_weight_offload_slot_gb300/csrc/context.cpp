@@ -17,7 +17,9 @@
 #include <mutex>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
+#include <deque>
 #include <memory>
 #include <string>
 #include <thread>
@@ -132,17 +134,117 @@ class CopyPool {
     bool stop_ = false;
 };
 
-struct PackJob {
-    CopyPool* pool;
-    void* dst;
-    const void* src;
-    size_t bytes;
+// Packs pageable host blocks into the two pinned host staging slots on a
+// thread of its own, so that the pack of one staging overlaps the
+// host-to-device copy of the one before ("Distributed Layerwise Offload",
+// Host backing and transfer composition: two bounded pinned host-staging
+// slots).  Staging n uses host slot n % 2; its pack may start once the copy
+// of staging n - 2, the slot's previous reader, has finished.  The copy
+// stream learns that a pack is done from a host function that waits for it
+// (wait_packed) and reports each finished copy through another (copied).
+// Host functions here call no CUDA API.
+class HostPacker {
+  public:
+    explicit HostPacker(int threads) : pool_(threads), thread_([this] { loop(); }) {}
+    ~HostPacker() {
+        {
+            std::lock_guard<std::mutex> g(mu_);
+            stop_ = true;
+        }
+        cv_.notify_all();
+        thread_.join();
+    }
+    // Queue the pack of staging n (stagings are submitted in order).
+    void submit(unsigned long long n, void* dst, const void* src, size_t bytes) {
+        {
+            std::lock_guard<std::mutex> g(mu_);
+            jobs_.push_back(Job{n, dst, src, bytes});
+        }
+        cv_.notify_all();
+    }
+    // Blocks until the pack of staging n is done.
+    void wait_packed(unsigned long long n) {
+        std::unique_lock<std::mutex> g(mu_);
+        cv_.wait(g, [&] { return packed_ > n || stop_; });
+    }
+    // The copy of staging n has finished.
+    void copied(unsigned long long n) {
+        {
+            std::lock_guard<std::mutex> g(mu_);
+            copied_ = std::max(copied_, n + 1);
+        }
+        cv_.notify_all();
+    }
+    // Packs that had to wait for their host slot (the copy two stagings
+    // earlier still running), for the statistics.
+    unsigned long long slot_waits() {
+        std::lock_guard<std::mutex> g(mu_);
+        return slot_waits_;
+    }
+
+  private:
+    struct Job {
+        unsigned long long n;
+        void* dst;
+        const void* src;
+        size_t bytes;
+    };
+    void loop() {
+        for (;;) {
+            Job j;
+            {
+                std::unique_lock<std::mutex> g(mu_);
+                cv_.wait(g, [&] { return stop_ || !jobs_.empty(); });
+                if (stop_ && jobs_.empty()) return;
+                j = jobs_.front();
+                jobs_.pop_front();
+                // the host slot's previous reader is the copy of staging n - 2
+                if (j.n >= 2 && copied_ < j.n - 1) {
+                    ++slot_waits_;
+                    cv_.wait(g, [&] { return stop_ || copied_ >= j.n - 1; });
+                    if (stop_) return;
+                }
+            }
+            pool_.copy(j.dst, j.src, j.bytes);
+            {
+                std::lock_guard<std::mutex> g(mu_);
+                packed_ = j.n + 1;
+            }
+            cv_.notify_all();
+        }
+    }
+    CopyPool pool_;
+    std::mutex mu_;
+    std::condition_variable cv_;
+    std::deque<Job> jobs_;
+    unsigned long long packed_ = 0, copied_ = 0, slot_waits_ = 0;
+    bool stop_ = false;
+    std::thread thread_;
 };
 
-void CUDART_CB pack_host_fn(void* arg) {
-    PackJob* j = static_cast<PackJob*>(arg);
-    j->pool->copy(j->dst, j->src, j->bytes);
-    delete j;
+// Host threads of one pack (the memcpy of a block into a pinned host slot):
+// DLO_PACK_THREADS, else 12.
+int pack_threads() {
+    const char* e = std::getenv("DLO_PACK_THREADS");
+    const int v = e ? std::atoi(e) : 0;
+    return v >= 1 && v <= 64 ? v : 12;
+}
+
+struct PackTicket {
+    HostPacker* packer;
+    unsigned long long n;
+};
+
+void CUDART_CB wait_packed_fn(void* arg) {
+    PackTicket* t = static_cast<PackTicket*>(arg);
+    t->packer->wait_packed(t->n);
+    delete t;
+}
+
+void CUDART_CB copied_fn(void* arg) {
+    PackTicket* t = static_cast<PackTicket*>(arg);
+    t->packer->copied(t->n);
+    delete t;
 }
 
 }  // namespace
@@ -173,8 +275,8 @@ struct dlo_ctx {
     bool reg_read_only = false;
     bool pageable = false;
     uint8_t* hstage[2] = {nullptr, nullptr};   // pinned host staging slots (pageable mode)
-    int hstage_next = 0;
-    std::unique_ptr<CopyPool> pool;
+    unsigned long long pack_seq = 0;            // pageable stagings so far (host slot = seq % 2)
+    std::unique_ptr<HostPacker> packer;
     std::vector<uint8_t*> resident;
     unsigned long long exec_counter = 0;
     int slot_block[2] = {-1, -1};
@@ -352,17 +454,28 @@ dlo_status stage(dlo_ctx* c, int blk, int s) {
             return launch_gather(c->slot[s], c->host_dev[blk], bytes, c->xs, &c->st.kernel_launches);
         });
     } else if (c->pageable) {
-        // pack into the next pinned host slot (stream-ordered host function),
-        // then copy that slot to the device slot
-        const int h = c->hstage_next;
-        c->hstage_next ^= 1;
-        PackJob* job = new PackJob{c->pool.get(), c->hstage[h], c->host[blk], bytes};
-        e = cudaLaunchHostFunc(c->xs, pack_host_fn, job);
+        // the packer thread packs the block into the next pinned host slot as
+        // soon as that slot's previous copy has finished; the copy stream
+        // waits for the pack, copies the slot and reports the copy
+        const unsigned long long n = c->pack_seq;
+        const int h = static_cast<int>(n & 1);
+        PackTicket* w = new PackTicket{c->packer.get(), n};
+        e = cudaLaunchHostFunc(c->xs, wait_packed_fn, w);
         if (e != cudaSuccess) {
-            delete job;
+            delete w;
         } else {
+            c->packer->submit(n, c->hstage[h], c->host[blk], bytes);
+            ++c->pack_seq;
             e = cudaMemcpyAsync(c->slot[s], c->hstage[h], bytes, cudaMemcpyHostToDevice, c->xs);
             ++c->st.h2d_copies;
+            if (e == cudaSuccess) {
+                PackTicket* d = new PackTicket{c->packer.get(), n};
+                e = cudaLaunchHostFunc(c->xs, copied_fn, d);
+                if (e != cudaSuccess) delete d;
+            }
+            // a copy that was not enqueued never reports: later packs into
+            // this slot would wait for it, so the context takes no more work
+            if (e != cudaSuccess) c->state = kBroken;
         }
     } else if (c->d.staging == DLO_STAGE_PER_TENSOR) {
         e = cudaSuccess;
@@ -719,7 +832,7 @@ extern "C" dlo_status dlo_register_host_blocks(dlo_ctx* c, int n, const void* co
                 return c->fail(DLO_ENOMEM, "pinned host staging slots: %s", cudaGetErrorString(e));
             }
         }
-        c->pool.reset(new CopyPool(8));
+        c->packer.reset(new HostPacker(pack_threads()));
         c->pageable = true;
         c->host.assign(reinterpret_cast<const uint8_t* const*>(host_blocks),
                        reinterpret_cast<const uint8_t* const*>(host_blocks) + n);
@@ -1209,7 +1322,7 @@ extern "C" dlo_status dlo_destroy(dlo_ctx* c) {
         for (int i = 0; i < 2; ++i)
             if (c->hstage[i]) cudaFreeHost(c->hstage[i]);
     }
-    c->pool.reset();
+    c->packer.reset();
     delete c;
     return first;
 }
@@ -1285,22 +1398,25 @@ extern "C" dlo_status dlo_verify_slot(dlo_ctx* c, int slot, int block) {
 
 namespace {
 unsigned long long g_op_launches = 0;
-dlo_status op_result(cudaError_t e) {
-    if (e == cudaSuccess) return DLO_OK;
-    g_create_error = std::string("kernel launch: ") + cudaGetErrorString(e);
-    cudaGetLastError();
-    return DLO_ECUDA;
-}
-dlo_status op_inval(const char* m) {
-    g_create_error = m;
-    return DLO_EINVAL;
-}
 }  // namespace
 
+namespace dlo {
+
+dlo_status op_fail(dlo_status st, const std::string& msg) {
+    g_create_error = msg;
+    return st;
+}
+
+dlo_status op_result(cudaError_t e) {
+    if (e == cudaSuccess) return DLO_OK;
+    cudaGetLastError();
+    return op_fail(DLO_ECUDA, std::string("kernel launch: ") + cudaGetErrorString(e));
+}
+
+}  // namespace dlo
+
 namespace {
-dlo_status gemm_op(const void* A, const void* W, int w_dtype, const float* scales, int scale_seg,
-                   const void* bias, int M, int N, int K, int epilogue, void* out, int ldo, const float* gate,
-                   int gate_ld, int rows_per_batch, int* err, void* stream, int a_dtype, const float* a_scale);
+dlo_status op_inval(const char* m) { return op_fail(DLO_EINVAL, m); }
 }  // namespace
 
 extern "C" dlo_status dlo_op_wait_selftest(int* err, void* stream) {
@@ -1334,22 +1450,32 @@ extern "C" dlo_status dlo_op_gemm_w8a8(const void* A, const float* a_scale, cons
                                        int* err, void* stream) {
     if (!a_scale || !scales) return op_inval("W8A8 needs the activation scale and the weight scales");
     if (!aligned(a_scale, 4)) return op_inval("a_scale misaligned");
-    return gemm_op(A, W, DLO_DT_E4M3, scales, scale_seg, bias, M, N, K, epilogue, out, ldo, gate, gate_ld,
-                   rows_per_batch, err, stream, DLO_DT_E4M3, a_scale);
+    GemmParams p;
+    dlo_status r = op_gemm_params(A, W, DLO_DT_E4M3, scales, scale_seg, bias, M, N, K, epilogue, out, ldo, gate,
+                                  gate_ld, rows_per_batch, DLO_DT_E4M3, a_scale, &p);
+    if (r != DLO_OK) return r;
+    p.err = err;
+    return op_launch_gemm(p, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" dlo_status dlo_op_gemm(const void* A, const void* W, int w_dtype, const float* scales,
                                   int scale_seg, const void* bias, int M, int N, int K, int epilogue,
                                   void* out, int ldo, const float* gate, int gate_ld,
                                   int rows_per_batch, int* err, void* stream) {
-    return gemm_op(A, W, w_dtype, scales, scale_seg, bias, M, N, K, epilogue, out, ldo, gate, gate_ld,
-                   rows_per_batch, err, stream, DLO_DT_BF16, nullptr);
+    GemmParams p;
+    dlo_status r = op_gemm_params(A, W, w_dtype, scales, scale_seg, bias, M, N, K, epilogue, out, ldo, gate,
+                                  gate_ld, rows_per_batch, DLO_DT_BF16, nullptr, &p);
+    if (r != DLO_OK) return r;
+    p.err = err;
+    return op_launch_gemm(p, static_cast<cudaStream_t>(stream));
 }
 
-namespace {
-dlo_status gemm_op(const void* A, const void* W, int w_dtype, const float* scales, int scale_seg,
-                   const void* bias, int M, int N, int K, int epilogue, void* out, int ldo, const float* gate,
-                   int gate_ld, int rows_per_batch, int* err, void* stream, int a_dtype, const float* a_scale) {
+namespace dlo {
+
+dlo_status op_gemm_params(const void* A, const void* W, int w_dtype, const float* scales, int scale_seg,
+                          const void* bias, int M, int N, int K, int epilogue, void* out, int ldo,
+                          const float* gate, int gate_ld, int rows_per_batch, int a_dtype,
+                          const float* a_scale, GemmParams* p) {
     if (!A || !W || !out) return op_inval("NULL operand");
     if (M < 1 || N < 16 || N % 16 || K < 16 || K % 16) return op_inval("need M >= 1, N % 16 == 0, K % 16 == 0");
     if (!aligned(A, 16) || !aligned(W, 16) || !aligned(out, 16) || ldo % 8 || ldo < N)
@@ -1359,28 +1485,33 @@ dlo_status gemm_op(const void* A, const void* W, int w_dtype, const float* scale
     if (scales && (scale_seg < 16 || scale_seg % 16)) return op_inval("scale_seg % 16 != 0");
     if (bias && !aligned(bias, 16)) return op_inval("bias must be 16-byte aligned");
     if (gate && (!aligned(gate, 16) || gate_ld % 4 || rows_per_batch < 1)) return op_inval("gate layout");
-    GemmParams p;
-    p.A = A;
-    p.W = W;
-    p.w_dtype = w_dtype;
-    p.scales = scales;
-    p.scale_seg = scale_seg;
-    p.bias = bias;
-    p.M = M;
-    p.N = N;
-    p.K = K;
-    p.epi = epilogue;
-    p.out = out;
-    p.ldo = ldo;
-    p.gate = gate;
-    p.gate_ld = gate_ld;
-    p.rows_per_batch = rows_per_batch > 0 ? rows_per_batch : 1;
-    p.err = err;
-    p.a_dtype = a_dtype;
-    p.a_scale = a_scale;
-    return op_result(launch_gemm(p, static_cast<cudaStream_t>(stream), &g_op_launches));
+    GemmParams q;
+    q.A = A;
+    q.W = W;
+    q.w_dtype = w_dtype;
+    q.scales = scales;
+    q.scale_seg = scale_seg;
+    q.bias = bias;
+    q.M = M;
+    q.N = N;
+    q.K = K;
+    q.epi = epilogue;
+    q.out = out;
+    q.ldo = ldo;
+    q.gate = gate;
+    q.gate_ld = gate_ld;
+    q.rows_per_batch = rows_per_batch > 0 ? rows_per_batch : 1;
+    q.a_dtype = a_dtype;
+    q.a_scale = a_scale;
+    *p = q;
+    return DLO_OK;
 }
-}  // namespace
+
+dlo_status op_launch_gemm(const GemmParams& p, cudaStream_t s) {
+    return op_result(launch_gemm(p, s, &g_op_launches));
+}
+
+}  // namespace dlo
 
 extern "C" dlo_status dlo_op_attention(const void* Q, const void* K, const void* V, void* O, int batch,
                                        int heads, int head_dim, int nq, int nk, int ldq, int ldk, int ldv,

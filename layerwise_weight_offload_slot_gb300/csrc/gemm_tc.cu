@@ -826,6 +826,7 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = 256;   // stated maximum scratch size
 constexpr size_t kNoAllocNeedBytes = sizeof(int);
 constexpr int kNoAllocMaxDevices = 64;
+static_assert(kNoAllocNeedBytes <= kNoAllocScratchBytes, "the GEMM's scratch must fit the static array");
 
 }  // namespace
 
@@ -838,7 +839,7 @@ int* g_noalloc_ptr[kNoAllocMaxDevices] = {};
 
 // Device address of the static scratch on the current device, looked up once
 // per device (the host-side name is only a stand-in, never a device address).
-cudaError_t noalloc_scratch(int* dev_out, int** ptr_out) {
+cudaError_t noalloc_scratch(int** ptr_out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -850,20 +851,9 @@ cudaError_t noalloc_scratch(int* dev_out, int** ptr_out) {
         if (e != cudaSuccess) return e;
         g_noalloc_ptr[dev] = static_cast<int*>(p);
     }
-    *dev_out = dev;
     *ptr_out = g_noalloc_ptr[dev];
     return cudaSuccess;
 }
-
-thread_local std::string g_noalloc_error;
-
-dlo_status noalloc_fail(dlo_status st, const char* msg) {
-    g_noalloc_error = msg;
-    std::fprintf(stderr, "dlo_op_gemm_noalloc: %s\n", msg);
-    return st;
-}
-
-bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
@@ -872,49 +862,21 @@ extern "C" dlo_status dlo_op_gemm_noalloc(const void* A, const void* W, int w_dt
                                           int M, int N, int K, int epilogue, void* out, int ldo,
                                           const float* gate, int gate_ld, int rows_per_batch,
                                           void* stream) {
-    if (kNoAllocNeedBytes > kNoAllocScratchBytes)
-        return noalloc_fail(DLO_EINVAL, "scratch need exceeds the 256-byte static scratch");
-    if (!A || !W || !out) return noalloc_fail(DLO_EINVAL, "NULL operand");
-    if (M < 1 || N < 16 || N % 16 || K < 16 || K % 16)
-        return noalloc_fail(DLO_EINVAL, "need M >= 1, N % 16 == 0, K % 16 == 0");
-    if (!al16(A) || !al16(W) || !al16(out) || ldo % 8 || ldo < N)
-        return noalloc_fail(DLO_EINVAL, "operands must be 16-byte aligned and ldo % 8 == 0, ldo >= N");
-    if (w_dtype != DLO_DT_BF16 && w_dtype != DLO_DT_E4M3) return noalloc_fail(DLO_EINVAL, "w_dtype");
-    if (epilogue < DLO_EPI_BIAS || epilogue > DLO_EPI_RESIDUAL) return noalloc_fail(DLO_EINVAL, "epilogue");
-    if (scales && (scale_seg < 16 || scale_seg % 16)) return noalloc_fail(DLO_EINVAL, "scale_seg % 16 != 0");
-    if (bias && !al16(bias)) return noalloc_fail(DLO_EINVAL, "bias must be 16-byte aligned");
-    if (gate && (!al16(gate) || gate_ld % 4 || rows_per_batch < 1))
-        return noalloc_fail(DLO_EINVAL, "gate layout");
-    int dev = 0;
+    // the same checks and parameters as dlo_op_gemm; only the error word differs
+    dlo::GemmParams p;
+    dlo_status r = dlo::op_gemm_params(A, W, w_dtype, scales, scale_seg, bias, M, N, K, epilogue, out, ldo,
+                                       gate, gate_ld, rows_per_batch, DLO_DT_BF16, nullptr, &p);
+    if (r != DLO_OK) return r;
     int* scratch = nullptr;
-    cudaError_t e = noalloc_scratch(&dev, &scratch);
-    if (e != cudaSuccess) return noalloc_fail(DLO_ECUDA, cudaGetErrorString(e));
+    cudaError_t e = noalloc_scratch(&scratch);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return dlo::op_fail(DLO_ECUDA, std::string("static scratch lookup: ") + cudaGetErrorString(e));
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the array keeps the previous call's contents: the error word starts at 0
     e = cudaMemsetAsync(scratch, 0, kNoAllocNeedBytes, s);
-    if (e != cudaSuccess) return noalloc_fail(DLO_ECUDA, cudaGetErrorString(e));
-    dlo::GemmParams p;
-    p.A = A;
-    p.W = W;
-    p.w_dtype = w_dtype;
-    p.scales = scales;
-    p.scale_seg = scale_seg;
-    p.bias = bias;
-    p.M = M;
-    p.N = N;
-    p.K = K;
-    p.epi = epilogue;
-    p.out = out;
-    p.ldo = ldo;
-    p.gate = gate;
-    p.gate_ld = gate_ld;
-    p.rows_per_batch = rows_per_batch > 0 ? rows_per_batch : 1;
+    if (e != cudaSuccess) return dlo::op_result(e);
     p.err = scratch;
-    unsigned long long launches = 0;
-    e = dlo::launch_gemm(p, s, &launches);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return noalloc_fail(DLO_ECUDA, cudaGetErrorString(e));
-    }
-    return DLO_OK;
+    return dlo::op_launch_gemm(p, s);
 }

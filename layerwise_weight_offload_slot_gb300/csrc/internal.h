@@ -115,6 +115,19 @@ struct GemmParams {
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches);
 int gemm_num_sms();
 
+// Unit-op plumbing shared by the C ABI's op entry points.  op_fail stores the
+// message that dlo_last_error(NULL) returns and passes the status through;
+// op_result turns a launch error into DLO_ECUDA the same way.
+dlo_status op_fail(dlo_status st, const std::string& msg);
+dlo_status op_result(cudaError_t e);
+// The argument checks of the GEMM ops and their GemmParams (p->err left NULL).
+dlo_status op_gemm_params(const void* A, const void* W, int w_dtype, const float* scales, int scale_seg,
+                          const void* bias, int M, int N, int K, int epilogue, void* out, int ldo,
+                          const float* gate, int gate_ld, int rows_per_batch, int a_dtype,
+                          const float* a_scale, GemmParams* p);
+// launch_gemm, counted with the unit ops' launches, through op_result.
+dlo_status op_launch_gemm(const GemmParams& p, cudaStream_t s);
+
 // cuTensorMapEncodeTiled, resolved once through the runtime's driver entry
 // point (no link-time dependency on libcuda) and wrapped by a table of
 // already-encoded maps keyed by every argument; NULL if unavailable.

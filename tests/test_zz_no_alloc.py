@@ -1,12 +1,18 @@
 """dlo_op_gemm_noalloc: the GEMM entry point for callers that cannot allocate
-device memory.  Its kernel scratch (the error word) lives in a static device
-array inside the library.  Checked through the C ABI against dlo_op_gemm, the
-entry point that takes caller-allocated scratch, on two calls in a row."""
+device memory (for example a plugin inside another framework whose caching
+allocator owns the device's memory).  Its kernel scratch, the error word,
+lives in a static device array inside the library.
+
+Checked through the C ABI against dlo_op_gemm, the entry point that takes
+caller-allocated scratch: both launch the same kernel with the same
+parameters, so their outputs must be bit-identical, on two calls in a row.
+Also checked: the device's free memory is unchanged across calls, and a bad
+argument is refused with a message.  This file is collected last."""
 import numpy as np
 import pytest
 import torch
 
-from oracle import dit
+from oracle import dit, fp8
 
 dlo = pytest.importorskip("layerwise_weight_offload_slot_gb300")
 
@@ -17,47 +23,111 @@ def _bf16(a):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).cuda()
 
 
-def _rel(y, ref):
-    y = y.float().cpu().numpy().astype(np.float64)
-    ref = ref.float().cpu().numpy().astype(np.float64)
-    return float(np.linalg.norm(y - ref) / np.linalg.norm(ref))
-
-
-def test_noalloc_gemm_matches_allocating_entry_on_two_calls():
-    stream = torch.cuda.current_stream().cuda_stream
-    cases = [(300, 272, 1152, dlo.EPI_BIAS), (2048, 1152, 1152, dlo.EPI_RESIDUAL)]
-    for call, (M, N, K, epi) in enumerate(cases):
-        g = np.random.default_rng(100 + call)
+def _cases():
+    """(name, M, N, K, epilogue, w_dtype) with every tensor allocated up front."""
+    specs = [("bias", 300, 272, 1152, dlo.EPI_BIAS, dlo.DT_BF16),
+             ("residual", 2048, 1152, 1152, dlo.EPI_RESIDUAL, dlo.DT_BF16),
+             ("e4m3_gelu", 512, 768, 640, dlo.EPI_GELU, dlo.DT_E4M3)]
+    out = []
+    for i, (name, M, N, K, epi, wdt) in enumerate(specs):
+        g = np.random.default_rng(100 + i)
         A = _bf16(g.standard_normal((M, K)))
-        W = _bf16(g.standard_normal((N, K)) * 0.05)
-        b = _bf16(g.standard_normal(N) * 0.1)
-        if epi == dlo.EPI_RESIDUAL:
-            gate = torch.from_numpy(g.standard_normal((2, N)).astype(np.float32)).cuda()
-            x0 = torch.from_numpy(g.standard_normal((M, N)).astype(np.float32)).cuda()
-            ref, new = x0.clone(), x0.clone()
-            args = (gate.data_ptr(), N, M // 2)
+        c = {"name": name, "M": M, "N": N, "K": K, "epi": epi, "wdt": wdt, "A": A,
+             "b": _bf16(g.standard_normal(N) * 0.1)}
+        if wdt == dlo.DT_E4M3:
+            codes = g.integers(0, 256, size=(N, K), dtype=np.uint8)
+            codes[codes == 0x7F] = 0x7E
+            codes[codes == 0xFF] = 0xFE
+            c["codes"] = codes
+            c["W"] = torch.from_numpy(codes).cuda()
+            c["scale_np"] = np.float32(0.02 / 448.0)
+            c["scales"] = torch.full((1,), float(c["scale_np"]), dtype=torch.float32, device="cuda")
         else:
-            ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-            new = torch.full((M, N), 3.0, dtype=torch.bfloat16, device="cuda")
-            args = (None, 0, 1)
-        err = torch.zeros(1, dtype=torch.int32, device="cuda")
-        dlo.dlo_op_gemm(A.data_ptr(), W.data_ptr(), dlo.DT_BF16, None, 0, b.data_ptr(), M, N, K,
-                        epi, ref.data_ptr(), N, *args, err.data_ptr(), stream)
-        dlo.dlo_op_gemm_noalloc(A.data_ptr(), W.data_ptr(), dlo.DT_BF16, None, 0, b.data_ptr(),
-                                M, N, K, epi, new.data_ptr(), N, *args, stream)
-        torch.cuda.synchronize()
-        assert int(err.item()) == 0
-        tol = 1e-5 if epi == dlo.EPI_RESIDUAL else 6e-3
-        assert _rel(new, ref) <= tol
-        # and both agree with the float64 oracle
-        r = dit.linear(A.double().cpu().numpy(), W.double().cpu().numpy(), b.double().cpu().numpy())
+            c["W"] = _bf16(g.standard_normal((N, K)) * 0.05)
+            c["scales"] = None
         if epi == dlo.EPI_RESIDUAL:
-            r = x0.double().cpu().numpy() + gate.double().cpu().numpy()[np.arange(M) // (M // 2)] * r
+            c["gate"] = torch.from_numpy(g.standard_normal((2, N)).astype(np.float32)).cuda()
+            c["x0"] = torch.from_numpy(g.standard_normal((M, N)).astype(np.float32)).cuda()
+            c["ref"] = torch.empty_like(c["x0"])
+            c["new"] = torch.empty_like(c["x0"])
+        else:
+            c["gate"] = None
+            c["ref"] = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            c["new"] = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        out.append(c)
+    return out
+
+
+def _run(c, entry, dst, err, stream):
+    if c["epi"] == dlo.EPI_RESIDUAL:
+        dst.copy_(c["x0"])
+        gate = (c["gate"].data_ptr(), c["N"], c["M"] // 2)
+    else:
+        dst.fill_(3.0)
+        gate = (None, 0, 1)
+    sc = c["scales"].data_ptr() if c["scales"] is not None else None
+    seg = c["N"] if c["scales"] is not None else 0
+    head = (c["A"].data_ptr(), c["W"].data_ptr(), c["wdt"], sc, seg, c["b"].data_ptr(), c["M"], c["N"],
+            c["K"], c["epi"], dst.data_ptr(), c["N"], *gate)
+    if entry == "alloc":
+        dlo.dlo_op_gemm(*head, err.data_ptr(), stream)
+    else:
+        dlo.dlo_op_gemm_noalloc(*head, stream)
+
+
+def _oracle(c):
+    A = c["A"].double().cpu().numpy()
+    if c["wdt"] == dlo.DT_E4M3:
+        W = fp8.decode_e4m3(c["codes"]) * float(c["scale_np"])
+    else:
+        W = c["W"].double().cpu().numpy()
+    r = dit.linear(A, W, c["b"].double().cpu().numpy())
+    if c["epi"] == dlo.EPI_GELU:
+        r = dit.gelu_tanh(r)
+    if c["epi"] == dlo.EPI_RESIDUAL:
+        M = c["M"]
+        r = c["x0"].double().cpu().numpy() + c["gate"].double().cpu().numpy()[np.arange(M) // (M // 2)] * r
+    return r
+
+
+def test_noalloc_gemm_bit_identical_to_allocating_entry_on_two_calls():
+    stream = torch.cuda.current_stream().cuda_stream
+    cases = _cases()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # one warm-up call of each kernel through both entries: a kernel's first
+    # launch may load its code onto the device, which takes device memory
+    for c in cases:
+        _run(c, "alloc", c["ref"], err, stream)
+        _run(c, "noalloc", c["new"], err, stream)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    snaps = []
+    for call in range(2):
+        for c in cases:
+            _run(c, "alloc", c["ref"], err, stream)
+            _run(c, "noalloc", c["new"], err, stream)
+        torch.cuda.synchronize()
+        if call == 0:
+            free1, _ = torch.cuda.mem_get_info()
+        snaps.append([(c["ref"].clone(), c["new"].clone()) for c in cases])
+    # nothing between the two readings allocated device memory: only the
+    # copies, fills and GEMM launches of the two entries ran
+    assert free1 == free0, f"free device memory changed by {free0 - free1} bytes"
+    assert int(err.item()) == 0
+    for call, snap in enumerate(snaps):
+        for c, (ref, new) in zip(cases, snap):
+            assert torch.equal(new, ref), f"{c['name']}: call {call} differs from dlo_op_gemm"
+    # and both agree with the float64 oracle
+    for c, (_, new) in zip(cases, snaps[1]):
         y = new.double().cpu().numpy()
-        assert np.linalg.norm(y - r) / np.linalg.norm(r) <= tol
+        r = _oracle(c)
+        tol = 1e-5 if c["epi"] == dlo.EPI_RESIDUAL else 6e-3
+        assert np.linalg.norm(y - r) / np.linalg.norm(r) <= tol, c["name"]
 
 
-def test_noalloc_gemm_rejects_bad_sizes():
-    with pytest.raises(dlo.DloError):
+def test_noalloc_gemm_rejects_bad_sizes_with_a_message():
+    with pytest.raises(dlo.DloError) as ei:
         dlo.dlo_op_gemm_noalloc(16, 16, dlo.DT_BF16, None, 0, None, 10, 15, 16, 0, 16, 16, None, 0,
                                 1, None)
+    assert ei.value.status == dlo.EINVAL
+    assert "N % 16" in str(ei.value)
