@@ -80,17 +80,17 @@ def attention(q, k, v, heads):
     Returns [Nq, H*hd].
     """
     nq, d = q.shape
-    nk = k.shape[0]
     hd = d // heads
-    qh = q.reshape(nq, heads, hd).transpose(1, 0, 2)
-    kh = k.reshape(nk, heads, hd).transpose(1, 0, 2)
-    vh = v.reshape(nk, heads, hd).transpose(1, 0, 2)
-    s = qh @ kh.transpose(0, 2, 1) / np.sqrt(hd)
-    s = s - s.max(axis=-1, keepdims=True)
-    p = np.exp(s)
-    p = p / p.sum(axis=-1, keepdims=True)
-    o = p @ vh
-    return o.transpose(1, 0, 2).reshape(nq, d)
+    o = np.empty((nq, d), dtype=np.float64)
+    # one head at a time: the scores of one head are [Nq, Nk]
+    for h in range(heads):
+        c = slice(h * hd, (h + 1) * hd)
+        s = q[:, c] @ k[:, c].T / np.sqrt(hd)
+        s = s - s.max(axis=-1, keepdims=True)
+        p = np.exp(s)
+        p = p / p.sum(axis=-1, keepdims=True)
+        o[:, c] = p @ v[:, c]
+    return o
 
 
 # ---------------------------------------------------------------- parameters

@@ -70,6 +70,39 @@ def test_full_size_block_sampled_rows(base, block):
     st.close()
 
 
+def test_w8a8_full_size_block_all_rows():
+    """One W8A8 block of the benchmarked 8192-token video workload, every row
+    against the oracle.  W8A8 quantises each linear's input with one scale
+    over the whole tensor (8192 x 5120, or 8192 x 13824 for fc2), so only a
+    full-size run exercises the device amax reduction across every CTA at the
+    size that is timed."""
+    base = synth.CFG_VIDEO_W8A8
+    cfg = base.with_(n_blocks=1)
+    params = synth.block_params(base, 0)
+    st = H.make_stack(cfg, blocks=[params])
+    st.attach()
+    x, cond, ctx = H.device_inputs(cfg)
+    out = st.forward(x, cond, ctx)
+    torch.cuda.synchronize()
+    st.wait()
+    assert st.verify_slot(0) and st.verify_slot(1)
+    y = out.float().cpu().numpy().astype(np.float64)
+    st.close()
+    ref = H.oracle_forward(cfg, x, cond, ctx, H.oracle_blocks(cfg, [params]))
+    err = H.rel_l2(y, ref)
+    # the update the block adds, y - x, carries the quantisation error: bound
+    # it relative to its own size as well, allowing for the bf16 rounding of
+    # the output itself
+    x64 = x.float().cpu().numpy().astype(np.float64)
+    upd = H.rel_l2(y - x64, ref - x64)
+    rounding = H.rel_l2(synth.round_bf16(ref.astype(np.float32)) - x64, ref - x64)
+    worst = float(np.abs(y - ref).max())
+    print(f"{base.name} block 0, all {cfg.tokens} rows: rel L2 {err:.3e}, update rel L2 {upd:.3e} "
+          f"(output rounding {rounding:.3e}), max abs {worst:.3e}")
+    assert err <= 5e-2
+    assert upd <= 5e-2 + 2 * rounding
+
+
 def test_residency_invariance_full_width():
     cfg = synth.CFG_SWEEP.with_(n_blocks=4)
     params = synth.stack_params(cfg)
@@ -93,7 +126,7 @@ def _host_sum(a: np.ndarray) -> int:
 
 @pytest.mark.parametrize("size_mb,n,k", [(16, 5, 0), (16, 5, 2), (256, 3, 1), (1024, 2, 0)])
 @pytest.mark.parametrize("staging,host", [(0, "pinned"), (1, "pinned"), (0, "register"),
-                                          (1, "register")])
+                                          (1, "register"), (0, "pageable")])
 def test_bytes_blocks_stage_and_checksum(size_mb, n, k, staging, host):
     from layerwise_weight_offload_slot_gb300.stack import OffloadStack
     size = size_mb << 20

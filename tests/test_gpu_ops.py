@@ -21,6 +21,29 @@ def rel(y, ref):
     return float(np.linalg.norm(y - ref) / max(np.linalg.norm(ref), 1e-30))
 
 
+# Element bound of fp32 outputs: fp32 accumulation over K products with unit
+# roundoff u = 2^-24 leaves a statistical error of about sqrt(K) u sum|a_k w_k|,
+# which at K = 5120 with the tests' operand scales is ~7e-5 of a row's largest
+# value; a wrong element or column is off by the order of the row scale.
+FP32_ELEMENT_TOL = 1e-4
+
+
+def close(y, ref, tol, scale=None, el_tol=None):
+    """The global relative L2 error is below tol, and every element is within
+    el_tol (default tol) times the largest |ref| of its row (or times `scale`),
+    so a few wrong elements or columns cannot hide inside the norm.  For bf16
+    outputs tol is at least twice the bf16 rounding (2^-9 relative) that
+    bounds one element; fp32 outputs take FP32_ELEMENT_TOL."""
+    y = np.asarray(y, np.float64)
+    ref = np.asarray(ref, np.float64)
+    r = rel(y, ref)
+    assert r < tol, f"relative L2 error {r:.3e} >= {tol}"
+    el = tol if el_tol is None else el_tol
+    s = np.abs(ref).max(axis=-1, keepdims=True) if scale is None else scale
+    worst = float((np.abs(y - ref) / np.maximum(s, 1e-30)).max())
+    assert worst <= el, f"element error {worst:.3e} of its row scale > {el}"
+
+
 def stream():
     return torch.cuda.current_stream().cuda_stream
 
@@ -59,7 +82,7 @@ def test_gemm_matches_oracle(M, N, K, epi):
         tol = 6e-3
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    assert rel(f64(out), ref) < tol
+    close(f64(out), ref, tol, el_tol=FP32_ELEMENT_TOL if tol < 1e-4 else None)
 
 
 def test_gemm_output_stride_and_no_bias():
@@ -71,7 +94,7 @@ def test_gemm_output_stride_and_no_bias():
     dlo.dlo_op_gemm(A.data_ptr(), W.data_ptr(), dlo.DT_BF16, None, 0, None, M, N, K, 0,
                     out.data_ptr(), ldo, None, 0, 1, None, stream())
     torch.cuda.synchronize()
-    assert rel(f64(out[:, :N]), f64(A) @ f64(W).T) < 6e-3
+    close(f64(out[:, :N]), f64(A) @ f64(W).T, 6e-3)
     assert bool((out[:, N:] == 7.0).all())
 
 
@@ -86,7 +109,7 @@ def test_gemm_scale_segments():
                     out.data_ptr(), N, None, 0, 1, None, stream())
     torch.cuda.synchronize()
     ref = f64(A) @ f64(W).T * np.repeat([0.5, 2.0, 3.0], 32)[None]
-    assert rel(f64(out), ref) < 6e-3
+    close(f64(out), ref, 6e-3)
 
 
 @pytest.mark.parametrize("B,H,hd,nq,nk", [(1, 1, 64, 64, 64), (2, 3, 72, 100, 300), (1, 2, 128, 257, 129),
@@ -108,7 +131,8 @@ def test_attention_matches_oracle(B, H, hd, nq, nk):
     q, k, v = f64(Q)[:, :D], f64(kv)[:, D:2 * D], f64(kv)[:, 2 * D:]
     for b in range(B):
         ref = dit.attention(q[b * nq:(b + 1) * nq], k[b * nk:(b + 1) * nk], v[b * nk:(b + 1) * nk], H)
-        assert rel(f64(O[b * nq:(b + 1) * nq]), ref) < 1e-2
+        # O is a convex combination of v rows: its error scales with max |v|
+        close(f64(O[b * nq:(b + 1) * nq]), ref, 1e-2, scale=np.abs(v[b * nk:(b + 1) * nk]).max())
 
 
 @pytest.mark.parametrize("mode", ["modulate", "affine", "plain"])
@@ -136,7 +160,7 @@ def test_layernorm_matches_oracle(mode):
         dlo.dlo_op_layernorm(x.data_ptr(), B * N, D, N, None, None, 0, None, None, 1e-6,
                              out.data_ptr(), stream())
     torch.cuda.synchronize()
-    assert rel(f64(out), ref) < 5e-3
+    close(f64(out), ref, 5e-3)
 
 
 def test_rmsnorm_matches_oracle():
@@ -149,7 +173,7 @@ def test_rmsnorm_matches_oracle():
     torch.cuda.synchronize()
     after = f64(buf)
     ref = dit.rmsnorm(before[:, col0:col0 + D], f64(w), 1e-6)
-    assert rel(after[:, col0:col0 + D], ref) < 5e-3
+    close(after[:, col0:col0 + D], ref, 5e-3)
     np.testing.assert_array_equal(after[:, :col0], before[:, :col0])
     np.testing.assert_array_equal(after[:, col0 + D:], before[:, col0 + D:])
 
@@ -165,7 +189,7 @@ def test_adaln_matches_oracle(B):
     dlo.dlo_op_adaln(c.data_ptr(), B, C, W.data_ptr(), bias.data_ptr(), N, m.data_ptr(), stream())
     torch.cuda.synchronize()
     ref = dit.linear(dit.silu(f64(c)), f64(W), f64(bias))
-    assert rel(f64(m), ref) < 1e-5
+    close(f64(m), ref, 1e-5, el_tol=FP32_ELEMENT_TOL)
 
 
 @pytest.mark.parametrize("mode", [0, 1])
@@ -224,7 +248,7 @@ def test_gemm_e4m3_weights_match_oracle(M, N, K, epi):
         tol = 6e-3
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    assert rel(f64(out), ref) < tol
+    close(f64(out), ref, tol, el_tol=FP32_ELEMENT_TOL if tol < 1e-4 else None)
 
 
 def test_gemm_e4m3_decodes_every_code_exactly():
@@ -333,7 +357,7 @@ def test_gemm_w8a8_matches_oracle(M, N, K, epi):
         tol = 6e-3
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    assert rel(f64(out), ref) < tol
+    close(f64(out), ref, tol, el_tol=FP32_ELEMENT_TOL if tol < 1e-4 else None)
 
 
 def test_gemm_w8a8_multiplies_every_code_pair_exactly():
@@ -389,4 +413,4 @@ def test_bounded_wait_times_out_without_a_fault():
                     out.data_ptr(), 64, None, 0, 1, err2.data_ptr(), stream())
     torch.cuda.synchronize()
     assert int(err2.item()) == 0
-    assert rel(f64(out), f64(A) @ f64(W).T) < 6e-3
+    close(f64(out), f64(A) @ f64(W).T, 6e-3)
