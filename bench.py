@@ -7,7 +7,7 @@ the two device slots, the next step's input being this step's output.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--staging memcpy|gather] [--resident k]
                     [--host pinned|register] [--no-cpu-baseline] [--no-graphs]
-                    [--sweep | --ops]
+                    [--sweep | --ops | --link]
 
 The timed forwards replay whole-forward CUDA graphs unless --no-graphs.
 Prints ONE JSON line (rank 0).  With N > 1 (torchrun) every rank runs an
@@ -40,7 +40,9 @@ FP8_OVER_BF16 = 2.0   # nominal dense tensor rates: fp8 4.5 PFLOP/s, bf16 2.25 P
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--passes", type=int, default=3,
+                   help="timed passes of --steps steps each; the line reports the median pass")
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default=synth.CFG_DITXL.name,
@@ -54,6 +56,9 @@ def parse():
     p.add_argument("--sweep", action="store_true",
                    help="residency sweep (k = 0,2,4,8) on the 40-block hidden-5120 stack at 8192 "
                         "tokens and a 16 MB..1 GB staging sweep; prints one JSON line")
+    p.add_argument("--link", action="store_true",
+                   help="host-to-device rates of 1 GiB: one copy engine, two at once, copy beside "
+                        "the gather kernel; prints one JSON line")
     p.add_argument("--ops", action="store_true",
                    help="time every unit op of one block of --workload at its shapes (CUDA "
                         "events over --steps back-to-back launches after --warmup); prints one "
@@ -181,15 +186,29 @@ def cores() -> int:
 L2_BYTES = 129 * 1000 * 1000   # GB300 L2
 
 
-def run_config(args, cfg, parts, container_bytes, world: int) -> dict:
-    """The `config` object of both arms' JSON lines."""
-    blocks = [b for p, b in zip(parts, container_bytes) for _ in range(p.n_blocks)]
+def weight_bytes(p) -> int:
+    """Bytes of one block's parameters as stored on the host: linear weights
+    1 byte per element for E4M3 stacks (plus one fp32 scale per linear), every
+    other tensor 2 bytes (bf16).  Alignment padding of the flat layout is not
+    counted (it is under 0.1% of a block)."""
+    n = 0
+    for _, shape, role in synth.param_specs(p):
+        k = int(np.prod(shape))
+        n += k * (1 if role == "linear_w" and synth.fp8_weights(p.wdtype) else 2)
+        if role == "linear_w" and synth.fp8_weights(p.wdtype):
+            n += 4
+    return n
+
+
+def run_config(args, cfg, parts, world: int) -> dict:
+    """The `config` object of both arms' JSON lines (host arithmetic only: the
+    reference arm loads nothing of the library)."""
+    blocks = [weight_bytes(p) for p in parts for _ in range(p.n_blocks)]
     streamed = sum(blocks[args.resident:])
     weights = {synth.W_BF16: "bf16", synth.W_E4M3: "e4m3", synth.W_E4M3_A8: "e4m3 (W8A8)"}
     return {"workload": cfg.name, "blocks": cfg.n_blocks, "hidden": cfg.hidden,
             "containers": [{"kind": "video" if p.kind else "dit", "blocks": p.n_blocks, "heads": p.heads,
-                            "ffn": p.ffn, "block_bytes": b, "weights": weights[p.wdtype]}
-                           for p, b in zip(parts, container_bytes)],
+                            "ffn": p.ffn, "weights": weights[p.wdtype]} for p in parts],
             "batch": cfg.batch, "tokens": cfg.tokens, "resident": args.resident,
             "staging": args.staging, "host": args.host, "graphs": not args.no_graphs,
             "parallelism": "replicas" if world > 1 else "single",
@@ -198,40 +217,30 @@ def run_config(args, cfg, parts, container_bytes, world: int) -> dict:
                    f"inputs smaller than L2 ({streamed / 1e6:.1f} MB streamed per step), L2 not flushed")}
 
 
-def container_bytes_of(parts):
-    """Flat block sizes from the library's layout table (a host function)."""
-    import layerwise_weight_offload_slot_gb300 as dlo
-    return [dlo.dlo_block_bytes(dlo.make_desc(block_kind=p.kind, n_blocks=p.n_blocks, hidden=p.hidden,
-                                              heads=p.heads, head_dim=p.head_dim, ffn=p.ffn,
-                                              cond_dim=p.cond_dim, text_dim=p.text_dim,
-                                              max_batch=p.batch, max_tokens=p.tokens,
-                                              max_text_tokens=p.text_tokens, wdtype=p.wdtype))
-            for p in parts]
-
-
 def run_reference(args, cfg, rank: int, world: int):
+    """The reference arm: the float64 CPU oracle, as it stands, on the host
+    cores.  Each timed step runs one block of every container (a bounded
+    sample); `ms_per_step` x `steps` is the time actually measured, and
+    `value` extrapolates each timed step to the whole stack's step."""
     if rank != 0:
         return
-    # each reference "step": one block of the stack's step on the host cores,
-    # the steps/s figure extrapolated to the whole stack (n_blocks blocks)
     parts = parts_of(cfg)
     if args.warmup:
         oracle_block_seconds(parts[0], 0.0, max_blocks=1)
-    step_s = []
+    sample_s, stack_s = [], []
     for s in range(args.steps):
-        # one block of every container per step, weighted by its block count
-        step_s.append(sum(oracle_block_seconds(p, 0.0, max_blocks=1)[0] * p.n_blocks for p in parts))
-    value = 1.0 / statistics.mean(step_s)
-    try:
-        config = run_config(args, cfg, parts, container_bytes_of(parts), world)
-    except ImportError:   # library not built: the fields that need no layout table
-        config = {"workload": cfg.name, "parallelism": "replicas" if world > 1 else "single"}
-    sample = (f"1 block of each of the {len(parts)} container(s) per step, float64 numpy oracle, "
-              f"extrapolated to the {cfg.n_blocks}-block step")
+        t = [oracle_block_seconds(p, 0.0, max_blocks=1)[0] for p in parts]
+        sample_s.append(sum(t))
+        stack_s.append(sum(ti * p.n_blocks for ti, p in zip(t, parts)))
+    value = 1.0 / statistics.mean(stack_s)
+    sample = (f"each timed step: 1 block of each of the {len(parts)} container(s), float64 numpy "
+              f"oracle; value extrapolated to the {cfg.n_blocks}-block step")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / value,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(sample_s),
+            "extrapolation": {"blocks_per_timed_step": len(parts), "blocks_per_stack_step": cfg.n_blocks,
+                              "stack_ms_per_step": 1e3 * statistics.mean(stack_s)},
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config,
+            "data": "synthetic", "config": run_config(args, cfg, parts, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -292,18 +301,9 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
     st.set_resident(args.resident)
     streamed_bytes = sum(st.block_sizes[args.resident:])
 
-    # link peak: best pinned 1 GiB host->device copy (copy engine), this run
-    hbuf = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
-    dbuf = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
-    link = 0.0
-    for _ in range(3):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        dbuf.copy_(hbuf, non_blocking=True)
-        e1.record()
-        torch.cuda.synchronize()
-        link = max(link, (1 << 30) / (e0.elapsed_time(e1) * 1e-3) / 1e9)
-    del hbuf, dbuf
+    # link peak: the best of one copy engine and two engines at once, this run
+    links = link_rates(torch, dev)
+    link = links["peak_gbs"]
 
     steps_total = args.warmup + args.steps
     x0 = torch.from_numpy(synth.activations(parts[0])).to(torch.bfloat16).to(dev)
@@ -338,28 +338,33 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
     torch.cuda.synchronize()
     st.wait()
 
-    # ---------------- timed region
+    # ---------------- timed region: `passes` passes of exactly `steps` steps
+    # each, bracketed by a barrier and a synchronize; the line reports the
+    # median pass (the host link is shared with a neighbouring GPU, whose
+    # traffic can slow a link-bound pass) and lists every pass
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
     s_before = st.stats()
     launches0 = s_before["kernel_launches"]
-    barrier()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(cs)
-    for i in range(args.steps):
-        step(args.warmup + i)
-    ev1.record(cs)
-    torch.cuda.synchronize()
-    barrier()
-    ms = ev0.elapsed_time(ev1)
+    pass_ms = []
+    for p_ in range(args.passes):
+        barrier()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(cs)
+        for i in range(args.steps):
+            step(args.warmup + i)
+        ev1.record(cs)
+        torch.cuda.synchronize()
+        barrier()
+        pass_ms.append(ev0.elapsed_time(ev1))
     clk = clocks.stop()
     st.wait()
     s_after = st.stats()
-    launches = s_after["kernel_launches"] - launches0
-    graph_launches = s_after["graph_launches"] - s_before["graph_launches"]
-    ms_local = ms
+    launches = (s_after["kernel_launches"] - launches0) // args.passes
+    graph_launches = (s_after["graph_launches"] - s_before["graph_launches"]) // args.passes
+    ms_local = statistics.median(pass_ms)
 
     # ---------------- overlap pass (events per streamed execution)
     st.set_timing(1)
@@ -425,7 +430,7 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
     t_link = streamed_bytes / (link * 1e9) * 1e3
     t_roof = max(t_compute, t_link)
     step_roof = {"t_roof_ms": t_roof, "compute_ms_at_peak": t_compute, "link_ms_at_peak": t_link,
-                 "link_gbs_measured": link, "streamed_bytes_per_step": streamed_bytes,
+                 "link_gbs_measured": link, "link": links, "streamed_bytes_per_step": streamed_bytes,
                  "flops_per_step": flops_step,
                  "bound": "link" if t_link >= t_compute else "tensor"}
     kernels = {n: {"launches_per_step": v["launches"] / args.steps,
@@ -474,6 +479,7 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
         host_step(args.warmup + i)
     e2e_s = time.perf_counter() - t0
     ms, value, e2e_s, e2e_value = aggregate(ms_local, e2e_s, args.steps, world, dist, dev)
+    pass_values = [aggregate(m, e2e_s, args.steps, world, dist, dev)[1] for m in pass_ms]
     ms_per_step = ms / args.steps
     step_roof["frac"] = step_roof["t_roof_ms"] / ms_per_step
     h2d = B * N * D * 2 + sum(c.numel() * c.element_size() for c in hconds[0]) + \
@@ -497,8 +503,10 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": {synth.W_E4M3: "bf16 (e4m3 weights)", synth.W_E4M3_A8: "e4m3 x e4m3 (W8A8)"}.get(
                     parts[0].wdtype, "bf16"), "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations)",
-                "config": run_config(args, cfg, parts, st.container_bytes, world),
+                "config": run_config(args, cfg, parts, world),
                 "roofline": roof, "step_roofline": step_roof, "overlap": overlap,
+                "passes": {"count": args.passes, "steps_per_pass": args.steps, "values": pass_values,
+                           "spread": (max(pass_values) - min(pass_values)) / statistics.median(pass_values)},
                 "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "graph_launches": graph_launches,
                 "clocks": clk, "registered_read_only": stats["registered_read_only"]}
@@ -519,18 +527,64 @@ def aggregate(ms: float, e2e_s: float, steps: int, world: int, dist=None, device
     return ms, world * steps / (ms * 1e-3), e2e_s, world * steps / e2e_s
 
 
-def link_peak_gbs(torch, dev) -> float:
-    hbuf = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
-    dbuf = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
-    best = 0.0
-    for _ in range(3):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        dbuf.copy_(hbuf, non_blocking=True)
-        e1.record()
-        torch.cuda.synchronize()
-        best = max(best, (1 << 30) / (e0.elapsed_time(e1) * 1e-3) / 1e9)
-    return best
+def link_rates(torch, dev, reps: int = 3) -> dict:
+    """Host-to-device rates of 1 GiB from pinned memory, best of `reps` each:
+    one copy-engine copy; two 512 MiB copies on two streams at once; one
+    512 MiB copy beside the SM gather kernel reading the other half through
+    the mapped host address.  `peak_gbs` is the best of the three and
+    `peak_method` names it."""
+    import layerwise_weight_offload_slot_gb300 as dlo
+    n = 1 << 30
+    half = n // 2
+    hbuf = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    hbuf[::4096] = 1
+    dbuf = torch.empty(n, dtype=torch.uint8, device=dev)
+    main = torch.cuda.current_stream(dev)
+    side = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+
+    def timed(fn):
+        best = 0.0
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(main)
+            for s in side:
+                s.wait_stream(main)
+            fn()
+            for s in side:
+                main.wait_stream(s)
+            e1.record(main)
+            torch.cuda.synchronize(dev)
+            best = max(best, n / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+        return best
+
+    def one():
+        with torch.cuda.stream(side[0]):
+            dbuf.copy_(hbuf, non_blocking=True)
+
+    def two():
+        for i, s in enumerate(side):
+            with torch.cuda.stream(s):
+                dbuf[i * half:(i + 1) * half].copy_(hbuf[i * half:(i + 1) * half], non_blocking=True)
+
+    def copy_gather():
+        with torch.cuda.stream(side[0]):
+            dbuf[:half].copy_(hbuf[:half], non_blocking=True)
+        dlo.dlo_op_stage(dbuf.data_ptr() + half, hbuf.data_ptr() + half, half, dlo.STAGE_GATHER,
+                         side[1].cuda_stream)
+
+    r = {"one_engine_gbs": timed(one), "two_copy_streams_gbs": timed(two),
+         "copy_plus_gather_gbs": timed(copy_gather)}
+    ok = bool(torch.equal(dbuf[::4096].cpu(), hbuf[::4096]))
+    del hbuf, dbuf
+    names = {"one_engine_gbs": "one 1 GiB cudaMemcpyAsync",
+             "two_copy_streams_gbs": "two 512 MiB cudaMemcpyAsync on two streams",
+             "copy_plus_gather_gbs": "512 MiB cudaMemcpyAsync beside the gather kernel on 512 MiB"}
+    best = max(names, key=lambda k: r[k])
+    r["peak_gbs"] = r[best]
+    r["peak_method"] = names[best]
+    r["bytes_checked"] = ok
+    return r
 
 
 def run_sweep(args):
@@ -540,8 +594,9 @@ def run_sweep(args):
     from layerwise_weight_offload_slot_gb300.stack import HostBlocks, OffloadStack
 
     dev = torch.device("cuda", 0)
-    link = link_peak_gbs(torch, dev)
-    out = {"metric": "residency and staging sweep", "link_gbs_measured": link}
+    links = link_rates(torch, dev)
+    link = links["peak_gbs"]
+    out = {"metric": "residency and staging sweep", "link_gbs_measured": link, "link": links}
 
     # ---- residency: k = 0, 2, 4, 8 resident leading blocks
     cfg = synth.CFG_SWEEP
@@ -706,7 +761,10 @@ def run_ops(args, cfg):
     import layerwise_weight_offload_slot_gb300 as dlo
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    st = torch.cuda.current_stream().cuda_stream
+    # every launch reads the stream from here: the timed launches are
+    # captured on a side stream into a CUDA graph and replayed, so the host
+    # cost of a Python call per launch is not timed
+    S = [torch.cuda.current_stream().cuda_stream]
     g = torch.Generator(device=dev).manual_seed(0)
     B, N, D, F, H, hd = cfg.batch, cfg.tokens, cfg.hidden, cfg.ffn, cfg.heads, cfg.head_dim
     BN = B * N
@@ -742,32 +800,32 @@ def run_ops(args, cfg):
         def run():
             if w8a8:
                 dlo.dlo_op_quantize_act(A.data_ptr(), M, K, K, qa.data_ptr(), qsc[-1:].data_ptr(),
-                                        qsc.data_ptr(), st)
+                                        qsc.data_ptr(), S[0])
                 dlo.dlo_op_gemm_w8a8(qa.data_ptr(), qsc[-1:].data_ptr(), Wt.data_ptr(), sc.data_ptr(),
                                      Nn, zeros.data_ptr(), M, Nn, K, epi, out.data_ptr(), ldo,
                                      gate.data_ptr() if gate is not None else None, 6 * D,
-                                     max(1, M // B), err.data_ptr(), st)
+                                     max(1, M // B), err.data_ptr(), S[0])
             else:
                 dlo.dlo_op_gemm(A.data_ptr(), Wt.data_ptr(), dlo.DT_E4M3 if w8a16 else dlo.DT_BF16,
                                 sc.data_ptr() if sc is not None else None, Nn, zeros.data_ptr(), M, Nn,
                                 K, epi, out.data_ptr(), ldo,
                                 gate.data_ptr() if gate is not None else None, 6 * D,
-                                max(1, M // B), err.data_ptr(), st)
+                                max(1, M // B), err.data_ptr(), S[0])
         ops.append((name, run, flops, nbytes, Wt))
 
     def ln(name, affine):
         def run():
             if affine:
                 dlo.dlo_op_layernorm(x.data_ptr(), BN, D, N, None, None, 0, ones.data_ptr(),
-                                     zeros.data_ptr(), 1e-6, h.data_ptr(), st)
+                                     zeros.data_ptr(), 1e-6, h.data_ptr(), S[0])
             else:
                 dlo.dlo_op_layernorm(x.data_ptr(), BN, D, N, mod.data_ptr(), mod[:, D:].data_ptr(),
-                                     6 * D, None, None, 1e-6, h.data_ptr(), st)
+                                     6 * D, None, None, 1e-6, h.data_ptr(), S[0])
         ops.append((name, run, 0.0, 6.0 * BN * D, None))
 
     def attn(name, q, k, v, nq, nk, ldq, ldk, ldv):
         def run():
-            dlo.dlo_op_attention(q, k, v, a.data_ptr(), B, H, hd, nq, nk, ldq, ldk, ldv, D, st)
+            dlo.dlo_op_attention(q, k, v, a.data_ptr(), B, H, hd, nq, nk, ldq, ldk, ldv, D, S[0])
         ops.append((name, run, 4.0 * B * H * nq * nk * hd, 0.0, None))
 
     bp = big.data_ptr()
@@ -776,7 +834,7 @@ def run_ops(args, cfg):
         cvec = rnd(B, cfg.cond_dim)
         Wada = rnd(6 * D, cfg.cond_dim, scale=0.02)
         ops.append(("adaln", lambda: dlo.dlo_op_adaln(cvec.data_ptr(), B, cfg.cond_dim, Wada.data_ptr(),
-                                                       zeros.data_ptr(), 6 * D, mod.data_ptr(), st),
+                                                       zeros.data_ptr(), 6 * D, mod.data_ptr(), S[0]),
                     0.0, 2.0 * 6 * D * cfg.cond_dim, Wada))
         ln("layernorm", False)
         gemm("gemm_qkv", h, BN, 3 * D, D, dlo.EPI_BIAS, big, 3 * D)
@@ -790,7 +848,7 @@ def run_ops(args, cfg):
         ln("layernorm", False)
         gemm("gemm_qkv", h, BN, 3 * D, D, dlo.EPI_BIAS, big, 3 * D)
         ops.append(("rmsnorm_qk", lambda: dlo.dlo_op_rmsnorm(big.data_ptr(), BN, D, 3 * D, 0,
-                                                              ones.data_ptr(), 1e-6, st),
+                                                              ones.data_ptr(), 1e-6, S[0]),
                     0.0, 4.0 * BN * D, None))
         attn("attention_self", bp, bp + 2 * D * es, bp + 4 * D * es, N, N, 3 * D, 3 * D, 3 * D)
         gemm("gemm_o", a, BN, D, D, dlo.EPI_RESIDUAL, x, D)
@@ -802,17 +860,26 @@ def run_ops(args, cfg):
         gemm("gemm_fc2", big, BN, D, F, dlo.EPI_RESIDUAL, x, D)
     peaks = measured_peaks()
     res = {}
+    cap = torch.cuda.Stream(dev)
     for name, run, flops, nbytes, _keep in ops:
         for _ in range(args.warmup):
             run()
         torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        S[0] = cap.cuda_stream
+        with torch.cuda.graph(graph, stream=cap):
+            for _ in range(args.steps):
+                run()
+        S[0] = torch.cuda.current_stream().cuda_stream
+        graph.replay()
+        torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for _ in range(args.steps):
-            run()
+        graph.replay()
         e1.record()
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / args.steps
+        del graph
         r = {"us": us}
         if flops:
             r["tflops"] = flops / us / 1e6
@@ -834,6 +901,10 @@ def main():
         return
     if args.ops:
         run_ops(args, synth.CONFIGS[args.workload])
+        return
+    if args.link:
+        import torch
+        print(json.dumps({"mode": "link", **link_rates(torch, torch.device("cuda", 0), reps=5)}), flush=True)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus else 1)))
