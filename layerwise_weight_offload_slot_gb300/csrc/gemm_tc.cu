@@ -21,6 +21,9 @@
 // and the per-tensor scale is applied to the fp32 accumulator in the epilogue.
 // The widened tiles live in CB buffers of their own (conv / conv_empty
 // barriers), so the ring of A tiles and raw codes is four stages deep.
+// E4M3-weight GEMMs with at least 256 rows run on CTA pairs instead
+// (gemm_pair_kernel, tcgen05 cta_group::2, below): one 256 x 256 MMA over two
+// SMs, each SM widening half of the weight tile.
 //
 // Every mbarrier wait is bounded (2 s); a wait that runs out sets the
 // kernel's error word and a CTA-wide abort flag, after which every role
@@ -571,6 +574,450 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT, CB>::THREADS, 1)
     }
 }
 
+// ------------------------------------------------------------------ CTA-pair E4M3-weight GEMM
+//
+// W8A16 on CTA pairs (tcgen05 cta_group::2).  A cluster of two CTAs computes
+// one 256 x 256 output tile.  CTA r (its rank in the cluster) loads the tile's
+// A rows 128r .. 128r+127 and the E4M3 codes of the tile's weight rows
+// 128r .. 128r+127, widens its own 128 weight rows to bf16 (12 converter
+// warps, as gemm_kernel's), and holds accumulator rows 128r .. 128r+127
+// (128 lanes x 256 fp32 columns, two sets) in its own tensor memory.  Rank
+// 0's MMA thread issues one M = 256, N = 256, K = 16 MMA per 32-byte K step
+// for both CTAs once both widened halves are ready; the MMA commits reach
+// both CTAs (multicast).  Readiness of rank 1's half crosses to rank 0 once
+// per step without a fence on any thread: rank 1's converter warps order
+// their stores for the async proxy (fence.proxy.async) and arrive on a
+// barrier of their own CTA; rank 1's warp 1, idle otherwise, then issues a
+// 16-byte bulk copy into rank 0's shared memory whose completion lands as
+// transaction bytes on rank 0's barrier for that widened buffer (ordered
+// after the stores like a TMA store of shared memory that threads wrote).
+// A cluster-scope release arrival would cost ~550 ns per step (measured),
+// more than the step's MMAs.  Each CTA runs gemm_kernel's
+// epilogue on its own 128 rows, then arrives on rank 0's accumulator-free
+// barrier.  Per SM a 64-K step is one 128 x 256 x 64 product -- the bf16
+// kernel's 256-wide MMA shape -- while each SM still widens 128 weight rows
+// per step, as the two-row-block gemm_kernel<..., MT = 2> does with twice as
+// many 128-wide MMAs.
+constexpr int PAIR_BN = 256;              // output columns of a pair tile
+constexpr int PAIR_HALF = PAIR_BN / 2;    // weight rows each CTA loads and widens
+constexpr int PAIR_BM = 2 * BM;           // output rows of a pair tile
+
+template <int STAGES, int CB>
+struct PairPlan {
+    static constexpr int RAW_TILE = PAIR_HALF * BK;       // codes of one CTA's weight rows
+    static constexpr int W_TILE = PAIR_HALF * BK * 2;     // the same rows widened (MMA reads)
+    static constexpr int A_OFF = 0;
+    static constexpr int W_OFF = STAGES * A_TILE;
+    static constexpr int RAW_OFF = W_OFF + CB * W_TILE;
+    static constexpr int STG_OFF = RAW_OFF + STAGES * RAW_TILE;   // 4 warps x 2 boxes
+    static constexpr int BAR_OFF = STG_OFF + 8 * STG_BYTES;
+    // full[STAGES], empty[STAGES], conv[CB], cempty[CB], wdone[CB], tfull[2], tempty[2], drain,
+    // then a 16-byte slot the forwarded bulk copies land in
+    static constexpr int SIG_OFF = (BAR_OFF + (2 * STAGES + 3 * CB + 5) * 8 + 15) / 16 * 16;
+    static constexpr int TMEM_SLOT_OFF = SIG_OFF + 16;
+    static constexpr uint32_t SIG_BYTES = 16;
+    static constexpr int ABORT_OFF = TMEM_SLOT_OFF + 4;
+    static constexpr int BYTES = ABORT_OFF + 4 + 1024;   // + alignment slack
+    static constexpr int THREADS = kThreads + kConvWarps * 32;
+    static constexpr uint32_t TX = A_TILE + RAW_TILE;
+    static constexpr uint32_t TMEM_COLS = 2 * PAIR_BN;   // two accumulator sets
+    static_assert(STG_OFF % 1024 == 0 && W_OFF % 1024 == 0, "swizzled buffers must be 1024-B aligned");
+};
+
+template <int STAGES, int CB>
+__global__ void __launch_bounds__(PairPlan<STAGES, CB>::THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmO, const EpiArgs args) {
+    using P = PairPlan<STAGES, CB>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_full = sbase + P::BAR_OFF;
+    const uint32_t bar_empty = bar_full + STAGES * 8;
+    const uint32_t bar_conv = bar_empty + STAGES * 8;
+    const uint32_t bar_cempty = bar_conv + CB * 8;
+    const uint32_t bar_wdone = bar_cempty + CB * 8;
+    const uint32_t bar_tfull = bar_wdone + CB * 8;
+    const uint32_t bar_tempty = bar_tfull + 2 * 8;
+    const uint32_t bar_drain = bar_tempty + 2 * 8;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + P::TMEM_SLOT_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P::ABORT_OFF);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + s * 8, 1);
+            mbar_init(bar_empty + s * 8, 1);
+        }
+        for (int c = 0; c < CB; ++c) {
+            // rank 0's converter warps (one of them also expects the bytes
+            // rank 1 forwards)
+            mbar_init(bar_conv + c * 8, kConvWarps);
+            mbar_init(bar_cempty + c * 8, 1);
+            mbar_init(bar_wdone + c * 8, kConvWarps);   // rank 1: its converter warps
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar_tfull + a * 8, 1);
+            mbar_init(bar_tempty + a * 8, 8);              // both CTAs' epilogue warps
+        }
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmO);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(sbase + P::TMEM_SLOT_OFF, P::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    // the peer's barriers are initialised before anything arrives on them
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int kblocks = (args.K + BK - 1) / BK;
+    // rank 0's barriers and signal slot that rank 1 reaches, as shared::cluster addresses
+    const uint32_t conv_r0 = mapa_shared(bar_conv, 0);
+    const uint32_t tempty_r0 = mapa_shared(bar_tempty, 0);
+    const uint32_t sig_r0 = mapa_shared(sbase + P::SIG_OFF, 0);
+    // weights are never the predecessor's output (w_ready): the producer's
+    // first code tiles may load before the programmatic-launch wait
+    const bool prefetch_w = args.w_ready && warp == 0 && lane == 0;
+    if (!prefetch_w) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
+
+    auto fail = [&]() {
+        *abort_flag = 1;
+        if (args.err) atomicExch(args.err, 1);
+    };
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer: this CTA's A rows and weight-code rows
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        uint32_t issued = 0, last_par = 0;
+        auto load_w = [&](int st, int kb, int nb) {
+            tma_load_2d(sbase + P::RAW_OFF + st * P::RAW_TILE, &tmB, kb * BK,
+                        nb * PAIR_BN + static_cast<int>(rank) * PAIR_HALF, bar_full + st * 8);
+        };
+        int pre = 0;
+        if (prefetch_w) {
+            if (pair < args.num_tiles) {
+                int mb0, nb0;
+                tile_coords(pair, args.num_m, args.num_n, args.n_major, mb0, nb0);
+                pre = kblocks < STAGES ? kblocks : STAGES;
+                for (int st = 0; st < pre; ++st) {
+                    mbar_arrive_expect_tx(bar_full + st * 8, P::TX);
+                    load_w(st, st, nb0);
+                    issued |= 1u << st;
+                }
+            }
+            pdl_wait();
+            pdl_launch_dependents();
+        }
+        for (int tile = pair; ok && tile < args.num_tiles; tile += npairs) {
+            int mb, nb;
+            tile_coords(tile, args.num_m, args.num_n, args.n_major, mb, nb);
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait(bar_empty + s * 8, ph ^ 1, abort_flag)) {
+                    fail();
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = bar_full + s * 8;
+                const bool w_done = tile == pair && kb < pre;
+                if (!w_done) mbar_arrive_expect_tx(fb, P::TX);
+                tma_load_2d(sbase + P::A_OFF + s * A_TILE, &tmA, kb * BK,
+                            mb * PAIR_BM + static_cast<int>(rank) * BM, fb);
+                if (!w_done) load_w(s, kb, nb);
+                issued |= 1u << s;
+                last_par = (last_par & ~(1u << s)) | (ph << s);
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+        }
+        if (!ok || *abort_flag) {
+            for (int i = 0; i < STAGES; ++i)
+                if (issued & (1u << i)) mbar_wait(bar_full + i * 8, (last_par >> i) & 1u, nullptr);
+        }
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ---------------- MMA issuer of the pair (rank 0 only)
+        constexpr uint32_t idesc = idesc_bf16_f32(PAIR_BM, PAIR_BN);
+        const uint64_t a_desc0 = sw128_kmajor_desc(sbase + P::A_OFF);
+        const uint64_t b_desc0 = sw128_kmajor_desc(sbase + P::W_OFF);
+        uint64_t a_desc = a_desc0, b_desc = b_desc0;
+        int s = 0, cb = 0;
+        uint32_t ph = 0, cph = 0;
+        int t = 0;
+        bool ok = true;
+        for (int tile = pair; ok && tile < args.num_tiles; tile += npairs, ++t) {
+            const int acc = t & 1;
+            const uint32_t aph = (t >> 1) & 1;
+            if (!mbar_wait_cluster(bar_tempty + acc * 8, aph ^ 1, abort_flag)) {
+                fail();
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * PAIR_BN;
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait_cluster(bar_conv + cb * 8, cph, abort_flag)) {
+                    fail();
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)   // 4 x 32 bytes of K per stage
+                    tc_mma_f16_pair(d_tmem, a_desc + ((kk * 32) >> 4), b_desc + ((kk * 32) >> 4), idesc,
+                                    (kb | kk) != 0);
+                tc_commit_pair_mc(bar_empty + s * 8, 3);
+                tc_commit_pair_mc(bar_cempty + cb * 8, 3);
+                if (++cb == CB) {
+                    cb = 0;
+                    cph ^= 1;
+                    b_desc = b_desc0;
+                } else {
+                    b_desc += P::W_TILE >> 4;
+                }
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1;
+                    a_desc = a_desc0;
+                } else {
+                    a_desc += A_TILE >> 4;
+                }
+            }
+            if (ok) tc_commit_pair_mc(bar_tfull + acc * 8, 3);
+        }
+        if (*abort_flag) {
+            // drain: wait (bounded) until every MMA issued so far completed
+            tc_commit_pair(bar_drain);
+            mbar_wait(bar_drain, 0, nullptr);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- rank 1: forward each widened half's readiness to rank 0
+        int cb = 0;
+        uint32_t cph = 0;
+        bool ok = true;
+        for (int tile = pair; ok && tile < args.num_tiles; tile += npairs) {
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait(bar_wdone + cb * 8, cph, abort_flag)) {
+                    fail();
+                    ok = false;
+                    break;
+                }
+                fence_proxy_async_smem();
+                bulk_s2s_cluster(sig_r0, sbase + P::SIG_OFF, P::SIG_BYTES, conv_r0 + cb * 8);
+                if (++cb == CB) {
+                    cb = 0;
+                    cph ^= 1;
+                }
+            }
+        }
+    } else if (warp >= 2 && warp < 6) {
+        // ---------------- epilogue: warp q owns this CTA's accumulator rows 32q .. 32q+31
+        const int q = warp & 3;
+        const uint32_t stg0 = sbase + P::STG_OFF + q * 2 * STG_BYTES;
+        uint8_t* stg0p = smem + P::STG_OFF + q * 2 * STG_BYTES;
+        int bi = 0;
+        int t = 0;
+        const bool residual = args.epi == DLO_EPI_RESIDUAL;
+        for (int tile = pair; tile < args.num_tiles; tile += npairs, ++t) {
+            const int acc = t & 1;
+            const uint32_t aph = (t >> 1) & 1;
+            int mb, nb;
+            tile_coords(tile, args.num_m, args.num_n, args.n_major, mb, nb);
+            bool ok = mbar_wait(bar_tfull + acc * 8, aph, abort_flag);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) {
+                if (lane == 0) fail();
+                break;
+            }
+            tc_fence_after();
+            const int row0 = mb * PAIR_BM + static_cast<int>(rank) * BM + q * 32;
+            const int row = row0 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * PAIR_BN;
+            if (residual) {
+                const float* grow = args.gate ? args.gate + static_cast<size_t>(min(row, args.M - 1) /
+                                                                                 args.rows_per_batch) *
+                                                                args.gate_ld
+                                              : nullptr;
+#pragma unroll 1
+                for (int c0 = 0; c0 < PAIR_BN; c0 += 32) {
+                    const int col0 = nb * PAIR_BN + c0;
+                    if (col0 >= args.N) break;
+                    EpiBS e;
+                    epi_load(args, 1.0f, col0, e);
+                    float4 gv[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        gv[j] = (grow && col0 + 4 * j < args.N)
+                                    ? *reinterpret_cast<const float4*>(grow + col0 + 4 * j)
+                                    : make_float4(1.f, 1.f, 1.f, 1.f);
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32_nc(taddr + c0, r);
+                    tmem_wait_ld_r(r);
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                    epi_apply(e, v);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        v[4 * j] *= gv[j].x;
+                        v[4 * j + 1] *= gv[j].y;
+                        v[4 * j + 2] *= gv[j].z;
+                        v[4 * j + 3] *= gv[j].w;
+                    }
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    uint8_t* box = stg0p + bi * STG_BYTES;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<float4*>(box + sw128(lane, j)) =
+                            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_reduce_add_2d(&tmO, stg0 + bi * STG_BYTES, col0, row0);
+                        bulk_commit();
+                    }
+                    bi ^= 1;
+                }
+            } else {
+#pragma unroll 1
+                for (int c0 = 0; c0 < PAIR_BN; c0 += 64) {
+                    const int col0 = nb * PAIR_BN + c0;
+                    if (col0 >= args.N) break;
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    uint8_t* box = stg0p + bi * STG_BYTES;
+                    EpiBS e2[2];
+                    epi_load(args, 1.0f, col0, e2[0]);
+                    epi_load(args, 1.0f, col0 + 32, e2[1]);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32_nc(taddr + c0 + 32 * half, r);
+                        tmem_wait_ld_r(r);
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                        epi_apply(e2[half], v);
+                        if (args.epi == DLO_EPI_GELU) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint4 w;
+                            w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+                            w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+                            w.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+                            w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+                            *reinterpret_cast<uint4*>(box + sw128(lane, 4 * half + j)) = w;
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmO, stg0 + bi * STG_BYTES, col0, row0);
+                        bulk_commit();
+                    }
+                    bi ^= 1;
+                }
+            }
+            // this CTA's accumulator rows are read: rank 0 may issue into the set again
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_r0 + acc * 8);
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    } else if (warp >= 6) {
+        // ---------------- e4m3 -> bf16 converters: this CTA's 128 weight rows
+        const int ct = threadIdx.x - 6 * 32;
+        constexpr int kChunks = PAIR_HALF * 8;                  // 8 codes each
+        constexpr int kIter = (kChunks + kConvWarps * 32 - 1) / (kConvWarps * 32);
+        int s = 0, cb = 0;
+        uint32_t ph = 0, cph = 0;
+        bool ok = true;
+        for (int tile = pair; ok && tile < args.num_tiles; tile += npairs) {
+            for (int kb = 0; kb < kblocks; ++kb) {
+                // the stage's A tile and codes have landed: the readiness
+                // signal below covers this CTA's A tile as well
+                bool got = mbar_wait(bar_full + s * 8, ph, abort_flag);
+                if (got) got = mbar_wait(bar_cempty + cb * 8, cph ^ 1, abort_flag);
+                got = __all_sync(0xFFFFFFFFu, got);
+                if (!got) {
+                    if (lane == 0) fail();
+                    ok = false;
+                    break;
+                }
+                const uint8_t* raw = smem + P::RAW_OFF + s * P::RAW_TILE;
+                uint8_t* dst = smem + P::W_OFF + cb * P::W_TILE;
+                // every load of this thread's share first (the compiler cannot
+                // move loads above stores to a buffer it cannot tell apart)
+                uint2 v[kIter];
+#pragma unroll
+                for (int j = 0; j < kIter; ++j) {
+                    const int i = ct + j * kConvWarps * 32;
+                    if (i < kChunks) v[j] = *reinterpret_cast<const uint2*>(raw + (i >> 3) * 64 + (i & 7) * 8);
+                }
+#pragma unroll
+                for (int j = 0; j < kIter; ++j) {
+                    const int i = ct + j * kConvWarps * 32;
+                    if (i < kChunks) {
+                        uint32_t o[4];
+                        e4m3x8_to_bf16x8(v[j].x, v[j].y, o);
+                        *reinterpret_cast<uint4*>(dst + sw128(i >> 3, i & 7)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (rank != 0)
+                        mbar_arrive(bar_wdone + cb * 8);
+                    else if (ct == 0)
+                        mbar_arrive_expect_tx(bar_conv + cb * 8, P::SIG_BYTES);   // rank 1's forwarded bytes
+                    else
+                        mbar_arrive(bar_conv + cb * 8);
+                }
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1;
+                }
+                if (++cb == CB) {
+                    cb = 0;
+                    cph ^= 1;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    // neither CTA leaves while the other may still arrive on its barriers or
+    // the pair's MMAs may still read its shared memory
+    cluster_sync_all();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, P::TMEM_COLS);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 EncodeTiledFn get_encode() { return tensor_map_encoder(); }
@@ -657,6 +1104,110 @@ cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* la
     cudaError_t le_ = launch_k(gemm_kernel<BN, STAGES, FP8, MT, A8, CB>, grid, PL::THREADS, PL::BYTES, s, ta, tb, to, a);
     ++*launches;
     return le_ != cudaSuccess ? le_ : cudaGetLastError();
+}
+
+// Clusters of two CTAs of gemm_pair_kernel that fit on the GPU at once
+// (queried once; an SM a pair cannot use stays idle).
+template <int STAGES, int CB>
+int pair_clusters() {
+    static int n = -1;
+    if (n < 0) {
+        using PL = PairPlan<STAGES, CB>;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (g_num_sms / 2), 1, 1);
+        cfg.blockDim = dim3(PL::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = PL::BYTES;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int c = 0;
+        if (cudaOccupancyMaxActiveClusters(&c, gemm_pair_kernel<STAGES, CB>, &cfg) != cudaSuccess || c < 1) {
+            cudaGetLastError();
+            c = g_num_sms / 2;
+        }
+        n = c;
+    }
+    return n;
+}
+
+template <int STAGES, int CB>
+cudaError_t run_gemm_pair(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
+    using PL = PairPlan<STAGES, CB>;
+    static_assert(PL::BYTES <= 227 * 1024, "shared memory plan exceeds 227 KB");
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<STAGES, CB>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, PL::BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    CUtensorMap ta, tb, to;
+    if (!make_map(&ta, p.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.M, p.K, p.K, BM, BK,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tb, p.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.N, p.K, p.K, PAIR_HALF, BK,
+                  CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    const bool residual = p.epi == DLO_EPI_RESIDUAL;
+    if (!make_map(&to, p.out, residual ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  residual ? 4 : 2, p.M, p.N, p.ldo, 32, residual ? 32 : 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    EpiArgs a;
+    a.M = p.M;
+    a.N = p.N;
+    a.K = p.K;
+    a.epi = p.epi;
+    a.bias = static_cast<const __nv_bfloat16*>(p.bias);
+    a.scales = p.scales;
+    a.scale_seg = p.scale_seg > 0 ? p.scale_seg : p.N;
+    a.act_scale = nullptr;
+    a.gate = p.gate;
+    a.gate_ld = p.gate_ld;
+    a.rows_per_batch = p.rows_per_batch > 0 ? p.rows_per_batch : 1;
+    a.w_ready = p.w_ready ? 1 : 0;
+    a.err = p.err;
+    a.num_m = (p.M + PAIR_BM - 1) / PAIR_BM;
+    a.num_n = (p.N + PAIR_BN - 1) / PAIR_BN;
+    a.num_tiles = a.num_m * a.num_n;
+    // groups of 8 row blocks re-read all of W once per group; groups of 8
+    // column blocks re-read all of A once per group: sweep the cheaper way
+    const double a_bytes = static_cast<double>(p.M) * p.K * 2;
+    const double w_bytes = static_cast<double>(p.N) * p.K;
+    const double m_sweep = a_bytes + w_bytes * ((a.num_m + 7) / 8);
+    const double n_sweep = w_bytes + a_bytes * ((a.num_n + 7) / 8);
+    a.n_major = n_sweep < m_sweep ? 1 : 0;
+    const int maxc = pair_clusters<STAGES, CB>();
+    const int pairs = a.num_tiles < maxc ? a.num_tiles : maxc;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.blockDim = dim3(PL::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = PL::BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    cudaError_t le_ = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<STAGES, CB>, ta, tb, to, a);
+    ++*launches;
+    return le_ != cudaSuccess ? le_ : cudaGetLastError();
+}
+
+// DLO_GEMM_PAIR=0 keeps E4M3-weight GEMMs on single CTAs (tuning).
+bool pair_enabled() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = std::getenv("DLO_GEMM_PAIR");
+        v = (e && std::atoi(e) == 0 && e[0] == '0') ? 0 : 1;
+    }
+    return v != 0;
 }
 
 int forced_mt() {
@@ -787,6 +1338,9 @@ cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long*
     if (cost(128) < cost(bn)) bn = 128;
     if (forced_bn() == 128 || forced_bn() == 192 || forced_bn() == 256) bn = forced_bn();
     if (p.w_dtype == DLO_DT_E4M3 && p.a_dtype != DLO_DT_E4M3) {
+        // E4M3 with at least one full 256-row pair tile: CTA pairs, 256 x 256
+        // tiles, one M = 256 MMA over both SMs (gemm_pair_kernel)
+        if (pair_enabled() && p.M >= PAIR_BM) return run_gemm_pair<6, 3>(p, s, launches);
         // E4M3: 256-row CTA tiles (two 128-row accumulators) share each
         // widened weight tile, halving the widening work per FLOP, when
         // there are enough row blocks to fill the SMs.  DLO_GEMM_MT=1 turns
