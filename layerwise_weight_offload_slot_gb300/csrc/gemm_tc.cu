@@ -66,24 +66,25 @@ struct EpiArgs {
     int* err;
     int num_m, num_n, num_tiles;
     int n_major;   // tile order: groups of N blocks sweep all M blocks (else the reverse)
+    int group;     // blocks per group of the sweep (sweep_plan)
     int w_ready;   // W is not the preceding kernel's output (see GemmParams::w_ready)
 };
 
-// Grouped tile order: groups of 8 M-blocks sweep all N-blocks, so one
+// Grouped tile order: groups of `group` M-blocks sweep all N-blocks, so one
 // group's A rows stay in L2 while the weights stream -- or, with n_major,
-// groups of 8 N-blocks sweep all M-blocks so the weight panel stays while A
-// streams.  The host picks the order that re-reads the smaller operand.
-__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int n_major, int& mb, int& nb) {
-    constexpr int G = 8;
-    const int outer = n_major ? num_n : num_m, inner = n_major ? num_m : num_n;
+// groups of N-blocks sweep all M-blocks so the weight panel stays while A
+// streams.  The host picks the order and group size (sweep_plan).
+__device__ __forceinline__ void tile_coords(int t, const EpiArgs& a, int& mb, int& nb) {
+    const int G = a.group;
+    const int outer = a.n_major ? a.num_n : a.num_m, inner = a.n_major ? a.num_m : a.num_n;
     const int per_group = G * inner;
     const int g = t / per_group;
     const int first = g * G;
     const int gsz = min(outer - first, G);
     const int r = t - g * per_group;
     const int o = first + r % gsz, i = r / gsz;
-    mb = n_major ? i : o;
-    nb = n_major ? o : i;
+    mb = a.n_major ? i : o;
+    nb = a.n_major ? o : i;
 }
 
 // GELU, tanh approximation; tanh from the hardware approximation
@@ -271,7 +272,7 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT, CB>::THREADS, 1)
         if (prefetch_w) {
             if (static_cast<int>(blockIdx.x) < args.num_tiles) {
                 int mb0, nb0;
-                tile_coords(blockIdx.x, args.num_m, args.num_n, args.n_major, mb0, nb0);
+                tile_coords(blockIdx.x, args, mb0, nb0);
                 pre = kblocks < STAGES ? kblocks : STAGES;
                 for (int st = 0; st < pre; ++st) {
                     mbar_arrive_expect_tx(bar_full + st * 8, P::TX);
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT, CB>::THREADS, 1)
         }
         for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
             int mb, nb;
-            tile_coords(tile, args.num_m, args.num_n, args.n_major, mb, nb);
+            tile_coords(tile, args, mb, nb);
             for (int kb = 0; kb < kblocks; ++kb) {
                 if (!mbar_wait(bar_empty + s * 8, ph ^ 1, abort_flag)) {
                     fail();
@@ -406,7 +407,7 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT, CB>::THREADS, 1)
             const int acc = t & 1;
             const uint32_t aph = (t >> 1) & 1;
             int mb, nb;
-            tile_coords(tile, args.num_m, args.num_n, args.n_major, mb, nb);
+            tile_coords(tile, args, mb, nb);
             const float sa = (args.scales && args.act_scale) ? *args.act_scale : 1.0f;
             bool ok = mbar_wait(bar_tfull + acc * 8, aph, abort_flag);
             ok = __all_sync(0xFFFFFFFFu, ok);
@@ -714,7 +715,7 @@ __global__ void __launch_bounds__(PairPlan<STAGES, CB>::THREADS, 1)
         if (prefetch_w) {
             if (pair < args.num_tiles) {
                 int mb0, nb0;
-                tile_coords(pair, args.num_m, args.num_n, args.n_major, mb0, nb0);
+                tile_coords(pair, args, mb0, nb0);
                 pre = kblocks < STAGES ? kblocks : STAGES;
                 for (int st = 0; st < pre; ++st) {
                     mbar_arrive_expect_tx(bar_full + st * 8, P::TX);
@@ -727,7 +728,7 @@ __global__ void __launch_bounds__(PairPlan<STAGES, CB>::THREADS, 1)
         }
         for (int tile = pair; ok && tile < args.num_tiles; tile += npairs) {
             int mb, nb;
-            tile_coords(tile, args.num_m, args.num_n, args.n_major, mb, nb);
+            tile_coords(tile, args, mb, nb);
             for (int kb = 0; kb < kblocks; ++kb) {
                 if (!mbar_wait(bar_empty + s * 8, ph ^ 1, abort_flag)) {
                     fail();
@@ -838,7 +839,7 @@ __global__ void __launch_bounds__(PairPlan<STAGES, CB>::THREADS, 1)
             const int acc = t & 1;
             const uint32_t aph = (t >> 1) & 1;
             int mb, nb;
-            tile_coords(tile, args.num_m, args.num_n, args.n_major, mb, nb);
+            tile_coords(tile, args, mb, nb);
             bool ok = mbar_wait(bar_tfull + acc * 8, aph, abort_flag);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) {
@@ -1040,6 +1041,25 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int es_b
 
 int g_num_sms = 0;
 
+// Sweep order and group size of a GEMM's tiles: a group's panel of the
+// re-read operand (group x the bytes of one row block of A, or of one column
+// block of W) is kept within kSweepL2 bytes so it stays in L2 while the
+// other operand streams past it once; the order that reads fewer DRAM bytes
+// in total (the streamed operand once per group) wins.
+constexpr double kSweepL2 = 40.0 * 1024 * 1024;   // of the 129 MB L2, leaving room for the streamed operand and outputs
+
+void sweep_plan(double a_bytes, double w_bytes, int num_m, int num_n, EpiArgs* a) {
+    const double a_blk = a_bytes / num_m, w_blk = w_bytes / num_n;
+    int gm = static_cast<int>(kSweepL2 / (a_blk > 1.0 ? a_blk : 1.0));
+    int gn = static_cast<int>(kSweepL2 / (w_blk > 1.0 ? w_blk : 1.0));
+    gm = gm < 1 ? 1 : (gm > num_m ? num_m : gm);
+    gn = gn < 1 ? 1 : (gn > num_n ? num_n : gn);
+    const double m_sweep = a_bytes + w_bytes * ((num_m + gm - 1) / gm);
+    const double n_sweep = w_bytes + a_bytes * ((num_n + gn - 1) / gn);
+    a->n_major = n_sweep < m_sweep ? 1 : 0;
+    a->group = a->n_major ? gn : gm;
+}
+
 template <int BN, int STAGES, bool FP8, int MT = 1, bool A8 = false, int CB = 0>
 cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
     using PL = SmemPlan<BN, STAGES, FP8, MT, CB>;
@@ -1093,13 +1113,8 @@ cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* la
     a.num_m = (p.M + MT * BM - 1) / (MT * BM);
     a.num_n = (p.N + BN - 1) / BN;
     a.num_tiles = a.num_m * a.num_n;
-    // bytes the sweep re-reads: groups of 8 M blocks read all of W once per
-    // group; groups of 8 N blocks read all of A once per group
-    const double a_bytes = static_cast<double>(p.M) * p.K * (A8 ? 1 : 2);
-    const double w_bytes = static_cast<double>(p.N) * p.K * (FP8 || A8 ? 1 : 2);
-    const double m_sweep = a_bytes + w_bytes * ((a.num_m + 7) / 8);
-    const double n_sweep = w_bytes + a_bytes * ((a.num_n + 7) / 8);
-    a.n_major = n_sweep < m_sweep ? 1 : 0;
+    sweep_plan(static_cast<double>(p.M) * p.K * (A8 ? 1 : 2), static_cast<double>(p.N) * p.K * (FP8 || A8 ? 1 : 2),
+               a.num_m, a.num_n, &a);
     const int grid = a.num_tiles < g_num_sms ? a.num_tiles : g_num_sms;
     cudaError_t le_ = launch_k(gemm_kernel<BN, STAGES, FP8, MT, A8, CB>, grid, PL::THREADS, PL::BYTES, s, ta, tb, to, a);
     ++*launches;
@@ -1172,13 +1187,7 @@ cudaError_t run_gemm_pair(const GemmParams& p, cudaStream_t s, unsigned long lon
     a.num_m = (p.M + PAIR_BM - 1) / PAIR_BM;
     a.num_n = (p.N + PAIR_BN - 1) / PAIR_BN;
     a.num_tiles = a.num_m * a.num_n;
-    // groups of 8 row blocks re-read all of W once per group; groups of 8
-    // column blocks re-read all of A once per group: sweep the cheaper way
-    const double a_bytes = static_cast<double>(p.M) * p.K * 2;
-    const double w_bytes = static_cast<double>(p.N) * p.K;
-    const double m_sweep = a_bytes + w_bytes * ((a.num_m + 7) / 8);
-    const double n_sweep = w_bytes + a_bytes * ((a.num_n + 7) / 8);
-    a.n_major = n_sweep < m_sweep ? 1 : 0;
+    sweep_plan(static_cast<double>(p.M) * p.K * 2, static_cast<double>(p.N) * p.K, a.num_m, a.num_n, &a);
     const int maxc = pair_clusters<STAGES, CB>();
     const int pairs = a.num_tiles < maxc ? a.num_tiles : maxc;
     cudaLaunchConfig_t cfg = {};
