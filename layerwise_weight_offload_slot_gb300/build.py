@@ -23,8 +23,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdlo.so")
 
-SOURCES = ["layout.cpp", "context.cpp", "kernels_misc.cu", "gemm_tc.cu", "attention.cu",
-           "attention_tc.cu"]
+SOURCES = ["layout.cpp", "context.cpp", "kernels_misc.cu", "gemm_tc.cu", "attention_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-ffp-contract=off",
          "-I" + INCLUDE, "-I" + CSRC]

@@ -1,9 +1,11 @@
 // Non-causal multi-head attention on the 5th-generation tensor cores.
-// O = softmax(Q K^T / sqrt(hd)) V.  Head dims 64 and 128 are whole 64-column
-// blocks; a head dim of 64 + t (t <= 16, e.g. 72) adds a 16-column tail block
-// loaded with the 32-byte swizzle, whose columns past hd TMA fills with zeros
-// (a 4-D tensor map [batch, rows, heads, hd] ends each head at hd), so the
-// padded columns add nothing to Q K^T and are dropped from O.
+// O = softmax(Q K^T / sqrt(hd)) V for every head dim that is a multiple of 8
+// up to 128.  Q, K and V tiles are whole 64-column blocks (one for hd <= 64,
+// two for hd > 80); a head dim of 64 + t (t <= 16, e.g. 72) instead adds a
+// 16-column tail block loaded with the 32-byte swizzle.  TMA fills the box
+// columns past hd with zeros (a 4-D tensor map [batch, rows, heads, hd] ends
+// each head at hd), so the padded columns add nothing to Q K^T and are
+// dropped from O.
 //
 // One CTA per (128 query rows, head, batch); 6 warps:
 //   warp 0      TMA: the Q tile once, then K_j and V_j tiles of 128 keys into
@@ -25,11 +27,19 @@
 // V is the B operand of P V in its natural [key][dim] layout, i.e. MN-major
 // (dims contiguous): 64-dim blocks of 128-byte rows, one row per key.
 //
+// DUO (head dims up to 80): two CTAs share an SM.  Each holds one S buffer
+// and O in 256 TMEM columns and two K/V stages in ~100 KB of shared memory;
+// its MMAs run S_j, PV_j, S_{j+1}, ... and the other CTA's softmax fills the
+// tensor core while this one's runs.  A grid of 1.7 waves of single CTAs then
+// fits in one wave.
+//
 // Every mbarrier wait is bounded; a wait that runs out sets the error word
 // and the abort flag, every role leaves its loop, in-flight TMA loads and
 // MMAs are drained (bounded) and TMEM is freed.
 #include <cuda.h>
 #include <cuda_bf16.h>
+
+#include <cstdlib>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -42,14 +52,15 @@ constexpr int TQ = 128;          // query rows per CTA (MMA M, TMEM lanes)
 constexpr int TK = 128;          // keys per tile
 constexpr int kThreadsA = 192;
 
-template <int NB, bool TAIL>
+template <int NB, bool TAIL, bool DUO = false>
 struct AttnPlan {
     static constexpr int HDP = NB * 64 + (TAIL ? 16 : 0);   // padded head dim
     static constexpr int BLK = 128 * 128;                   // 128 rows x 128 B (64 cols)
     static constexpr int TBLK = TAIL ? 128 * 32 : 0;        // 128 rows x 32 B (16 cols)
     static constexpr int TILE = NB * BLK + TBLK;            // one Q, K or V tile
     // K/V ring depth: three stages when they fit next to Q in shared memory
-    static constexpr int STAGES = (TILE * 7 + 2048 <= 227 * 1024) ? 3 : 2;
+    // (DUO: two, so two CTAs fit on one SM)
+    static constexpr int STAGES = DUO ? 2 : (TILE * 7 + 2048 <= 227 * 1024) ? 3 : 2;
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = Q_OFF + TILE;              // STAGES stages
     static constexpr int V_OFF = K_OFF + STAGES * TILE;     // STAGES stages
@@ -60,10 +71,13 @@ struct AttnPlan {
     static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
     static constexpr int ABORT_OFF = TMEM_SLOT_OFF + 4;
     static constexpr int USED = ABORT_OFF + 4 + 1024;
-    // at least 116 KB, so one CTA per SM owns all 512 TMEM columns
-    static constexpr int BYTES = USED > 118784 ? USED : 118784;
-    static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t O_COL = 256;             // S buffers at columns 0 and 128
+    // single CTAs: at least 116 KB, so one CTA per SM owns all 512 TMEM
+    // columns; DUO: two CTAs of 256 columns each
+    static constexpr int BYTES = DUO ? USED : (USED > 118784 ? USED : 118784);
+    static constexpr uint32_t TMEM_COLS = DUO ? 256 : 512;
+    static constexpr int SBUF = DUO ? 1 : 2;           // S buffers (128 columns each, from 0)
+    static constexpr uint32_t O_COL = SBUF * 128;
+    static_assert(!DUO || (NB == 1 && 2 * (USED + 1024) <= 228 * 1024), "DUO: two CTAs per SM");
 };
 
 struct AttnMaps {
@@ -75,17 +89,17 @@ template <int NB, bool TAIL>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* main,
                                           const CUtensorMap* tail, int h, int row0, int b,
                                           uint32_t bar) {
-    using P = AttnPlan<NB, TAIL>;
+    using P = AttnPlan<NB, TAIL>;   // BLK and TBLK do not depend on DUO
 #pragma unroll
     for (int blk = 0; blk < NB; ++blk) tma_load_4d(dst + blk * P::BLK, main, blk * 64, h, row0, b, bar);
     if constexpr (TAIL) tma_load_4d(dst + NB * P::BLK, tail, NB * 64, h, row0, b, bar);
 }
 
-template <int NB, bool TAIL>
-__global__ void __launch_bounds__(kThreadsA, 1)
+template <int NB, bool TAIL, bool DUO>
+__global__ void __launch_bounds__(kThreadsA, DUO ? 2 : 1)
     attn_tc_kernel(const __grid_constant__ AttnMaps maps, __nv_bfloat16* __restrict__ O, int hd,
                    int nq, int nk, int ldo, float scale_log2, int* err) {
-    using P = AttnPlan<NB, TAIL>;
+    using P = AttnPlan<NB, TAIL, DUO>;
     constexpr int HDP = P::HDP;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -186,7 +200,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         auto issue_s = [&](int j) -> bool {
             const int st = j % NS;                 // K stage
             const uint32_t ph = (j / NS) & 1;
-            const int sbuf = j & 1;                // S buffer
+            const int sbuf = j % P::SBUF;          // S buffer
             // S_j overwrites the columns of S_{j-2} / P_{j-2}: the softmax
             // finished with them before p_full(j-2), and PV_{j-2}, issued
             // earlier by this thread, reads P_{j-2} before this MMA writes
@@ -207,7 +221,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         };
         auto issue_pv = [&](int j) -> bool {
             const int st = j % NS;                 // V stage: landed with K_j (waited in issue_s)
-            const int sbuf = j & 1;                // P lives in S buffer sbuf
+            const int sbuf = j % P::SBUF;          // P lives in S buffer sbuf
             if (!mbar_wait(p_full, j & 1, abort_flag)) return false;
             tc_fence_after();
             const uint32_t so = (st * P::TILE) >> 4;
@@ -225,7 +239,10 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             return true;
         };
         if (ok) ok = issue_s(0);
-        for (int j = 1; ok && j < ntiles; ++j) ok = issue_s(j) && issue_pv(j - 1);
+        // two S buffers: S_{j+1} runs while the softmax works on S_j; one
+        // (DUO): S_{j+1} follows PV_j, which reads P_j from the same columns
+        // (MMAs of one thread execute in issue order)
+        for (int j = 1; ok && j < ntiles; ++j) ok = DUO ? (issue_pv(j - 1) && issue_s(j)) : (issue_s(j) && issue_pv(j - 1));
         if (ok) ok = issue_pv(ntiles - 1);
         if (!ok) fail();
         if (*abort_flag) {
@@ -240,8 +257,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            const int st = j & 1;
-            const uint32_t ph = (j >> 1) & 1;
+            const int st = j % P::SBUF;
+            const uint32_t ph = (j / P::SBUF) & 1;
             bool got = mbar_wait(s_full + 8 * st, ph, abort_flag);
             got = __all_sync(0xFFFFFFFFu, got);
             if (!got) { ok = false; break; }
@@ -379,15 +396,15 @@ bool make_map4(CUtensorMap* m, const void* base, int batch, int rows, int heads,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NB, bool TAIL>
+template <int NB, bool TAIL, bool DUO>
 cudaError_t run_tc(const void* Q, const void* K, const void* V, void* O, int batch, int heads,
                    int hd, int nq, int nk, int ldq, int ldk, int ldv, int ldo, int* err,
                    cudaStream_t s, unsigned long long* launches) {
-    using P = AttnPlan<NB, TAIL>;
+    using P = AttnPlan<NB, TAIL, DUO>;
     static_assert(P::BYTES <= 227 * 1024, "attention shared memory plan exceeds 227 KB");
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NB, TAIL>,
+        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<NB, TAIL, DUO>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, P::BYTES);
         if (e != cudaSuccess) return e;
         attr = true;
@@ -410,27 +427,49 @@ cudaError_t run_tc(const void* Q, const void* K, const void* V, void* O, int bat
     }
     const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(hd));
     dim3 grid((nq + TQ - 1) / TQ, heads, batch);
-    cudaError_t le_ = launch_k(attn_tc_kernel<NB, TAIL>, grid, kThreadsA, P::BYTES, s, maps, static_cast<__nv_bfloat16*>(O), hd, nq, nk, ldo, scale_log2, err);
+    cudaError_t le_ = launch_k(attn_tc_kernel<NB, TAIL, DUO>, grid, kThreadsA, P::BYTES, s, maps, static_cast<__nv_bfloat16*>(O), hd, nq, nk, ldo, scale_log2, err);
     ++*launches;
     return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
 
+// DLO_ATTN_DUO=0 keeps head dims up to 80 on one CTA per SM (tuning).
+bool attn_duo_enabled() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = std::getenv("DLO_ATTN_DUO");
+        v = (e && e[0] == '0') ? 0 : 1;
+    }
+    return v != 0;
+}
+
 }  // namespace
 
-bool attention_tc_supported(int hd) {
-    return hd == 64 || hd == 128 || (hd > 64 && hd <= 80 && hd % 8 == 0);
-}
+bool attention_tc_supported(int hd) { return hd >= 8 && hd <= 128 && hd % 8 == 0; }
 
 cudaError_t launch_attention_tc(const void* Q, const void* K, const void* V, void* O, int batch,
                                 int heads, int hd, int nq, int nk, int ldq, int ldk, int ldv,
                                 int ldo, int* err, cudaStream_t s, unsigned long long* launches) {
-    if (hd == 64)
-        return run_tc<1, false>(Q, K, V, O, batch, heads, hd, nq, nk, ldq, ldk, ldv, ldo, err, s, launches);
-    if (hd == 128)
-        return run_tc<2, false>(Q, K, V, O, batch, heads, hd, nq, nk, ldq, ldk, ldv, ldo, err, s, launches);
-    if (hd > 64 && hd <= 80 && hd % 8 == 0)
-        return run_tc<1, true>(Q, K, V, O, batch, heads, hd, nq, nk, ldq, ldk, ldv, ldo, err, s, launches);
-    return cudaErrorInvalidValue;
+    // DUO when one CTA per SM would take more than one wave: with fewer CTAs
+    // than SMs nothing shares an SM and the serial S / softmax / PV order of
+    // a DUO CTA only costs time
+    const long long ctas = static_cast<long long>((nq + TQ - 1) / TQ) * heads * batch;
+    const bool duo = attn_duo_enabled() && ctas > gemm_num_sms();
+    if (!attention_tc_supported(hd)) return cudaErrorInvalidValue;
+    if (hd <= 64)
+        return duo ? run_tc<1, false, true>(Q, K, V, O, batch, heads, hd, nq, nk, ldq, ldk, ldv, ldo, err, s, launches)
+                   : run_tc<1, false, false>(Q, K, V, O, batch, heads, hd, nq, nk, ldq, ldk, ldv, ldo, err, s, launches);
+    if (hd <= 80)
+        return duo ? run_tc<1, true, true>(Q, K, V, O, batch, heads, hd, nq, nk, ldq, ldk, ldv, ldo, err, s, launches)
+                   : run_tc<1, true, false>(Q, K, V, O, batch, heads, hd, nq, nk, ldq, ldk, ldv, ldo, err, s, launches);
+    return run_tc<2, false, false>(Q, K, V, O, batch, heads, hd, nq, nk, ldq, ldk, ldv, ldo, err, s, launches);
+}
+
+cudaError_t launch_attention(const void* Q, const void* K, const void* V, void* O, int batch,
+                             int heads, int hd, int nq, int nk, int ldq, int ldk, int ldv, int ldo,
+                             int* err, cudaStream_t s, unsigned long long* launches) {
+    if (nq <= 0 || batch <= 0 || heads <= 0) return cudaSuccess;
+    if (nk <= 0) return cudaErrorInvalidValue;
+    return launch_attention_tc(Q, K, V, O, batch, heads, hd, nq, nk, ldq, ldk, ldv, ldo, err, s, launches);
 }
 
 }  // namespace dlo

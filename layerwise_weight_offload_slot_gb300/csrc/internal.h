@@ -137,8 +137,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn tensor_map_encoder();
 
-// Attention: the tcgen05 kernel for head dims 64 and 128, the mma.sync
-// kernel otherwise (or when DLO_ATTN=sync).  err: device error word or NULL.
+// Attention on the tcgen05 kernel (head dims: multiples of 8 up to 128).
+// err: device error word or NULL.
 cudaError_t launch_attention(const void* Q, const void* K, const void* V, void* O, int batch,
                              int heads, int hd, int nq, int nk, int ldq, int ldk, int ldv, int ldo,
                              int* err, cudaStream_t s, unsigned long long* launches);

@@ -112,9 +112,14 @@ def test_gemm_scale_segments():
     close(f64(out), ref, 6e-3)
 
 
+# head dims: every multiple of 8 up to 128 runs on the tcgen05 kernel (box
+# columns past hd are zero-filled); (2, 16, 72, 1024, 1024) has more CTAs
+# than SMs, so two CTAs share an SM (DUO)
 @pytest.mark.parametrize("B,H,hd,nq,nk", [(1, 1, 64, 64, 64), (2, 3, 72, 100, 300), (1, 2, 128, 257, 129),
                                           (2, 16, 72, 1024, 1024), (1, 4, 64, 1, 5), (1, 2, 32, 70, 512),
-                                          (1, 40, 128, 200, 512), (1, 40, 128, 1024, 8192)])
+                                          (1, 40, 128, 200, 512), (1, 40, 128, 1024, 8192),
+                                          (1, 3, 8, 130, 77), (2, 2, 48, 129, 256), (1, 3, 96, 130, 200),
+                                          (1, 2, 112, 64, 300), (2, 40, 64, 512, 512)])
 def test_attention_matches_oracle(B, H, hd, nq, nk):
     g = np.random.default_rng(B + H + hd + nq + nk)
     D = H * hd
