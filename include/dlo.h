@@ -343,12 +343,12 @@ typedef struct dlo_stats {
     int registered_ranges;               /* host ranges this library registered  */
     int registered_read_only;            /* 1 if they were registered read-only  */
     int device_error;                    /* kernels' error word (0 = none)       */
-    /* With dlo_set_timing(ctx, >= 1): sums over timed streamed executions, ms. */
+    /* With dlo_set_timing(ctx, 1 or 2): sums over timed streamed executions, ms. */
     int timed_execs;
     double copy_ms;                      /* slot copy durations                  */
     double compute_ms;                   /* block compute durations              */
     double exposed_wait_ms;              /* compute stream idle waiting on copies */
-    /* With dlo_set_timing(ctx, 2): per kernel class (DLO_K_*), CUDA-event time
+    /* With dlo_set_timing(ctx, 2 or 3): per kernel class (DLO_K_*), CUDA-event time
      * of each launch on its own stream, launches, and the algorithmic work of
      * those launches: 2*M*N*K per GEMM, 4*B*H*nq*nk*hd per attention, bytes
      * read + written once per element for the bandwidth-bound kernels. */
@@ -387,11 +387,17 @@ dlo_status dlo_reset_log(dlo_ctx* ctx);
 
 /* CUDA-event timing: 0 off (default); 1 five events per streamed execution
  * (copy, wait and compute intervals); 2 also an event pair around every
- * kernel launch (per-class stats).  Timing adds event records to the streams. */
+ * kernel launch (per-class stats); 3 the per-kernel pairs alone, and these
+ * also inside CUDA graphs (dlo_set_graphs): a forward captured at level 3
+ * holds its pairs as event-record nodes, read back after each launch of the
+ * graph (a graph launched again before its last launch was read first waits
+ * for that launch).  Timing adds event records to the streams; between two
+ * kernels an event record also takes the place of their programmatic-launch
+ * edge, so a kernel's time includes its own launch and prologue. */
 dlo_status dlo_set_timing(dlo_ctx* ctx, int on);
 
 /* Whole-forward CUDA graphs: 0 off (default), 1 on.  With graphs on and
- * timing 0, dlo_forward / dlo_forward_multi / dlo_forward_host capture the
+ * timing 0 or 3, dlo_forward / dlo_forward_multi / dlo_forward_host capture the
  * forward's work on both streams (staging copies, event dependencies and
  * every kernel, with their programmatic-launch edges) into a CUDA graph the
  * first time they see a set of arguments (pointers, batch, tokens, text
@@ -403,7 +409,8 @@ dlo_status dlo_set_timing(dlo_ctx* ctx, int on);
  * enqueued directly (kernels' one-time set-up stays outside captures).  Results, staging order, slot contents,
  * log and counters are the same as without graphs; the graph's launch waits
  * for all earlier work of both streams.  The pageable host mode and timing
- * levels >= 1 enqueue directly.  If a capture fails, nothing of it has run:
+ * levels 1 and 2 enqueue directly; a graph is reused only at the timing
+ * level it was captured at.  If a capture fails, nothing of it has run:
  * graphs are turned off for the context, the forward is enqueued directly
  * and dlo_last_error keeps the reason.  Turning graphs off frees the
  * captured graphs.  Not thread-safe with concurrent calls on one context. */

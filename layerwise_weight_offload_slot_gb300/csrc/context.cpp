@@ -298,6 +298,9 @@ struct dlo_ctx {
     struct GraphRec {
         cudaGraphExec_t exec = nullptr;
         int par = 0;
+        int timing = 0;                 // timing level the graph was captured at (0 or 3)
+        std::vector<TimedKernel> tk;    // level 3: the kernel event pairs inside the graph
+        bool tk_pending = false;        // a launch's pairs not read yet
         unsigned long long last_use = 0;
         const void* x_in = nullptr;
         std::vector<const void*> conds;
@@ -317,8 +320,16 @@ struct dlo_ctx {
     unsigned long long graph_uses = 0;
     cudaEvent_t g_ev[2] = {nullptr, nullptr};
     void drop_graphs() {
+        bool events = false;
+        for (GraphRec& g : gr) events |= !g.tk.empty();
+        // a graph's event pairs may still be recorded by a launch in flight
+        if (events) cudaStreamSynchronize(cs);
         for (GraphRec& g : gr) {
             if (g.exec) cudaGraphExecDestroy(g.exec);
+            for (TimedKernel& t : g.tk) {
+                cudaEventDestroy(t.a);
+                cudaEventDestroy(t.b);
+            }
             g = GraphRec();
         }
     }
@@ -347,15 +358,18 @@ struct dlo_ctx {
     int* err_word() { return reinterpret_cast<int*>(wsp + ws.err); }
     const Container& cont(int blk) const { return conts[cont_of[blk]]; }
     size_t bytes_of(int blk) const { return conts[cont_of[blk]].block_bytes; }
-    // Launch through f(); with timing level 2 bracket it with events on `s`
-    // and remember its class and algorithmic work.
+    // Launch through f(); with timing level 2 or 3 bracket it with events on
+    // `s` and remember its class and algorithmic work.  Inside a graph
+    // capture (level 3) the records are external event-record nodes, so the
+    // events are recorded each time the graph runs.
     template <class Fn>
     cudaError_t timed(int cls, double flops, double bytes, cudaStream_t s, Fn f) {
         if (timing < 2) return f();
         TimedKernel t{cls, get_event(), get_event(), flops, bytes};
-        cudaError_t e = cudaEventRecord(t.a, s);
+        const unsigned fl = capturing ? cudaEventRecordExternal : cudaEventRecordDefault;
+        cudaError_t e = cudaEventRecordWithFlags(t.a, s, fl);
         if (e == cudaSuccess) e = f();
-        if (e == cudaSuccess) e = cudaEventRecord(t.b, s);
+        if (e == cudaSuccess) e = cudaEventRecordWithFlags(t.b, s, fl);
         kernels_pending.push_back(t);
         return e;
     }
@@ -643,7 +657,34 @@ dlo_status run_block(dlo_ctx* c, const uint8_t* W, int B, int N, int L, const vo
     return DLO_OK;
 }
 
+// The kernel event pairs of the last launch of each graph captured at timing
+// level 3, once that launch has run (wait: block until it has).
+void collect_graph_timing(dlo_ctx* c, bool wait) {
+    for (dlo_ctx::GraphRec& g : c->gr) {
+        if (!g.tk_pending) continue;
+        if (wait) cudaEventSynchronize(g.tk.back().b);
+        float probe = 0;
+        if (cudaEventElapsedTime(&probe, g.tk.back().a, g.tk.back().b) != cudaSuccess) {
+            cudaGetLastError();
+            continue;   // still running
+        }
+        for (TimedKernel& t : g.tk) {
+            float ms = 0;
+            if (cudaEventElapsedTime(&ms, t.a, t.b) != cudaSuccess) {
+                cudaGetLastError();
+                continue;
+            }
+            c->st.kclass_ms[t.cls] += ms;
+            c->st.kclass_flops[t.cls] += t.flops;
+            c->st.kclass_bytes[t.cls] += t.bytes;
+            ++c->st.kclass_launches[t.cls];
+        }
+        g.tk_pending = false;
+    }
+}
+
 void collect_timing(dlo_ctx* c) {
+    collect_graph_timing(c, false);
     std::vector<TimedExec> keep;
     for (auto& t : c->timed_pending) {
         float cp = 0, cm = 0, wt = 0;
@@ -999,7 +1040,7 @@ dlo_status forward_stack(dlo_ctx* c, const void* x_in, const void* const* conds,
     }
     // the first forward is enqueued directly: kernels' one-time set-up
     // (attributes, tensor-map encoders) runs outside any capture
-    if (c->graphs && c->timing == 0 && !c->pageable && c->st.forwards > 0)
+    if (c->graphs && (c->timing == 0 || c->timing == 3) && !c->pageable && c->st.forwards > 0)
         r = forward_graph(c, x_in, conds, ctx_tokens, batch, tokens, text_tokens, x_out);
     else
         r = enqueue_forward(c, x_in, conds, ctx_tokens, batch, tokens, text_tokens, x_out);
@@ -1035,7 +1076,8 @@ dlo_status enqueue_forward(dlo_ctx* c, const void* x_in, const void* const* cond
         const int s = static_cast<int>(c->exec_counter & 1), t = s ^ 1;
         const int nb = i < n - 1 ? i + 1 : k;
         TimedExec te{};
-        if (c->timing) {
+        const bool per_exec = c->timing == 1 || c->timing == 2;   // level 3 times kernels only
+        if (per_exec) {
             te.copy0 = c->get_event();
             te.copy1 = c->get_event();
             te.wait0 = c->get_event();
@@ -1045,24 +1087,24 @@ dlo_status enqueue_forward(dlo_ctx* c, const void* x_in, const void* const* cond
         // prefetch the next block into the other slot once its last reader is done
         if (!c->capturing || c->cap_comp[t])
             LCHECK(cudaStreamWaitEvent(c->xs, c->compute_done[t], 0), "copy waits compute");
-        if (c->timing) LCHECK(cudaEventRecord(te.copy0, c->xs), "event");
+        if (per_exec) LCHECK(cudaEventRecord(te.copy0, c->xs), "event");
         r = stage(c, nb, t);
         if (r != DLO_OK) return r;
-        if (c->timing) LCHECK(cudaEventRecord(te.copy1, c->xs), "event");
+        if (per_exec) LCHECK(cudaEventRecord(te.copy1, c->xs), "event");
         LCHECK(cudaEventRecord(c->copy_done[t], c->xs), "event record");
         c->cap_copy[t] = c->capturing;
         // compute block i from slot s once its copy landed
-        if (c->timing) LCHECK(cudaEventRecord(te.wait0, c->cs), "event");
+        if (per_exec) LCHECK(cudaEventRecord(te.wait0, c->cs), "event");
         if (!c->capturing || c->cap_copy[s])
             LCHECK(cudaStreamWaitEvent(c->cs, c->copy_done[s], 0), "compute waits copy");
-        if (c->timing) LCHECK(cudaEventRecord(te.comp0, c->cs), "event");
+        if (per_exec) LCHECK(cudaEventRecord(te.comp0, c->cs), "event");
         c->log(1, i, s);
         r = run_block(c, c->slot[s], batch, tokens, text_tokens, conds[c->cont_of[i]], ctx_tokens, i, x_out);
         if (r != DLO_OK) return r;
-        if (c->timing) LCHECK(cudaEventRecord(te.comp1, c->cs), "event");
+        if (per_exec) LCHECK(cudaEventRecord(te.comp1, c->cs), "event");
         LCHECK(cudaEventRecord(c->compute_done[s], c->cs), "event record");
         c->cap_comp[s] = c->capturing;
-        if (c->timing) c->timed_pending.push_back(te);
+        if (per_exec) c->timed_pending.push_back(te);
         ++c->exec_counter;
         ++c->st.streamed_execs;
     }
@@ -1113,7 +1155,8 @@ dlo_status forward_graph(dlo_ctx* c, const void* x_in, const void* const* conds,
     dlo_ctx::GraphRec* found = nullptr;
     dlo_ctx::GraphRec* victim = nullptr;    // the first free entry, else the least recently used
     for (dlo_ctx::GraphRec& r : c->gr) {
-        if (r.exec && r.par == par && r.x_in == x_in && r.ctx == ctx_tokens && r.x_out == x_out &&
+        if (r.exec && r.par == par && r.timing == c->timing && r.x_in == x_in && r.ctx == ctx_tokens &&
+            r.x_out == x_out &&
             r.B == batch && r.N == tokens && r.L == text_tokens &&
             std::equal(r.conds.begin(), r.conds.end(), conds, conds + nc)) {
             found = &r;
@@ -1131,7 +1174,10 @@ dlo_status forward_graph(dlo_ctx* c, const void* x_in, const void* const* conds,
     LCHECK(cudaEventRecord(c->g_ev[0], c->xs), "event record");
     LCHECK(cudaStreamWaitEvent(c->cs, c->g_ev[0], 0), "join copy stream");
     if (hit) {
+        // the graph's kernel event pairs hold its last launch until read
+        if (g.tk_pending) collect_graph_timing(c, true);
         LCHECK(cudaGraphLaunch(g.exec, c->cs), "graph launch");
+        g.tk_pending = !g.tk.empty();
         c->st.stagings += g.d_stagings;
         c->st.staged_bytes += g.d_staged_bytes;
         c->st.streamed_execs += g.d_streamed;
@@ -1143,11 +1189,18 @@ dlo_status forward_graph(dlo_ctx* c, const void* x_in, const void* const* conds,
         c->slot_block[1] = g.slot_block_after[1];
         ++c->st.graph_launches;
     } else {
+        if (g.tk_pending) collect_graph_timing(c, true);
         if (g.exec) cudaGraphExecDestroy(g.exec);
+        for (TimedKernel& t : g.tk) {
+            cudaEventDestroy(t.a);
+            cudaEventDestroy(t.b);
+        }
         g = dlo_ctx::GraphRec();
         g.last_use = c->graph_uses;
         g.par = par;
+        g.timing = c->timing;
         const HostSnap h0 = snap(c);
+        const size_t k0 = c->kernels_pending.size();
         cudaError_t e = cudaStreamBeginCapture(c->cs, cudaStreamCaptureModeThreadLocal);
         if (e != cudaSuccess) return c->cuda_fail(e, "begin capture");
         c->capturing = true;
@@ -1175,6 +1228,11 @@ dlo_status forward_graph(dlo_ctx* c, const void* x_in, const void* const* conds,
             // off for this context and enqueue the forward directly
             cudaGetLastError();
             restore(c, h0);
+            for (size_t i = k0; i < c->kernels_pending.size(); ++i) {
+                c->ev_pool.push_back(c->kernels_pending[i].a);
+                c->ev_pool.push_back(c->kernels_pending[i].b);
+            }
+            c->kernels_pending.resize(k0);
             if (r == DLO_OK) c->cuda_fail(e, "graph capture failed; graphs turned off");
             c->graphs = 0;
             c->drop_graphs();
@@ -1199,8 +1257,12 @@ dlo_status forward_graph(dlo_ctx* c, const void* x_in, const void* const* conds,
         g.ls.assign(c->log_slot.begin() + h0.log_n, c->log_slot.end());
         g.slot_block_after[0] = c->slot_block[0];
         g.slot_block_after[1] = c->slot_block[1];
+        // timing level 3: the captured event pairs now belong to the graph
+        g.tk.assign(c->kernels_pending.begin() + k0, c->kernels_pending.end());
+        c->kernels_pending.resize(k0);
         ++c->st.graph_captures;
         LCHECK(cudaGraphLaunch(g.exec, c->cs), "graph launch");
+        g.tk_pending = !g.tk.empty();
         ++c->st.graph_launches;
     }
     for (int i = 0; i < 2; ++i) {
@@ -1371,7 +1433,7 @@ extern "C" dlo_status dlo_set_graphs(dlo_ctx* c, int on) {
 
 extern "C" dlo_status dlo_set_timing(dlo_ctx* c, int on) {
     if (!c) return DLO_EINVAL;
-    if (on < 0 || on > 2) return c->fail(DLO_EINVAL, "timing level must be 0, 1 or 2");
+    if (on < 0 || on > 3) return c->fail(DLO_EINVAL, "timing level must be 0, 1, 2 or 3");
     c->timing = on;
     return DLO_OK;
 }

@@ -1,7 +1,8 @@
 """Whole-forward CUDA graphs (dlo_set_graphs): a graph-launched forward gives
 the same bits, staging order, slot contents, log and counters as the same
 forward enqueued directly, across steps whose first streamed block sits in
-either slot, argument changes, timing switches, residency, several
+either slot, argument changes, timing switches (and per-kernel timing inside
+the graphs), residency, several
 containers, the host-buffer entry point and opaque byte blocks."""
 import numpy as np
 import pytest
@@ -169,6 +170,48 @@ def test_timing_switch_between_graph_and_direct_forwards():
     ya = a.forward(x, cond)
     torch.cuda.synchronize()
     assert torch.equal(y, ya)
+    a.close()
+    b.close()
+
+
+def test_kernel_timing_inside_graphs():
+    """Timing level 3 keeps graphs on: per-kernel event pairs are nodes of the
+    captured graph.  Each forward is counted once per kernel, as the direct
+    level-2 forward counts it; results stay bit-identical."""
+    cfg = DIT5
+    a = _stack(cfg, False)
+    b = _stack(cfg, True)
+    a.set_timing(2)
+    b.set_timing(3)
+    x, cond, _ = H.device_inputs(cfg, 0)
+    out_a, out_b = torch.empty_like(x), torch.empty_like(x)
+    steps = 6
+    for s in range(steps):
+        if s == 4:
+            b.set_timing(0)      # a graph captured at another level is not reused
+        a.forward(x, cond, out=out_a)
+        b.forward(x, cond, out=out_b)
+        torch.cuda.synchronize()
+        assert torch.equal(out_a, out_b), s
+    b.set_timing(3)
+    b.forward(x, cond, out=out_b)   # the level-3 graph again: reads the last launch first
+    a.forward(x, cond, out=out_a)
+    torch.cuda.synchronize()
+    a.wait()
+    b.wait()
+    assert torch.equal(out_a, out_b)
+    sa, sb = a.stats(), b.stats()
+    assert sb["graph_launches"] >= 5 and sb["graph_captures"] >= 2
+    assert a.log() == b.log()
+    # b timed 5 forwards (steps 0-3 and the last), a all 7
+    for j, name in enumerate(dlo.KCLASS_NAMES):
+        na, nb = sa["kclass_launches"][j], sb["kclass_launches"][j]
+        assert na % 7 == 0 and nb * 7 == na * 5, name
+        if nb:
+            assert sb["kclass_ms"][j] > 0
+            assert sb["kclass_flops"][j] * 7 == pytest.approx(sa["kclass_flops"][j] * 5)
+            assert sb["kclass_bytes"][j] * 7 == pytest.approx(sa["kclass_bytes"][j] * 5)
+    assert sb["timed_execs"] == 0      # level 3 times kernels only
     a.close()
     b.close()
 
