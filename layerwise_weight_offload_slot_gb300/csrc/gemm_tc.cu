@@ -575,71 +575,82 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT, CB>::THREADS, 1)
     }
 }
 
-// ------------------------------------------------------------------ CTA-pair E4M3-weight GEMM
+// ------------------------------------------------------------------ CTA-pair GEMM
 //
-// W8A16 on CTA pairs (tcgen05 cta_group::2).  A cluster of two CTAs computes
-// one 256 x 256 output tile.  CTA r (its rank in the cluster) loads the tile's
-// A rows 128r .. 128r+127 and the E4M3 codes of the tile's weight rows
-// 128r .. 128r+127, widens its own 128 weight rows to bf16 (12 converter
-// warps, as gemm_kernel's), and holds accumulator rows 128r .. 128r+127
-// (128 lanes x 256 fp32 columns, two sets) in its own tensor memory.  Rank
-// 0's MMA thread issues one M = 256, N = 256, K = 16 MMA per 32-byte K step
-// for both CTAs once both widened halves are ready; the MMA commits reach
-// both CTAs (multicast).  Readiness of rank 1's half crosses to rank 0 once
-// per step without a fence on any thread: rank 1's converter warps order
-// their stores for the async proxy (fence.proxy.async) and arrive on a
-// barrier of their own CTA; rank 1's warp 1, idle otherwise, then issues a
-// 16-byte bulk copy into rank 0's shared memory whose completion lands as
-// transaction bytes on rank 0's barrier for that widened buffer (ordered
-// after the stores like a TMA store of shared memory that threads wrote).
-// A cluster-scope release arrival would cost ~550 ns per step (measured),
-// more than the step's MMAs.  Each CTA runs gemm_kernel's
-// epilogue on its own 128 rows, then arrives on rank 0's accumulator-free
-// barrier.  Per SM a 64-K step is one 128 x 256 x 64 product -- the bf16
-// kernel's 256-wide MMA shape -- while each SM still widens 128 weight rows
-// per step, as the two-row-block gemm_kernel<..., MT = 2> does with twice as
-// many 128-wide MMAs.
-constexpr int PAIR_BN = 256;              // output columns of a pair tile
-constexpr int PAIR_HALF = PAIR_BN / 2;    // weight rows each CTA loads and widens
-constexpr int PAIR_BM = 2 * BM;           // output rows of a pair tile
-
-template <int STAGES, int CB>
+// GEMMs on CTA pairs (tcgen05 cta_group::2).  A cluster of two CTAs computes
+// one 256 x BN output tile.  CTA r (its rank in the cluster) loads the tile's
+// A rows 128r .. 128r+127 and the tile's weight rows BN/2*r .. BN/2*r+BN/2-1,
+// and holds accumulator rows 128r .. 128r+127 (128 lanes x BN fp32 columns,
+// two sets) in its own tensor memory.  Rank 0's MMA thread issues one
+// M = 256, N = BN, K = 16 MMA per 32-byte K step for both CTAs once both
+// halves of the stage are ready; the MMA commits reach both CTAs (multicast).
+// Per SM a 64-K step is a 128 x BN x 64 product fed by 16 KB of A and only
+// BN/2 weight rows: half the weight bytes per FLOP of a single-CTA tile of
+// the same width, which matters because an SM takes in operand bytes from L2
+// at ~70 bytes per cycle while all SMs stream.
+//
+// bf16 weights (FP8 = false): TMA loads both operands into a STAGES-deep
+// ring.  E4M3 weights (FP8 = true, BN = 256): TMA loads the raw codes, twelve
+// converter warps widen this CTA's weight rows into CB widened buffers of
+// their own (as gemm_kernel's), and the per-tensor scale is applied in the
+// epilogue.
+//
+// Readiness of rank 1's half crosses to rank 0 once per step without a fence
+// on any thread: rank 1's warp 1, idle otherwise, waits until the half is
+// ready in its own CTA (its stage's TMA loads landed; with E4M3 also its
+// converter warps' widened tile, ordered for the async proxy by
+// fence.proxy.async) and then issues a 16-byte bulk copy into rank 0's
+// shared memory whose completion lands as transaction bytes on the rank-0
+// barrier the MMA thread waits on.  A cluster-scope release arrival would
+// cost ~550 ns per step (measured), more than the step's MMAs.  Each CTA runs
+// gemm_kernel's epilogue on its own 128 rows, then arrives on rank 0's
+// accumulator-free barrier.
+template <int BN, int STAGES, int CB, bool FP8>
 struct PairPlan {
-    static constexpr int RAW_TILE = PAIR_HALF * BK;       // codes of one CTA's weight rows
-    static constexpr int W_TILE = PAIR_HALF * BK * 2;     // the same rows widened (MMA reads)
+    static constexpr int HALF = BN / 2;                    // weight rows each CTA loads
+    static constexpr int BM2 = 2 * BM;                     // output rows of a pair tile
+    static constexpr int NW = FP8 ? CB : STAGES;           // bf16 weight buffers the MMA reads
+    static constexpr int NCB = FP8 ? CB : 0;               // widened-buffer barrier sets
+    static constexpr int RAW_TILE = FP8 ? HALF * BK : 0;   // codes of one CTA's weight rows
+    static constexpr int W_TILE = HALF * BK * 2;           // bf16 weight rows (MMA reads)
     static constexpr int A_OFF = 0;
     static constexpr int W_OFF = STAGES * A_TILE;
-    static constexpr int RAW_OFF = W_OFF + CB * W_TILE;
+    static constexpr int RAW_OFF = W_OFF + NW * W_TILE;
     static constexpr int STG_OFF = RAW_OFF + STAGES * RAW_TILE;   // 4 warps x 2 boxes
     static constexpr int BAR_OFF = STG_OFF + 8 * STG_BYTES;
-    // full[STAGES], empty[STAGES], conv[CB], cempty[CB], wdone[CB], tfull[2], tempty[2], drain,
-    // then a 16-byte slot the forwarded bulk copies land in
-    static constexpr int SIG_OFF = (BAR_OFF + (2 * STAGES + 3 * CB + 5) * 8 + 15) / 16 * 16;
+    // full[STAGES], empty[STAGES], (E4M3: conv[CB], cempty[CB], wdone[CB]),
+    // tfull[2], tempty[2], drain, then a 16-byte slot the forwarded bulk
+    // copies land in
+    static constexpr int SIG_OFF = (BAR_OFF + (2 * STAGES + 3 * NCB + 5) * 8 + 15) / 16 * 16;
     static constexpr int TMEM_SLOT_OFF = SIG_OFF + 16;
     static constexpr uint32_t SIG_BYTES = 16;
     static constexpr int ABORT_OFF = TMEM_SLOT_OFF + 4;
     static constexpr int BYTES = ABORT_OFF + 4 + 1024;   // + alignment slack
-    static constexpr int THREADS = kThreads + kConvWarps * 32;
-    static constexpr uint32_t TX = A_TILE + RAW_TILE;
-    static constexpr uint32_t TMEM_COLS = 2 * PAIR_BN;   // two accumulator sets
-    static_assert(STG_OFF % 1024 == 0 && W_OFF % 1024 == 0, "swizzled buffers must be 1024-B aligned");
+    static constexpr int THREADS = kThreads + (FP8 ? kConvWarps * 32 : 0);
+    static constexpr uint32_t TX = A_TILE + (FP8 ? RAW_TILE : W_TILE);
+    // two accumulator sets of BN fp32 columns; allocated in powers of two
+    static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256u : 512u;
+    static_assert(BN % 64 == 0 && BN >= 128 && BN <= 256, "pair tile width: 128, 192 or 256");
+    static_assert(!FP8 || (BN == 256 && CB > 0), "E4M3 pairs: 256-wide tiles, widened buffers");
+    static_assert(W_OFF % 1024 == 0 && RAW_OFF % 1024 == 0 && STG_OFF % 1024 == 0 && W_TILE % 1024 == 0,
+                  "swizzled buffers must be 1024-B aligned");
 };
 
-template <int STAGES, int CB>
-__global__ void __launch_bounds__(PairPlan<STAGES, CB>::THREADS, 1)
+template <int BN, int STAGES, int CB, bool FP8>
+__global__ void __launch_bounds__(PairPlan<BN, STAGES, CB, FP8>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmO, const EpiArgs args) {
-    using P = PairPlan<STAGES, CB>;
+    using P = PairPlan<BN, STAGES, CB, FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar_full = sbase + P::BAR_OFF;
     const uint32_t bar_empty = bar_full + STAGES * 8;
-    const uint32_t bar_conv = bar_empty + STAGES * 8;
-    const uint32_t bar_cempty = bar_conv + CB * 8;
-    const uint32_t bar_wdone = bar_cempty + CB * 8;
-    const uint32_t bar_tfull = bar_wdone + CB * 8;
+    const uint32_t bar_conv = bar_empty + STAGES * 8;     // E4M3 only (NCB = 0 otherwise)
+    const uint32_t bar_cempty = bar_conv + P::NCB * 8;
+    const uint32_t bar_wdone = bar_cempty + P::NCB * 8;
+    const uint32_t bar_tfull = bar_wdone + P::NCB * 8;
     const uint32_t bar_tempty = bar_tfull + 2 * 8;
     const uint32_t bar_drain = bar_tempty + 2 * 8;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + P::TMEM_SLOT_OFF);
@@ -655,7 +666,7 @@ __global__ void __launch_bounds__(PairPlan<STAGES, CB>::THREADS, 1)
             mbar_init(bar_full + s * 8, 1);
             mbar_init(bar_empty + s * 8, 1);
         }
-        for (int c = 0; c < CB; ++c) {
+        for (int c = 0; c < P::NCB; ++c) {
             // rank 0's converter warps (one of them also expects the bytes
             // rank 1 forwards)
             mbar_init(bar_conv + c * 8, kConvWarps);
@@ -684,12 +695,14 @@ __global__ void __launch_bounds__(PairPlan<STAGES, CB>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int kblocks = (args.K + BK - 1) / BK;
-    // rank 0's barriers and signal slot that rank 1 reaches, as shared::cluster addresses
-    const uint32_t conv_r0 = mapa_shared(bar_conv, 0);
+    // the rank-0 barriers rank 1's readiness lands on (E4M3: the widened
+    // buffers'; bf16: the stages'), its accumulator-free barriers and the
+    // signal slot, as shared::cluster addresses
+    const uint32_t ready_r0 = mapa_shared(FP8 ? bar_conv : bar_full, 0);
     const uint32_t tempty_r0 = mapa_shared(bar_tempty, 0);
     const uint32_t sig_r0 = mapa_shared(sbase + P::SIG_OFF, 0);
     // weights are never the predecessor's output (w_ready): the producer's
-    // first code tiles may load before the programmatic-launch wait
+    // first weight tiles may load before the programmatic-launch wait
     const bool prefetch_w = args.w_ready && warp == 0 && lane == 0;
     if (!prefetch_w) {
         pdl_wait();
@@ -702,14 +715,20 @@ __global__ void __launch_bounds__(PairPlan<STAGES, CB>::THREADS, 1)
     };
 
     if (warp == 0 && lane == 0) {
-        // ---------------- TMA producer: this CTA's A rows and weight-code rows
+        // ---------------- TMA producer: this CTA's A rows and weight rows
+        // (bf16: rank 0's stage also waits for rank 1's forwarded bytes)
+        constexpr uint32_t tx0 = FP8 ? P::TX : P::TX + P::SIG_BYTES;
+        const uint32_t tx = rank == 0 ? tx0 : P::TX;
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
         uint32_t issued = 0, last_par = 0;
         auto load_w = [&](int st, int kb, int nb) {
-            tma_load_2d(sbase + P::RAW_OFF + st * P::RAW_TILE, &tmB, kb * BK,
-                        nb * PAIR_BN + static_cast<int>(rank) * PAIR_HALF, bar_full + st * 8);
+            const int wrow = nb * BN + static_cast<int>(rank) * P::HALF;
+            if constexpr (FP8)
+                tma_load_2d(sbase + P::RAW_OFF + st * P::RAW_TILE, &tmB, kb * BK, wrow, bar_full + st * 8);
+            else
+                tma_load_2d(sbase + P::W_OFF + st * P::W_TILE, &tmB, kb * BK, wrow, bar_full + st * 8);
         };
         int pre = 0;
         if (prefetch_w) {
@@ -718,7 +737,7 @@ __global__ void __launch_bounds__(PairPlan<STAGES, CB>::THREADS, 1)
                 tile_coords(pair, args, mb0, nb0);
                 pre = kblocks < STAGES ? kblocks : STAGES;
                 for (int st = 0; st < pre; ++st) {
-                    mbar_arrive_expect_tx(bar_full + st * 8, P::TX);
+                    mbar_arrive_expect_tx(bar_full + st * 8, tx);
                     load_w(st, st, nb0);
                     issued |= 1u << st;
                 }
@@ -737,9 +756,9 @@ __global__ void __launch_bounds__(PairPlan<STAGES, CB>::THREADS, 1)
                 }
                 const uint32_t fb = bar_full + s * 8;
                 const bool w_done = tile == pair && kb < pre;
-                if (!w_done) mbar_arrive_expect_tx(fb, P::TX);
+                if (!w_done) mbar_arrive_expect_tx(fb, tx);
                 tma_load_2d(sbase + P::A_OFF + s * A_TILE, &tmA, kb * BK,
-                            mb * PAIR_BM + static_cast<int>(rank) * BM, fb);
+                            mb * P::BM2 + static_cast<int>(rank) * BM, fb);
                 if (!w_done) load_w(s, kb, nb);
                 issued |= 1u << s;
                 last_par = (last_par & ~(1u << s)) | (ph << s);
@@ -755,7 +774,7 @@ __global__ void __launch_bounds__(PairPlan<STAGES, CB>::THREADS, 1)
         }
     } else if (warp == 1 && lane == 0 && rank == 0) {
         // ---------------- MMA issuer of the pair (rank 0 only)
-        constexpr uint32_t idesc = idesc_bf16_f32(PAIR_BM, PAIR_BN);
+        constexpr uint32_t idesc = idesc_bf16_f32(P::BM2, BN);
         const uint64_t a_desc0 = sw128_kmajor_desc(sbase + P::A_OFF);
         const uint64_t b_desc0 = sw128_kmajor_desc(sbase + P::W_OFF);
         uint64_t a_desc = a_desc0, b_desc = b_desc0;
@@ -771,9 +790,11 @@ __global__ void __launch_bounds__(PairPlan<STAGES, CB>::THREADS, 1)
                 break;
             }
             tc_fence_after();
-            const uint32_t d_tmem = tmem_base + acc * PAIR_BN;
+            const uint32_t d_tmem = tmem_base + acc * BN;
             for (int kb = 0; kb < kblocks; ++kb) {
-                if (!mbar_wait_cluster(bar_conv + cb * 8, cph, abort_flag)) {
+                const bool got = FP8 ? mbar_wait_cluster(bar_conv + cb * 8, cph, abort_flag)
+                                     : mbar_wait_cluster(bar_full + s * 8, ph, abort_flag);
+                if (!got) {
                     fail();
                     ok = false;
                     break;
@@ -784,20 +805,30 @@ __global__ void __launch_bounds__(PairPlan<STAGES, CB>::THREADS, 1)
                     tc_mma_f16_pair(d_tmem, a_desc + ((kk * 32) >> 4), b_desc + ((kk * 32) >> 4), idesc,
                                     (kb | kk) != 0);
                 tc_commit_pair_mc(bar_empty + s * 8, 3);
-                tc_commit_pair_mc(bar_cempty + cb * 8, 3);
-                if (++cb == CB) {
-                    cb = 0;
-                    cph ^= 1;
-                    b_desc = b_desc0;
-                } else {
-                    b_desc += P::W_TILE >> 4;
-                }
-                if (++s == STAGES) {
+                if constexpr (FP8) {
+                    tc_commit_pair_mc(bar_cempty + cb * 8, 3);
+                    if (++cb == CB) {
+                        cb = 0;
+                        cph ^= 1;
+                        b_desc = b_desc0;
+                    } else {
+                        b_desc += P::W_TILE >> 4;
+                    }
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1;
+                        a_desc = a_desc0;
+                    } else {
+                        a_desc += A_TILE >> 4;
+                    }
+                } else if (++s == STAGES) {
                     s = 0;
                     ph ^= 1;
                     a_desc = a_desc0;
+                    b_desc = b_desc0;
                 } else {
                     a_desc += A_TILE >> 4;
+                    b_desc += P::W_TILE >> 4;
                 }
             }
             if (ok) tc_commit_pair_mc(bar_tfull + acc * 8, 3);
@@ -808,22 +839,26 @@ __global__ void __launch_bounds__(PairPlan<STAGES, CB>::THREADS, 1)
             mbar_wait(bar_drain, 0, nullptr);
         }
     } else if (warp == 1 && lane == 0) {
-        // ---------------- rank 1: forward each widened half's readiness to rank 0
-        int cb = 0;
-        uint32_t cph = 0;
+        // ---------------- rank 1: forward each ready half to rank 0
+        // (E4M3: per widened buffer, after its converter warps; bf16: per
+        // stage, after its TMA loads)
+        constexpr int NR = FP8 ? CB : STAGES;
+        const uint32_t ready_local = FP8 ? bar_wdone : bar_full;
+        int r = 0;
+        uint32_t rph = 0;
         bool ok = true;
         for (int tile = pair; ok && tile < args.num_tiles; tile += npairs) {
             for (int kb = 0; kb < kblocks; ++kb) {
-                if (!mbar_wait(bar_wdone + cb * 8, cph, abort_flag)) {
+                if (!mbar_wait(ready_local + r * 8, rph, abort_flag)) {
                     fail();
                     ok = false;
                     break;
                 }
                 fence_proxy_async_smem();
-                bulk_s2s_cluster(sig_r0, sbase + P::SIG_OFF, P::SIG_BYTES, conv_r0 + cb * 8);
-                if (++cb == CB) {
-                    cb = 0;
-                    cph ^= 1;
+                bulk_s2s_cluster(sig_r0, sbase + P::SIG_OFF, P::SIG_BYTES, ready_r0 + r * 8);
+                if (++r == NR) {
+                    r = 0;
+                    rph ^= 1;
                 }
             }
         }
@@ -847,17 +882,17 @@ __global__ void __launch_bounds__(PairPlan<STAGES, CB>::THREADS, 1)
                 break;
             }
             tc_fence_after();
-            const int row0 = mb * PAIR_BM + static_cast<int>(rank) * BM + q * 32;
+            const int row0 = mb * P::BM2 + static_cast<int>(rank) * BM + q * 32;
             const int row = row0 + lane;
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * PAIR_BN;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
             if (residual) {
                 const float* grow = args.gate ? args.gate + static_cast<size_t>(min(row, args.M - 1) /
                                                                                  args.rows_per_batch) *
                                                                 args.gate_ld
                                               : nullptr;
 #pragma unroll 1
-                for (int c0 = 0; c0 < PAIR_BN; c0 += 32) {
-                    const int col0 = nb * PAIR_BN + c0;
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    const int col0 = nb * BN + c0;
                     if (col0 >= args.N) break;
                     EpiBS e;
                     epi_load(args, 1.0f, col0, e);
@@ -898,8 +933,8 @@ __global__ void __launch_bounds__(PairPlan<STAGES, CB>::THREADS, 1)
                 }
             } else {
 #pragma unroll 1
-                for (int c0 = 0; c0 < PAIR_BN; c0 += 64) {
-                    const int col0 = nb * PAIR_BN + c0;
+                for (int c0 = 0; c0 < BN; c0 += 64) {
+                    const int col0 = nb * BN + c0;
                     if (col0 >= args.N) break;
                     if (lane == 0) bulk_wait_read<1>();
                     __syncwarp();
@@ -946,62 +981,65 @@ __global__ void __launch_bounds__(PairPlan<STAGES, CB>::THREADS, 1)
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
-    } else if (warp >= 6) {
-        // ---------------- e4m3 -> bf16 converters: this CTA's 128 weight rows
-        const int ct = threadIdx.x - 6 * 32;
-        constexpr int kChunks = PAIR_HALF * 8;                  // 8 codes each
-        constexpr int kIter = (kChunks + kConvWarps * 32 - 1) / (kConvWarps * 32);
-        int s = 0, cb = 0;
-        uint32_t ph = 0, cph = 0;
-        bool ok = true;
-        for (int tile = pair; ok && tile < args.num_tiles; tile += npairs) {
-            for (int kb = 0; kb < kblocks; ++kb) {
-                // the stage's A tile and codes have landed: the readiness
-                // signal below covers this CTA's A tile as well
-                bool got = mbar_wait(bar_full + s * 8, ph, abort_flag);
-                if (got) got = mbar_wait(bar_cempty + cb * 8, cph ^ 1, abort_flag);
-                got = __all_sync(0xFFFFFFFFu, got);
-                if (!got) {
-                    if (lane == 0) fail();
-                    ok = false;
-                    break;
-                }
-                const uint8_t* raw = smem + P::RAW_OFF + s * P::RAW_TILE;
-                uint8_t* dst = smem + P::W_OFF + cb * P::W_TILE;
-                // every load of this thread's share first (the compiler cannot
-                // move loads above stores to a buffer it cannot tell apart)
-                uint2 v[kIter];
-#pragma unroll
-                for (int j = 0; j < kIter; ++j) {
-                    const int i = ct + j * kConvWarps * 32;
-                    if (i < kChunks) v[j] = *reinterpret_cast<const uint2*>(raw + (i >> 3) * 64 + (i & 7) * 8);
-                }
-#pragma unroll
-                for (int j = 0; j < kIter; ++j) {
-                    const int i = ct + j * kConvWarps * 32;
-                    if (i < kChunks) {
-                        uint32_t o[4];
-                        e4m3x8_to_bf16x8(v[j].x, v[j].y, o);
-                        *reinterpret_cast<uint4*>(dst + sw128(i >> 3, i & 7)) = make_uint4(o[0], o[1], o[2], o[3]);
+    } else if constexpr (FP8) {
+        if (warp >= 6) {
+            // ---------------- e4m3 -> bf16 converters: this CTA's weight rows
+            const int ct = threadIdx.x - 6 * 32;
+            constexpr int kChunks = P::HALF * 8;                  // 8 codes each
+            constexpr int kIter = (kChunks + kConvWarps * 32 - 1) / (kConvWarps * 32);
+            int s = 0, cb = 0;
+            uint32_t ph = 0, cph = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < args.num_tiles; tile += npairs) {
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    // the stage's A tile and codes have landed: the readiness
+                    // signal below covers this CTA's A tile as well
+                    bool got = mbar_wait(bar_full + s * 8, ph, abort_flag);
+                    if (got) got = mbar_wait(bar_cempty + cb * 8, cph ^ 1, abort_flag);
+                    got = __all_sync(0xFFFFFFFFu, got);
+                    if (!got) {
+                        if (lane == 0) fail();
+                        ok = false;
+                        break;
                     }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (rank != 0)
-                        mbar_arrive(bar_wdone + cb * 8);
-                    else if (ct == 0)
-                        mbar_arrive_expect_tx(bar_conv + cb * 8, P::SIG_BYTES);   // rank 1's forwarded bytes
-                    else
-                        mbar_arrive(bar_conv + cb * 8);
-                }
-                if (++s == STAGES) {
-                    s = 0;
-                    ph ^= 1;
-                }
-                if (++cb == CB) {
-                    cb = 0;
-                    cph ^= 1;
+                    const uint8_t* raw = smem + P::RAW_OFF + s * P::RAW_TILE;
+                    uint8_t* dst = smem + P::W_OFF + cb * P::W_TILE;
+                    // every load of this thread's share first (the compiler cannot
+                    // move loads above stores to a buffer it cannot tell apart)
+                    uint2 v[kIter];
+#pragma unroll
+                    for (int j = 0; j < kIter; ++j) {
+                        const int i = ct + j * kConvWarps * 32;
+                        if (i < kChunks) v[j] = *reinterpret_cast<const uint2*>(raw + (i >> 3) * 64 + (i & 7) * 8);
+                    }
+#pragma unroll
+                    for (int j = 0; j < kIter; ++j) {
+                        const int i = ct + j * kConvWarps * 32;
+                        if (i < kChunks) {
+                            uint32_t o[4];
+                            e4m3x8_to_bf16x8(v[j].x, v[j].y, o);
+                            *reinterpret_cast<uint4*>(dst + sw128(i >> 3, i & 7)) =
+                                make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (rank != 0)
+                            mbar_arrive(bar_wdone + cb * 8);
+                        else if (ct == 0)
+                            mbar_arrive_expect_tx(bar_conv + cb * 8, P::SIG_BYTES);   // rank 1's forwarded bytes
+                        else
+                            mbar_arrive(bar_conv + cb * 8);
+                    }
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                    if (++cb == CB) {
+                        cb = 0;
+                        cph ^= 1;
+                    }
                 }
             }
         }
@@ -1123,11 +1161,11 @@ cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* la
 
 // Clusters of two CTAs of gemm_pair_kernel that fit on the GPU at once
 // (queried once; an SM a pair cannot use stays idle).
-template <int STAGES, int CB>
+template <int BN, int STAGES, int CB, bool FP8>
 int pair_clusters() {
     static int n = -1;
     if (n < 0) {
-        using PL = PairPlan<STAGES, CB>;
+        using PL = PairPlan<BN, STAGES, CB, FP8>;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (g_num_sms / 2), 1, 1);
         cfg.blockDim = dim3(PL::THREADS, 1, 1);
@@ -1140,7 +1178,8 @@ int pair_clusters() {
         cfg.attrs = at;
         cfg.numAttrs = 1;
         int c = 0;
-        if (cudaOccupancyMaxActiveClusters(&c, gemm_pair_kernel<STAGES, CB>, &cfg) != cudaSuccess || c < 1) {
+        if (cudaOccupancyMaxActiveClusters(&c, gemm_pair_kernel<BN, STAGES, CB, FP8>, &cfg) != cudaSuccess ||
+            c < 1) {
             cudaGetLastError();
             c = g_num_sms / 2;
         }
@@ -1149,22 +1188,25 @@ int pair_clusters() {
     return n;
 }
 
-template <int STAGES, int CB>
+template <int BN, int STAGES, int CB, bool FP8>
 cudaError_t run_gemm_pair(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
-    using PL = PairPlan<STAGES, CB>;
+    using PL = PairPlan<BN, STAGES, CB, FP8>;
     static_assert(PL::BYTES <= 227 * 1024, "shared memory plan exceeds 227 KB");
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<STAGES, CB>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<BN, STAGES, CB, FP8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, PL::BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     CUtensorMap ta, tb, to;
     if (!make_map(&ta, p.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.M, p.K, p.K, BM, BK,
-                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&tb, p.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.N, p.K, p.K, PAIR_HALF, BK,
-                  CU_TENSOR_MAP_SWIZZLE_NONE))
+                  CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (FP8 ? !make_map(&tb, p.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.N, p.K, p.K, PL::HALF, BK,
+                        CU_TENSOR_MAP_SWIZZLE_NONE)
+            : !make_map(&tb, p.W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.N, p.K, p.K, PL::HALF, BK,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const bool residual = p.epi == DLO_EPI_RESIDUAL;
     if (!make_map(&to, p.out, residual ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
@@ -1184,11 +1226,12 @@ cudaError_t run_gemm_pair(const GemmParams& p, cudaStream_t s, unsigned long lon
     a.rows_per_batch = p.rows_per_batch > 0 ? p.rows_per_batch : 1;
     a.w_ready = p.w_ready ? 1 : 0;
     a.err = p.err;
-    a.num_m = (p.M + PAIR_BM - 1) / PAIR_BM;
-    a.num_n = (p.N + PAIR_BN - 1) / PAIR_BN;
+    a.num_m = (p.M + PL::BM2 - 1) / PL::BM2;
+    a.num_n = (p.N + BN - 1) / BN;
     a.num_tiles = a.num_m * a.num_n;
-    sweep_plan(static_cast<double>(p.M) * p.K * 2, static_cast<double>(p.N) * p.K, a.num_m, a.num_n, &a);
-    const int maxc = pair_clusters<STAGES, CB>();
+    sweep_plan(static_cast<double>(p.M) * p.K * 2, static_cast<double>(p.N) * p.K * (FP8 ? 1 : 2), a.num_m,
+               a.num_n, &a);
+    const int maxc = pair_clusters<BN, STAGES, CB, FP8>();
     const int pairs = a.num_tiles < maxc ? a.num_tiles : maxc;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs, 1, 1);
@@ -1204,19 +1247,21 @@ cudaError_t run_gemm_pair(const GemmParams& p, cudaStream_t s, unsigned long lon
     at[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    cudaError_t le_ = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<STAGES, CB>, ta, tb, to, a);
+    cudaError_t le_ = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, STAGES, CB, FP8>, ta, tb, to, a);
     ++*launches;
     return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
 
-// DLO_GEMM_PAIR=0 keeps E4M3-weight GEMMs on single CTAs (tuning).
-bool pair_enabled() {
-    static int v = -1;
-    if (v < 0) {
+// DLO_GEMM_PAIR=0 keeps every GEMM on single CTAs; =1 puts every GEMM with
+// at least 256 rows on CTA pairs; unset, E4M3-weight GEMMs with 256 rows or
+// more run on pairs and bf16 GEMMs follow the tile model (tuning).
+int pair_mode() {
+    static int v = -2;
+    if (v == -2) {
         const char* e = std::getenv("DLO_GEMM_PAIR");
-        v = (e && std::atoi(e) == 0 && e[0] == '0') ? 0 : 1;
+        v = (e && e[0] == '0' && e[1] == 0) ? 0 : (e && e[0] == '1' && e[1] == 0) ? 1 : -1;
     }
-    return v != 0;
+    return v;
 }
 
 int forced_mt() {
@@ -1349,7 +1394,7 @@ cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long*
     if (p.w_dtype == DLO_DT_E4M3 && p.a_dtype != DLO_DT_E4M3) {
         // E4M3 with at least one full 256-row pair tile: CTA pairs, 256 x 256
         // tiles, one M = 256 MMA over both SMs (gemm_pair_kernel)
-        if (pair_enabled() && p.M >= PAIR_BM) return run_gemm_pair<6, 3>(p, s, launches);
+        if (pair_mode() != 0 && p.M >= 2 * BM) return run_gemm_pair<256, 6, 3, true>(p, s, launches);
         // E4M3: 256-row CTA tiles (two 128-row accumulators) share each
         // widened weight tile, halving the widening work per FLOP, when
         // there are enough row blocks to fill the SMs.  DLO_GEMM_MT=1 turns
@@ -1369,8 +1414,53 @@ cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long*
         return run_gemm<128, 6, false, 1, true>(p, s, launches);
     }
     if (p.w_dtype != DLO_DT_BF16) return cudaErrorNotSupported;
-    if (bn == 256) return run_gemm<256, 4, false>(p, s, launches);
-    if (bn == 192) return run_gemm<192, 4, false>(p, s, launches);
+    // bf16: single CTAs (128-row tiles) or CTA pairs (256-row tiles), and the
+    // N tile, from the cost of one 64-K step per SM times the waves of tiles.
+    // Single CTAs: SM cycles measured on GB300 while every SM streams its
+    // operands from L2 (a step moves 16 KB of A and BN x 128 bytes of
+    // weights into the SM, which takes in ~70 bytes per cycle).  Pairs: an
+    // SM takes in only BN/2 weight rows, but its MMAs also read the peer's
+    // half; their costs are set from graph-timed runs of both kernels at
+    // 2048- and 8192-row shapes (pairs 11-15% faster at 8192 rows, 0-4%
+    // slower at 2048), so pairs win where many waves of wide tiles run.
+    // DLO_GEMM_BN forces the width, DLO_GEMM_PAIR=0 or 1 single CTAs or
+    // pairs (tuning).
+    const int widths[3] = {128, 192, 256};
+    const double single_cyc[3] = {509, 543, 651};
+    const double pair_cyc[3] = {530, 580, 600};
+    const int max_pairs = g_num_sms / 2 > 0 ? g_num_sms / 2 : 1;
+    const bool pairs_ok = pair_mode() != 0 && p.M >= 2 * BM;
+    const bool singles_ok = !(pair_mode() == 1 && pairs_ok);
+    double best = 0;
+    int best_bn = 256;
+    bool best_pair = false;
+    for (int i = 0; i < 3; ++i) {
+        const int w = widths[i];
+        if (forced_bn() > 0 && forced_bn() != w) continue;
+        const long long nn = (p.N + w - 1) / w;
+        const double t1 = static_cast<double>((num_m * nn + g_num_sms - 1) / g_num_sms) * single_cyc[i];
+        if (singles_ok && (best == 0 || t1 < best)) {
+            best = t1;
+            best_bn = w;
+            best_pair = false;
+        }
+        if (pairs_ok) {
+            const long long tiles = ((p.M + 2 * BM - 1) / (2 * BM)) * nn;
+            const double t2 = static_cast<double>((tiles + max_pairs - 1) / max_pairs) * pair_cyc[i];
+            if (best == 0 || t2 < best) {
+                best = t2;
+                best_bn = w;
+                best_pair = true;
+            }
+        }
+    }
+    if (best_pair) {
+        if (best_bn == 256) return run_gemm_pair<256, 6, 0, false>(p, s, launches);
+        if (best_bn == 192) return run_gemm_pair<192, 6, 0, false>(p, s, launches);
+        return run_gemm_pair<128, 7, 0, false>(p, s, launches);
+    }
+    if (best_bn == 256) return run_gemm<256, 4, false>(p, s, launches);
+    if (best_bn == 192) return run_gemm<192, 4, false>(p, s, launches);
     return run_gemm<128, 6, false>(p, s, launches);
 }
 
