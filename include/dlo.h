@@ -157,7 +157,10 @@ dlo_status dlo_block_layout(const dlo_desc* desc, dlo_tensor_info* out, int cap,
 
 /* Device workspace bytes dlo_create needs for this desc (activations of
  * max_batch x max_tokens, scratch for the block kernels, the kernels' error
- * word).  Returns 0 for an invalid desc. */
+ * word; with W8A16 weights also a bf16 copy of the block's largest linear,
+ * into which each linear of a forward with at least DLO_WIDEN_ROWS rows --
+ * default 4096 -- is widened before its GEMM).  Returns 0 for an invalid
+ * desc. */
 size_t dlo_workspace_bytes(const dlo_desc* desc);
 
 /* Workspace bytes of a multi-container stack (dlo_create_multi): one carve-up

@@ -230,6 +230,20 @@ int pack_threads() {
     return v >= 1 && v <= 64 ? v : 12;
 }
 
+// Rows from which a W8A16 linear is widened to bf16 before its GEMM
+// (DLO_WIDEN_ROWS, read once; default 4096).  Below that the widening stays
+// inside the GEMM's mainloop, where a separate pass over the weights would
+// cost more than it saves.
+int widen_rows() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = std::getenv("DLO_WIDEN_ROWS");
+        const long long r = e ? std::atoll(e) : 0;
+        v = r >= 1 && r <= (1ll << 30) ? static_cast<int>(r) : 4096;
+    }
+    return v;
+}
+
 struct PackTicket {
     HostPacker* packer;
     unsigned long long n;
@@ -578,6 +592,23 @@ dlo_status run_block(dlo_ctx* c, const uint8_t* W, int B, int N, int L, const vo
         }
         p.W = W + woff;
         p.w_dtype = e4m3 ? DLO_DT_E4M3 : DLO_DT_BF16;
+        p.w_ready = true;   // weights live in a slot or resident buffer, never a kernel's output
+        // W8A16 at many rows: widen this linear's codes to bf16 once (an
+        // HBM-bound pass, 3 bytes per weight) and multiply in bf16 on CTA
+        // pairs, which outpace widening inside every CTA's mainloop; the
+        // per-tensor scale stays in the epilogue, so the products are the same
+        const size_t nk = static_cast<size_t>(Nn) * K;
+        const bool widen = e4m3 && !w8a8 && M >= widen_rows() && nk * 2 <= c->ws.wide_bytes &&
+                           (reinterpret_cast<uintptr_t>(p.W) & 15) == 0;
+        if (widen) {
+            void* wide = w + c->ws.wide;
+            cudaError_t e = c->timed(DLO_K_CONVERT, 0.0, 3.0 * nk, s,
+                                     [&] { return launch_widen_e4m3(p.W, nk, wide, s, nl); });
+            if (e != cudaSuccess) return e;
+            p.W = wide;
+            p.w_dtype = DLO_DT_BF16;
+            p.w_ready = false;   // the widening kernel just wrote it
+        }
         p.scales = o.has_scales ? reinterpret_cast<const float*>(W + o.scales) + scale_idx : nullptr;
         p.scale_seg = seg;
         p.bias = W + boff;
@@ -591,9 +622,8 @@ dlo_status run_block(dlo_ctx* c, const uint8_t* W, int B, int N, int L, const vo
         p.gate_ld = D6;
         p.rows_per_batch = rpb;
         p.err = c->err_word();
-        p.w_ready = true;   // weights live in a slot or resident buffer, never a kernel's output
         const double flops = 2.0 * M * Nn * K;
-        const double bytes = 1.0 * M * K * (w8a8 ? 1 : 2) + 1.0 * Nn * K * wsize +
+        const double bytes = 1.0 * M * K * (w8a8 ? 1 : 2) + 1.0 * Nn * K * (widen ? 2 : wsize) +
                              1.0 * M * Nn * (epi == DLO_EPI_RESIDUAL ? 8 : 2);
         return c->timed(w8a8 ? DLO_K_GEMM_FP8 : e4m3 ? DLO_K_GEMM_E4M3 : DLO_K_GEMM_BF16, flops,
                         bytes, s, [&] { return launch_gemm(p, s, nl); });

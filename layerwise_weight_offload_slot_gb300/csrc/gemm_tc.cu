@@ -158,6 +158,40 @@ __device__ __forceinline__ void e4m3x8_to_bf16x8(uint32_t x0, uint32_t x1, uint3
     }
 }
 
+// E4M3 codes -> bf16, 16 codes per step and four steps in flight per thread
+// (HBM-bound: 1 byte read, 2 written per weight); the last n % 16 codes
+// (tail) by the first threads of block 0.
+__global__ void __launch_bounds__(256) widen_e4m3_kernel(const uint4* __restrict__ codes,
+                                                         uint4* __restrict__ out, size_t n16,
+                                                         const uint8_t* __restrict__ tail_src,
+                                                         uint16_t* __restrict__ tail_dst, int tail) {
+    // the buffer written here may still be read by the preceding GEMM
+    pdl_wait();
+    pdl_launch_dependents();
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    auto widen16 = [&](size_t k, const uint4& v) {
+        uint32_t lo[4], hi[4];
+        e4m3x8_to_bf16x8(v.x, v.y, lo);
+        e4m3x8_to_bf16x8(v.z, v.w, hi);
+        out[2 * k] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        out[2 * k + 1] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    };
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = __ldg(codes + i + j * stride);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) widen16(i + j * stride, v[j]);
+    }
+    for (; i < n16; i += stride) widen16(i, __ldg(codes + i));
+    if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < tail) {
+        uint32_t o[4];
+        e4m3x8_to_bf16x8(tail_src[threadIdx.x], 0u, o);
+        tail_dst[threadIdx.x] = static_cast<uint16_t>(o[0] & 0xFFFFu);
+    }
+}
+
 template <int BN, int STAGES, bool FP8, int MT = 1, int CB = 0>
 struct SmemPlan {
     static constexpr int A_STAGE = MT * A_TILE;           // MT 128-row A boxes per stage
@@ -1372,6 +1406,20 @@ int gemm_num_sms() {
         if (g_num_sms <= 0) g_num_sms = 1;
     }
     return g_num_sms;
+}
+
+cudaError_t launch_widen_e4m3(const void* codes, size_t n, void* out, cudaStream_t s,
+                              unsigned long long* launches) {
+    if (n == 0) return cudaSuccess;
+    if ((reinterpret_cast<uintptr_t>(codes) | reinterpret_cast<uintptr_t>(out)) & 15) return cudaErrorInvalidValue;
+    const size_t n16 = n / 16;
+    const int tail = static_cast<int>(n % 16);
+    const cudaError_t e = launch_k(widen_e4m3_kernel, gemm_num_sms() * 4, 256, 0, s,
+                                   static_cast<const uint4*>(codes), static_cast<uint4*>(out), n16,
+                                   static_cast<const uint8_t*>(codes) + n16 * 16,
+                                   static_cast<uint16_t*>(out) + n16 * 16, tail);
+    ++*launches;
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {

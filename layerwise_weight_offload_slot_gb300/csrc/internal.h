@@ -73,10 +73,17 @@ struct Workspace {
     size_t in_ctx = 0;   // bf16 [B*L, Dt] (forward_host)
     size_t qa = 0;       // W8A8: E4M3 codes of the current linear's input
     size_t qs = 0;       // W8A8: kQuantScratch partial maxima, then the scale
+    size_t wide = 0;     // W8A16: bf16 copy of the current linear's weights
+    size_t wide_bytes = 0;   // its size (0: no such buffer)
     size_t err = 0;      // int[64] kernels' error words
     size_t total = 0;
 };
-Workspace plan_workspace(const dlo_desc& d);
+// wide_min: bytes of the W8A16 widened-weight buffer at least (a stack
+// whose containers differ in weight type).
+Workspace plan_workspace(const dlo_desc& d, size_t wide_min = 0);
+// Bytes of the W8A16 widened-weight buffer of one block type (its largest
+// linear in bf16), 0 unless its weights are W8A16.
+size_t widen_buffer_bytes(const dlo_desc& d);
 // One workspace that serves every container of a stack.
 Workspace plan_workspace_stack(const dlo_desc* ds, int n);
 
@@ -113,6 +120,10 @@ struct GemmParams {
     bool w_ready = false;
 };
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches);
+// E4M3 codes [n] -> bf16 [n], exactly (the codes' values; a per-tensor scale
+// stays with the GEMM's epilogue).  codes and out 16-byte aligned.
+cudaError_t launch_widen_e4m3(const void* codes, size_t n, void* out, cudaStream_t s,
+                              unsigned long long* launches);
 int gemm_num_sms();
 
 // Unit-op plumbing shared by the C ABI's op entry points.  op_fail stores the

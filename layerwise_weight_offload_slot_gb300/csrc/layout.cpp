@@ -106,10 +106,13 @@ dlo_status validate_stack(const dlo_desc* ds, int n, dlo_desc* stack, std::strin
 }
 
 Workspace plan_workspace_stack(const dlo_desc* ds, int n) {
-    // one carve-up that serves every container: the widest FFN, and the
-    // cross-attention buffers when any container is a video one
+    // one carve-up that serves every container: the widest FFN, the
+    // cross-attention buffers when any container is a video one, and the
+    // largest W8A16 widened-weight buffer
     dlo_desc u = ds[0];
+    size_t wide = 0;
     for (int i = 0; i < n; ++i) {
+        wide = std::max(wide, widen_buffer_bytes(ds[i]));
         u.ffn = std::max(u.ffn, ds[i].ffn);
         u.cond_dim = std::max(u.cond_dim, ds[i].cond_dim);
         if (ds[i].wdtype == DLO_W_E4M3_A8) u.wdtype = DLO_W_E4M3_A8;
@@ -119,7 +122,15 @@ Workspace plan_workspace_stack(const dlo_desc* ds, int n) {
             u.max_text_tokens = ds[i].max_text_tokens;
         }
     }
-    return plan_workspace(u);
+    return plan_workspace(u, wide);
+}
+
+size_t widen_buffer_bytes(const dlo_desc& d) {
+    if (d.wdtype != DLO_W_E4M3 || d.block_kind == DLO_BLOCK_BYTES) return 0;
+    const size_t D = d.hidden, F = d.ffn;
+    size_t nk = std::max(3 * D * D, F * D);   // qkv; fc1 and fc2
+    if (d.block_kind == DLO_BLOCK_VIDEO) nk = std::max(nk, 2 * D * static_cast<size_t>(d.text_dim));   // cross k|v
+    return nk * 2;
 }
 
 namespace {
@@ -213,7 +224,7 @@ int find_entry(const std::vector<Entry>& L, const char* name) {
     return -1;
 }
 
-Workspace plan_workspace(const dlo_desc& d) {
+Workspace plan_workspace(const dlo_desc& d, size_t wide_min) {
     Workspace w;
     if (d.block_kind == DLO_BLOCK_BYTES) {
         // error words, then the per-block checksums of dlo_forward_host
@@ -252,6 +263,8 @@ Workspace plan_workspace(const dlo_desc& d) {
         w.qa = take(std::max(BN * std::max(D, F), BL * static_cast<size_t>(d.text_dim)));
         w.qs = take((kQuantScratch + 64) * sizeof(float));
     }
+    w.wide_bytes = std::max(widen_buffer_bytes(d), wide_min);
+    if (w.wide_bytes) w.wide = take(w.wide_bytes);
     w.err = take(64 * sizeof(int));
     w.total = align_up(cur, 256);
     return w;

@@ -295,6 +295,45 @@ def test_programmatic_dependent_launch_changes_no_bit():
     assert _stack_output_digest("1") == _stack_output_digest("0")
 
 
+def test_w8a16_widened_linears_match_oracle(tmp_path):
+    """W8A16 linears with at least DLO_WIDEN_ROWS rows are widened to bf16 in
+    the workspace before a bf16 GEMM (the 8192-token video block takes that
+    path by default).  Forced here on the small E4M3 video stack (every
+    linear, ragged rows, a 77-token text context) in a process of its own;
+    the output stays within the W8A16 stack tolerance of the oracle, the
+    widening kernel ran once per linear, and the output equals the fused
+    path's within the same tolerance."""
+    import os
+    import subprocess
+    import sys
+    cfg = SMALL_VID_FP8
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = (
+        "import sys, numpy as np, torch\n"
+        "from tests import helpers as H\n"
+        "from tests.test_gpu_stack import SMALL_VID_FP8 as cfg\n"
+        "import layerwise_weight_offload_slot_gb300 as dlo\n"
+        "st = H.make_stack(cfg); st.attach(); st.set_timing(2)\n"
+        "x, c, t = H.device_inputs(cfg)\n"
+        "y = st.forward(x, c, t); torch.cuda.synchronize(); st.wait()\n"
+        "np.save(sys.argv[1], y.float().cpu().numpy())\n"
+        "print(st.stats()['kclass_launches'][dlo.KCLASS_NAMES.index('convert')])\n")
+    outs = {}
+    for rows in ("1", "1000000000"):
+        path = str(tmp_path / f"y_{len(rows)}.npy")
+        r = subprocess.run([sys.executable, "-c", code, path], cwd=root, capture_output=True, text=True,
+                           timeout=600, env=dict(os.environ, DLO_WIDEN_ROWS=rows, PYTHONPATH=root))
+        assert r.returncode == 0, r.stderr[-2000:]
+        outs[rows] = (np.load(path), int(r.stdout.split()[-1]))
+    (yw, nw), (yf, nf) = outs["1"], outs["1000000000"]
+    assert nw - nf == 7 * cfg.n_blocks      # self qkv, self o, cross q, cross k|v, cross o, fc1, fc2
+    x, cond, ctx = H.device_inputs(cfg)
+    ref = H.oracle_forward(cfg, x, cond, ctx, H.oracle_blocks(cfg))
+    assert H.rel_l2(yw, ref) <= 5e-2
+    assert H.rel_l2(yw, yf) <= 5e-2
+    print("widened vs fused: max |diff|", float(np.abs(yw - yf).max()), "bit-identical", bool((yw == yf).all()))
+
+
 def test_device_wait_timeout_is_reported_and_the_context_survives():
     cfg = synth.CFG_TINY
     st = H.make_stack(cfg)
