@@ -249,16 +249,16 @@ def run_reference(args, cfg, rank: int, world: int):
 
 # ----------------------------------------------------------------------------- our arm
 
-def traffic_record(kernel_class: str):
-    """ncu DRAM bytes per launch of the dominant kernel, if the committed
-    record was taken on the current source of that kernel."""
+def traffic_record(workload: str, kernel_class: str):
+    """ncu DRAM bytes per launch of a workload's dominant kernel class, if the
+    committed record was taken on the current source of that kernel."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f)
-    r = rec.get(kernel_class)
+    r = rec.get(workload, {}).get(kernel_class)
     if not r:
         return None
     src = os.path.join(ROOT, "layerwise_weight_offload_slot_gb300", "csrc", r["source"])
@@ -428,7 +428,7 @@ def run_ours(args, cfg, rank: int, world: int, local_rank: int):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "peak_source": f"{peaks['source']} hbm_gbs"}
     roof["frac"] = achieved / peak
-    tr = traffic_record(dom)
+    tr = traffic_record(cfg.name, dom)
     roof["traffic"] = tr["bytes_per_launch"] if tr else None
     roof["kernel"] = dom
     roof["launches_per_step"] = d["launches"] / args.steps
