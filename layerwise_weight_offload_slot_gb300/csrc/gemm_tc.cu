@@ -627,7 +627,9 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT, CB>::THREADS, 1)
 // ring.  E4M3 weights (FP8 = true, BN = 256): TMA loads the raw codes, twelve
 // converter warps widen this CTA's weight rows into CB widened buffers of
 // their own (as gemm_kernel's), and the per-tensor scale is applied in the
-// epilogue.
+// epilogue.  W8A8 (A8): both operands are E4M3 codes in the same 128-byte
+// rows (128 K per stage), multiplied by kind::f8f6f4 MMAs of K = 32; the
+// epilogue applies the activation scale times the weight scale.
 //
 // Readiness of rank 1's half crosses to rank 0 once per step without a fence
 // on any thread: rank 1's warp 1, idle otherwise, waits until the half is
@@ -639,8 +641,9 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT, CB>::THREADS, 1)
 // cost ~550 ns per step (measured), more than the step's MMAs.  Each CTA runs
 // gemm_kernel's epilogue on its own 128 rows, then arrives on rank 0's
 // accumulator-free barrier.
-template <int BN, int STAGES, int CB, bool FP8>
+template <int BN, int STAGES, int CB, bool FP8, bool A8 = false>
 struct PairPlan {
+    static constexpr int KS = A8 ? 128 : BK;               // K elements per stage (128-byte rows)
     static constexpr int HALF = BN / 2;                    // weight rows each CTA loads
     static constexpr int BM2 = 2 * BM;                     // output rows of a pair tile
     static constexpr int NW = FP8 ? CB : STAGES;           // bf16 weight buffers the MMA reads
@@ -666,15 +669,17 @@ struct PairPlan {
     static constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256u : 512u;
     static_assert(BN % 64 == 0 && BN >= 128 && BN <= 256, "pair tile width: 128, 192 or 256");
     static_assert(!FP8 || (BN == 256 && CB > 0), "E4M3 pairs: 256-wide tiles, widened buffers");
+    static_assert(!(FP8 && A8), "W8A8 multiplies the codes, nothing to widen");
     static_assert(W_OFF % 1024 == 0 && RAW_OFF % 1024 == 0 && STG_OFF % 1024 == 0 && W_TILE % 1024 == 0,
                   "swizzled buffers must be 1024-B aligned");
 };
 
-template <int BN, int STAGES, int CB, bool FP8>
-__global__ void __launch_bounds__(PairPlan<BN, STAGES, CB, FP8>::THREADS, 1)
+template <int BN, int STAGES, int CB, bool FP8, bool A8 = false>
+__global__ void __launch_bounds__(PairPlan<BN, STAGES, CB, FP8, A8>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmO, const EpiArgs args) {
-    using P = PairPlan<BN, STAGES, CB, FP8>;
+    using P = PairPlan<BN, STAGES, CB, FP8, A8>;
+    constexpr int KS = P::KS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -728,7 +733,7 @@ __global__ void __launch_bounds__(PairPlan<BN, STAGES, CB, FP8>::THREADS, 1)
     cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int kblocks = (args.K + BK - 1) / BK;
+    const int kblocks = (args.K + KS - 1) / KS;
     // the rank-0 barriers rank 1's readiness lands on (E4M3: the widened
     // buffers'; bf16: the stages'), its accumulator-free barriers and the
     // signal slot, as shared::cluster addresses
@@ -760,9 +765,9 @@ __global__ void __launch_bounds__(PairPlan<BN, STAGES, CB, FP8>::THREADS, 1)
         auto load_w = [&](int st, int kb, int nb) {
             const int wrow = nb * BN + static_cast<int>(rank) * P::HALF;
             if constexpr (FP8)
-                tma_load_2d(sbase + P::RAW_OFF + st * P::RAW_TILE, &tmB, kb * BK, wrow, bar_full + st * 8);
+                tma_load_2d(sbase + P::RAW_OFF + st * P::RAW_TILE, &tmB, kb * KS, wrow, bar_full + st * 8);
             else
-                tma_load_2d(sbase + P::W_OFF + st * P::W_TILE, &tmB, kb * BK, wrow, bar_full + st * 8);
+                tma_load_2d(sbase + P::W_OFF + st * P::W_TILE, &tmB, kb * KS, wrow, bar_full + st * 8);
         };
         int pre = 0;
         if (prefetch_w) {
@@ -791,7 +796,7 @@ __global__ void __launch_bounds__(PairPlan<BN, STAGES, CB, FP8>::THREADS, 1)
                 const uint32_t fb = bar_full + s * 8;
                 const bool w_done = tile == pair && kb < pre;
                 if (!w_done) mbar_arrive_expect_tx(fb, tx);
-                tma_load_2d(sbase + P::A_OFF + s * A_TILE, &tmA, kb * BK,
+                tma_load_2d(sbase + P::A_OFF + s * A_TILE, &tmA, kb * KS,
                             mb * P::BM2 + static_cast<int>(rank) * BM, fb);
                 if (!w_done) load_w(s, kb, nb);
                 issued |= 1u << s;
@@ -808,7 +813,7 @@ __global__ void __launch_bounds__(PairPlan<BN, STAGES, CB, FP8>::THREADS, 1)
         }
     } else if (warp == 1 && lane == 0 && rank == 0) {
         // ---------------- MMA issuer of the pair (rank 0 only)
-        constexpr uint32_t idesc = idesc_bf16_f32(P::BM2, BN);
+        constexpr uint32_t idesc = A8 ? idesc_e4m3_f32(P::BM2, BN) : idesc_bf16_f32(P::BM2, BN);
         const uint64_t a_desc0 = sw128_kmajor_desc(sbase + P::A_OFF);
         const uint64_t b_desc0 = sw128_kmajor_desc(sbase + P::W_OFF);
         uint64_t a_desc = a_desc0, b_desc = b_desc0;
@@ -835,9 +840,14 @@ __global__ void __launch_bounds__(PairPlan<BN, STAGES, CB, FP8>::THREADS, 1)
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)   // 4 x 32 bytes of K per stage
-                    tc_mma_f16_pair(d_tmem, a_desc + ((kk * 32) >> 4), b_desc + ((kk * 32) >> 4), idesc,
-                                    (kb | kk) != 0);
+                for (int kk = 0; kk < 4; ++kk) {   // 4 x 32 bytes of K per stage
+                    if constexpr (A8)
+                        tc_mma_f8_pair(d_tmem, a_desc + ((kk * 32) >> 4), b_desc + ((kk * 32) >> 4), idesc,
+                                       (kb | kk) != 0);
+                    else
+                        tc_mma_f16_pair(d_tmem, a_desc + ((kk * 32) >> 4), b_desc + ((kk * 32) >> 4), idesc,
+                                        (kb | kk) != 0);
+                }
                 tc_commit_pair_mc(bar_empty + s * 8, 3);
                 if constexpr (FP8) {
                     tc_commit_pair_mc(bar_cempty + cb * 8, 3);
@@ -909,6 +919,8 @@ __global__ void __launch_bounds__(PairPlan<BN, STAGES, CB, FP8>::THREADS, 1)
             const uint32_t aph = (t >> 1) & 1;
             int mb, nb;
             tile_coords(tile, args, mb, nb);
+            // W8A8: the activation scale times the weight scale (epi_load)
+            const float sa = (args.scales && args.act_scale) ? *args.act_scale : 1.0f;
             bool ok = mbar_wait(bar_tfull + acc * 8, aph, abort_flag);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) {
@@ -929,7 +941,7 @@ __global__ void __launch_bounds__(PairPlan<BN, STAGES, CB, FP8>::THREADS, 1)
                     const int col0 = nb * BN + c0;
                     if (col0 >= args.N) break;
                     EpiBS e;
-                    epi_load(args, 1.0f, col0, e);
+                    epi_load(args, sa, col0, e);
                     float4 gv[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
@@ -974,8 +986,8 @@ __global__ void __launch_bounds__(PairPlan<BN, STAGES, CB, FP8>::THREADS, 1)
                     __syncwarp();
                     uint8_t* box = stg0p + bi * STG_BYTES;
                     EpiBS e2[2];
-                    epi_load(args, 1.0f, col0, e2[0]);
-                    epi_load(args, 1.0f, col0 + 32, e2[1]);
+                    epi_load(args, sa, col0, e2[0]);
+                    epi_load(args, sa, col0 + 32, e2[1]);
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         uint32_t r[32];
@@ -1195,11 +1207,11 @@ cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* la
 
 // Clusters of two CTAs of gemm_pair_kernel that fit on the GPU at once
 // (queried once; an SM a pair cannot use stays idle).
-template <int BN, int STAGES, int CB, bool FP8>
+template <int BN, int STAGES, int CB, bool FP8, bool A8>
 int pair_clusters() {
     static int n = -1;
     if (n < 0) {
-        using PL = PairPlan<BN, STAGES, CB, FP8>;
+        using PL = PairPlan<BN, STAGES, CB, FP8, A8>;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (g_num_sms / 2), 1, 1);
         cfg.blockDim = dim3(PL::THREADS, 1, 1);
@@ -1212,7 +1224,7 @@ int pair_clusters() {
         cfg.attrs = at;
         cfg.numAttrs = 1;
         int c = 0;
-        if (cudaOccupancyMaxActiveClusters(&c, gemm_pair_kernel<BN, STAGES, CB, FP8>, &cfg) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveClusters(&c, gemm_pair_kernel<BN, STAGES, CB, FP8, A8>, &cfg) != cudaSuccess ||
             c < 1) {
             cudaGetLastError();
             c = g_num_sms / 2;
@@ -1222,26 +1234,35 @@ int pair_clusters() {
     return n;
 }
 
-template <int BN, int STAGES, int CB, bool FP8>
+template <int BN, int STAGES, int CB, bool FP8, bool A8 = false>
 cudaError_t run_gemm_pair(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
-    using PL = PairPlan<BN, STAGES, CB, FP8>;
+    using PL = PairPlan<BN, STAGES, CB, FP8, A8>;
     static_assert(PL::BYTES <= 227 * 1024, "shared memory plan exceeds 227 KB");
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<BN, STAGES, CB, FP8>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<BN, STAGES, CB, FP8, A8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, PL::BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     CUtensorMap ta, tb, to;
-    if (!make_map(&ta, p.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.M, p.K, p.K, BM, BK,
-                  CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    if (FP8 ? !make_map(&tb, p.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.N, p.K, p.K, PL::HALF, BK,
-                        CU_TENSOR_MAP_SWIZZLE_NONE)
-            : !make_map(&tb, p.W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.N, p.K, p.K, PL::HALF, BK,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
+    if (A8) {
+        // E4M3 codes of both operands, 128 K per box (128-byte rows)
+        if (!make_map(&ta, p.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.M, p.K, p.K, BM, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map(&tb, p.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.N, p.K, p.K, PL::HALF, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    } else {
+        if (!make_map(&ta, p.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.M, p.K, p.K, BM, BK,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+        if (FP8 ? !make_map(&tb, p.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.N, p.K, p.K, PL::HALF, BK,
+                            CU_TENSOR_MAP_SWIZZLE_NONE)
+                : !make_map(&tb, p.W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.N, p.K, p.K, PL::HALF, BK,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
     const bool residual = p.epi == DLO_EPI_RESIDUAL;
     if (!make_map(&to, p.out, residual ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                   residual ? 4 : 2, p.M, p.N, p.ldo, 32, residual ? 32 : 64, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -1254,7 +1275,7 @@ cudaError_t run_gemm_pair(const GemmParams& p, cudaStream_t s, unsigned long lon
     a.bias = static_cast<const __nv_bfloat16*>(p.bias);
     a.scales = p.scales;
     a.scale_seg = p.scale_seg > 0 ? p.scale_seg : p.N;
-    a.act_scale = nullptr;
+    a.act_scale = A8 ? p.a_scale : nullptr;
     a.gate = p.gate;
     a.gate_ld = p.gate_ld;
     a.rows_per_batch = p.rows_per_batch > 0 ? p.rows_per_batch : 1;
@@ -1263,9 +1284,9 @@ cudaError_t run_gemm_pair(const GemmParams& p, cudaStream_t s, unsigned long lon
     a.num_m = (p.M + PL::BM2 - 1) / PL::BM2;
     a.num_n = (p.N + BN - 1) / BN;
     a.num_tiles = a.num_m * a.num_n;
-    sweep_plan(static_cast<double>(p.M) * p.K * 2, static_cast<double>(p.N) * p.K * (FP8 ? 1 : 2), a.num_m,
-               a.num_n, &a);
-    const int maxc = pair_clusters<BN, STAGES, CB, FP8>();
+    sweep_plan(static_cast<double>(p.M) * p.K * (A8 ? 1 : 2), static_cast<double>(p.N) * p.K * (FP8 || A8 ? 1 : 2),
+               a.num_m, a.num_n, &a);
+    const int maxc = pair_clusters<BN, STAGES, CB, FP8, A8>();
     const int pairs = a.num_tiles < maxc ? a.num_tiles : maxc;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs, 1, 1);
@@ -1281,7 +1302,7 @@ cudaError_t run_gemm_pair(const GemmParams& p, cudaStream_t s, unsigned long lon
     at[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    cudaError_t le_ = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, STAGES, CB, FP8>, ta, tb, to, a);
+    cudaError_t le_ = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, STAGES, CB, FP8, A8>, ta, tb, to, a);
     ++*launches;
     return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
@@ -1422,13 +1443,63 @@ cudaError_t launch_widen_e4m3(const void* codes, size_t n, void* out, cudaStream
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+namespace {
+
+// bf16 and W8A8 GEMMs: single CTAs (128-row tiles) or CTA pairs (256-row
+// tiles), and the N tile, from the cost of one 128-byte-wide K step per SM
+// times the waves of tiles.  Single CTAs: SM cycles measured on GB300 while
+// every SM streams its operands from L2 (a step moves 16 KB of A and BN x 128
+// bytes of weights into the SM, which takes in ~70 bytes per cycle).  Pairs:
+// an SM takes in only BN/2 weight rows, but its MMAs also read the peer's
+// half; their costs are set from graph-timed runs of both kernels at 2048-
+// and 8192-row shapes (pairs 11-15% faster at 8192 rows, 0-4% slower at
+// 2048), so pairs win where many waves of wide tiles run.  A W8A8 step (128
+// K of E4M3, MMAs at twice the bf16 rate) has the bf16 step's bytes and
+// cycles.  DLO_GEMM_BN forces the width, DLO_GEMM_PAIR=0 or 1 single CTAs or
+// pairs (tuning).
+void pick_tile(const GemmParams& p, int* bn, bool* pair) {
+    const int widths[3] = {128, 192, 256};
+    const double single_cyc[3] = {509, 543, 651};
+    const double pair_cyc[3] = {530, 580, 600};
+    const long long num_m = (p.M + BM - 1) / BM;
+    const int max_pairs = g_num_sms / 2 > 0 ? g_num_sms / 2 : 1;
+    const bool pairs_ok = pair_mode() != 0 && p.M >= 2 * BM;
+    const bool singles_ok = !(pair_mode() == 1 && pairs_ok);
+    double best = 0;
+    *bn = 256;
+    *pair = false;
+    for (int i = 0; i < 3; ++i) {
+        const int w = widths[i];
+        if (forced_bn() > 0 && forced_bn() != w) continue;
+        const long long nn = (p.N + w - 1) / w;
+        const double t1 = static_cast<double>((num_m * nn + g_num_sms - 1) / g_num_sms) * single_cyc[i];
+        if (singles_ok && (best == 0 || t1 < best)) {
+            best = t1;
+            *bn = w;
+            *pair = false;
+        }
+        if (pairs_ok) {
+            const long long tiles = ((p.M + 2 * BM - 1) / (2 * BM)) * nn;
+            const double t2 = static_cast<double>((tiles + max_pairs - 1) / max_pairs) * pair_cyc[i];
+            if (best == 0 || t2 < best) {
+                best = t2;
+                *bn = w;
+                *pair = true;
+            }
+        }
+    }
+}
+
+}  // namespace
+
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
     if (p.M <= 0) return cudaSuccess;
     gemm_num_sms();
-    // N tile from a small cost model: time ~ waves x tile width / efficiency,
-    // where narrower tiles move more shared-memory bytes per FLOP (128-wide
-    // tiles are limited to about 3/4 of the MMA rate, 192-wide to ~0.95).
-    // DLO_GEMM_BN=128|192|256 forces one (tuning).
+    // Single-CTA E4M3-weight GEMMs: N tile from a small cost model, time ~
+    // waves x tile width / efficiency, where narrower tiles move more
+    // shared-memory bytes per FLOP (128-wide tiles are limited to about 3/4
+    // of the MMA rate, 192-wide to ~0.95).  DLO_GEMM_BN=128|192|256 forces
+    // one (tuning).
     const long long num_m = (p.M + BM - 1) / BM;
     auto cost = [&](int bn) {
         const long long tiles = num_m * ((p.N + bn - 1) / bn);
@@ -1457,51 +1528,22 @@ cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long*
     if (p.a_dtype == DLO_DT_E4M3) {
         // W8A8: both operands E4M3; same stage bytes as bf16
         if (p.w_dtype != DLO_DT_E4M3 || !p.a_scale || !p.scales) return cudaErrorInvalidValue;
-        if (bn == 256) return run_gemm<256, 4, false, 1, true>(p, s, launches);
-        if (bn == 192) return run_gemm<192, 4, false, 1, true>(p, s, launches);
+        int w8_bn = 256;
+        bool w8_pair = false;
+        pick_tile(p, &w8_bn, &w8_pair);
+        if (w8_pair) {
+            if (w8_bn == 256) return run_gemm_pair<256, 6, 0, false, true>(p, s, launches);
+            if (w8_bn == 192) return run_gemm_pair<192, 6, 0, false, true>(p, s, launches);
+            return run_gemm_pair<128, 7, 0, false, true>(p, s, launches);
+        }
+        if (w8_bn == 256) return run_gemm<256, 4, false, 1, true>(p, s, launches);
+        if (w8_bn == 192) return run_gemm<192, 4, false, 1, true>(p, s, launches);
         return run_gemm<128, 6, false, 1, true>(p, s, launches);
     }
     if (p.w_dtype != DLO_DT_BF16) return cudaErrorNotSupported;
-    // bf16: single CTAs (128-row tiles) or CTA pairs (256-row tiles), and the
-    // N tile, from the cost of one 64-K step per SM times the waves of tiles.
-    // Single CTAs: SM cycles measured on GB300 while every SM streams its
-    // operands from L2 (a step moves 16 KB of A and BN x 128 bytes of
-    // weights into the SM, which takes in ~70 bytes per cycle).  Pairs: an
-    // SM takes in only BN/2 weight rows, but its MMAs also read the peer's
-    // half; their costs are set from graph-timed runs of both kernels at
-    // 2048- and 8192-row shapes (pairs 11-15% faster at 8192 rows, 0-4%
-    // slower at 2048), so pairs win where many waves of wide tiles run.
-    // DLO_GEMM_BN forces the width, DLO_GEMM_PAIR=0 or 1 single CTAs or
-    // pairs (tuning).
-    const int widths[3] = {128, 192, 256};
-    const double single_cyc[3] = {509, 543, 651};
-    const double pair_cyc[3] = {530, 580, 600};
-    const int max_pairs = g_num_sms / 2 > 0 ? g_num_sms / 2 : 1;
-    const bool pairs_ok = pair_mode() != 0 && p.M >= 2 * BM;
-    const bool singles_ok = !(pair_mode() == 1 && pairs_ok);
-    double best = 0;
     int best_bn = 256;
     bool best_pair = false;
-    for (int i = 0; i < 3; ++i) {
-        const int w = widths[i];
-        if (forced_bn() > 0 && forced_bn() != w) continue;
-        const long long nn = (p.N + w - 1) / w;
-        const double t1 = static_cast<double>((num_m * nn + g_num_sms - 1) / g_num_sms) * single_cyc[i];
-        if (singles_ok && (best == 0 || t1 < best)) {
-            best = t1;
-            best_bn = w;
-            best_pair = false;
-        }
-        if (pairs_ok) {
-            const long long tiles = ((p.M + 2 * BM - 1) / (2 * BM)) * nn;
-            const double t2 = static_cast<double>((tiles + max_pairs - 1) / max_pairs) * pair_cyc[i];
-            if (best == 0 || t2 < best) {
-                best = t2;
-                best_bn = w;
-                best_pair = true;
-            }
-        }
-    }
+    pick_tile(p, &best_bn, &best_pair);
     if (best_pair) {
         if (best_bn == 256) return run_gemm_pair<256, 6, 0, false>(p, s, launches);
         if (best_bn == 192) return run_gemm_pair<192, 6, 0, false>(p, s, launches);

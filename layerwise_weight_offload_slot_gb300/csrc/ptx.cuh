@@ -457,6 +457,16 @@ __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc
         : "memory");
 }
 
+// The same over a CTA pair with E4M3 A and B (kind::f8f6f4, K = 32).
+__device__ __forceinline__ void tc_mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on the mbarrier at shared offset `bar` in every CTA of `mask`
 // when the pair MMAs issued so far by this thread completed.
 __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {

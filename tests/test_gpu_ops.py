@@ -472,17 +472,18 @@ def test_gemm_e4m3_single_cta_path_matches_oracle():
                                  {"DLO_GEMM_PAIR": "1", "DLO_GEMM_BN": "256"}],
                          ids=["single-192", "single-256", "pair-128", "pair-192", "pair-256"])
 def test_gemm_tile_paths_match_oracle(env):
-    """Every bf16 GEMM kernel the tile model can pick (single CTAs or CTA
-    pairs, 128-, 192- or 256-wide tiles) passes the GEMM parity cases, each
-    forced in turn (pairs take the cases with at least 256 rows; the others
-    run on single CTAs); the default run covers the model's own picks.  Each
-    setting runs in a process of its own (the switches are read once)."""
+    """Every bf16 and W8A8 GEMM kernel the tile model can pick (single CTAs or
+    CTA pairs, 128-, 192- or 256-wide tiles) passes the GEMM parity cases,
+    each forced in turn (pairs take the cases with at least 256 rows; the
+    others run on single CTAs); the default run covers the model's own
+    picks.  Each setting runs in a process of its own (the switches are read
+    once)."""
     import os
     import subprocess
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        "tests/test_gpu_ops.py::test_gemm_matches_oracle"],
+                        "tests/test_gpu_ops.py", "-k", "test_gemm_matches_oracle or test_gemm_w8a8"],
                        env=dict(os.environ, **env), cwd=root, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
     assert " passed" in r.stdout and "failed" not in r.stdout
