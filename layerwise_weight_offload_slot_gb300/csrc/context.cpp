@@ -593,22 +593,6 @@ dlo_status run_block(dlo_ctx* c, const uint8_t* W, int B, int N, int L, const vo
         p.W = W + woff;
         p.w_dtype = e4m3 ? DLO_DT_E4M3 : DLO_DT_BF16;
         p.w_ready = true;   // weights live in a slot or resident buffer, never a kernel's output
-        // W8A16 at many rows: widen this linear's codes to bf16 once (an
-        // HBM-bound pass, 3 bytes per weight) and multiply in bf16 on CTA
-        // pairs, which outpace widening inside every CTA's mainloop; the
-        // per-tensor scale stays in the epilogue, so the products are the same
-        const size_t nk = static_cast<size_t>(Nn) * K;
-        const bool widen = e4m3 && !w8a8 && M >= widen_rows() && nk * 2 <= c->ws.wide_bytes &&
-                           (reinterpret_cast<uintptr_t>(p.W) & 15) == 0;
-        if (widen) {
-            void* wide = w + c->ws.wide;
-            cudaError_t e = c->timed(DLO_K_CONVERT, 0.0, 3.0 * nk, s,
-                                     [&] { return launch_widen_e4m3(p.W, nk, wide, s, nl); });
-            if (e != cudaSuccess) return e;
-            p.W = wide;
-            p.w_dtype = DLO_DT_BF16;
-            p.w_ready = false;   // the widening kernel just wrote it
-        }
         p.scales = o.has_scales ? reinterpret_cast<const float*>(W + o.scales) + scale_idx : nullptr;
         p.scale_seg = seg;
         p.bias = W + boff;
@@ -623,10 +607,37 @@ dlo_status run_block(dlo_ctx* c, const uint8_t* W, int B, int N, int L, const vo
         p.rows_per_batch = rpb;
         p.err = c->err_word();
         const double flops = 2.0 * M * Nn * K;
-        const double bytes = 1.0 * M * K * (w8a8 ? 1 : 2) + 1.0 * Nn * K * (widen ? 2 : wsize) +
-                             1.0 * M * Nn * (epi == DLO_EPI_RESIDUAL ? 8 : 2);
-        return c->timed(w8a8 ? DLO_K_GEMM_FP8 : e4m3 ? DLO_K_GEMM_E4M3 : DLO_K_GEMM_BF16, flops,
-                        bytes, s, [&] { return launch_gemm(p, s, nl); });
+        const size_t nk = static_cast<size_t>(Nn) * K;
+        auto bytes_of = [&](double w_bytes) {
+            return 1.0 * M * K * (w8a8 ? 1 : 2) + w_bytes + 1.0 * M * Nn * (epi == DLO_EPI_RESIDUAL ? 8 : 2);
+        };
+        const int cls = w8a8 ? DLO_K_GEMM_FP8 : e4m3 ? DLO_K_GEMM_E4M3 : DLO_K_GEMM_BF16;
+        // W8A16 at many rows: the GEMM kernel first widens this linear's codes
+        // to bf16 in a workspace buffer (every CTA a share, then a grid
+        // barrier) and then multiplies in bf16 on CTA pairs, which outpaces
+        // widening each tile inside every CTA's mainloop; the per-tensor scale
+        // stays in the epilogue, so the products are the same.  Where that
+        // kernel form is unavailable, a separate widening kernel runs first.
+        const bool widen = e4m3 && !w8a8 && M >= widen_rows() && nk * 2 <= c->ws.wide_bytes &&
+                           (reinterpret_cast<uintptr_t>(p.W) & 15) == 0;
+        if (widen) {
+            void* wide = w + c->ws.wide;
+            GemmParams q = p;
+            q.w_codes = p.W;
+            q.W = wide;
+            q.w_dtype = DLO_DT_BF16;
+            q.w_sync = reinterpret_cast<unsigned*>(w + c->ws.gsync);
+            q.w_ready = false;
+            cudaError_t e = c->timed(cls, flops, bytes_of(1.0 * nk), s, [&] { return launch_gemm(q, s, nl); });
+            if (e != cudaErrorNotSupported) return e;
+            e = c->timed(DLO_K_CONVERT, 0.0, 3.0 * nk, s, [&] { return launch_widen_e4m3(p.W, nk, wide, s, nl); });
+            if (e != cudaSuccess) return e;
+            p.W = wide;
+            p.w_dtype = DLO_DT_BF16;
+            p.w_ready = false;   // the widening kernel just wrote it
+        }
+        return c->timed(cls, flops, bytes_of(1.0 * nk * (widen ? 2 : wsize)), s,
+                        [&] { return launch_gemm(p, s, nl); });
     };
     auto attn = [&](const void* q, const void* k, const void* v, void* out, int nq, int nk, int ldq, int ldk,
                     int ldv) {

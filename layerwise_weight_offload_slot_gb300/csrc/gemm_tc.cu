@@ -68,6 +68,13 @@ struct EpiArgs {
     int n_major;   // tile order: groups of N blocks sweep all M blocks (else the reverse)
     int group;     // blocks per group of the sweep (sweep_plan)
     int w_ready;   // W is not the preceding kernel's output (see GemmParams::w_ready)
+    // W8A16 widened inside the pair kernel: E4M3 codes [N, K], the bf16
+    // buffer the weight map reads, 16-code chunks, and the grid barrier's
+    // counter (zero at launch)
+    const uint4* wcodes;
+    uint4* wwide;
+    size_t wn16;
+    unsigned* gbar;
 };
 
 // Grouped tile order: groups of `group` M-blocks sweep all N-blocks, so one
@@ -674,11 +681,12 @@ struct PairPlan {
                   "swizzled buffers must be 1024-B aligned");
 };
 
-template <int BN, int STAGES, int CB, bool FP8, bool A8 = false>
+template <int BN, int STAGES, int CB, bool FP8, bool A8 = false, bool WIDEN = false>
 __global__ void __launch_bounds__(PairPlan<BN, STAGES, CB, FP8, A8>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmO, const EpiArgs args) {
     using P = PairPlan<BN, STAGES, CB, FP8, A8>;
+    static_assert(!WIDEN || (!FP8 && !A8), "widening prologue: bf16 mainloop");
     constexpr int KS = P::KS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -752,6 +760,37 @@ __global__ void __launch_bounds__(PairPlan<BN, STAGES, CB, FP8, A8>::THREADS, 1)
         *abort_flag = 1;
         if (args.err) atomicExch(args.err, 1);
     };
+
+    if constexpr (WIDEN) {
+        // ---------------- W8A16 inside the GEMM: every thread of the grid
+        // widens a share of the linear's E4M3 codes into the bf16 buffer the
+        // weight map reads (the predecessor, which may have read that buffer,
+        // has completed: every thread passed the programmatic-launch wait),
+        // then the grid meets at a barrier (cooperative launch: all CTAs
+        // co-resident; bounded) before the first weight tile is loaded
+        const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+        size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+        auto widen16 = [&](size_t k, const uint4& v) {
+            uint32_t lo[4], hi[4];
+            e4m3x8_to_bf16x8(v.x, v.y, lo);
+            e4m3x8_to_bf16x8(v.z, v.w, hi);
+            args.wwide[2 * k] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            args.wwide[2 * k + 1] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        };
+        for (; i + 7 * stride < args.wn16; i += 8 * stride) {
+            uint4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __ldg(args.wcodes + i + j * stride);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) widen16(i + j * stride, v[j]);
+        }
+        for (; i < args.wn16; i += stride) widen16(i, __ldg(args.wcodes + i));
+        fence_proxy_async_global();
+        __syncthreads();
+        if (threadIdx.x == 0 && !grid_arrive_wait(args.gbar, gridDim.x, abort_flag)) fail();
+        __syncthreads();
+        fence_proxy_async_global();
+    }
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer: this CTA's A rows and weight rows
@@ -1180,7 +1219,7 @@ cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* la
     if (!make_map(&to, p.out, residual ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                   residual ? 4 : 2, p.M, p.N, p.ldo, 32, residual ? 32 : 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    EpiArgs a;
+    EpiArgs a = {};
     a.M = p.M;
     a.N = p.N;
     a.K = p.K;
@@ -1234,13 +1273,13 @@ int pair_clusters() {
     return n;
 }
 
-template <int BN, int STAGES, int CB, bool FP8, bool A8 = false>
+template <int BN, int STAGES, int CB, bool FP8, bool A8 = false, bool WIDEN = false>
 cudaError_t run_gemm_pair(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
     using PL = PairPlan<BN, STAGES, CB, FP8, A8>;
     static_assert(PL::BYTES <= 227 * 1024, "shared memory plan exceeds 227 KB");
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<BN, STAGES, CB, FP8, A8>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<BN, STAGES, CB, FP8, A8, WIDEN>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, PL::BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -1267,7 +1306,7 @@ cudaError_t run_gemm_pair(const GemmParams& p, cudaStream_t s, unsigned long lon
     if (!make_map(&to, p.out, residual ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                   residual ? 4 : 2, p.M, p.N, p.ldo, 32, residual ? 32 : 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    EpiArgs a;
+    EpiArgs a = {};
     a.M = p.M;
     a.N = p.N;
     a.K = p.K;
@@ -1288,21 +1327,32 @@ cudaError_t run_gemm_pair(const GemmParams& p, cudaStream_t s, unsigned long lon
                a.num_m, a.num_n, &a);
     const int maxc = pair_clusters<BN, STAGES, CB, FP8, A8>();
     const int pairs = a.num_tiles < maxc ? a.num_tiles : maxc;
+    if (WIDEN) {
+        // the codes, their widened copy (p.W) and the barrier counter
+        a.wcodes = static_cast<const uint4*>(p.w_codes);
+        a.wwide = static_cast<uint4*>(const_cast<void*>(p.W));
+        a.wn16 = static_cast<size_t>(p.N) * p.K / 16;
+        a.gbar = p.w_sync;
+        cudaError_t e = cudaMemsetAsync(p.w_sync, 0, sizeof(unsigned), s);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs, 1, 1);
     cfg.blockDim = dim3(PL::THREADS, 1, 1);
     cfg.dynamicSmemBytes = PL::BYTES;
     cfg.stream = s;
-    cudaLaunchAttribute at[2];
+    cudaLaunchAttribute at[3];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 2;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
     at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    at[2].id = cudaLaunchAttributeCooperative;   // WIDEN: the grid barrier needs every CTA resident
+    at[2].val.cooperative = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 2;
-    cudaError_t le_ = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, STAGES, CB, FP8, A8>, ta, tb, to, a);
+    cfg.numAttrs = WIDEN ? 3 : 2;
+    cudaError_t le_ = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, STAGES, CB, FP8, A8, WIDEN>, ta, tb, to, a);
     ++*launches;
     return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
@@ -1492,9 +1542,49 @@ void pick_tile(const GemmParams& p, int* bn, bool* pair) {
 
 }  // namespace
 
+namespace {
+
+// W8A16 with the widening inside the bf16 pair GEMM (GemmParams::w_codes).
+// cudaErrorNotSupported when this GEMM or this driver cannot take that form;
+// the caller then widens with launch_widen_e4m3 and runs launch_gemm.  The
+// cooperative cluster launch is first tried outside a stream capture; if the
+// driver refuses it, the form is not tried again in this process.
+int g_widen_in_gemm = -1;   // -1 not tried, 0 refused, 1 works
+
+cudaError_t launch_gemm_widen(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
+    if (g_widen_in_gemm == 0 || !p.w_sync || p.w_dtype != DLO_DT_BF16 || p.a_dtype != DLO_DT_BF16)
+        return cudaErrorNotSupported;
+    const size_t nk = static_cast<size_t>(p.N) * p.K;
+    if (nk % 16 || ((reinterpret_cast<uintptr_t>(p.w_codes) | reinterpret_cast<uintptr_t>(p.W)) & 15))
+        return cudaErrorNotSupported;
+    int bn = 256;
+    bool pair = false;
+    pick_tile(p, &bn, &pair);
+    if (!pair || bn != 256) return cudaErrorNotSupported;
+    if (g_widen_in_gemm < 0) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+            return cudaErrorNotSupported;
+    }
+    const cudaError_t e = run_gemm_pair<256, 6, 0, false, false, true>(p, s, launches);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        if (g_widen_in_gemm < 0) {
+            g_widen_in_gemm = 0;
+            return cudaErrorNotSupported;
+        }
+        return e;
+    }
+    g_widen_in_gemm = 1;
+    return cudaSuccess;
+}
+
+}  // namespace
+
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
     if (p.M <= 0) return cudaSuccess;
     gemm_num_sms();
+    if (p.w_codes) return launch_gemm_widen(p, s, launches);
     // Single-CTA E4M3-weight GEMMs: N tile from a small cost model, time ~
     // waves x tile width / efficiency, where narrower tiles move more
     // shared-memory bytes per FLOP (128-wide tiles are limited to about 3/4

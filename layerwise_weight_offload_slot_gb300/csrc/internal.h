@@ -75,6 +75,7 @@ struct Workspace {
     size_t qs = 0;       // W8A8: kQuantScratch partial maxima, then the scale
     size_t wide = 0;     // W8A16: bf16 copy of the current linear's weights
     size_t wide_bytes = 0;   // its size (0: no such buffer)
+    size_t gsync = 0;    // W8A16: the widening GEMM's grid-barrier counter
     size_t err = 0;      // int[64] kernels' error words
     size_t total = 0;
 };
@@ -118,6 +119,12 @@ struct GemmParams {
     // producer then loads the first stages' weight tiles before the
     // programmatic-launch wait, overlapping the predecessor's tail.
     bool w_ready = false;
+    // W8A16 dequantised inside the GEMM: E4M3 codes [N, K] (16-B aligned,
+    // N*K a multiple of 16) that the kernel widens into W (a bf16 [N, K]
+    // buffer it then multiplies, w_dtype bf16, scales applied as usual) before
+    // its mainloop, with w_sync a device counter for its grid barrier.
+    const void* w_codes = nullptr;
+    unsigned* w_sync = nullptr;
 };
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches);
 // E4M3 codes [n] -> bf16 [n], exactly (the codes' values; a per-tensor scale

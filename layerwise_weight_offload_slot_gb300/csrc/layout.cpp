@@ -264,7 +264,10 @@ Workspace plan_workspace(const dlo_desc& d, size_t wide_min) {
         w.qs = take((kQuantScratch + 64) * sizeof(float));
     }
     w.wide_bytes = std::max(widen_buffer_bytes(d), wide_min);
-    if (w.wide_bytes) w.wide = take(w.wide_bytes);
+    if (w.wide_bytes) {
+        w.wide = take(w.wide_bytes);
+        w.gsync = take(256);
+    }
     w.err = take(64 * sizeof(int));
     w.total = align_up(cur, 256);
     return w;

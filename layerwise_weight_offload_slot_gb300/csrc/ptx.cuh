@@ -84,6 +84,34 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     }
 }
 
+// ------------------------------------------------------------------ grid barrier
+
+// Generic-proxy global writes of this thread ordered before later async-proxy
+// (TMA) accesses, and the reverse.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Barrier over the n CTAs of a cooperative launch (all co-resident): one
+// thread per CTA arrives on *count, which was zero before the launch, and
+// waits, bounded, until every CTA has.  Release / acquire at GPU scope: global
+// writes made before a CTA's arrival (after a __syncthreads) are visible to
+// every CTA once it returns true.
+__device__ __forceinline__ bool grid_arrive_wait(unsigned* count, unsigned n, const volatile int* abort) {
+    __threadfence();
+    atomicAdd(count, 1u);
+    const unsigned long long t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
+        if (v >= n) return true;
+        if ((i & 63u) == 0) {
+            if (abort && *abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {

@@ -297,12 +297,16 @@ def test_programmatic_dependent_launch_changes_no_bit():
 
 def test_w8a16_widened_linears_match_oracle(tmp_path):
     """W8A16 linears with at least DLO_WIDEN_ROWS rows are widened to bf16 in
-    the workspace before a bf16 GEMM (the 8192-token video block takes that
-    path by default).  Forced here on the small E4M3 video stack (every
-    linear, ragged rows, a 77-token text context) in a process of its own;
-    the output stays within the W8A16 stack tolerance of the oracle, the
-    widening kernel ran once per linear, and the output equals the fused
-    path's within the same tolerance."""
+    the workspace and multiplied in bf16 (the 8192-token video block takes
+    that path by default): inside the CTA-pair GEMM kernel (its CTAs widen the
+    codes, meet at a grid barrier, then run the bf16 mainloop), or, where the
+    tile model picks another kernel, by a separate widening kernel first.
+    Forced here on the small E4M3 video stack (ragged rows, a 77-token text
+    context), each in a process of its own: pairs forced (six linears widen
+    inside the GEMM; the 154-row cross k|v is too short for a pair and widens
+    separately), the tile model's picks (all seven widen separately), and no
+    widening (the GEMMs widen each tile in their mainloop).  All three stay
+    within the W8A16 stack tolerance of the oracle and of each other."""
     import os
     import subprocess
     import sys
@@ -318,20 +322,27 @@ def test_w8a16_widened_linears_match_oracle(tmp_path):
         "y = st.forward(x, c, t); torch.cuda.synchronize(); st.wait()\n"
         "np.save(sys.argv[1], y.float().cpu().numpy())\n"
         "print(st.stats()['kclass_launches'][dlo.KCLASS_NAMES.index('convert')])\n")
+    runs = {"in_gemm": {"DLO_WIDEN_ROWS": "1", "DLO_GEMM_PAIR": "1", "DLO_GEMM_BN": "256"},
+            "separate": {"DLO_WIDEN_ROWS": "1"},
+            "mainloop": {"DLO_WIDEN_ROWS": "1000000000"}}
     outs = {}
-    for rows in ("1", "1000000000"):
-        path = str(tmp_path / f"y_{len(rows)}.npy")
+    for name, env in runs.items():
+        path = str(tmp_path / f"y_{name}.npy")
         r = subprocess.run([sys.executable, "-c", code, path], cwd=root, capture_output=True, text=True,
-                           timeout=600, env=dict(os.environ, DLO_WIDEN_ROWS=rows, PYTHONPATH=root))
+                           timeout=600, env=dict(os.environ, PYTHONPATH=root, **env))
         assert r.returncode == 0, r.stderr[-2000:]
-        outs[rows] = (np.load(path), int(r.stdout.split()[-1]))
-    (yw, nw), (yf, nf) = outs["1"], outs["1000000000"]
-    assert nw - nf == 7 * cfg.n_blocks      # self qkv, self o, cross q, cross k|v, cross o, fc1, fc2
+        outs[name] = (np.load(path), int(r.stdout.split()[-1]))
+    base = outs["mainloop"][1]
+    assert outs["separate"][1] - base == 7 * cfg.n_blocks   # every linear: a widening launch
+    assert outs["in_gemm"][1] - base == 1 * cfg.n_blocks    # only the cross k|v
     x, cond, ctx = H.device_inputs(cfg)
     ref = H.oracle_forward(cfg, x, cond, ctx, H.oracle_blocks(cfg))
-    assert H.rel_l2(yw, ref) <= 5e-2
-    assert H.rel_l2(yw, yf) <= 5e-2
-    print("widened vs fused: max |diff|", float(np.abs(yw - yf).max()), "bit-identical", bool((yw == yf).all()))
+    ym = outs["mainloop"][0]
+    for name, (y, _) in outs.items():
+        assert H.rel_l2(y, ref) <= 5e-2, name
+        assert H.rel_l2(y, ym) <= 5e-2, name
+        print(name, "vs in-mainloop widening: max |diff|", float(np.abs(y - ym).max()),
+              "bit-identical", bool((y == ym).all()))
 
 
 def test_device_wait_timeout_is_reported_and_the_context_survives():
