@@ -199,10 +199,12 @@ __global__ void __launch_bounds__(256) widen_e4m3_kernel(const uint4* __restrict
     }
 }
 
-template <int BN, int STAGES, bool FP8, int MT = 1, int CB = 0>
+template <int BN, int STAGES, bool FP8, int MT = 1, int CB = 0, int KB = 1>
 struct SmemPlan {
-    static constexpr int A_STAGE = MT * A_TILE;           // MT 128-row A boxes per stage
-    static constexpr int B_TILE = BN * BK * 2;            // bf16 operand tile (MMA reads)
+    // KB 64-wide K boxes per operand per stage (bf16: 128-K stages when 2)
+    static constexpr int A_STAGE = MT * KB * A_TILE;      // MT x KB 128-row A boxes per stage
+    static constexpr int W_BOX = BN * BK * 2;             // one bf16 weight box
+    static constexpr int B_TILE = KB * W_BOX;             // bf16 operand tile (MMA reads)
     static constexpr int RAW_TILE = FP8 ? BN * BK : 0;     // e4m3 tile as loaded by TMA
     // bf16 B buffers: one per stage, or (E4M3, CB > 0) CB widened tiles that
     // cycle on their own, so the A / raw-code ring can be deeper than the
@@ -222,20 +224,23 @@ struct SmemPlan {
     // two accumulator sets of MT x BN fp32 columns; allocated in powers of two
     static constexpr uint32_t TMEM_COLS = 2 * MT * BN <= 256 ? 256u : 512u;
     static_assert(2 * MT * BN <= 512, "accumulators exceed TMEM");
+    static_assert(KB == 1 || (!FP8 && CB == 0), "two K boxes per stage: bf16 operands");
 };
 
 // MT > 1: a CTA tile is MT x 128 rows; every weight tile (and, for E4M3,
 // its widening) serves MT row blocks.  A8: A and W are both E4M3 codes
 // (W8A8), multiplied by kind::f8f6f4 at 128 K per stage (the same 128-byte
 // swizzled rows as bf16 at 64 K); no widening.
-template <int BN, int STAGES, bool FP8, int MT, bool A8, int CB = 0>
-__global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT, CB>::THREADS, 1)
+template <int BN, int STAGES, bool FP8, int MT, bool A8, int CB = 0, int KB = 1>
+__global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT, CB, KB>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO, const EpiArgs args) {
     static_assert(!(A8 && FP8), "W8A8 loads 8-bit codes for both operands, nothing to widen");
-    using P = SmemPlan<BN, STAGES, FP8, MT, CB>;
+    static_assert(KB == 1 || !A8, "W8A8 stages are one 128-byte box wide");
+    using P = SmemPlan<BN, STAGES, FP8, MT, CB, KB>;
     constexpr bool DEC = FP8 && CB > 0;   // widened tiles decoupled from the stages
-    constexpr int KS = A8 ? 128 : BK;   // K elements per stage (128 bytes of a row either way)
+    // K elements per stage: 128 bytes of a row per box either way
+    constexpr int KS = A8 ? 128 : BK * KB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -302,10 +307,14 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT, CB>::THREADS, 1)
         bool ok = true;
         uint32_t issued = 0, last_par = 0;   // per-stage bit masks
         auto load_w = [&](int st, int kb, int nb) {
-            if constexpr (FP8)
+            if constexpr (FP8) {
                 tma_load_2d(sbase + P::RAW_OFF + st * P::RAW_TILE, &tmB, kb * KS, nb * BN, bar_full + st * 8);
-            else
-                tma_load_2d(sbase + P::B_OFF + st * P::B_TILE, &tmB, kb * KS, nb * BN, bar_full + st * 8);
+            } else {
+#pragma unroll
+                for (int b = 0; b < KB; ++b)
+                    tma_load_2d(sbase + P::B_OFF + st * P::B_TILE + b * P::W_BOX, &tmB, kb * KS + b * BK, nb * BN,
+                                bar_full + st * 8);
+            }
         };
         // weight tiles of the first tile's first stages (the stages start
         // empty), before the programmatic-launch wait
@@ -338,8 +347,10 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT, CB>::THREADS, 1)
                 if (!w_done) mbar_arrive_expect_tx(fb, P::TX);
 #pragma unroll
                 for (int i = 0; i < MT; ++i)
-                    tma_load_2d(sbase + P::A_OFF + s * P::A_STAGE + i * A_TILE, &tmA, kb * KS,
-                                (mb * MT + i) * BM, fb);
+#pragma unroll
+                    for (int b = 0; b < KB; ++b)
+                        tma_load_2d(sbase + P::A_OFF + s * P::A_STAGE + (i * KB + b) * A_TILE, &tmA,
+                                    kb * KS + b * BK, (mb * MT + i) * BM, fb);
                 if (!w_done) load_w(s, kb, nb);
                 issued |= 1u << s;
                 last_par = (last_par & ~(1u << s)) | (ph << s);
@@ -393,13 +404,16 @@ __global__ void __launch_bounds__(SmemPlan<BN, STAGES, FP8, MT, CB>::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < MT; ++i) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {   // 4 x 32 bytes of K per stage
-                        const uint64_t ad = a_desc + ((i * A_TILE + kk * 32) >> 4);
-                        const uint64_t bd = b_desc + ((kk * 32) >> 4);
-                        if constexpr (A8)
-                            tc_mma_f8(d_tmem + i * BN, ad, bd, idesc, (kb | kk) != 0);
-                        else
-                            tc_mma_f16(d_tmem + i * BN, ad, bd, idesc, (kb | kk) != 0);
+                    for (int b = 0; b < KB; ++b) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {   // 4 x 32 bytes of K per box
+                            const uint64_t ad = a_desc + (((i * KB + b) * A_TILE + kk * 32) >> 4);
+                            const uint64_t bd = b_desc + ((b * P::W_BOX + kk * 32) >> 4);
+                            if constexpr (A8)
+                                tc_mma_f8(d_tmem + i * BN, ad, bd, idesc, (kb | kk) != 0);
+                            else
+                                tc_mma_f16(d_tmem + i * BN, ad, bd, idesc, (kb | b | kk) != 0);
+                        }
                     }
                 }
                 tc_commit(bar_empty + s * 8);
@@ -1183,13 +1197,13 @@ void sweep_plan(double a_bytes, double w_bytes, int num_m, int num_n, EpiArgs* a
     a->group = a->n_major ? gn : gm;
 }
 
-template <int BN, int STAGES, bool FP8, int MT = 1, bool A8 = false, int CB = 0>
+template <int BN, int STAGES, bool FP8, int MT = 1, bool A8 = false, int CB = 0, int KB = 1>
 cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
-    using PL = SmemPlan<BN, STAGES, FP8, MT, CB>;
+    using PL = SmemPlan<BN, STAGES, FP8, MT, CB, KB>;
     static_assert(PL::BYTES <= 227 * 1024, "shared memory plan exceeds 227 KB");
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, STAGES, FP8, MT, A8, CB>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, STAGES, FP8, MT, A8, CB, KB>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, PL::BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -1239,7 +1253,7 @@ cudaError_t run_gemm(const GemmParams& p, cudaStream_t s, unsigned long long* la
     sweep_plan(static_cast<double>(p.M) * p.K * (A8 ? 1 : 2), static_cast<double>(p.N) * p.K * (FP8 || A8 ? 1 : 2),
                a.num_m, a.num_n, &a);
     const int grid = a.num_tiles < g_num_sms ? a.num_tiles : g_num_sms;
-    cudaError_t le_ = launch_k(gemm_kernel<BN, STAGES, FP8, MT, A8, CB>, grid, PL::THREADS, PL::BYTES, s, ta, tb, to, a);
+    cudaError_t le_ = launch_k(gemm_kernel<BN, STAGES, FP8, MT, A8, CB, KB>, grid, PL::THREADS, PL::BYTES, s, ta, tb, to, a);
     ++*launches;
     return le_ != cudaSuccess ? le_ : cudaGetLastError();
 }
@@ -1367,6 +1381,16 @@ int pair_mode() {
         v = (e && e[0] == '0' && e[1] == 0) ? 0 : (e && e[0] == '1' && e[1] == 0) ? 1 : -1;
     }
     return v;
+}
+
+// DLO_GEMM_K128=0: 128-wide bf16 tiles on 64-K stages (tuning).
+bool k128_enabled() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = std::getenv("DLO_GEMM_K128");
+        v = (e && e[0] == '0' && e[1] == 0) ? 0 : 1;
+    }
+    return v != 0;
 }
 
 int forced_mt() {
@@ -1641,6 +1665,9 @@ cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, unsigned long long*
     }
     if (best_bn == 256) return run_gemm<256, 4, false>(p, s, launches);
     if (best_bn == 192) return run_gemm<192, 4, false>(p, s, launches);
+    // 128-wide tiles: 128-K stages (two boxes per operand, three stages)
+    // halve the stage hand-overs per K; DLO_GEMM_K128=0 keeps 64-K stages
+    if (k128_enabled()) return run_gemm<128, 3, false, 1, false, 0, 2>(p, s, launches);
     return run_gemm<128, 6, false>(p, s, launches);
 }
 

@@ -465,15 +465,17 @@ def test_gemm_e4m3_single_cta_path_matches_oracle():
     assert rel_l2 < 6e-3 and element <= 6e-3
 
 
-@pytest.mark.parametrize("env", [{"DLO_GEMM_PAIR": "0", "DLO_GEMM_BN": "192"},
+@pytest.mark.parametrize("env", [{"DLO_GEMM_PAIR": "0", "DLO_GEMM_BN": "128", "DLO_GEMM_K128": "0"},
+                                 {"DLO_GEMM_PAIR": "0", "DLO_GEMM_BN": "192"},
                                  {"DLO_GEMM_PAIR": "0", "DLO_GEMM_BN": "256"},
                                  {"DLO_GEMM_PAIR": "1", "DLO_GEMM_BN": "128"},
                                  {"DLO_GEMM_PAIR": "1", "DLO_GEMM_BN": "192"},
                                  {"DLO_GEMM_PAIR": "1", "DLO_GEMM_BN": "256"}],
-                         ids=["single-192", "single-256", "pair-128", "pair-192", "pair-256"])
+                         ids=["single-128-k64", "single-192", "single-256", "pair-128", "pair-192", "pair-256"])
 def test_gemm_tile_paths_match_oracle(env):
     """Every bf16 and W8A8 GEMM kernel the tile model can pick (single CTAs or
-    CTA pairs, 128-, 192- or 256-wide tiles) passes the GEMM parity cases,
+    CTA pairs, 128-, 192- or 256-wide tiles; 128-wide single-CTA bf16 tiles
+    on 128-K stages by default, 64-K ones here) passes the GEMM parity cases,
     each forced in turn (pairs take the cases with at least 256 rows; the
     others run on single CTAs); the default run covers the model's own
     picks.  Each setting runs in a process of its own (the switches are read
