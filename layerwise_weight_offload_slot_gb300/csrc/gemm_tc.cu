@@ -1527,13 +1527,16 @@ namespace {
 // an SM takes in only BN/2 weight rows, but its MMAs also read the peer's
 // half; their costs are set from graph-timed runs of both kernels at 2048-
 // and 8192-row shapes (pairs 11-15% faster at 8192 rows, 0-4% slower at
-// 2048), so pairs win where many waves of wide tiles run.  A W8A8 step (128
+// 2048), so pairs win where many waves of wide tiles run.  128-wide bf16
+// single-CTA tiles on 128-K stages take 433 cycles per 64 K (measured the
+// same way).  A W8A8 step (128
 // K of E4M3, MMAs at twice the bf16 rate) has the bf16 step's bytes and
 // cycles.  DLO_GEMM_BN forces the width, DLO_GEMM_PAIR=0 or 1 single CTAs or
 // pairs (tuning).
 void pick_tile(const GemmParams& p, int* bn, bool* pair) {
     const int widths[3] = {128, 192, 256};
-    const double single_cyc[3] = {509, 543, 651};
+    const bool k128 = p.a_dtype == DLO_DT_BF16 && k128_enabled();
+    const double single_cyc[3] = {k128 ? 433.0 : 509.0, 543, 651};
     const double pair_cyc[3] = {530, 580, 600};
     const long long num_m = (p.M + BM - 1) / BM;
     const int max_pairs = g_num_sms / 2 > 0 ? g_num_sms / 2 : 1;
