@@ -719,6 +719,13 @@ __global__ void __launch_bounds__(PairPlan<BN, STAGES, CB, FP8, A8>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // launched in anything but clusters of two (a tool replaying the launch
+    // without its cluster shape, say), the pair instructions below would be
+    // invalid: report it and do nothing
+    if (cluster_nctarank() != 2) {
+        if (threadIdx.x == 0 && args.err) atomicExch(args.err, 1);
+        return;
+    }
     const uint32_t rank = cluster_ctarank();
     const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
 
@@ -1576,9 +1583,15 @@ namespace {
 // the caller then widens with launch_widen_e4m3 and runs launch_gemm.  The
 // cooperative cluster launch is first tried outside a stream capture; if the
 // driver refuses it, the form is not tried again in this process.
-int g_widen_in_gemm = -1;   // -1 not tried, 0 refused, 1 works
+int g_widen_in_gemm = -1;   // -1 not tried, 0 refused (or DLO_WIDEN_IN_GEMM=0), 1 works
 
 cudaError_t launch_gemm_widen(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
+    if (g_widen_in_gemm < 0) {
+        // DLO_WIDEN_IN_GEMM=0: always the separate widening kernel (tuning;
+        // also the form a profiler can replay)
+        const char* e = std::getenv("DLO_WIDEN_IN_GEMM");
+        if (e && e[0] == '0' && e[1] == 0) g_widen_in_gemm = 0;
+    }
     if (g_widen_in_gemm == 0 || !p.w_sync || p.w_dtype != DLO_DT_BF16 || p.a_dtype != DLO_DT_BF16)
         return cudaErrorNotSupported;
     const size_t nk = static_cast<size_t>(p.N) * p.K;

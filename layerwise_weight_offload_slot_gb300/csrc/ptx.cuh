@@ -413,6 +413,13 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     return r;
 }
 
+// CTAs in this CTA's cluster.
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
 // shared::cluster address of the shared variable at `saddr` in cluster CTA `rank`.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     uint32_t d;
