@@ -643,12 +643,15 @@ def run_sweep(args):
         else:
             exact = bool(torch.equal(y, ref))
         cs = st.compute_stream
+        clocks = ClockSampler(0)
+        clocks.start()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(cs)
         for _ in range(args.steps):
             st.forward(x0, e, ctx, out=y)
         e1.record(cs)
         torch.cuda.synchronize()
+        clk = clocks.stop()
         ms = e0.elapsed_time(e1) / args.steps
         st.set_timing(1)
         s0 = st.stats()
@@ -658,13 +661,15 @@ def run_sweep(args):
         s1 = st.stats()
         copy = s1["copy_ms"] - s0["copy_ms"]
         exposed = s1["exposed_wait_ms"] - s0["exposed_wait_ms"]
+        compute = s1["compute_ms"] - s0["compute_ms"]
         n_exec = s1["timed_execs"] - s0["timed_execs"]
         slots_ok = all(st.verify_slot(s) for s in (0, 1) if st.stats()["slot_block"][s] >= 0)
         res.append({"k": k, "steps_per_s": 1e3 / ms, "ms_per_step": ms,
                     "streamed_gb_per_step": (cfg.n_blocks - k) * bb / 1e9,
                     "h2d_gbs": n_exec * bb / (copy * 1e-3) / 1e9 if copy > 0 else None,
                     "overlap_fraction": 1.0 - exposed / copy if copy > 0 else None,
-                    "output_equals_k0": exact, "slots_bit_exact": slots_ok})
+                    "compute_ms_per_step": compute,
+                    "output_equals_k0": exact, "slots_bit_exact": slots_ok, "clocks": clk})
         st._own_host = False      # the host blocks are shared by the four contexts
         st.close()
 
@@ -698,6 +703,8 @@ def run_sweep(args):
         st.wait()
         cs = st.compute_stream
         c0 = st.stats()["h2d_copies"]
+        clocks = ClockSampler(0)
+        clocks.start()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(cs)
         for _ in range(args.steps):
@@ -705,6 +712,7 @@ def run_sweep(args):
         e1.record(cs)
         torch.cuda.synchronize()
         st.wait()
+        clk = clocks.stop()
         ms = e0.elapsed_time(e1) / args.steps
         copies = (st.stats()["h2d_copies"] - c0) / args.steps
         st.set_timing(1)
@@ -720,7 +728,8 @@ def run_sweep(args):
                     "staging_gbs": n_exec * bb / (copy * 1e-3) / 1e9 if copy > 0 else None,
                     "overlap_fraction": 1.0 - (s1["exposed_wait_ms"] - s0["exposed_wait_ms"]) / copy
                     if copy > 0 else None,
-                    "output_equals_memcpy_k0": exact})
+                    "compute_ms_per_step": s1["compute_ms"] - s0["compute_ms"],
+                    "output_equals_memcpy_k0": exact, "clocks": clk})
         st._own_host = False
         st.close()
     if page is not None:
