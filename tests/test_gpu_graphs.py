@@ -287,3 +287,56 @@ def test_graphs_with_byte_blocks_and_gather_staging():
         for s in (0, 1):
             assert st.verify_slot(s)
         st.close()
+
+
+_WIDEN_GRAPHS = """
+import sys, numpy as np, torch
+from tests import helpers as H
+from tests.test_gpu_stack import SMALL_VID_FP8 as cfg
+
+def steps(graphs, k, n=4):
+    st = H.make_stack(cfg)
+    st.attach()
+    if k:
+        st.set_resident(k)
+    st.set_graphs(graphs)
+    x, c, t = H.device_inputs(cfg)
+    out = torch.empty_like(x)
+    outs = []
+    for s in range(n):
+        st.forward(x, c, t, out=out)
+        torch.cuda.synchronize()
+        outs.append(out.clone())
+        x.copy_(out)
+    st.wait()
+    stats = st.stats()
+    st.close()
+    return outs, stats
+
+direct, _ = steps(False, 0)
+graph, sg = steps(True, 0)
+resident, _ = steps(True, 2)
+assert sg["graph_launches"] >= 2, sg["graph_launches"]
+for s in range(len(direct)):
+    assert torch.equal(direct[s], graph[s]), ("graph", s)
+    assert torch.equal(direct[s], resident[s]), ("resident", s)
+print("ok", sg["graph_launches"])
+"""
+
+
+def test_w8a16_widening_inside_the_gemm_in_graphs_and_with_residency():
+    """The W8A16 GEMM that widens its codes inside the kernel (a cooperative
+    launch of CTA pairs with a grid barrier), forced on the small E4M3 video
+    stack: whole-forward CUDA graphs replay it, and two resident leading
+    blocks change nothing; four chained steps are bit-identical to direct
+    forwards with every block streamed.  In a process of its own (the
+    switches are read once)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PYTHONPATH=root, DLO_WIDEN_ROWS="1", DLO_GEMM_PAIR="1", DLO_GEMM_BN="256")
+    r = subprocess.run([sys.executable, "-c", _WIDEN_GRAPHS], cwd=root, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-3000:]
+    assert r.stdout.split()[-2] == "ok"
