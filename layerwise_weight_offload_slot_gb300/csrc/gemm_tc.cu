@@ -32,6 +32,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -1583,7 +1584,7 @@ namespace {
 // the caller then widens with launch_widen_e4m3 and runs launch_gemm.  The
 // cooperative cluster launch is first tried outside a stream capture; if the
 // driver refuses it, the form is not tried again in this process.
-int g_widen_in_gemm = -1;   // -1 not tried, 0 refused (or DLO_WIDEN_IN_GEMM=0), 1 works
+std::atomic<int> g_widen_in_gemm{-1};   // -1 not tried, 0 refused (or DLO_WIDEN_IN_GEMM=0), 1 works
 
 cudaError_t launch_gemm_widen(const GemmParams& p, cudaStream_t s, unsigned long long* launches) {
     if (g_widen_in_gemm < 0) {
