@@ -41,7 +41,7 @@ def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=100)
-    p.add_argument("--passes", type=int, default=3,
+    p.add_argument("--passes", type=int, default=5,
                    help="timed passes of --steps steps each; the line reports the median pass")
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
