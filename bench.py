@@ -249,10 +249,22 @@ def run_reference(args, cfg, rank: int, world: int):
 
 # ----------------------------------------------------------------------------- our arm
 
+def source_digest(path: str) -> str:
+    """sha256 (16 hex digits) of a C++/CUDA source with its comments and
+    whitespace removed: a change of code changes it, a change of comments
+    does not."""
+    import hashlib
+    import re
+    text = open(path, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    text = re.sub(r"\s+", "", text)
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
+
+
 def traffic_record(workload: str, kernel_class: str):
     """ncu DRAM bytes per launch of a workload's dominant kernel class, if the
-    committed record was taken on the current source of that kernel."""
-    import hashlib
+    committed record was taken on the current code of that kernel's source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -262,8 +274,7 @@ def traffic_record(workload: str, kernel_class: str):
     if not r:
         return None
     src = os.path.join(ROOT, "layerwise_weight_offload_slot_gb300", "csrc", r["source"])
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if h != r.get("source_sha"):
+    if source_digest(src) != r.get("source_sha"):
         return None
     return r
 

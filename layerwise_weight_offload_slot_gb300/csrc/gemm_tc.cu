@@ -1,8 +1,9 @@
 // Y = A W^T on the 5th-generation tensor cores (tcgen05), sm_103a.
 //
 // Persistent kernel, one CTA per SM, 6 warps (+12 converter warps for E4M3):
-//   warp 0      TMA producer: 128x64 A tile and BNx64 W tile per stage,
-//               128-byte swizzle, into a STAGES-deep shared-memory ring
+//   warp 0      TMA producer: 128x64 A tile and BNx64 W tile per stage (two
+//               of each for 128-K stages), 128-byte swizzle, into a
+//               STAGES-deep shared-memory ring
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16 (M=128,
 //               N=BN, K=16) x 4 per stage into one of two fp32 TMEM
 //               accumulators; tcgen05.commit frees the stage / publishes the
@@ -21,9 +22,11 @@
 // and the per-tensor scale is applied to the fp32 accumulator in the epilogue.
 // The widened tiles live in CB buffers of their own (conv / conv_empty
 // barriers), so the ring of A tiles and raw codes is four stages deep.
-// E4M3-weight GEMMs with at least 256 rows run on CTA pairs instead
-// (gemm_pair_kernel, tcgen05 cta_group::2, below): one 256 x 256 MMA over two
-// SMs, each SM widening half of the weight tile.
+// CTA pairs (gemm_pair_kernel, tcgen05 cta_group::2, below) take E4M3-weight
+// GEMMs with at least 256 rows, and bf16 and W8A8 GEMMs where the tile model
+// (pick_tile) finds them faster: one 256 x BN MMA over two SMs, each SM
+// loading half of the weight tile.  W8A16 linears with many rows are widened
+// to bf16 once, inside the pair kernel before its mainloop (WIDEN).
 //
 // Every mbarrier wait is bounded (2 s); a wait that runs out sets the
 // kernel's error word and a CTA-wide abort flag, after which every role

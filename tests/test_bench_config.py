@@ -61,3 +61,19 @@ def test_reference_arm_reports_what_it_timed(capsys):
     assert ex["blocks_per_timed_step"] == 1 and ex["blocks_per_stack_step"] == 4
     assert abs(ex["stack_ms_per_step"] - 4 * line["ms_per_step"]) <= 1e-6 * ex["stack_ms_per_step"]
     assert abs(line["value"] - 1e3 / ex["stack_ms_per_step"]) <= 1e-9 * line["value"]
+
+
+def test_traffic_records_follow_code_not_comments(tmp_path):
+    """A committed ncu traffic record is shown only while its kernel source's
+    code is unchanged: comments and whitespace may change, code may not; the
+    committed records match the committed sources."""
+    base = "__global__ void k(int* p) { p[0] = 1; }  // store one\n"
+    a, b, c = tmp_path / "a.cu", tmp_path / "b.cu", tmp_path / "c.cu"
+    a.write_text(base)
+    b.write_text("/* a kernel */\n__global__  void k(int* p) {\n  p[0] = 1;  // store\n}\n")
+    c.write_text(base.replace("= 1", "= 2"))
+    assert bench.source_digest(str(a)) == bench.source_digest(str(b))
+    assert bench.source_digest(str(a)) != bench.source_digest(str(c))
+    assert bench.traffic_record("dit-xl-28x1152-b2-n1024", "gemm_bf16") is not None
+    assert bench.traffic_record("video-fp8-40x5120-n8192", "gemm_e4m3") is not None
+    assert bench.traffic_record("dit-xl-28x1152-b2-n1024", "attention") is None
