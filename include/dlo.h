@@ -66,7 +66,13 @@ typedef int dlo_status;
 
 /* weight storage of the linears in a block */
 #define DLO_W_BF16       0
-#define DLO_W_E4M3       1   /* e4m3 weight + one fp32 scale per linear tensor   */
+/* W8A16: e4m3 weights + one fp32 scale per linear tensor, streamed as codes
+ * (half the bytes of bf16) and dequantised inside the GEMM kernel: widened
+ * to exact bf16 values per weight tile in the mainloop, or, for linears with
+ * at least DLO_WIDEN_ROWS rows (default 4096), once per launch by the
+ * kernel's own CTAs before its mainloop; activations stay bf16 and the scale
+ * multiplies the fp32 accumulator (y = s * (x q^T) + b). */
+#define DLO_W_E4M3       1
 /* W8A8: the DLO_W_E4M3 weights (same layout and bytes), and every linear's
  * input activation quantised to E4M3 on the fly with one dynamic per-tensor
  * scale (dlo_op_quantize_act); the product runs on the 8-bit tensor cores:
