@@ -263,15 +263,18 @@ __global__ void __launch_bounds__(kThreadsA, DUO ? 2 : 1)
             got = __all_sync(0xFFFFFFFFu, got);
             if (!got) { ok = false; break; }
             tc_fence_after();
+            // all of S_j's loads in flight before one wait (the first wait
+            // covers every load; the others tie each array to it)
+            uint32_t r[TK / 32][32];
+#pragma unroll
+            for (int c = 0; c < TK / 32; ++c) tmem_ld_32x32b_x32(tl + st * TK + c * 32, r[c]);
+#pragma unroll
+            for (int c = 0; c < TK / 32; ++c) tmem_wait_ld_r(r[c]);
             float v[TK];
 #pragma unroll
-            for (int c = 0; c < TK / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tl + st * TK + c * 32, r);
-                tmem_wait_ld();
+            for (int c = 0; c < TK / 32; ++c)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[c * 32 + i] = __uint_as_float(r[i]);
-            }
+                for (int i = 0; i < 32; ++i) v[c * 32 + i] = __uint_as_float(r[c][i]);
             // raw scores: the row max is taken before scaling (scale > 0), and
             // keys past nk exist only in the last tile
             const int kvalid = nk - j * TK;
