@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(kThreadsA, DUO ? 2 : 1)
                 for (int c = 0; c < (HDP + 31) / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tl + P::O_COL + c * 32, r);
-                    tmem_wait_ld();
+                    tmem_wait_ld_r(r);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
                     tmem_st_32x32b_x32(tl + P::O_COL + c * 32, r);
@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(kThreadsA, DUO ? 2 : 1)
             for (int c = 0; c < (HDP + 31) / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tl + P::O_COL + c * 32, r);
-                tmem_wait_ld();
+                tmem_wait_ld_r(r);
                 if (grow < nq) {
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4) {

@@ -237,10 +237,6 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_wait_ld() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 // tcgen05.ld of 32 columns without a memory clobber, and a wait that takes the
 // loaded registers as operands: the registers' uses are ordered after the
 // wait by data dependence, and global loads issued around them (epilogue
